@@ -1,0 +1,168 @@
+"""Double-precision CPU oracle for the Simple GLA mixer (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the entry module's smoke check and
+the benchmark's CPU-baseline / reference leg are the only users. The CUDA
+library never imports, links or calls it, and it shares no code with it.
+
+The arithmetic lives in gla_oracle.c; this file compiles it with gcc (no
+fast-math, no FMA contraction) and marshals numpy arrays. Every array is
+promoted to float64 before the call, so the oracle sees exactly the values
+the GPU receives (bf16-rounded inputs stay bf16 values).
+
+Functions (all layouts token-major, see gla_oracle.c):
+  fwd_recurrent  -- the token recurrence (O2)
+  fwd_quadratic  -- brute-force unrolled form, tiny inputs only (O1)
+  fwd_chunked    -- the chunked form in double (O5)
+  bwd            -- analytic two-pass backward (O3)
+  bwd_chunked    -- the chunk-level backward equations in double (O6)
+  decode         -- one recurrent step per (sequence, head) (O4)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gla_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_L = ctypes.c_long
+
+
+def build(force: bool = False) -> str:
+    """Compile gla_oracle.c into liboracle.so next to it (gcc, -O2, no fast-math)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            fwd_sig = [_D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L, _L, _L, _D, _D, ctypes.c_int]
+            lib.gla_oracle_fwd_recurrent.argtypes = fwd_sig
+            lib.gla_oracle_fwd_quadratic.argtypes = fwd_sig
+            lib.gla_oracle_fwd_chunked.argtypes = fwd_sig[:11] + [_L] + fwd_sig[11:]
+            bwd_sig = [_D, _D, _D, _D, _D, ctypes.c_double, _D, _D, _L, _L, _L, _L, _L,
+                       _D, _D, _D, _D, ctypes.c_int]
+            lib.gla_oracle_bwd.argtypes = bwd_sig
+            lib.gla_oracle_bwd_chunked.argtypes = bwd_sig[:13] + [_L] + bwd_sig[13:]
+            lib.gla_oracle_decode.argtypes = [_D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L, _L,
+                                              _D, ctypes.c_int]
+            lib.gla_oracle_threads.argtypes = [ctypes.c_int]
+            for f in ("gla_oracle_fwd_recurrent", "gla_oracle_fwd_quadratic", "gla_oracle_fwd_chunked",
+                      "gla_oracle_bwd", "gla_oracle_bwd_chunked", "gla_oracle_decode",
+                      "gla_oracle_threads"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def threads(nthreads: int = 0) -> int:
+    """Number of host threads the oracle uses for `nthreads` (0 = all online cores)."""
+    return int(_load().gla_oracle_threads(int(nthreads)))
+
+
+def _f64(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _p(x):
+    return None if x is None else x.ctypes.data_as(_D)
+
+
+def _dims(q, v):
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    return B, T, H, dk, dv
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise ValueError(f"oracle {name}: invalid arguments")
+
+
+def _fwd(fn_name, q, k, v, log_lambda, h0, scale, nthreads, chunk=None, want_o=True, want_hT=True):
+    lib = _load()
+    q, k, v, ll, h0 = _f64(q), _f64(k), _f64(v), _f64(log_lambda), _f64(h0)
+    B, T, H, dk, dv = _dims(q, v)
+    o = np.zeros((B, T, H, dv)) if want_o else None
+    hT = np.zeros((B, H, dk, dv)) if want_hT else None
+    args = [_p(q), _p(k), _p(v), _p(ll), _p(h0), float(scale), B, T, H, dk, dv]
+    if chunk is not None:
+        args.append(int(chunk))
+    args += [_p(o), _p(hT), int(nthreads)]
+    _check(getattr(lib, fn_name)(*args), fn_name)
+    return o, hT
+
+
+def fwd_recurrent(q, k, v, log_lambda, h0=None, scale=1.0, nthreads=0, want_o=True):
+    """O2: o_t = scale * S_t^T q_t with S_t = lambda S_{t-1} + k_t v_t^T. Returns (o, hT)."""
+    return _fwd("gla_oracle_fwd_recurrent", q, k, v, log_lambda, h0, scale, nthreads, want_o=want_o)
+
+
+def fwd_quadratic(q, k, v, log_lambda, h0=None, scale=1.0, nthreads=0):
+    """O1: brute-force unrolled sum (O(T^2)). Returns (o, hT)."""
+    return _fwd("gla_oracle_fwd_quadratic", q, k, v, log_lambda, h0, scale, nthreads)
+
+
+def fwd_chunked(q, k, v, log_lambda, h0=None, scale=1.0, chunk=128, nthreads=0):
+    """O5: the chunked form in double with chunk length `chunk`. Returns (o, hT)."""
+    return _fwd("gla_oracle_fwd_chunked", q, k, v, log_lambda, h0, scale, nthreads, chunk=chunk)
+
+
+def _bwd(fn_name, q, k, v, log_lambda, h0, scale, do, dhT, nthreads, chunk=None):
+    lib = _load()
+    q, k, v, ll, h0, do, dhT = map(_f64, (q, k, v, log_lambda, h0, do, dhT))
+    B, T, H, dk, dv = _dims(q, v)
+    dq = np.zeros((B, T, H, dk))
+    dk_ = np.zeros((B, T, H, dk))
+    dv_ = np.zeros((B, T, H, dv))
+    dh0 = np.zeros((B, H, dk, dv))
+    args = [_p(q), _p(k), _p(v), _p(ll), _p(h0), float(scale), _p(do), _p(dhT), B, T, H, dk, dv]
+    if chunk is not None:
+        args.append(int(chunk))
+    args += [_p(dq), _p(dk_), _p(dv_), _p(dh0), int(nthreads)]
+    _check(getattr(lib, fn_name)(*args), fn_name)
+    return dq, dk_, dv_, dh0
+
+
+def bwd(q, k, v, log_lambda, h0, scale, do, dhT=None, nthreads=0):
+    """O3: gradients of sum<do, o> + <dhT, hT>. Returns (dq, dk, dv, dh0)."""
+    return _bwd("gla_oracle_bwd", q, k, v, log_lambda, h0, scale, do, dhT, nthreads)
+
+
+def bwd_chunked(q, k, v, log_lambda, h0, scale, do, dhT=None, chunk=128, nthreads=0):
+    """O6: the chunk-level backward equations in double. Returns (dq, dk, dv, dh0)."""
+    return _bwd("gla_oracle_bwd_chunked", q, k, v, log_lambda, h0, scale, do, dhT, nthreads, chunk)
+
+
+def decode(q, k, v, log_lambda, S, scale=1.0, nthreads=0):
+    """O4: one recurrent step per (n, h). q, k [N,H,dk], v [N,H,dv], S [N,H,dk,dv].
+    Returns (o, S_new); the input S is not modified."""
+    lib = _load()
+    q, k, v, ll = map(_f64, (q, k, v, log_lambda))
+    S_new = np.array(S, dtype=np.float64, copy=True, order="C")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((N, H, dv))
+    _check(lib.gla_oracle_decode(_p(q), _p(k), _p(v), _p(ll), _p(S_new), float(scale), N, H, dk, dv,
+                                 _p(o), int(nthreads)), "decode")
+    return o, S_new

@@ -1,0 +1,514 @@
+/*
+ * gla_oracle.c -- plain, slow, double-precision CPU oracle for the Simple
+ * Gated Linear Attention (Simple GLA) mixer.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path links, loads or
+ * calls this file: only the test suite, the smoke check of the entry module
+ * and the CPU-baseline / reference leg of the benchmark use it. It shares no
+ * code, header, table or helper with the CUDA library.
+ *
+ * Source: "Beyond the KV cache: Training and serving i14's Laplace 3B linear
+ * attention model on AWS Trainium2 with native PyTorch",
+ *   - section "i14 and the Laplace 3B architecture", paragraph "GLA mixer"
+ *     (the "GLA recurrent-state update equation" and the "GLA state-readout
+ *     equation"): per head h a dk x dv state, S_t = lambda_h * S_{t-1} +
+ *     k_t v_t^T with a fixed per-head decay lambda_h, read out by the query;
+ *   - section "Engineering challenges", "Challenge 1: Using native PyTorch on
+ *     Trainium for GLA" (the "Chunked GLA intra-chunk output" and "Chunked
+ *     GLA state update" equations, Figure 3): masked linear attention inside
+ *     a chunk plus the running state, and the state advanced by lambda^C;
+ *   - "Challenge 3: Backward-pass unrolling for a sequential recurrence":
+ *     gradients flow through every serial state update.
+ *
+ * The equations themselves are images that did not survive extraction. The
+ * readings used here (all stated in the design notes):
+ *   - readout after the update: o_t = scale * S_t^T q_t;
+ *   - the scale multiplies the readout only; S and hT are unscaled;
+ *   - lambda = exp(log_lambda[h]); lambda^0 = 1 even when lambda = 0;
+ *   - S_0 = h0 (zero when h0 is NULL).
+ *
+ * Layouts: q, k, do, dq, dk [B,T,H,dk]; v, o, dv [B,T,H,dv];
+ * h0, hT, dhT, dh0 [B,H,dk,dv]; decode q, k [N,H,dk], v, o [N,H,dv],
+ * S [N,H,dk,dv]. Everything is double. Work is split over independent
+ * (b, h) pairs with pthreads; nothing else is reordered.
+ *
+ * Parity pins live in the test suite: brute force against the recurrence,
+ * lambda = 1 (causal linear attention) and lambda = 0 special cases, the
+ * closed-form final state, chunk-size invariance, split-call invariance,
+ * linearity, hand-worked fixtures and central finite differences.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ---------------------------------------------------------------- threads */
+typedef void (*unit_fn)(void *ctx, long unit);
+
+typedef struct {
+    unit_fn fn;
+    void *ctx;
+    long n_units;
+    long next;
+    pthread_mutex_t lock;
+} pool_t;
+
+static void *pool_worker(void *arg) {
+    pool_t *p = (pool_t *)arg;
+    for (;;) {
+        long u;
+        pthread_mutex_lock(&p->lock);
+        u = p->next++;
+        pthread_mutex_unlock(&p->lock);
+        if (u >= p->n_units) break;
+        p->fn(p->ctx, u);
+    }
+    return NULL;
+}
+
+static int resolve_threads(int nthreads) {
+    if (nthreads > 0) return nthreads;
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+static void run_units(long n_units, int nthreads, unit_fn fn, void *ctx) {
+    int nt = resolve_threads(nthreads);
+    if (nt > n_units) nt = (int)(n_units > 0 ? n_units : 1);
+    pool_t p;
+    p.fn = fn; p.ctx = ctx; p.n_units = n_units; p.next = 0;
+    pthread_mutex_init(&p.lock, NULL);
+    if (nt <= 1) {
+        pool_worker(&p);
+    } else {
+        pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nt);
+        int started = 0;
+        for (int i = 0; i < nt; ++i)
+            if (pthread_create(&th[i], NULL, pool_worker, &p) == 0) ++started;
+        if (started == 0) pool_worker(&p);
+        for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+        free(th);
+    }
+    pthread_mutex_destroy(&p.lock);
+}
+
+int gla_oracle_threads(int nthreads) { return resolve_threads(nthreads); }
+
+/* lambda^n with lambda^0 = 1 (also for lambda = 0). */
+static double lam_pow(double lam, long n) {
+    if (n == 0) return 1.0;
+    return pow(lam, (double)n);
+}
+
+/* ------------------------------------------------------------ arguments */
+typedef struct {
+    const double *q, *k, *v, *log_lambda, *h0, *do_, *dhT;
+    double scale;
+    long B, T, H, dk, dv, chunk;
+    double *o, *hT, *dq, *dk_out, *dv_out, *dh0;
+} args_t;
+
+#define QIDX(a, b, t, h, i) ((((b) * (a)->T + (t)) * (a)->H + (h)) * (a)->dk + (i))
+#define VIDX(a, b, t, h, j) ((((b) * (a)->T + (t)) * (a)->H + (h)) * (a)->dv + (j))
+#define SIDX(a, b, h) (((b) * (a)->H + (h)) * (a)->dk * (a)->dv)
+
+/* ------------------------------------------------- O2: recurrent forward */
+/* The recurrence as the "GLA mixer" paragraph states it, one token at a time:
+ *   S_t = lambda * S_{t-1} + k_t v_t^T,   o_t = scale * S_t^T q_t.         */
+static void fwd_recurrent_unit(void *ctx, long unit) {
+    const args_t *a = (const args_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv;
+    double lam = exp(a->log_lambda[h]);
+    double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    if (a->h0) memcpy(S, a->h0 + SIDX(a, b, h), sizeof(double) * (size_t)(dk * dv));
+    for (long t = 0; t < a->T; ++t) {
+        const double *kt = a->k + QIDX(a, b, t, h, 0);
+        const double *vt = a->v + VIDX(a, b, t, h, 0);
+        const double *qt = a->q + QIDX(a, b, t, h, 0);
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < dv; ++j)
+                S[i * dv + j] = lam * S[i * dv + j] + kt[i] * vt[j];
+        if (a->o) {
+            double *ot = a->o + VIDX(a, b, t, h, 0);
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += S[i * dv + j] * qt[i];
+                ot[j] = a->scale * acc;
+            }
+        }
+    }
+    if (a->hT) memcpy(a->hT + SIDX(a, b, h), S, sizeof(double) * (size_t)(dk * dv));
+    free(S);
+}
+
+int gla_oracle_fwd_recurrent(const double *q, const double *k, const double *v,
+                             const double *log_lambda, const double *h0, double scale,
+                             long B, long T, long H, long dk, long dv,
+                             double *o, double *hT, int nthreads) {
+    if (!q || !k || !v || !log_lambda || B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    args_t a; memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.log_lambda = log_lambda; a.h0 = h0; a.scale = scale;
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.o = o; a.hT = hT;
+    run_units(B * H, nthreads, fwd_recurrent_unit, &a);
+    return 0;
+}
+
+/* ---------------------------------------------- O1: brute-force quadratic */
+/* Unrolling the recurrence from S_0 = h0 (0-based t):
+ *   o_t = scale * ( lambda^(t+1) h0^T q_t + sum_{u<=t} lambda^(t-u) (q_t.k_u) v_u )
+ *   hT  = lambda^T h0 + sum_u lambda^(T-1-u) k_u v_u^T.
+ * O(T^2); for tiny inputs only.                                             */
+static void fwd_quadratic_unit(void *ctx, long unit) {
+    const args_t *a = (const args_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv;
+    double lam = exp(a->log_lambda[h]);
+    const double *H0 = a->h0 ? a->h0 + SIDX(a, b, h) : NULL;
+    for (long t = 0; t < a->T; ++t) {
+        const double *qt = a->q + QIDX(a, b, t, h, 0);
+        double *ot = a->o + VIDX(a, b, t, h, 0);
+        for (long j = 0; j < dv; ++j) ot[j] = 0.0;
+        if (H0) {
+            double w = lam_pow(lam, t + 1);
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += H0[i * dv + j] * qt[i];
+                ot[j] += w * acc;
+            }
+        }
+        for (long u = 0; u <= t; ++u) {
+            const double *ku = a->k + QIDX(a, b, u, h, 0);
+            const double *vu = a->v + VIDX(a, b, u, h, 0);
+            double qk = 0.0;
+            for (long i = 0; i < dk; ++i) qk += qt[i] * ku[i];
+            double w = lam_pow(lam, t - u) * qk;
+            for (long j = 0; j < dv; ++j) ot[j] += w * vu[j];
+        }
+        for (long j = 0; j < dv; ++j) ot[j] *= a->scale;
+    }
+    if (a->hT) {
+        double *S = a->hT + SIDX(a, b, h);
+        double w0 = lam_pow(lam, a->T);
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < dv; ++j) S[i * dv + j] = H0 ? w0 * H0[i * dv + j] : 0.0;
+        for (long u = 0; u < a->T; ++u) {
+            const double *ku = a->k + QIDX(a, b, u, h, 0);
+            const double *vu = a->v + VIDX(a, b, u, h, 0);
+            double w = lam_pow(lam, a->T - 1 - u);
+            for (long i = 0; i < dk; ++i)
+                for (long j = 0; j < dv; ++j) S[i * dv + j] += w * ku[i] * vu[j];
+        }
+    }
+}
+
+int gla_oracle_fwd_quadratic(const double *q, const double *k, const double *v,
+                             const double *log_lambda, const double *h0, double scale,
+                             long B, long T, long H, long dk, long dv,
+                             double *o, double *hT, int nthreads) {
+    if (!q || !k || !v || !log_lambda || !o || B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    args_t a; memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.log_lambda = log_lambda; a.h0 = h0; a.scale = scale;
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.o = o; a.hT = hT;
+    run_units(B * H, nthreads, fwd_quadratic_unit, &a);
+    return 0;
+}
+
+/* ------------------------------------------------ O5: chunked forward */
+/* The chunked form of "Challenge 1" with chunk length C (0-based position i
+ * inside a chunk of Cc valid tokens, S_prev the state entering the chunk):
+ *   o_i   = scale * ( lambda^(i+1) S_prev^T q_i
+ *                     + sum_{j<=i} lambda^(i-j) (q_i.k_j) v_j )   [intra-chunk output]
+ *   S_new = lambda^Cc S_prev + sum_{j<Cc} lambda^(Cc-1-j) k_j v_j^T [chunk state update]
+ * It is an exact regrouping of the recurrence; it serves to pin the chunk
+ * equations, not as the CUDA path's reference.                              */
+static void fwd_chunked_unit(void *ctx, long unit) {
+    const args_t *a = (const args_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv, C = a->chunk;
+    double lam = exp(a->log_lambda[h]);
+    double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    double *Sn = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    if (a->h0) memcpy(S, a->h0 + SIDX(a, b, h), sizeof(double) * (size_t)(dk * dv));
+    for (long c0 = 0; c0 < a->T; c0 += C) {
+        long Cc = a->T - c0 < C ? a->T - c0 : C;
+        for (long i = 0; i < Cc; ++i) {
+            const double *qi = a->q + QIDX(a, b, c0 + i, h, 0);
+            double *oi = a->o ? a->o + VIDX(a, b, c0 + i, h, 0) : NULL;
+            if (!oi) break;
+            double wi = lam_pow(lam, i + 1);
+            for (long jv = 0; jv < dv; ++jv) {
+                double acc = 0.0;
+                for (long r = 0; r < dk; ++r) acc += S[r * dv + jv] * qi[r];
+                oi[jv] = wi * acc;
+            }
+            for (long j = 0; j <= i; ++j) {
+                const double *kj = a->k + QIDX(a, b, c0 + j, h, 0);
+                const double *vj = a->v + VIDX(a, b, c0 + j, h, 0);
+                double qk = 0.0;
+                for (long r = 0; r < dk; ++r) qk += qi[r] * kj[r];
+                double w = lam_pow(lam, i - j) * qk;
+                for (long jv = 0; jv < dv; ++jv) oi[jv] += w * vj[jv];
+            }
+            for (long jv = 0; jv < dv; ++jv) oi[jv] *= a->scale;
+        }
+        double wC = lam_pow(lam, Cc);
+        for (long r = 0; r < dk * dv; ++r) Sn[r] = wC * S[r];
+        for (long j = 0; j < Cc; ++j) {
+            const double *kj = a->k + QIDX(a, b, c0 + j, h, 0);
+            const double *vj = a->v + VIDX(a, b, c0 + j, h, 0);
+            double w = lam_pow(lam, Cc - 1 - j);
+            for (long r = 0; r < dk; ++r)
+                for (long jv = 0; jv < dv; ++jv) Sn[r * dv + jv] += w * kj[r] * vj[jv];
+        }
+        double *tmp = S; S = Sn; Sn = tmp;
+    }
+    if (a->hT) memcpy(a->hT + SIDX(a, b, h), S, sizeof(double) * (size_t)(dk * dv));
+    free(S); free(Sn);
+}
+
+int gla_oracle_fwd_chunked(const double *q, const double *k, const double *v,
+                           const double *log_lambda, const double *h0, double scale,
+                           long B, long T, long H, long dk, long dv, long chunk,
+                           double *o, double *hT, int nthreads) {
+    if (!q || !k || !v || !log_lambda || chunk <= 0 || B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    args_t a; memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.log_lambda = log_lambda; a.h0 = h0; a.scale = scale;
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk; a.o = o; a.hT = hT;
+    run_units(B * H, nthreads, fwd_chunked_unit, &a);
+    return 0;
+}
+
+/* ---------------------------------------------------- O3: backward */
+/* Loss L = sum_t <do_t, o_t> + <dhT, hT>. With G_t = dL/dS_t (all paths):
+ *   forward pass :  dq_t = scale * S_t do_t
+ *   reverse pass :  G_{T-1} = dhT + scale q_{T-1} do_{T-1}^T,
+ *                   G_{t-1} = lambda G_t + scale q_{t-1} do_{t-1}^T,
+ *                   dk_t = G_t v_t,  dv_t = G_t^T k_t,  dh0 = lambda G_0.
+ * Two passes over the sequence; nothing is stored between them.            */
+static void bwd_unit(void *ctx, long unit) {
+    const args_t *a = (const args_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv;
+    double lam = exp(a->log_lambda[h]);
+    double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    /* forward pass: dq */
+    if (a->h0) memcpy(S, a->h0 + SIDX(a, b, h), sizeof(double) * (size_t)(dk * dv));
+    for (long t = 0; t < a->T; ++t) {
+        const double *kt = a->k + QIDX(a, b, t, h, 0);
+        const double *vt = a->v + VIDX(a, b, t, h, 0);
+        const double *dot = a->do_ + VIDX(a, b, t, h, 0);
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < dv; ++j)
+                S[i * dv + j] = lam * S[i * dv + j] + kt[i] * vt[j];
+        if (a->dq) {
+            double *dqt = a->dq + QIDX(a, b, t, h, 0);
+            for (long i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (long j = 0; j < dv; ++j) acc += S[i * dv + j] * dot[j];
+                dqt[i] = a->scale * acc;
+            }
+        }
+    }
+    /* reverse pass: dk, dv, dh0 (S is reused as G) */
+    if (a->dhT) memcpy(S, a->dhT + SIDX(a, b, h), sizeof(double) * (size_t)(dk * dv));
+    else memset(S, 0, sizeof(double) * (size_t)(dk * dv));
+    for (long t = a->T - 1; t >= 0; --t) {
+        const double *qt = a->q + QIDX(a, b, t, h, 0);
+        const double *kt = a->k + QIDX(a, b, t, h, 0);
+        const double *vt = a->v + VIDX(a, b, t, h, 0);
+        const double *dot = a->do_ + VIDX(a, b, t, h, 0);
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < dv; ++j) S[i * dv + j] += a->scale * qt[i] * dot[j];
+        if (a->dk_out) {
+            double *dkt = a->dk_out + QIDX(a, b, t, h, 0);
+            for (long i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (long j = 0; j < dv; ++j) acc += S[i * dv + j] * vt[j];
+                dkt[i] = acc;
+            }
+        }
+        if (a->dv_out) {
+            double *dvt = a->dv_out + VIDX(a, b, t, h, 0);
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += S[i * dv + j] * kt[i];
+                dvt[j] = acc;
+            }
+        }
+        for (long r = 0; r < dk * dv; ++r) S[r] *= lam;
+    }
+    if (a->dh0) memcpy(a->dh0 + SIDX(a, b, h), S, sizeof(double) * (size_t)(dk * dv));
+    free(S);
+}
+
+int gla_oracle_bwd(const double *q, const double *k, const double *v,
+                   const double *log_lambda, const double *h0, double scale,
+                   const double *do_, const double *dhT,
+                   long B, long T, long H, long dk, long dv,
+                   double *dq, double *dk_out, double *dv_out, double *dh0, int nthreads) {
+    if (!q || !k || !v || !log_lambda || !do_ || B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    args_t a; memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.log_lambda = log_lambda; a.h0 = h0; a.scale = scale;
+    a.do_ = do_; a.dhT = dhT;
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv;
+    a.dq = dq; a.dk_out = dk_out; a.dv_out = dv_out; a.dh0 = dh0;
+    run_units(B * H, nthreads, bwd_unit, &a);
+    return 0;
+}
+
+/* ---------------------------------------------- O6: chunked backward */
+/* The backward of the chunked form, chunk by chunk (G the gradient of the
+ * state leaving the chunk; S_prev the state entering it):
+ *   dq_i = scale*( lambda^(i+1) S_prev do_i + sum_{j<=i} lambda^(i-j) (do_i.v_j) k_j )
+ *   dk_j = scale*sum_{i>=j} lambda^(i-j) (do_i.v_j) q_i + lambda^(Cc-1-j) G v_j
+ *   dv_j = scale*sum_{i>=j} lambda^(i-j) (q_i.k_j) do_i + lambda^(Cc-1-j) G^T k_j
+ *   G   <- lambda^Cc G + scale * sum_i lambda^(i+1) q_i do_i^T   (to the previous chunk)
+ *   dh0  = G after the first chunk.
+ * Pins the chunk-level backward equations against O3.                        */
+static void bwd_chunked_unit(void *ctx, long unit) {
+    const args_t *a = (const args_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv, C = a->chunk, T = a->T;
+    double lam = exp(a->log_lambda[h]);
+    long nck = (T + C - 1) / C;
+    double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    double *Sn = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    /* chunk order: dq with the state entering each chunk */
+    if (a->h0) memcpy(S, a->h0 + SIDX(a, b, h), sizeof(double) * (size_t)(dk * dv));
+    for (long c = 0; c < nck; ++c) {
+        long c0 = c * C, Cc = T - c0 < C ? T - c0 : C;
+        for (long i = 0; i < Cc && a->dq; ++i) {
+            const double *doi = a->do_ + VIDX(a, b, c0 + i, h, 0);
+            double *dqi = a->dq + QIDX(a, b, c0 + i, h, 0);
+            double wi = lam_pow(lam, i + 1);
+            for (long r = 0; r < dk; ++r) {
+                double acc = 0.0;
+                for (long jv = 0; jv < dv; ++jv) acc += S[r * dv + jv] * doi[jv];
+                dqi[r] = wi * acc;
+            }
+            for (long j = 0; j <= i; ++j) {
+                const double *vj = a->v + VIDX(a, b, c0 + j, h, 0);
+                const double *kj = a->k + QIDX(a, b, c0 + j, h, 0);
+                double dv_ = 0.0;
+                for (long jv = 0; jv < dv; ++jv) dv_ += doi[jv] * vj[jv];
+                double w = lam_pow(lam, i - j) * dv_;
+                for (long r = 0; r < dk; ++r) dqi[r] += w * kj[r];
+            }
+            for (long r = 0; r < dk; ++r) dqi[r] *= a->scale;
+        }
+        double wC = lam_pow(lam, Cc);
+        for (long r = 0; r < dk * dv; ++r) Sn[r] = wC * S[r];
+        for (long j = 0; j < Cc; ++j) {
+            const double *kj = a->k + QIDX(a, b, c0 + j, h, 0);
+            const double *vj = a->v + VIDX(a, b, c0 + j, h, 0);
+            double w = lam_pow(lam, Cc - 1 - j);
+            for (long r = 0; r < dk; ++r)
+                for (long jv = 0; jv < dv; ++jv) Sn[r * dv + jv] += w * kj[r] * vj[jv];
+        }
+        double *tmp = S; S = Sn; Sn = tmp;
+    }
+    /* reverse chunk order: dk, dv and the state gradient G */
+    if (a->dhT) memcpy(S, a->dhT + SIDX(a, b, h), sizeof(double) * (size_t)(dk * dv));
+    else memset(S, 0, sizeof(double) * (size_t)(dk * dv));
+    for (long c = nck - 1; c >= 0; --c) {
+        long c0 = c * C, Cc = T - c0 < C ? T - c0 : C;
+        for (long j = 0; j < Cc; ++j) {
+            const double *kj = a->k + QIDX(a, b, c0 + j, h, 0);
+            const double *vj = a->v + VIDX(a, b, c0 + j, h, 0);
+            double wj = lam_pow(lam, Cc - 1 - j);
+            if (a->dk_out) {
+                double *dkj = a->dk_out + QIDX(a, b, c0 + j, h, 0);
+                for (long r = 0; r < dk; ++r) {
+                    double acc = 0.0;
+                    for (long jv = 0; jv < dv; ++jv) acc += S[r * dv + jv] * vj[jv];
+                    dkj[r] = wj * acc;
+                }
+                for (long i = j; i < Cc; ++i) {
+                    const double *doi = a->do_ + VIDX(a, b, c0 + i, h, 0);
+                    const double *qi = a->q + QIDX(a, b, c0 + i, h, 0);
+                    double dv_ = 0.0;
+                    for (long jv = 0; jv < dv; ++jv) dv_ += doi[jv] * vj[jv];
+                    double w = a->scale * lam_pow(lam, i - j) * dv_;
+                    for (long r = 0; r < dk; ++r) dkj[r] += w * qi[r];
+                }
+            }
+            if (a->dv_out) {
+                double *dvj = a->dv_out + VIDX(a, b, c0 + j, h, 0);
+                for (long jv = 0; jv < dv; ++jv) {
+                    double acc = 0.0;
+                    for (long r = 0; r < dk; ++r) acc += S[r * dv + jv] * kj[r];
+                    dvj[jv] = wj * acc;
+                }
+                for (long i = j; i < Cc; ++i) {
+                    const double *doi = a->do_ + VIDX(a, b, c0 + i, h, 0);
+                    const double *qi = a->q + QIDX(a, b, c0 + i, h, 0);
+                    double qk = 0.0;
+                    for (long r = 0; r < dk; ++r) qk += qi[r] * kj[r];
+                    double w = a->scale * lam_pow(lam, i - j) * qk;
+                    for (long jv = 0; jv < dv; ++jv) dvj[jv] += w * doi[jv];
+                }
+            }
+        }
+        double wC = lam_pow(lam, Cc);
+        for (long r = 0; r < dk * dv; ++r) Sn[r] = wC * S[r];
+        for (long i = 0; i < Cc; ++i) {
+            const double *qi = a->q + QIDX(a, b, c0 + i, h, 0);
+            const double *doi = a->do_ + VIDX(a, b, c0 + i, h, 0);
+            double w = a->scale * lam_pow(lam, i + 1);
+            for (long r = 0; r < dk; ++r)
+                for (long jv = 0; jv < dv; ++jv) Sn[r * dv + jv] += w * qi[r] * doi[jv];
+        }
+        double *tmp = S; S = Sn; Sn = tmp;
+    }
+    if (a->dh0) memcpy(a->dh0 + SIDX(a, b, h), S, sizeof(double) * (size_t)(dk * dv));
+    free(S); free(Sn);
+}
+
+int gla_oracle_bwd_chunked(const double *q, const double *k, const double *v,
+                           const double *log_lambda, const double *h0, double scale,
+                           const double *do_, const double *dhT,
+                           long B, long T, long H, long dk, long dv, long chunk,
+                           double *dq, double *dk_out, double *dv_out, double *dh0, int nthreads) {
+    if (!q || !k || !v || !log_lambda || !do_ || chunk <= 0 || B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    args_t a; memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.log_lambda = log_lambda; a.h0 = h0; a.scale = scale;
+    a.do_ = do_; a.dhT = dhT; a.chunk = chunk;
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv;
+    a.dq = dq; a.dk_out = dk_out; a.dv_out = dv_out; a.dh0 = dh0;
+    run_units(B * H, nthreads, bwd_chunked_unit, &a);
+    return 0;
+}
+
+/* ------------------------------------------------------- O4: decode */
+/* One recurrent step per (n, h), as served ("Inference optimization on
+ * Trainium2": one fixed state page per sequence, O(1) work per token):
+ *   S <- lambda S + k v^T (in place),  o = scale * S^T q (after the update). */
+typedef struct {
+    const double *q, *k, *v, *log_lambda;
+    double *S, *o;
+    double scale;
+    long N, H, dk, dv;
+} dec_t;
+
+static void decode_unit(void *ctx, long unit) {
+    const dec_t *a = (const dec_t *)ctx;
+    long h = unit % a->H, dk = a->dk, dv = a->dv;
+    double lam = exp(a->log_lambda[h]);
+    const double *q = a->q + unit * dk, *k = a->k + unit * dk, *v = a->v + unit * dv;
+    double *S = a->S + unit * dk * dv, *o = a->o + unit * dv;
+    for (long i = 0; i < dk; ++i)
+        for (long j = 0; j < dv; ++j) S[i * dv + j] = lam * S[i * dv + j] + k[i] * v[j];
+    for (long j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (long i = 0; i < dk; ++i) acc += S[i * dv + j] * q[i];
+        o[j] = a->scale * acc;
+    }
+}
+
+int gla_oracle_decode(const double *q, const double *k, const double *v,
+                      const double *log_lambda, double *S, double scale,
+                      long N, long H, long dk, long dv, double *o, int nthreads) {
+    if (!q || !k || !v || !log_lambda || !S || !o || N < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    dec_t a;
+    a.q = q; a.k = k; a.v = v; a.log_lambda = log_lambda; a.S = S; a.o = o; a.scale = scale;
+    a.N = N; a.H = H; a.dk = dk; a.dv = dv;
+    run_units(N * H, nthreads, decode_unit, &a);
+    return 0;
+}
