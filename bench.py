@@ -1,0 +1,620 @@
+#!/usr/bin/env python3
+"""Benchmark of libgla, the Simple GLA mixer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
+                    [--mode all|fwd|fwd_bwd|decode] [--batch B] [--no-e2e] [--no-cpu-baseline]
+
+Prints ONE JSON line (rank 0). The headline `value` is the chunked forward
+over the Laplace-layer workload (bf16, B=8, H=16, T=2048, dk=96, dv=192,
+C=128: tokens/s = B*T per call over all heads). `modes` carries the same
+measurement for the training forward+backward workload (B=16, tokens/s)
+and for the serving decode workload (1,280 sequences x 16 heads x 24
+distinct layer states per step, seq-steps/s), each with its own roofline.
+
+Timing: W untimed warm-up steps, then exactly K steps between two
+barrier + synchronize pairs, on the device with CUDA events recorded on the
+stream the kernels run on; the max over ranks is taken. Every workload's
+inputs exceed the 129 MB L2, so no flush is done between steps.
+`--impl reference` times the double-precision CPU oracle instead (rank 0
+only), on bounded samples of the same workloads.
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload on its
+own GPU (independent batches, no collective on the data path); `value` is
+the total over ranks divided by the slowest rank's time (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gla_gen as gen  # noqa: E402
+
+METRIC = "Simple-GLA tokens/s (fwd, fwd+bwd), decode seq-steps/s; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+DK, DV, H = 96, 192, 16
+STATE_BYTES = DK * DV * 4
+CHUNK = 128
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------------- peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def committed_traffic(kernel: str):
+    """Per-launch DRAM traffic of `kernel` from its committed ncu summary, if
+    the summary's recorded source hash still matches the kernel source."""
+    import hashlib
+    prof = os.path.join(ROOT, "profiles", f"{kernel}.md")
+    if not os.path.exists(prof):
+        return None, None
+    fields = {}
+    for line in open(prof):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    src = fields.get("source_file")
+    if not src or "traffic_bytes_per_launch" not in fields:
+        return None, None
+    try:
+        digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None, None
+    if digest != fields.get("source_sha256_16"):
+        return None, fields.get("workload")
+    try:
+        return float(fields["traffic_bytes_per_launch"]), fields.get("workload")
+    except ValueError:
+        return None, None
+
+
+# ------------------------------------------------------------ algorithmic work
+def fwd_work(B, T, with_h0, with_hT, C=CHUNK):
+    """Bytes and tensor-core FLOPs of one gla_chunk_fwd call (bf16 q,k,v,o)."""
+    ht = B * H * T
+    bytes_ = ht * (2 * DK * 2 + 2 * DV * 2) + B * H * STATE_BYTES * (int(with_h0) + int(with_hT))
+    flops_full = ht * (2 * C * DK + 2 * C * DV + 4 * DK * DV)
+    flops_causal = ht * ((C + 1) * DK + (C + 1) * DV + 4 * DK * DV)
+    return bytes_, flops_full, flops_causal
+
+
+def bwd_work(B, T, with_h0, with_dhT, with_dh0, C=CHUNK):
+    ht = B * H * T
+    bytes_ = ht * (4 * DK * 2 + 3 * DV * 2 + DV * 2) + \
+        B * H * STATE_BYTES * (int(with_h0) + int(with_dhT) + int(with_dh0))
+    # dq chain: dO V^T (C*DV), dP K (C*DK), dO S^T (DK*DV), state K^T V (DK*DV)  [x2 per MAC]
+    # dk/dv chain: QK^T, dO V^T, dP^T Q, P^T dO, V G^T, K G, Q^T dO
+    macs = (C * DV + C * DK + 2 * DK * DV) + (C * DK + C * DV + C * DK + C * DV + 3 * DK * DV)
+    return bytes_, 2 * ht * macs
+
+
+def decode_work(N):
+    per = 2 * STATE_BYTES + 2 * DK * 2 + 2 * DV * 2
+    return N * H * per, N * H * 4 * DK * DV
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; summarised over a
+    time window (the timed region)."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if bus_id:
+            cmd.insert(1, f"--id={bus_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for (t, p) in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not win:
+            # a timed region shorter than the sampling period: nearest samples
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            win = [p for (_, p) in near]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(win[0][1]), "power_w_max": max((num(p[2]) or 0) for p in win),
+                "samples": len(win), "reasons": reasons}
+
+
+# -------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------ our kernels
+def dev_tensor(x, dtype_str, device):
+    import torch
+    if dtype_str == "bf16":
+        return torch.from_numpy(gen.bf16_bits(x).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device)
+
+
+def time_steps(step_fns, K, W, dist, stream):
+    """Run W warm-up steps, then K timed steps. Returns (total_ms, per-step ms
+    list, wall window, launches in timed region)."""
+    import torch
+    from linear_attention_chunk_gb300 import gla_check
+    for _ in range(W):
+        step_fns()
+    gla_check()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    launches = 0
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            starts[i].record(stream)
+            launches += step_fns()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    dist.barrier()
+    gla_check()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total = starts[0].elapsed_time(ends[-1])
+    return total, per, (t0, t1), launches
+
+
+def bench_fwd(args, dist, device, stream, peaks, sampler):
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    B = args.batch or 8
+    T = 2048
+    c = gen.layer_fwd(seed=1, B=B, T=T)
+    q, k, v = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v))
+    ll = torch.from_numpy(c.log_lambda).to(device)
+    o = torch.empty((B, T, H, DV), dtype=torch.bfloat16, device=device)
+    hT = torch.empty((B, H, DK, DV), dtype=torch.float32, device=device)
+    ws_n = gla.gla_chunk_fwd_workspace_size(B, T, H, DK, DV, CHUNK)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
+
+    def step():
+        gla.gla_chunk_fwd(q, k, v, ll, None, c.scale, CHUNK, o=o, hT=hT, workspace=ws, stream=stream)
+        return gla.gla_last_launch_count()
+
+    total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    tokens = B * T * dist.world
+    bytes_, fl_full, fl_causal = fwd_work(B, T, False, True)
+    avg_ms = statistics.mean(per)
+    ach_gbs = bytes_ / (avg_ms * 1e-3) / 1e9
+    ach_tf = fl_full / (avg_ms * 1e-3) / 1e12
+    traffic, traffic_wl = committed_traffic("gla_fwd_tc")
+    res = {
+        "value": tokens * args.steps / (total * 1e-3), "unit": "tokens/s", "ms_per_step": total / args.steps,
+        "config": {"workload": c.name, "B": B, "T": T, "H": H, "dk": DK, "dv": DV, "chunk": CHUNK,
+                   "h0": "none", "hT": "written", "l2": f"inputs larger than L2 ({bytes_ / 1e6:.0f} MB per step), no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach_gbs / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": bytes_, "avg_launch_ms": avg_ms,
+                     "peak_source": peaks["source"]},
+        "tensor": {"achieved": ach_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                   "frac": ach_tf / peaks["bf16_tflops"], "flops_per_launch": fl_full,
+                   "causal_flops_per_launch": fl_causal, "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    if not args.no_e2e:
+        res["e2e"] = e2e_fwd(args, dist, device, stream, c, ll)
+    del q, k, v, o, hT
+    return res
+
+
+def e2e_fwd(args, dist, device, stream, c, ll):
+    """Same metric through the public API with host buffers: every step
+    copies q, k, v from pinned host memory, runs the forward, and reads o and
+    hT back to pinned host memory."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    B, T = c.B, c.T
+    pin = lambda x: torch.from_numpy(gen.bf16_bits(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+    qh, kh, vh = pin(c.q), pin(c.k), pin(c.v)
+    oh = torch.empty((B, T, H, DV), dtype=torch.bfloat16).pin_memory()
+    hh = torch.empty((B, H, DK, DV), dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.empty_like(x, device=device) for x in (qh, kh, vh))
+    od = torch.empty((B, T, H, DV), dtype=torch.bfloat16, device=device)
+    hd = torch.empty((B, H, DK, DV), dtype=torch.float32, device=device)
+
+    def step():
+        with torch.cuda.stream(stream):
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            gla.gla_chunk_fwd(qd, kd, vd, ll, None, c.scale, CHUNK, o=od, hT=hd, stream=stream)
+            n = gla.gla_last_launch_count()
+            oh.copy_(od, non_blocking=True)
+            hh.copy_(hd, non_blocking=True)
+        return n
+
+    total, _, _, _ = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    bi = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
+    bo = oh.numel() * oh.element_size() + hh.numel() * hh.element_size()
+    return {"value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def bench_fwd_bwd(args, dist, device, stream, peaks, sampler):
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    B, T = 16, 2048
+    c = gen.train_fwd_bwd(seed=2, B=B, T=T)
+    q, k, v, do = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v, c.do))
+    ll = torch.from_numpy(c.log_lambda).to(device)
+    h0 = torch.from_numpy(c.h0).to(device)
+    o = torch.empty((B, T, H, DV), dtype=torch.bfloat16, device=device)
+    hT = torch.empty((B, H, DK, DV), dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dh0 = torch.empty_like(h0)
+    wsf = torch.empty(max(gla.gla_chunk_fwd_workspace_size(B, T, H, DK, DV, CHUNK), 16), dtype=torch.uint8, device=device)
+    wsb = torch.empty(max(gla.gla_chunk_bwd_workspace_size(B, T, H, DK, DV, CHUNK), 16), dtype=torch.uint8, device=device)
+    t_f, t_b = [], []
+
+    def step():
+        gla.gla_chunk_fwd(q, k, v, ll, h0, c.scale, CHUNK, o=o, hT=hT, workspace=wsf, stream=stream)
+        n = gla.gla_last_launch_count()
+        gla.gla_chunk_bwd(q, k, v, ll, do, h0, None, c.scale, CHUNK, dq=dq, dk=dk, dv=dv, dh0=dh0,
+                          workspace=wsb, stream=stream)
+        return n + gla.gla_last_launch_count()
+
+    total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    fb, ff, _ = fwd_work(B, T, True, True)
+    bb, bf = bwd_work(B, T, True, False, True)
+    avg_ms = statistics.mean(per)
+    ach = (fb + bb) / (avg_ms * 1e-3) / 1e9
+    ach_tf = (ff + bf) / (avg_ms * 1e-3) / 1e12
+    res = {
+        "value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+        "ms_per_step": total / args.steps,
+        "config": {"workload": c.name, "B": B, "T": T, "H": H, "chunk": CHUNK, "h0": "N(0,0.02)", "dhT": "none",
+                   "l2": f"inputs larger than L2 ({(fb + bb) / 1e6:.0f} MB per step), no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes_per_step": fb + bb, "avg_step_ms": avg_ms, "peak_source": peaks["source"]},
+        "tensor": {"achieved": ach_tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                   "frac": ach_tf / peaks["bf16_tflops_sustained"], "flops_per_step": ff + bf},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    return res
+
+
+def bench_decode(args, dist, device, stream, peaks, sampler):
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    N, L = 1280, 24
+    g = torch.Generator(device=device)
+    g.manual_seed(3)
+    states = []
+    for _ in range(L):
+        S = torch.randn((N, H, DK, DV), generator=g, device=device, dtype=torch.float32)
+        S.mul_(0.1)
+        states.append(S)
+    toks = []
+    for layer in range(L):
+        dc = gen.decode_tokens(N, H, DK, DV, seed=3 + 1000 * layer)
+        toks.append(tuple(dev_tensor(x, "bf16", device) for x in (dc["q"], dc["k"], dc["v"])))
+    ll = torch.from_numpy(gen.log_lambda_of(gen.decay_layer_schedule(H))).to(device)
+    outs = [torch.empty((N, H, DV), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    scale = 1.0 / math.sqrt(DK)
+    per_layer = []
+
+    def step():
+        n = 0
+        for layer in range(L):
+            q, k, v = toks[layer]
+            gla.gla_decode_step(q, k, v, ll, states[layer], scale, o=outs[layer], stream=stream)
+            n += gla.gla_last_launch_count()
+        return n
+
+    total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    bytes_, flops = decode_work(N)
+    avg_launch_ms = statistics.mean(per) / L
+    ach = bytes_ / (avg_launch_ms * 1e-3) / 1e9
+    res = {
+        "value": N * dist.world * args.steps / (total * 1e-3), "unit": "seq-steps/s",
+        "ms_per_step": total / args.steps, "ms_per_layer_step": total / args.steps / L,
+        "config": {"workload": f"serving_decode_bf16_N{N}_H16_L{L}", "N": N, "H": H, "layers": L,
+                   "state": "fp32 N(0,0.1), 24 distinct buffers, 36.2 GB",
+                   "l2": "24 distinct 1.5 GB states per step, larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": committed_traffic("gla_decode")[0],
+                     "algorithmic_bytes_per_launch": bytes_, "avg_launch_ms": avg_launch_ms,
+                     "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    if not args.no_e2e:
+        res["e2e"] = e2e_decode(args, dist, device, stream, toks, states, ll, scale, N, L)
+    del states
+    return res
+
+
+def e2e_decode(args, dist, device, stream, toks, states, ll, scale, N, L):
+    """Decode through the public API with host token buffers: per step the 24
+    layers' q, k, v come from pinned host memory and the 24 outputs go back;
+    the recurrent states stay resident on the device (the serving page)."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    host_in = [tuple(x.cpu().pin_memory() for x in t) for t in toks]
+    dev_in = [tuple(torch.empty_like(x) for x in t) for t in toks]
+    host_out = [torch.empty((N, H, DV), dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    dev_out = [torch.empty((N, H, DV), dtype=torch.bfloat16, device=device) for _ in range(L)]
+
+    def step():
+        n = 0
+        with torch.cuda.stream(stream):
+            for layer in range(L):
+                for d, h in zip(dev_in[layer], host_in[layer]):
+                    d.copy_(h, non_blocking=True)
+                q, k, v = dev_in[layer]
+                gla.gla_decode_step(q, k, v, ll, states[layer], scale, o=dev_out[layer], stream=stream)
+                n += gla.gla_last_launch_count()
+                host_out[layer].copy_(dev_out[layer], non_blocking=True)
+        return n
+
+    total, _, _, _ = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    bi = sum(x.numel() * x.element_size() for t in host_in for x in t)
+    bo = sum(x.numel() * x.element_size() for x in host_out)
+    return {"value": N * dist.world * args.steps / (total * 1e-3), "unit": "seq-steps/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+# ------------------------------------------------------------- CPU oracle
+def oracle_fwd_sample(units, seed=1):
+    """The oracle's recurrent forward over `units` (b, h) chains of the
+    layer-forward workload (T=2048). Returns (seconds, tokens-equivalent, threads)."""
+    import oracle
+    B = max(1, math.ceil(units / H))
+    c = gen.layer_fwd(seed=seed, B=B, T=2048)
+    hs = min(units, H)
+    q, k, v = c.q[:, :, :hs], c.k[:, :, :hs], c.v[:, :, :hs]
+    ll = c.log_lambda[:hs]
+    nthreads = oracle.threads(0)
+    t0 = time.perf_counter()
+    oracle.fwd_recurrent(q, k, v, ll, None, c.scale, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    head_tokens = B * hs * 2048
+    return dt, head_tokens / H, nthreads, f"{B}x{hs} (b,h) chains of T=2048 (of 8x16)"
+
+
+def oracle_bwd_sample(units, seed=2):
+    import oracle
+    B = max(1, math.ceil(units / H))
+    c = gen.train_fwd_bwd(seed=seed, B=B, T=2048)
+    hs = min(units, H)
+    sl = lambda x: x[:, :, :hs]
+    nthreads = oracle.threads(0)
+    t0 = time.perf_counter()
+    oracle.fwd_recurrent(sl(c.q), sl(c.k), sl(c.v), c.log_lambda[:hs], c.h0[:, :hs], c.scale, nthreads=nthreads)
+    oracle.bwd(sl(c.q), sl(c.k), sl(c.v), c.log_lambda[:hs], c.h0[:, :hs], c.scale, sl(c.do), None,
+               nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, B * hs * 2048 / H, nthreads, f"{B}x{hs} (b,h) chains of T=2048 fwd+bwd (of 16x16)"
+
+
+def oracle_decode_sample(layers=1, N=640):
+    import oracle
+    nthreads = oracle.threads(0)
+    dt = 0.0
+    for layer in range(layers):
+        dc = gen.decode_tokens(N, H, DK, DV, seed=3 + 1000 * layer)
+        rng = np.random.default_rng(10_000 + layer)
+        S = (rng.standard_normal((N, H, DK, DV), dtype=np.float32) * np.float32(0.1))
+        t0 = time.perf_counter()
+        oracle.decode(dc["q"], dc["k"], dc["v"], gen.log_lambda_of(gen.decay_layer_schedule(H)), S,
+                      1.0 / math.sqrt(DK), nthreads=nthreads)
+        dt += time.perf_counter() - t0
+    # seq-steps: one token of one sequence through all 24 layers
+    return dt, N * layers / 24.0, nthreads, f"{layers} of 24 layer-steps over N={N} (of 1,280) x 16 heads"
+
+
+def cpu_baseline():
+    dt, toks, nt, sample = oracle_fwd_sample(64)
+    base = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle", "sample": sample,
+            "seconds": dt}
+    modes = {}
+    dt, toks, nt, sample = oracle_bwd_sample(32)
+    modes["fwd_bwd"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                        "sample": sample, "seconds": dt}
+    dt, ss, nt, sample = oracle_decode_sample(1)
+    modes["decode"] = {"value": ss / dt, "unit": "seq-steps/s", "cores": nt, "kind": "oracle",
+                       "sample": sample, "seconds": dt}
+    return base, modes
+
+
+def run_reference(args, dist):
+    """The reference arm: the double-precision oracle on the host cores."""
+    if dist.rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_fwd_sample(16)
+    total, toks = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, tk, nt, sample = oracle_fwd_sample(16)
+        total += dt
+        toks += tk
+    value = toks / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "layer_fwd_bf16_B8_H16_T2048_C128", "B": 8, "T": 2048, "H": H, "dk": DK,
+                   "dv": DV, "chunk": CHUNK, "parallelism": "host threads over (b, h)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                         "sample": f"per step: {sample}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- main
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("gla", "reference"), default="gla")
+    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode"), default="all")
+    ap.add_argument("--batch", type=int, default=0, help="override the forward workload's B (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 0)
+
+    dist = Dist()
+    if args.impl == "reference":
+        return run_reference(args, dist)
+
+    import torch
+    from linear_attention_chunk_gb300.build import build
+    if dist.rank == 0 or not os.path.exists(os.path.join(ROOT, "linear_attention_chunk_gb300", "_lib", "libgla.so")):
+        build()
+    torch.cuda.set_device(dist.local_rank)
+    dist.init("nccl")
+    device = torch.device("cuda", dist.local_rank)
+    stream = torch.cuda.Stream(device=device)
+    peaks = load_peaks()
+    bus = None
+    try:
+        props = torch.cuda.get_device_properties(device)
+        bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus)
+    results = {}
+    try:
+        if args.mode in ("all", "fwd"):
+            results["fwd"] = bench_fwd(args, dist, device, stream, peaks, sampler)
+        if args.mode in ("all", "fwd_bwd"):
+            results["fwd_bwd"] = bench_fwd_bwd(args, dist, device, stream, peaks, sampler)
+        if args.mode in ("all", "decode"):
+            results["decode"] = bench_decode(args, dist, device, stream, peaks, sampler)
+    finally:
+        sampler.stop()
+
+    head_key = "fwd" if "fwd" in results else next(iter(results))
+    head = results[head_key]
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the Laplace 3B mixer)",
+        "config": dict(head["config"], parallelism=f"replicas x{dist.world} (independent batches)"),
+        "roofline": head["roofline"],
+        "tensor": head.get("tensor"),
+        "e2e": head.get("e2e"),
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "modes": {k: v for k, v in results.items() if k != head_key},
+        "peaks": peaks,
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        base, base_modes = cpu_baseline()
+        line["cpu_baseline"] = base
+        for k, v in base_modes.items():
+            if k in line["modes"]:
+                line["modes"][k]["cpu_baseline"] = v
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

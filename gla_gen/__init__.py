@@ -251,3 +251,13 @@ def serving_decode(seed: int = 3, N: int = 1280, layer: int = 0) -> DecodeCase:
     state S ~ N(0, 0.1) fp32; each layer of the 24 draws from seed + 1000*layer."""
     return make_decode_case(N, LAYER_H, LAYER_DK, LAYER_DV, seed=seed + 1000 * layer,
                             dtype=BF16, name=f"serving_decode_bf16_N{N}_H16_layer{layer}")
+
+
+def decode_tokens(N: int, H: int, dk: int, dv: int, *, seed: int, dtype: str = BF16) -> dict:
+    """Only the per-token q, k, v of a decode step (same draw order and
+    distribution as make_decode_case, without drawing the state)."""
+    rng = np.random.default_rng(seed)
+    q = _store(_normal(rng, (N, H, dk)), dtype)
+    k = _store(_normal(rng, (N, H, dk)), dtype)
+    v = _store(_normal(rng, (N, H, dv)), dtype)
+    return {"q": q, "k": k, "v": v}

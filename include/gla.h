@@ -1,0 +1,165 @@
+/*
+ * gla.h -- C ABI of libgla, the Simple Gated Linear Attention (Simple GLA)
+ * mixer for NVIDIA GB300 (sm_103a).
+ *
+ * Source of the operation: "Beyond the KV cache: Training and serving i14's
+ * Laplace 3B linear attention model on AWS Trainium2 with native PyTorch".
+ *   - Section "i14 and the Laplace 3B architecture", paragraph "GLA mixer"
+ *     ("GLA recurrent-state update equation", "GLA state-readout equation"):
+ *     each head h keeps a dk x dv matrix state (96 x 192 in the model),
+ *     decayed by a fixed per-head factor lambda_h and written by the rank-1
+ *     outer product k_t v_t^T; the query reads the state out.
+ *   - Section "Engineering challenges", "Challenge 1" ("Chunked GLA
+ *     intra-chunk output", "Chunked GLA state update", Figure 3): the
+ *     chunked form -- masked linear attention inside a chunk plus the
+ *     running state, the state advanced by lambda^C; only the state chain
+ *     is serial.
+ *   - "Challenge 3: Backward-pass unrolling for a sequential recurrence":
+ *     the backward passes through every serial state update.
+ *   - "Inference optimization on Trainium2": one fixed state page per
+ *     sequence, constant work per generated token.
+ *
+ * What is computed (0-based token t, per batch row b and head h, with
+ * lambda = exp(log_lambda[h]) and lambda^0 = 1 even for lambda = 0):
+ *     S_{-1} = h0  (zero when h0 is NULL)
+ *     S_t    = lambda * S_{t-1} + k_t v_t^T          (dk x dv, fp32)
+ *     o_t    = scale * S_t^T q_t                     (readout after the update)
+ *     hT     = S_{T-1}                               (unscaled)
+ * The scale multiplies the readout only.
+ *
+ * Layouts (row-major, contiguous, token-major as a fused per-token QKV
+ * projection emits them):
+ *     q, k, do, dq, dk   [B, T, H, dk]
+ *     v, o, dv           [B, T, H, dv]
+ *     h0, hT, dhT, dh0   [B, H, dk, dv]  fp32, dv fastest
+ *     decode q, k        [N, H, dk];  v, o [N, H, dv];  S_inout [N, H, dk, dv] fp32
+ *     log_lambda         [H] fp32, natural log of the decay (<= 0, -inf allowed)
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers (cudaMalloc'd or equivalent), owned by the
+ *     caller; the library never frees or retains them. They must be 16-byte
+ *     aligned. Input and output buffers must not alias, except that decode
+ *     updates S_inout in place.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL means the legacy default stream). Argument errors are detected on
+ *     the host and returned before anything is launched.
+ *   - The library allocates no device memory. Scratch, when a path needs
+ *     it, is the caller's `workspace`.
+ *   - `dtype` selects the element type of q, k, v, o, do, dq, dk, dv
+ *     (GLA_BF16: bf16 bit patterns; GLA_FP32: float). States are fp32 in
+ *     both modes. GLA_BF16 requires dk = 96, dv = 192 (the tensor-core path);
+ *     GLA_FP32 is the validation mode and accepts 1 <= dk <= 128, 1 <= dv <= 256.
+ *   - `chunk` is the chunk length C, 64 or 128. T need not be a multiple of
+ *     C: the last chunk is ragged. Results do not depend on C beyond rounding.
+ *   - B, H, N may be 0 (nothing is launched); T may be 0 for the forward
+ *     (then hT = h0, or zero).
+ *   - Device-side failures (a wait that timed out) are recorded in a device
+ *     status word; gla_check() synchronises the stream and reports them.
+ */
+#ifndef LIBGLA_GLA_H
+#define LIBGLA_GLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GLA_OK = 0,
+    GLA_ERR_INVALID_ARG = 1,   /* null or misaligned pointer, bad size, overflow */
+    GLA_ERR_UNSUPPORTED = 2,   /* shape or mode this build does not implement   */
+    GLA_ERR_CUDA = 3,          /* a CUDA runtime call failed (see gla_last_error) */
+    GLA_ERR_TIMEOUT = 4,       /* a device-side wait gave up (reported by gla_check) */
+    GLA_ERR_WORKSPACE = 5      /* workspace smaller than the *_workspace_size query */
+} gla_status;
+
+typedef enum {
+    GLA_BF16 = 0,
+    GLA_FP32 = 1
+} gla_dtype;
+
+/*
+ * gla_chunk_fwd -- chunked forward ("Challenge 1": intra-chunk masked linear
+ * attention plus the running state; the state advanced by lambda^C).
+ *
+ *   q, k [B,T,H,dk], v [B,T,H,dv] (dtype), log_lambda [H] fp32,
+ *   h0 [B,H,dk,dv] fp32 or NULL (zero initial state), scale (readout factor),
+ *   chunk 64 or 128, o [B,T,H,dv] (dtype, written), hT [B,H,dk,dv] fp32 or
+ *   NULL (final state not wanted), workspace/workspace_bytes: optional device
+ *   scratch. With at least gla_chunk_fwd_workspace_size() bytes the library
+ *   may split long sequences into segments processed in parallel (same
+ *   result up to rounding); with less (or NULL) it runs one serial chain per
+ *   (b, h). Never fails for lack of workspace.
+ */
+gla_status gla_chunk_fwd(const void *q, const void *k, const void *v,
+                         const float *log_lambda, const float *h0, float scale,
+                         int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype,
+                         void *o, float *hT,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace that let gla_chunk_fwd use sequence segmentation for
+ * this shape (0 when the shape has enough (b, h) pairs to fill the GPU). */
+size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
+                                    gla_dtype dtype);
+
+/*
+ * gla_chunk_bwd -- gradients of L = sum_t <do_t, o_t> + <dhT, hT> through
+ * the chunked forward ("Challenge 3": through every serial state update).
+ * lambda is fixed (not learned), so there is no gradient for log_lambda.
+ *
+ *   q, k, v, log_lambda, h0, scale, B..dtype as for gla_chunk_fwd,
+ *   do [B,T,H,dv] (dtype), dhT [B,H,dk,dv] fp32 or NULL (zero),
+ *   dq, dk_ [B,T,H,dk], dv_ [B,T,H,dv] (dtype, written),
+ *   dh0 [B,H,dk,dv] fp32 or NULL (not wanted),
+ *   workspace: at least gla_chunk_bwd_workspace_size() bytes (may be 0).
+ */
+gla_status gla_chunk_bwd(const void *q, const void *k, const void *v,
+                         const float *log_lambda, const float *h0, float scale,
+                         const void *do_, const float *dhT,
+                         int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype,
+                         void *dq, void *dk_, void *dv_, float *dh0,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
+                                    gla_dtype dtype);
+
+/*
+ * gla_decode_step -- one recurrent step per (sequence n, head h), the
+ * serving path ("Inference optimization on Trainium2": the state lives in a
+ * fixed page per sequence):
+ *     S <- lambda * S + k v^T   (in place, fp32)
+ *     o  = scale * S^T q        (after the update)
+ *
+ *   q, k [N,H,dk], v [N,H,dv] (dtype), log_lambda [H], S_inout [N,H,dk,dv]
+ *   fp32 (read and written), o [N,H,dv] (dtype, written).
+ */
+gla_status gla_decode_step(const void *q, const void *k, const void *v,
+                           const float *log_lambda, float *S_inout, float scale,
+                           int N, int H, int dk, int dv, gla_dtype dtype,
+                           void *o, void *stream);
+
+/* Synchronise `stream` and report: GLA_ERR_CUDA if the stream or an earlier
+ * launch failed, GLA_ERR_TIMEOUT if a device-side wait gave up since the last
+ * gla_check (the status word is cleared on read), else GLA_OK. */
+gla_status gla_check(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *gla_status_string(gla_status status);
+
+/* Detail of the last error raised on this host thread (empty if none). */
+const char *gla_last_error(void);
+
+/* Number of kernels the last gla_chunk_fwd / gla_chunk_bwd / gla_decode_step
+ * call on this host thread launched (0 after an argument error). */
+int gla_last_launch_count(void);
+
+/* Library version, e.g. "libgla 0.1.0 sm_103a". */
+const char *gla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBGLA_GLA_H */

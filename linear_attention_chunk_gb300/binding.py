@@ -1,0 +1,223 @@
+"""ctypes binding of libgla (include/gla.h), with the C ABI's names.
+
+Argument marshalling only: every step of the mixer runs in libgla's CUDA
+kernels. PyTorch supplies device memory and the current stream; the
+functions below read shapes from the tensors, allocate outputs that the
+caller did not pass, and forward raw device pointers. There is no CPU path:
+if libgla.so is missing or a call fails, a GlaError is raised.
+
+Functions:
+  gla_chunk_fwd(q, k, v, log_lambda, h0=None, scale=None, chunk=128, ...) -> (o, hT)
+  gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, ...)          -> (dq, dk, dv, dh0)
+  gla_decode_step(q, k, v, log_lambda, S, scale=None, ...)                -> o  (S updated in place)
+  gla_check(stream=None), gla_status_string(code), gla_version()
+  gla_chunk_fwd_workspace_size(...), gla_chunk_bwd_workspace_size(...)
+`lib()` returns the loaded ctypes library for callers that hold raw pointers.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_lib", "libgla.so")
+
+GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_CUDA, GLA_ERR_TIMEOUT, GLA_ERR_WORKSPACE = range(6)
+GLA_BF16, GLA_FP32 = 0, 1
+
+# The public entry points declared in include/gla.h.
+ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_bwd",
+                 "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_check",
+                 "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
+
+
+class GlaError(RuntimeError):
+    def __init__(self, status: int, func: str, detail: str = ""):
+        self.status = status
+        name = _status_name(status)
+        super().__init__(f"{func} failed: {name}" + (f" -- {detail}" if detail else ""))
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+
+def lib():
+    """Load libgla.so (built in-tree by linear_attention_chunk_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise GlaError(GLA_ERR_CUDA, "load",
+                               f"{LIB_PATH} is not built; run `python -m linear_attention_chunk_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            L.gla_chunk_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i,
+                                        _vp, _vp, _vp, _sz, _vp]
+            L.gla_chunk_fwd.restype = _i
+            L.gla_chunk_fwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+            L.gla_chunk_fwd_workspace_size.restype = _sz
+            L.gla_chunk_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                        _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+            L.gla_chunk_bwd.restype = _i
+            L.gla_chunk_bwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+            L.gla_chunk_bwd_workspace_size.restype = _sz
+            L.gla_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _vp, _vp]
+            L.gla_decode_step.restype = _i
+            L.gla_check.argtypes = [_vp]
+            L.gla_check.restype = _i
+            L.gla_status_string.argtypes = [_i]
+            L.gla_status_string.restype = ctypes.c_char_p
+            L.gla_last_error.argtypes = []
+            L.gla_last_error.restype = ctypes.c_char_p
+            L.gla_last_launch_count.argtypes = []
+            L.gla_last_launch_count.restype = _i
+            L.gla_version.argtypes = []
+            L.gla_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return lib().gla_status_string(int(status)).decode()
+    except Exception:
+        return f"status {status}"
+
+
+def _raise_on(status: int, func: str):
+    if status != GLA_OK:
+        raise GlaError(status, func, lib().gla_last_error().decode(errors="replace"))
+
+
+def gla_status_string(status: int) -> str:
+    return lib().gla_status_string(int(status)).decode()
+
+
+def gla_version() -> str:
+    return lib().gla_version().decode()
+
+
+def gla_last_launch_count() -> int:
+    """Kernels launched by the last entry-point call on this thread."""
+    return int(lib().gla_last_launch_count())
+
+
+# ------------------------------------------------------------------ helpers
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return GLA_BF16
+    if t.dtype == torch.float32:
+        return GLA_FP32
+    raise GlaError(GLA_ERR_INVALID_ARG, "dtype", f"unsupported tensor dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise GlaError(GLA_ERR_INVALID_ARG, "argument", "tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise GlaError(GLA_ERR_INVALID_ARG, "argument", "tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+# --------------------------------------------------------------- entry points
+def gla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk=128, dtype=GLA_BF16) -> int:
+    return int(lib().gla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dtype))
+
+
+def gla_chunk_bwd_workspace_size(B, T, H, dk, dv, chunk=128, dtype=GLA_BF16) -> int:
+    return int(lib().gla_chunk_bwd_workspace_size(B, T, H, dk, dv, chunk, dtype))
+
+
+def gla_chunk_fwd(q, k, v, log_lambda, h0=None, scale=None, chunk=128, *, o=None, hT=None,
+                  want_hT=True, workspace=None, stream=None):
+    """Chunked forward. q, k [B,T,H,dk], v [B,T,H,dv] (bf16 or fp32, CUDA),
+    log_lambda [H] fp32, h0 [B,H,dk,dv] fp32 or None. Returns (o, hT)."""
+    torch = _torch()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    ws_need = gla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dt)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), float(scale),
+                             B, T, H, dk, dv, int(chunk), dt, _ptr(o), _ptr(hT),
+                             _ptr(workspace), ws_bytes, _stream(stream))
+    _raise_on(st, "gla_chunk_fwd")
+    return o, hT
+
+
+def gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, scale=None, chunk=128, *,
+                  dq=None, dk=None, dv=None, dh0=None, want_dh0=True, workspace=None, stream=None):
+    """Chunked backward. Returns (dq, dk, dv, dh0)."""
+    torch = _torch()
+    B, T, H, dk_ = q.shape
+    dv_ = v.shape[-1]
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk_)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dh0 is None and want_dh0:
+        dh0 = torch.empty((B, H, dk_, dv_), dtype=torch.float32, device=q.device)
+    ws_need = gla_chunk_bwd_workspace_size(B, T, H, dk_, dv_, chunk, dt)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gla_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), float(scale),
+                             _ptr(do), _ptr(dhT), B, T, H, dk_, dv_, int(chunk), dt,
+                             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dh0), _ptr(workspace), ws_bytes,
+                             _stream(stream))
+    _raise_on(st, "gla_chunk_bwd")
+    return dq, dk, dv, dh0
+
+
+def gla_decode_step(q, k, v, log_lambda, S, scale=None, *, o=None, stream=None):
+    """One recurrent step. q, k [N,H,dk], v [N,H,dv], S [N,H,dk,dv] fp32
+    (updated in place). Returns o [N,H,dv]."""
+    torch = _torch()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    st = lib().gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(S), float(scale),
+                               N, H, dk, dv, dt, _ptr(o), _stream(stream))
+    _raise_on(st, "gla_decode_step")
+    return o
+
+
+def gla_check(stream=None):
+    """Synchronise the stream; raise GlaError on a CUDA error or a device-side timeout."""
+    st = lib().gla_check(_stream(stream))
+    _raise_on(st, "gla_check")

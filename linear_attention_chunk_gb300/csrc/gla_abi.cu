@@ -1,0 +1,275 @@
+// gla_abi.cu -- the C ABI of libgla (declared in include/gla.h): host-side
+// argument validation, the device status word, and dispatch to the kernels.
+//
+// The operations are those of "Beyond the KV cache: Training and serving
+// i14's Laplace 3B linear attention model on AWS Trainium2 with native
+// PyTorch": the Simple GLA recurrence of the "GLA mixer" paragraph, its
+// chunked form ("Challenge 1"), its backward through the serial state chain
+// ("Challenge 3") and the serving step ("Inference optimization on
+// Trainium2"). Every argument error is caught here, before any launch.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "gla.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gla {
+
+// One status word per device that loads the library; kernels set bits in it
+// (kDevTimeout, ...) and gla_check() reads and clears it.
+static __device__ unsigned int g_status_word;
+
+namespace {
+
+thread_local char t_err[512] = {0};
+thread_local int t_launches = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int *g_status_ptr[kMaxDevices] = {nullptr};
+
+gla_status fail(gla_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+gla_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(GLA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device address of this device's status word (looked up once per device).
+gla_status status_word(unsigned int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GLA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+        g_status_ptr[dev] = static_cast<unsigned int *>(ptr);
+    }
+    *out = g_status_ptr[dev];
+    return GLA_OK;
+}
+
+// Common shape checks of the chunk entry points.
+gla_status check_chunk_shape(int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype) {
+    if (dtype != GLA_BF16 && dtype != GLA_FP32) return fail(GLA_ERR_INVALID_ARG, "dtype %d is not GLA_BF16/GLA_FP32", (int)dtype);
+    if (B < 0 || T < 0 || H < 0) return fail(GLA_ERR_INVALID_ARG, "negative size B=%d T=%d H=%d", B, T, H);
+    if (dk <= 0 || dv <= 0) return fail(GLA_ERR_INVALID_ARG, "dk=%d dv=%d must be positive", dk, dv);
+    if (chunk != 64 && chunk != 128) return fail(GLA_ERR_UNSUPPORTED, "chunk %d is not 64 or 128", chunk);
+    if (dtype == GLA_BF16 && (dk != 96 || dv != 192))
+        return fail(GLA_ERR_UNSUPPORTED, "GLA_BF16 needs dk=96, dv=192 (got %d, %d)", dk, dv);
+    if (dtype == GLA_FP32 && (dk > 128 || dv > 256))
+        return fail(GLA_ERR_UNSUPPORTED, "GLA_FP32 needs dk <= 128, dv <= 256 (got %d, %d)", dk, dv);
+    const long double elems = (long double)B * T * H * (dk > dv ? dk : dv);
+    if (elems > (long double)(1ull << 40)) return fail(GLA_ERR_INVALID_ARG, "tensor too large (%Lg elements)", elems);
+    if ((long double)B * H > 2147483647.0L) return fail(GLA_ERR_INVALID_ARG, "B*H too large");
+    return GLA_OK;
+}
+
+#define REQUIRE_PTR(p, name)                                                              \
+    do {                                                                                  \
+        if (!(p)) return fail(GLA_ERR_INVALID_ARG, "%s is NULL", name);                   \
+        if (!aligned16(p)) return fail(GLA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
+    } while (0)
+
+#define OPTIONAL_PTR(p, name)                                                             \
+    do {                                                                                  \
+        if ((p) && !aligned16(p)) return fail(GLA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
+    } while (0)
+
+}  // namespace
+
+void set_error_detail(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+}
+
+}  // namespace gla
+
+using namespace gla;
+
+extern "C" {
+
+gla_status gla_chunk_fwd(const void *q, const void *k, const void *v, const float *log_lambda,
+                         const float *h0, float scale, int B, int T, int H, int dk, int dv, int chunk,
+                         gla_dtype dtype, void *o, float *hT, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_chunk_shape(B, T, H, dk, dv, chunk, dtype);
+    if (st != GLA_OK) return st;
+    OPTIONAL_PTR(h0, "h0");
+    OPTIONAL_PTR(hT, "hT");
+    OPTIONAL_PTR(workspace, "workspace");
+    if (B == 0 || H == 0) return GLA_OK;
+    REQUIRE_PTR(log_lambda, "log_lambda");
+    if (T > 0) {
+        REQUIRE_PTR(q, "q");
+        REQUIRE_PTR(k, "k");
+        REQUIRE_PTR(v, "v");
+        REQUIRE_PTR(o, "o");
+    }
+    unsigned int *status = nullptr;
+    if ((st = status_word(&status)) != GLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    cudaError_t e;
+    if (T == 0) {
+        e = launch_copy_state(h0, hT, (size_t)B * H * dk * dv, s, &launches);
+        t_launches = launches;
+        return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd(T=0)");
+    }
+    FwdParams p{q, k, v, log_lambda, h0, scale, B, T, H, dk, dv, chunk, o, hT,
+                workspace, workspace ? workspace_bytes : 0, status};
+    if (dtype == GLA_BF16)
+        e = launch_fwd_tc(p, s, &launches);
+    else
+        e = launch_fwd_simt(p, false, s, &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd launch");
+}
+
+size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype) {
+    if (check_chunk_shape(B, T, H, dk, dv, chunk, dtype) != GLA_OK) return 0;
+    if (dtype != GLA_BF16) return 0;
+    return fwd_tc_workspace_size(B, T, H, chunk);
+}
+
+gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const float *log_lambda,
+                         const float *h0, float scale, const void *do_, const float *dhT, int B, int T,
+                         int H, int dk, int dv, int chunk, gla_dtype dtype, void *dq, void *dk_, void *dv_,
+                         float *dh0, void *workspace, size_t workspace_bytes, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_chunk_shape(B, T, H, dk, dv, chunk, dtype);
+    if (st != GLA_OK) return st;
+    OPTIONAL_PTR(h0, "h0");
+    OPTIONAL_PTR(dhT, "dhT");
+    OPTIONAL_PTR(dh0, "dh0");
+    OPTIONAL_PTR(workspace, "workspace");
+    if (B == 0 || H == 0) return GLA_OK;
+    REQUIRE_PTR(log_lambda, "log_lambda");
+    const size_t need = gla_chunk_bwd_workspace_size(B, T, H, dk, dv, chunk, dtype);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+        return fail(GLA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (T > 0) {
+        REQUIRE_PTR(q, "q");
+        REQUIRE_PTR(k, "k");
+        REQUIRE_PTR(v, "v");
+        REQUIRE_PTR(do_, "do");
+        REQUIRE_PTR(dq, "dq");
+        REQUIRE_PTR(dk_, "dk");
+        REQUIRE_PTR(dv_, "dv");
+    }
+    unsigned int *status = nullptr;
+    if ((st = status_word(&status)) != GLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    cudaError_t e;
+    if (T == 0) {
+        // No tokens: dh0 = dhT (the state passes through untouched).
+        e = launch_copy_state(dhT, dh0, (size_t)B * H * dk * dv, s, &launches);
+        t_launches = launches;
+        return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_bwd(T=0)");
+    }
+    BwdParams p{q, k, v, log_lambda, h0, scale, do_, dhT, B, T, H, dk, dv, chunk, dq, dk_, dv_, dh0,
+                workspace, workspace ? workspace_bytes : 0, status};
+    if (dtype == GLA_BF16)
+        e = launch_bwd_tc(p, s, &launches);
+    else
+        e = launch_bwd_simt(p, false, s, &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_bwd launch");
+}
+
+size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype) {
+    if (check_chunk_shape(B, T, H, dk, dv, chunk, dtype) != GLA_OK) return 0;
+    if (dtype != GLA_BF16) return 0;
+    return bwd_tc_workspace_size(B, T, H, chunk);
+}
+
+gla_status gla_decode_step(const void *q, const void *k, const void *v, const float *log_lambda,
+                           float *S_inout, float scale, int N, int H, int dk, int dv, gla_dtype dtype,
+                           void *o, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    if (dtype != GLA_BF16 && dtype != GLA_FP32) return fail(GLA_ERR_INVALID_ARG, "dtype %d invalid", (int)dtype);
+    if (N < 0 || H < 0) return fail(GLA_ERR_INVALID_ARG, "negative size N=%d H=%d", N, H);
+    if (dk <= 0 || dv <= 0) return fail(GLA_ERR_INVALID_ARG, "dk=%d dv=%d must be positive", dk, dv);
+    if (dtype == GLA_BF16 && (dk != 96 || dv != 192))
+        return fail(GLA_ERR_UNSUPPORTED, "GLA_BF16 needs dk=96, dv=192 (got %d, %d)", dk, dv);
+    if (dtype == GLA_FP32 && (dk > 128 || dv > 256))
+        return fail(GLA_ERR_UNSUPPORTED, "GLA_FP32 needs dk <= 128, dv <= 256 (got %d, %d)", dk, dv);
+    if ((long double)N * H > 2147483647.0L) return fail(GLA_ERR_INVALID_ARG, "N*H too large");
+    if (N == 0 || H == 0) return GLA_OK;
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(log_lambda, "log_lambda");
+    REQUIRE_PTR(S_inout, "S_inout");
+    REQUIRE_PTR(o, "o");
+    unsigned int *status = nullptr;
+    gla_status st = status_word(&status);
+    if (st != GLA_OK) return st;
+    DecodeParams p{q, k, v, log_lambda, S_inout, scale, N, H, dk, dv, o, status};
+    int launches = 0;
+    cudaError_t e = launch_decode(p, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_decode_step launch");
+}
+
+gla_status gla_check(void *stream) {
+    t_err[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "earlier launch");
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "read status word");
+    if (word != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+        if (word & kDevTimeout) return fail(GLA_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", word);
+        return fail(GLA_ERR_CUDA, "device reported an internal error (status 0x%x)", word);
+    }
+    return GLA_OK;
+}
+
+const char *gla_status_string(gla_status status) {
+    switch (status) {
+    case GLA_OK: return "GLA_OK";
+    case GLA_ERR_INVALID_ARG: return "GLA_ERR_INVALID_ARG";
+    case GLA_ERR_UNSUPPORTED: return "GLA_ERR_UNSUPPORTED";
+    case GLA_ERR_CUDA: return "GLA_ERR_CUDA";
+    case GLA_ERR_TIMEOUT: return "GLA_ERR_TIMEOUT";
+    case GLA_ERR_WORKSPACE: return "GLA_ERR_WORKSPACE";
+    }
+    return "GLA_ERR_UNKNOWN";
+}
+
+const char *gla_last_error(void) { return t_err; }
+
+int gla_last_launch_count(void) { return t_launches; }
+
+const char *gla_version(void) { return "libgla 0.1.0 sm_103a"; }
+
+}  // extern "C"

