@@ -1,0 +1,450 @@
+// fwd_tc.cu -- chunked Simple GLA forward on the 5th-generation tensor core
+// (tcgen05 MMA with TMEM accumulators, TMA-staged bf16 tiles), sm_103a.
+//
+// The chunked form of "Beyond the KV cache: Training and serving i14's
+// Laplace 3B linear attention model on AWS Trainium2 with native PyTorch",
+// section "Engineering challenges", "Challenge 1" (equations "Chunked GLA
+// intra-chunk output" and "Chunked GLA state update", Figure 3). For a chunk
+// of Cc valid tokens entering with state S_prev (0-based i, j inside it):
+//   P     = (Q K^T) .* D,   D_ij = lambda^(i-j) for j <= i, else 0
+//   O     = scale * ( P V + diag(lambda^(i+1)) Q S_prev )
+//   S_new = lambda^Cc S_prev + (diag(lambda^(Cc-1-j)) K)^T V
+// Only the state chain is serial; everything inside a chunk is a dense
+// contraction.
+//
+// Work split: one CTA per (b, h, half of dv). Each CTA walks the chunks of
+// its sequence in order and keeps its 96 x 96 slice of the fp32 state in
+// TMEM for the whole sequence. Sibling CTAs (the two dv halves of one head)
+// are adjacent in the grid, so the second read of q and k hits L2.
+//
+// Per chunk (M = 128 rows always; C = 64 uses the first 64 rows):
+//   MMA1  A  = Q K^T                      (TMEM cols [0, C))
+//   math  P  = bf16(A .* D) -> smem; Q <- diag(lambda^(i+1)) Q and
+//         K <- diag(lambda^(Cc-1-j)) K scaled in place
+//   MMA2  O  = Q~ S_prev                  (S_prev as a bf16 smem copy)
+//   MMA3  O += P V
+//   MMA4  S += K~^T V                     (fp32 in TMEM; rows dk padded to 128 by a zero block)
+//   math  S_prev' = bf16(S) -> smem and S <- lambda^C' S in TMEM (next chunk);
+//         O * scale -> bf16 -> smem -> TMA store
+// Roles: warp 0 issues TMA loads (two-stage ring), warp 1 owns TMEM and
+// issues the MMAs, warps 2-5 (128 threads, one TMEM lane each) do the
+// element-wise work. Decay powers lambda^n (n = 0..128) come from a table
+// computed once per CTA; lambda^i / lambda^j quotients are never formed.
+//
+// Operand layouts in shared memory (all 64-byte swizzle, 32-column blocks
+// of 128 rows x 64 B):
+//   Q, K, V tiles [token][d]:   K-major for Q K^T and Q~ S, MN-major for
+//                               the state update (K~^T as A, V as B) and P V (V as B)
+//   P [i][j]:                   K-major A operand
+//   S_prev copy [dk row][dv]:   MN-major B operand (96 rows per block)
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tmap.h"
+
+namespace gla {
+namespace {
+
+using namespace ptx;
+
+constexpr int kDk = 96, kDv = 192, kDvHalf = 96;
+constexpr int kThreads = 192;
+constexpr uint32_t kMathThreads = 128;
+
+constexpr uint32_t kBlk = 128 * 64;                  // [128 rows][32 bf16] block = 8 KB
+constexpr uint32_t kStageQ = 0;                      // 3 blocks
+constexpr uint32_t kStageK = 3 * kBlk;               // 4 blocks (the 4th stays zero: dk pad to 128)
+constexpr uint32_t kStageV = 7 * kBlk;               // 3 blocks (this CTA's 96 dv columns)
+constexpr uint32_t kStageBytes = 10 * kBlk;          // 80 KB
+constexpr uint32_t kOffP = 2 * kStageBytes;          // P, also the output staging tile
+constexpr uint32_t kSbBlk = kDk * 64;                // [96 rows][32 bf16] = 6 KB
+constexpr uint32_t kOffSb = kOffP + 4 * kBlk;
+constexpr uint32_t kOffPw = kOffSb + 3 * kSbBlk;     // lambda^n, n = 0..128 (+pad)
+enum { BAR_FULL0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_MMA1, BAR_PREADY, BAR_SBREADY, BAR_OFULL,
+       BAR_SFULL, BAR_OEMPTY, BAR_AEMPTY, BAR_DONE, kNumBars };
+constexpr uint32_t kOffBar = kOffPw + 132 * 4;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag, 2 decision slots
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
+
+constexpr uint32_t kTmemCols = 512, kColA = 0, kColO = 128, kColS = 256;
+
+struct FwdTcArgs {
+    const float *log_lambda;
+    const float *h0;
+    float *hT;
+    float scale;
+    int T, H, C, nck;
+    unsigned int *status;
+};
+
+// Multiply the 32 bf16 values of one 64-byte row in place by w. The 64-byte
+// swizzle only permutes the row's 16-byte chunks, so the row is scaled as is.
+__device__ __forceinline__ void scale_row64(uint32_t row_addr, float w) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint4 v = ld_shared_v4(row_addr + 16 * c);
+        uint32_t *u = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float2 f = unpack_bf16x2(u[e]);
+            u[e] = pack_bf16x2(f.x * w, f.y * w);
+        }
+        st_shared_v4(row_addr + 16 * c, v.x, v.y, v.z, v.w);
+    }
+}
+
+// Write 32 fp32 values as bf16 into row `row` of a 64-byte-swizzled block.
+__device__ __forceinline__ void write_row_sw64(uint32_t blk_addr, uint32_t row, const float (&x)[32]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        st_shared_v4(blk_addr + sw64_offset(row, c), pack_bf16x2(x[8 * c + 0], x[8 * c + 1]),
+                     pack_bf16x2(x[8 * c + 2], x[8 * c + 3]), pack_bf16x2(x[8 * c + 4], x[8 * c + 5]),
+                     pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+}
+
+// One elected thread of the 128-thread math group waits on an mbarrier; the
+// verdict is published through a two-slot flag so every thread of the group
+// takes the same branch after the named barrier.
+__device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl,
+                                           volatile int *decision, uint32_t mt, uint32_t &k) {
+    if (mt == 0) decision[k & 1] = mbar_wait(bar, parity, ctl) ? 0 : 1;
+    named_sync(1, kMathThreads);
+    return decision[(k++) & 1] == 0;
+}
+
+__device__ __forceinline__ bool lane0_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, parity, ctl) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const FwdTcArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                          ~static_cast<uintptr_t>(1023));
+    const uint32_t base = smem_u32(sm);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int half = blockIdx.x & 1;
+    const int bh = blockIdx.x >> 1;
+    const int b = bh / a.H, h = bh % a.H;
+    const int C = a.C, T = a.T, nck = a.nck;
+    const int ksteps_tok = C / 16;
+
+    float *pw = reinterpret_cast<float *>(sm + kOffPw);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+    volatile int *decision = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);
+    const WaitCtl ctl{abort_flag, a.status};
+    auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        decision[0] = 0;
+        decision[1] = 0;
+        mbar_init(bar(BAR_FULL0), 1);
+        mbar_init(bar(BAR_FULL1), 1);
+        mbar_init(bar(BAR_EMPTY0), 1);
+        mbar_init(bar(BAR_EMPTY1), 1);
+        mbar_init(bar(BAR_MMA1), 1);
+        mbar_init(bar(BAR_PREADY), 1);
+        mbar_init(bar(BAR_SBREADY), 1);
+        mbar_init(bar(BAR_OFULL), 1);
+        mbar_init(bar(BAR_SFULL), 1);
+        mbar_init(bar(BAR_OEMPTY), 1);
+        mbar_init(bar(BAR_AEMPTY), 1);
+        mbar_init(bar(BAR_DONE), 1);
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_o);
+    }
+    // Zero what TMA never writes: the dk padding block of K (both stages),
+    // and for C = 64 the rows 64..127 of every Q, K, V block.
+    for (uint32_t i = threadIdx.x; i < 2 * (kBlk / 16); i += kThreads) {
+        const uint32_t s = i / (kBlk / 16), o = (i % (kBlk / 16)) * 16;
+        st_shared_v4(base + s * kStageBytes + kStageK + 3 * kBlk + o, 0, 0, 0, 0);
+    }
+    if (C < 128) {
+        const uint32_t lo = (uint32_t)C * 64, per_blk = (kBlk - lo) / 16;
+        for (uint32_t i = threadIdx.x; i < 2 * 10 * per_blk; i += kThreads) {
+            const uint32_t blk = i / per_blk, o = lo + (i % per_blk) * 16;
+            st_shared_v4(base + blk * kBlk + o, 0, 0, 0, 0);   // blocks 0..19 = both stages
+        }
+    }
+    fence_proxy_async_smem();
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        const uint32_t tx_bytes = 9u * (uint32_t)C * 64u;
+        int issued = 0;
+        for (int c = 0; c < nck; ++c) {
+            const int s = c & 1;
+            if (c >= 2 && !lane0_wait(bar(BAR_EMPTY0 + s), ((c >> 1) - 1) & 1, ctl, lane)) break;
+            if (lane == 0) {
+                const uint32_t st = base + (uint32_t)s * kStageBytes;
+                const uint32_t fb = bar(BAR_FULL0 + s);
+                mbar_arrive_expect_tx(fb, tx_bytes);
+                const int t0 = c * C;
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    tma_load_4d(st + kStageQ + j * kBlk, &tm_q, fb, 32 * j, h, t0, b);
+                    tma_load_4d(st + kStageK + j * kBlk, &tm_k, fb, 32 * j, h, t0, b);
+                    tma_load_4d(st + kStageV + j * kBlk, &tm_v, fb, kDvHalf * half + 32 * j, h, t0, b);
+                }
+            }
+            __syncwarp();
+            issued = c + 1;
+        }
+        // Drain: every load issued must have landed before the CTA exits.
+        for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c)
+            lane0_wait(bar(BAR_FULL0 + (c & 1)), (c >> 1) & 1, ctl, lane);
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        const uint32_t idA = idesc_bf16(128, C, false, false);
+        const uint32_t idO = idesc_bf16(128, kDvHalf, false, true);
+        const uint32_t idS = idesc_bf16(128, kDvHalf, true, true);
+        for (int c = 0; c < nck; ++c) {
+            const int s = c & 1;
+            const uint32_t st = base + (uint32_t)s * kStageBytes;
+            if (!lane0_wait(bar(BAR_FULL0 + s), (c >> 1) & 1, ctl, lane)) break;
+            if (c >= 1 && !lane0_wait(bar(BAR_AEMPTY), (c - 1) & 1, ctl, lane)) break;
+            tc_fence_after();
+            if (lane == 0) {
+                // MMA1: A = Q K^T over dk (6 steps of 16)
+#pragma unroll
+                for (int ks = 0; ks < 6; ++ks) {
+                    const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
+                    mma_bf16_ss(tmem + kColA, smem_desc(st + kStageQ + off, 16, 512, 4),
+                                smem_desc(st + kStageK + off, 16, 512, 4), idA, ks > 0);
+                }
+                mma_commit(bar(BAR_MMA1));
+            }
+            __syncwarp();
+            if (!lane0_wait(bar(BAR_PREADY), c & 1, ctl, lane)) break;
+            if (!lane0_wait(bar(BAR_SBREADY), c & 1, ctl, lane)) break;
+            if (c >= 1 && !lane0_wait(bar(BAR_OEMPTY), (c - 1) & 1, ctl, lane)) break;
+            tc_fence_after();
+            if (lane == 0) {
+                // MMA2: O = Q~ S_prev over dk
+#pragma unroll
+                for (int ks = 0; ks < 6; ++ks) {
+                    const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
+                    mma_bf16_ss(tmem + kColO, smem_desc(st + kStageQ + off, 16, 512, 4),
+                                smem_desc(base + kOffSb + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
+                }
+                // MMA3: O += P V over the chunk's tokens
+                for (int ks = 0; ks < ksteps_tok; ++ks) {
+                    const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
+                    mma_bf16_ss(tmem + kColO, smem_desc(base + kOffP + off, 16, 512, 4),
+                                smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idO, 1);
+                }
+                mma_commit(bar(BAR_OFULL));
+                // MMA4: S += K~^T V over the chunk's tokens
+                for (int ks = 0; ks < ksteps_tok; ++ks) {
+                    mma_bf16_ss(tmem + kColS, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
+                                smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
+                }
+                mma_commit(bar(BAR_SFULL));
+                mma_commit(bar(BAR_EMPTY0 + s));
+            }
+            __syncwarp();
+        }
+        // Every MMA issued must be complete before TMEM is released.
+        if (lane == 0) mma_commit(bar(BAR_DONE));
+        __syncwarp();
+        lane0_wait(bar(BAR_DONE), 0, ctl, lane);
+    } else {
+        // ------------------------------------------------ math warps (2..5)
+        const uint32_t quad = (uint32_t)(warp & 3);
+        const uint32_t row = quad * 32 + (uint32_t)lane;          // TMEM lane = tile row
+        const uint32_t mt = (uint32_t)threadIdx.x - 64;           // 0..127 within the group
+        const uint32_t tl = tmem + ((quad * 32) << 16);
+        uint32_t kw = 0;                                          // group-wait counter
+        const float l2 = log2_of_decay(a.log_lambda[h]);
+        for (uint32_t n = mt; n < 132; n += kMathThreads) pw[n] = n <= 128 ? decay_pow(l2, (int)n) : 0.f;
+        named_sync(1, kMathThreads);
+
+        // Initial state: S_prev copy = bf16(h0 slice), TMEM S = lambda^C0 * h0.
+        {
+            const int C0 = min(C, T);
+            const float w0 = pw[C0];
+            if (row < (uint32_t)kDk) {
+                const float *src = a.h0 ? a.h0 + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half : nullptr;
+#pragma unroll
+                for (int blk = 0; blk < 3; ++blk) {
+                    float x[32];
+                    uint32_t r[32];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        float4 v4 = src ? *reinterpret_cast<const float4 *>(src + blk * 32 + e)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                        x[e] = v4.x; x[e + 1] = v4.y; x[e + 2] = v4.z; x[e + 3] = v4.w;
+                    }
+                    write_row_sw64(base + kOffSb + blk * kSbBlk, row, x);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(x[e] * w0);
+                    tmem_st_32cols(tl + kColS + blk * 32, r);
+                }
+            }
+            // Warps 2..5 include quadrant 3 (rows 96..127), which holds no
+            // state rows; tcgen05.st is warp-collective, so that warp skips it.
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(1, kMathThreads);
+            if (mt == 0) mbar_arrive(bar(BAR_SBREADY));
+        }
+
+        for (int c = 0; c < nck; ++c) {
+            const int s = c & 1;
+            const uint32_t st = base + (uint32_t)s * kStageBytes;
+            const int t0 = c * C;
+            const int Cc = min(C, T - t0);
+            if (!group_wait(bar(BAR_MMA1), c & 1, ctl, decision, mt, kw)) break;
+            tc_fence_after();
+            // The output tile of the previous chunk (same buffer as P) must
+            // have been read by its TMA store before P is overwritten.
+            if (mt == 0) tma_store_wait_read_all();
+            named_sync(1, kMathThreads);
+
+            // P = bf16((Q K^T) .* D) for this thread's row i = row.
+            for (int blk = 0; blk < C / 32; ++blk) {
+                uint32_t r[32];
+                float x[32];
+                tmem_ld_32cols(tl + kColA + blk * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int j = blk * 32 + e;
+                    const int n = (int)row - j;
+                    x[e] = (n >= 0 && j < Cc) ? __uint_as_float(r[e]) * pw[n] : 0.f;
+                }
+                write_row_sw64(base + kOffP + blk * kBlk, row, x);
+            }
+            tc_fence_before();
+            // In-place decay scaling of this row of Q (lambda^(i+1)) and K
+            // (lambda^(Cc-1-j), zero past the end of the sequence).
+            {
+                const float wq = pw[row + 1];
+                const float wk = row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f;
+#pragma unroll
+                for (int blk = 0; blk < 3; ++blk) {
+                    scale_row64(st + kStageQ + blk * kBlk + row * 64, wq);
+                    scale_row64(st + kStageK + blk * kBlk + row * 64, wk);
+                }
+            }
+            fence_proxy_async_smem();
+            named_sync(1, kMathThreads);
+            if (mt == 0) {
+                mbar_arrive(bar(BAR_AEMPTY));
+                mbar_arrive(bar(BAR_PREADY));
+            }
+
+            // State: bf16 copy for the next chunk's Q~ S and the lambda^C' rescale,
+            // or the final state after the last chunk.
+            if (!group_wait(bar(BAR_SFULL), c & 1, ctl, decision, mt, kw)) break;
+            tc_fence_after();
+            if (quad < 3) {
+                const bool last = (c == nck - 1);
+                const float wn = last ? 1.f : pw[min(C, T - t0 - C)];
+                float *dst = (last && a.hT) ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
+                                            : nullptr;
+#pragma unroll
+                for (int blk = 0; blk < 3; ++blk) {
+                    uint32_t r[32];
+                    float x[32];
+                    tmem_ld_32cols(tl + kColS + blk * 32, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+                    if (last) {
+                        if (dst) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 4)
+                                *reinterpret_cast<float4 *>(dst + blk * 32 + e) =
+                                    make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                        }
+                    } else {
+                        write_row_sw64(base + kOffSb + blk * kSbBlk, row, x);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(x[e] * wn);
+                        tmem_st_32cols(tl + kColS + blk * 32, r);
+                    }
+                }
+                tmem_st_wait();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(1, kMathThreads);
+            if (mt == 0 && c < nck - 1) mbar_arrive(bar(BAR_SBREADY));
+
+            // Output tile: O * scale -> bf16 -> staging (the P buffer) -> TMA store.
+            if (!group_wait(bar(BAR_OFULL), c & 1, ctl, decision, mt, kw)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int blk = 0; blk < 3; ++blk) {
+                uint32_t r[32];
+                float x[32];
+                tmem_ld_32cols(tl + kColO + blk * 32, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]) * a.scale;
+                write_row_sw64(base + kOffP + blk * kBlk, row, x);
+            }
+            tc_fence_before();
+            fence_proxy_async_smem();
+            named_sync(1, kMathThreads);
+            if (mt == 0) {
+                mbar_arrive(bar(BAR_OEMPTY));
+#pragma unroll
+                for (int blk = 0; blk < 3; ++blk)
+                    tma_store_4d(&tm_o, base + kOffP + blk * kBlk, kDvHalf * half + 32 * blk, h, t0, b);
+                tma_store_commit();
+            }
+        }
+        if (mt == 0) tma_store_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+size_t fwd_tc_workspace_size(int, int, int, int) { return 0; }
+
+cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
+    if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mo;
+    cudaError_t e;
+    if ((e = make_token_map(&mq, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mk, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mo, p.o, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gla_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, p.T, p.H, p.chunk, (p.T + p.chunk - 1) / p.chunk, p.status};
+    const unsigned grid = (unsigned)(p.B * p.H * 2);
+    gla_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, a);
+    if (launches) ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace gla

@@ -1,14 +1,10 @@
-// tc_interim.cu -- bf16 chunk entry points routed to the SIMT kernels until
-// the tcgen05 kernels are in place.
+// tc_interim.cu -- bf16 backward routed to the SIMT kernels until the
+// tcgen05 backward kernel is in place.
 #include "kernels.h"
 
 namespace gla {
-cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
-    return launch_fwd_simt(p, true, s, launches);
-}
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches) {
     return launch_bwd_simt(p, true, s, launches);
 }
-size_t fwd_tc_workspace_size(int, int, int, int) { return 0; }
 size_t bwd_tc_workspace_size(int, int, int, int) { return 0; }
 }  // namespace gla
