@@ -17,26 +17,34 @@
 // TMEM for the whole sequence. Sibling CTAs (the two dv halves of one head)
 // are adjacent in the grid, so the second read of q and k hits L2.
 //
-// Per chunk (M = 128 rows always; C = 64 uses the first 64 rows):
-//   MMA1  A  = Q K^T                      (TMEM cols [0, C))
-//   math  P  = bf16(A .* D) -> smem; Q <- diag(lambda^(i+1)) Q and
-//         K <- diag(lambda^(Cc-1-j)) K scaled in place
-//   MMA2  O  = Q~ S_prev                  (S_prev as a bf16 smem copy)
-//   MMA3  O += P V
-//   MMA4  S += K~^T V                     (fp32 in TMEM; rows dk padded to 128 by a zero block)
-//   math  S_prev' = bf16(S) -> smem and S <- lambda^C' S in TMEM (next chunk);
-//         O * scale -> bf16 -> smem -> TMA store
-// Roles: warp 0 issues TMA loads (two-stage ring), warp 1 owns TMEM and
-// issues the MMAs, warps 2-5 (128 threads, one TMEM lane each) do the
-// element-wise work. Decay powers lambda^n (n = 0..128) come from a table
-// computed once per CTA; lambda^i / lambda^j quotients are never formed.
+// Warp roles (320 threads):
+//   warp 0      TMA producer: Q, K, V tiles of chunk c into stage c%2
+//   warp 1      TMEM owner and MMA issuer
+//   warps 2-5   "P group": A -> P = bf16(A .* D) into TMEM; Q and K scaled
+//               in place by lambda^(i+1) and lambda^(Cc-1-j)
+//   warps 6-9   "E group": the state hand-off (bf16 copy of S for the next
+//               chunk's Q~ S, S <- lambda^C' S in TMEM, hT at the end) and the
+//               output epilogue (O * scale -> bf16 -> smem -> TMA store)
+// Each element-wise group has one thread per TMEM lane (= tile row).
 //
-// Operand layouts in shared memory (all 64-byte swizzle, 32-column blocks
-// of 128 rows x 64 B):
-//   Q, K, V tiles [token][d]:   K-major for Q K^T and Q~ S, MN-major for
-//                               the state update (K~^T as A, V as B) and P V (V as B)
-//   P [i][j]:                   K-major A operand
-//   S_prev copy [dk row][dv]:   MN-major B operand (96 rows per block)
+// TMEM (512 columns): R0, R1 = [0,128), [128,256) hold A = Q K^T of chunk c
+// in R[c%2], then that chunk's O (first 96 columns); S = [256,352) fp32;
+// P0, P1 = [352,416), [416,480) bf16 pairs, the A operand of P V.
+// MMA issue order per chunk c (one thread):
+//   MMA1(c+1) into R[(c+1)%2]            -- before waiting on chunk c's P,
+//   MMA2(c)  R[c%2]  = Q~ S_prev          so the next Q K^T overlaps it
+//   MMA4(c)  S      += K~^T V      -> state ready (E group)
+//   MMA3(c)  R[c%2] += P V          -> output ready (E group)
+// The serial chain per chunk is MMA2 + MMA4 + the state hand-off; the P
+// computation of the next chunk runs beside the hand-off.
+//
+// Shared-memory operand layouts (64-byte swizzle, 32-column blocks of
+// 128 rows x 64 B): Q, K, V tiles [token][d] are K-major for Q K^T and
+// Q~ S and MN-major for the state update (K~^T as A; the fourth dk block of
+// K is a zero block, padding dk = 96 to M = 128) and for P V (V as B); the
+// bf16 S_prev copy [dk][dv] is an MN-major B operand (96-row blocks,
+// double-buffered so the hand-off of chunk c can run while MMA2(c+1) still
+// waits for P).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -50,26 +58,29 @@ namespace {
 using namespace ptx;
 
 constexpr int kDk = 96, kDv = 192, kDvHalf = 96;
-constexpr int kThreads = 192;
-constexpr uint32_t kMathThreads = 128;
+constexpr int kThreads = 320;
+constexpr uint32_t kGroupThreads = 128;
+constexpr uint32_t kBarP = 1, kBarE = 2;             // named barriers of the two groups
 
 constexpr uint32_t kBlk = 128 * 64;                  // [128 rows][32 bf16] block = 8 KB
 constexpr uint32_t kStageQ = 0;                      // 3 blocks
 constexpr uint32_t kStageK = 3 * kBlk;               // 4 blocks (the 4th stays zero: dk pad to 128)
 constexpr uint32_t kStageV = 7 * kBlk;               // 3 blocks (this CTA's 96 dv columns)
 constexpr uint32_t kStageBytes = 10 * kBlk;          // 80 KB
-constexpr uint32_t kOffP = 2 * kStageBytes;          // P, also the output staging tile
 constexpr uint32_t kSbBlk = kDk * 64;                // [96 rows][32 bf16] = 6 KB
-constexpr uint32_t kOffSb = kOffP + 4 * kBlk;
-constexpr uint32_t kOffPw = kOffSb + 3 * kSbBlk;     // lambda^n, n = 0..128 (+pad)
-enum { BAR_FULL0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_MMA1, BAR_PREADY, BAR_SBREADY, BAR_OFULL,
-       BAR_SFULL, BAR_OEMPTY, BAR_AEMPTY, BAR_DONE, kNumBars };
+constexpr uint32_t kSbBytes = 3 * kSbBlk;
+constexpr uint32_t kOffSb = 2 * kStageBytes;         // two S_prev copies
+constexpr uint32_t kOffOut = kOffSb + 2 * kSbBytes;  // output staging, 3 blocks
+constexpr uint32_t kOffPw = kOffOut + 3 * kBlk;      // lambda^n, n = 0..128 (+pad)
+enum { BAR_FULL0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_MMA1_0, BAR_MMA1_1, BAR_PREADY0, BAR_PREADY1, BAR_SBREADY,
+       BAR_SFULL, BAR_OFULL0, BAR_OFULL1, BAR_OEMPTY, BAR_DONE, kNumBars };
 constexpr uint32_t kOffBar = kOffPw + 132 * 4;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag, 2 decision slots
-constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, 2+2 decision slots
+constexpr uint32_t kSmemUsed = kOffMisc + 24;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr uint32_t kTmemCols = 512, kColA = 0, kColO = 128, kColS = 256;
+constexpr uint32_t kTmemCols = 512, kColR = 0, kColS = 256, kColP = 352;
 
 struct FwdTcArgs {
     const float *log_lambda;
@@ -105,13 +116,13 @@ __device__ __forceinline__ void write_row_sw64(uint32_t blk_addr, uint32_t row, 
                      pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
 }
 
-// One elected thread of the 128-thread math group waits on an mbarrier; the
-// verdict is published through a two-slot flag so every thread of the group
-// takes the same branch after the named barrier.
+// One elected thread of a 128-thread group waits on an mbarrier; the verdict
+// is published through a two-slot flag so every thread of the group takes
+// the same branch after the group's named barrier.
 __device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl,
-                                           volatile int *decision, uint32_t mt, uint32_t &k) {
-    if (mt == 0) decision[k & 1] = mbar_wait(bar, parity, ctl) ? 0 : 1;
-    named_sync(1, kMathThreads);
+                                           volatile int *decision, uint32_t gt, uint32_t named, uint32_t &k) {
+    if (gt == 0) decision[k & 1] = mbar_wait(bar, parity, ctl) ? 0 : 1;
+    named_sync(named, kGroupThreads);
     return decision[(k++) & 1] == 0;
 }
 
@@ -139,31 +150,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
-    volatile int *decision = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);
+    volatile int *decP = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);
+    volatile int *decE = reinterpret_cast<volatile int *>(sm + kOffMisc + 16);
     const WaitCtl ctl{abort_flag, a.status};
     auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        decision[0] = 0;
-        decision[1] = 0;
-        mbar_init(bar(BAR_FULL0), 1);
-        mbar_init(bar(BAR_FULL1), 1);
-        mbar_init(bar(BAR_EMPTY0), 1);
-        mbar_init(bar(BAR_EMPTY1), 1);
-        mbar_init(bar(BAR_MMA1), 1);
-        mbar_init(bar(BAR_PREADY), 1);
-        mbar_init(bar(BAR_SBREADY), 1);
-        mbar_init(bar(BAR_OFULL), 1);
-        mbar_init(bar(BAR_SFULL), 1);
-        mbar_init(bar(BAR_OEMPTY), 1);
-        mbar_init(bar(BAR_AEMPTY), 1);
-        mbar_init(bar(BAR_DONE), 1);
+        decP[0] = decP[1] = decE[0] = decE[1] = 0;
+        for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_o);
+    }
+    {
+        const float l2 = log2_of_decay(a.log_lambda[h]);
+        for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
     }
     // Zero what TMA never writes: the dk padding block of K (both stages),
     // and for C = 64 the rows 64..127 of every Q, K, V block.
@@ -218,48 +222,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t idA = idesc_bf16(128, C, false, false);
         const uint32_t idO = idesc_bf16(128, kDvHalf, false, true);
         const uint32_t idS = idesc_bf16(128, kDvHalf, true, true);
-        for (int c = 0; c < nck; ++c) {
+        // MMA1(c): A = Q K^T into R[c%2], once its tiles landed and R[c%2]
+        // is free (the epilogue of chunk c-2 read its output).
+        auto issue_qk = [&](int c) -> bool {
             const int s = c & 1;
-            const uint32_t st = base + (uint32_t)s * kStageBytes;
-            if (!lane0_wait(bar(BAR_FULL0 + s), (c >> 1) & 1, ctl, lane)) break;
-            if (c >= 1 && !lane0_wait(bar(BAR_AEMPTY), (c - 1) & 1, ctl, lane)) break;
+            if (!lane0_wait(bar(BAR_FULL0 + s), (c >> 1) & 1, ctl, lane)) return false;
+            if (c >= 2 && !lane0_wait(bar(BAR_OEMPTY), (c - 2) & 1, ctl, lane)) return false;
             tc_fence_after();
             if (lane == 0) {
-                // MMA1: A = Q K^T over dk (6 steps of 16)
+                const uint32_t st = base + (uint32_t)s * kStageBytes;
 #pragma unroll
                 for (int ks = 0; ks < 6; ++ks) {
                     const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
-                    mma_bf16_ss(tmem + kColA, smem_desc(st + kStageQ + off, 16, 512, 4),
+                    mma_bf16_ss(tmem + kColR + 128u * s, smem_desc(st + kStageQ + off, 16, 512, 4),
                                 smem_desc(st + kStageK + off, 16, 512, 4), idA, ks > 0);
                 }
-                mma_commit(bar(BAR_MMA1));
+                mma_commit(bar(BAR_MMA1_0 + s));
             }
             __syncwarp();
-            if (!lane0_wait(bar(BAR_PREADY), c & 1, ctl, lane)) break;
+            return true;
+        };
+        bool ok = issue_qk(0);
+        for (int c = 0; ok && c < nck; ++c) {
+            const int s = c & 1;
+            const uint32_t st = base + (uint32_t)s * kStageBytes;
+            if (c + 1 < nck && !issue_qk(c + 1)) break;
+            if (!lane0_wait(bar(BAR_PREADY0 + s), (c >> 1) & 1, ctl, lane)) break;
             if (!lane0_wait(bar(BAR_SBREADY), c & 1, ctl, lane)) break;
-            if (c >= 1 && !lane0_wait(bar(BAR_OEMPTY), (c - 1) & 1, ctl, lane)) break;
             tc_fence_after();
             if (lane == 0) {
+                const uint32_t dR = tmem + kColR + 128u * s;
+                const uint32_t sb = base + kOffSb + (uint32_t)s * kSbBytes;
                 // MMA2: O = Q~ S_prev over dk
 #pragma unroll
                 for (int ks = 0; ks < 6; ++ks) {
                     const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
-                    mma_bf16_ss(tmem + kColO, smem_desc(st + kStageQ + off, 16, 512, 4),
-                                smem_desc(base + kOffSb + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
+                    mma_bf16_ss(dR, smem_desc(st + kStageQ + off, 16, 512, 4),
+                                smem_desc(sb + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
                 }
-                // MMA3: O += P V over the chunk's tokens
-                for (int ks = 0; ks < ksteps_tok; ++ks) {
-                    const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
-                    mma_bf16_ss(tmem + kColO, smem_desc(base + kOffP + off, 16, 512, 4),
-                                smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idO, 1);
-                }
-                mma_commit(bar(BAR_OFULL));
                 // MMA4: S += K~^T V over the chunk's tokens
-                for (int ks = 0; ks < ksteps_tok; ++ks) {
+                for (int ks = 0; ks < ksteps_tok; ++ks)
                     mma_bf16_ss(tmem + kColS, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
                                 smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
-                }
                 mma_commit(bar(BAR_SFULL));
+                // MMA3: O += P V (P from TMEM)
+                for (int ks = 0; ks < ksteps_tok; ++ks)
+                    mma_bf16_ts(dR, tmem + kColP + 64u * s + 8u * (uint32_t)ks,
+                                smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idO, 1);
+                mma_commit(bar(BAR_OFULL0 + s));
                 mma_commit(bar(BAR_EMPTY0 + s));
             }
             __syncwarp();
@@ -268,23 +278,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mma_commit(bar(BAR_DONE));
         __syncwarp();
         lane0_wait(bar(BAR_DONE), 0, ctl, lane);
-    } else {
-        // ------------------------------------------------ math warps (2..5)
+    } else if (warp < 6) {
+        // ------------------------------------------------- P group (2..5)
         const uint32_t quad = (uint32_t)(warp & 3);
-        const uint32_t row = quad * 32 + (uint32_t)lane;          // TMEM lane = tile row
-        const uint32_t mt = (uint32_t)threadIdx.x - 64;           // 0..127 within the group
+        const uint32_t row = quad * 32 + (uint32_t)lane;          // TMEM lane = token row
+        const uint32_t gt = (uint32_t)threadIdx.x - 64;            // 0..127
         const uint32_t tl = tmem + ((quad * 32) << 16);
-        uint32_t kw = 0;                                          // group-wait counter
-        const float l2 = log2_of_decay(a.log_lambda[h]);
-        for (uint32_t n = mt; n < 132; n += kMathThreads) pw[n] = n <= 128 ? decay_pow(l2, (int)n) : 0.f;
-        named_sync(1, kMathThreads);
-
-        // Initial state: S_prev copy = bf16(h0 slice), TMEM S = lambda^C0 * h0.
+        uint32_t kw = 0;
+        for (int c = 0; c < nck; ++c) {
+            const int s = c & 1;
+            const uint32_t st = base + (uint32_t)s * kStageBytes;
+            const int Cc = min(C, T - c * C);
+            if (!group_wait(bar(BAR_MMA1_0 + s), (c >> 1) & 1, ctl, decP, gt, kBarP, kw)) break;
+            tc_fence_after();
+            // P = bf16((Q K^T) .* D), row i = row, packed pairs into TMEM P[c%2].
+            for (int blk = 0; blk < C / 32; ++blk) {
+                uint32_t r[32];
+                tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, r);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const int j = blk * 32 + e;
+                    const int n = (int)row - j;
+                    const float x0 = (n >= 0 && j < Cc) ? __uint_as_float(r[e]) * pw[n] : 0.f;
+                    const float x1 = (n >= 1 && j + 1 < Cc) ? __uint_as_float(r[e + 1]) * pw[n - 1] : 0.f;
+                    pk[e >> 1] = pack_bf16x2(x0, x1);
+                }
+                // 32 tokens = 16 packed columns of P[c%2]
+                tmem_st_16cols(tl + kColP + 64u * s + 16u * blk, pk);
+            }
+            tmem_st_wait();
+            // In-place decay scaling of this row of Q (lambda^(i+1)) and K
+            // (lambda^(Cc-1-j), zero past the end of the sequence).
+            {
+                const float wq = pw[row + 1];
+                const float wk = row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f;
+#pragma unroll
+                for (int blk = 0; blk < 3; ++blk) {
+                    scale_row64(st + kStageQ + blk * kBlk + row * 64, wq);
+                    scale_row64(st + kStageK + blk * kBlk + row * 64, wk);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(kBarP, kGroupThreads);
+            if (gt == 0) mbar_arrive(bar(BAR_PREADY0 + s));
+        }
+    } else {
+        // ------------------------------------------------- E group (6..9)
+        const uint32_t quad = (uint32_t)(warp & 3);
+        const uint32_t row = quad * 32 + (uint32_t)lane;
+        const uint32_t gt = (uint32_t)threadIdx.x - 192;           // 0..127
+        const uint32_t tl = tmem + ((quad * 32) << 16);
+        uint32_t kw = 0;
+        // Initial state: S_prev copy 0 = bf16(h0 slice), TMEM S = lambda^C0 * h0.
         {
-            const int C0 = min(C, T);
-            const float w0 = pw[C0];
-            if (row < (uint32_t)kDk) {
-                const float *src = a.h0 ? a.h0 + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half : nullptr;
+            const float w0 = pw[min(C, T)];
+            if (quad < 3) {
+                const float *src =
+                    a.h0 ? a.h0 + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half : nullptr;
 #pragma unroll
                 for (int blk = 0; blk < 3; ++blk) {
                     float x[32];
@@ -300,68 +353,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(x[e] * w0);
                     tmem_st_32cols(tl + kColS + blk * 32, r);
                 }
+                tmem_st_wait();
             }
-            // Warps 2..5 include quadrant 3 (rows 96..127), which holds no
-            // state rows; tcgen05.st is warp-collective, so that warp skips it.
-            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(1, kMathThreads);
-            if (mt == 0) mbar_arrive(bar(BAR_SBREADY));
+            named_sync(kBarE, kGroupThreads);
+            if (gt == 0) mbar_arrive(bar(BAR_SBREADY));
         }
-
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
-            const uint32_t st = base + (uint32_t)s * kStageBytes;
             const int t0 = c * C;
-            const int Cc = min(C, T - t0);
-            if (!group_wait(bar(BAR_MMA1), c & 1, ctl, decision, mt, kw)) break;
+            // State hand-off (rows 0..95 = quadrants 0..2).
+            if (!group_wait(bar(BAR_SFULL), c & 1, ctl, decE, gt, kBarE, kw)) break;
             tc_fence_after();
-            // The output tile of the previous chunk (same buffer as P) must
-            // have been read by its TMA store before P is overwritten.
-            if (mt == 0) tma_store_wait_read_all();
-            named_sync(1, kMathThreads);
-
-            // P = bf16((Q K^T) .* D) for this thread's row i = row.
-            for (int blk = 0; blk < C / 32; ++blk) {
-                uint32_t r[32];
-                float x[32];
-                tmem_ld_32cols(tl + kColA + blk * 32, r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = blk * 32 + e;
-                    const int n = (int)row - j;
-                    x[e] = (n >= 0 && j < Cc) ? __uint_as_float(r[e]) * pw[n] : 0.f;
-                }
-                write_row_sw64(base + kOffP + blk * kBlk, row, x);
-            }
-            tc_fence_before();
-            // In-place decay scaling of this row of Q (lambda^(i+1)) and K
-            // (lambda^(Cc-1-j), zero past the end of the sequence).
-            {
-                const float wq = pw[row + 1];
-                const float wk = row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f;
-#pragma unroll
-                for (int blk = 0; blk < 3; ++blk) {
-                    scale_row64(st + kStageQ + blk * kBlk + row * 64, wq);
-                    scale_row64(st + kStageK + blk * kBlk + row * 64, wk);
-                }
-            }
-            fence_proxy_async_smem();
-            named_sync(1, kMathThreads);
-            if (mt == 0) {
-                mbar_arrive(bar(BAR_AEMPTY));
-                mbar_arrive(bar(BAR_PREADY));
-            }
-
-            // State: bf16 copy for the next chunk's Q~ S and the lambda^C' rescale,
-            // or the final state after the last chunk.
-            if (!group_wait(bar(BAR_SFULL), c & 1, ctl, decision, mt, kw)) break;
-            tc_fence_after();
+            const bool last = (c == nck - 1);
             if (quad < 3) {
-                const bool last = (c == nck - 1);
                 const float wn = last ? 1.f : pw[min(C, T - t0 - C)];
+                const uint32_t sb_next = base + kOffSb + (uint32_t)(s ^ 1) * kSbBytes;
                 float *dst = (last && a.hT) ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
                                             : nullptr;
 #pragma unroll
@@ -380,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
                         }
                     } else {
-                        write_row_sw64(base + kOffSb + blk * kSbBlk, row, x);
+                        write_row_sw64(sb_next + blk * kSbBlk, row, x);
 #pragma unroll
                         for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(x[e] * wn);
                         tmem_st_32cols(tl + kColS + blk * 32, r);
@@ -390,34 +398,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(1, kMathThreads);
-            if (mt == 0 && c < nck - 1) mbar_arrive(bar(BAR_SBREADY));
+            named_sync(kBarE, kGroupThreads);
+            if (gt == 0 && !last) mbar_arrive(bar(BAR_SBREADY));
 
-            // Output tile: O * scale -> bf16 -> staging (the P buffer) -> TMA store.
-            if (!group_wait(bar(BAR_OFULL), c & 1, ctl, decision, mt, kw)) break;
+            // Output tile: O * scale -> bf16 -> staging -> TMA store.
+            if (!group_wait(bar(BAR_OFULL0 + s), (c >> 1) & 1, ctl, decE, gt, kBarE, kw)) break;
             tc_fence_after();
+            if (gt == 0) tma_store_wait_read_all();   // staging free (store of chunk c-1 read it)
+            named_sync(kBarE, kGroupThreads);
 #pragma unroll
             for (int blk = 0; blk < 3; ++blk) {
                 uint32_t r[32];
                 float x[32];
-                tmem_ld_32cols(tl + kColO + blk * 32, r);
+                tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, r);
                 tmem_ld_wait();
 #pragma unroll
                 for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]) * a.scale;
-                write_row_sw64(base + kOffP + blk * kBlk, row, x);
+                write_row_sw64(base + kOffOut + blk * kBlk, row, x);
             }
             tc_fence_before();
             fence_proxy_async_smem();
-            named_sync(1, kMathThreads);
-            if (mt == 0) {
+            named_sync(kBarE, kGroupThreads);
+            if (gt == 0) {
                 mbar_arrive(bar(BAR_OEMPTY));
 #pragma unroll
                 for (int blk = 0; blk < 3; ++blk)
-                    tma_store_4d(&tm_o, base + kOffP + blk * kBlk, kDvHalf * half + 32 * blk, h, t0, b);
+                    tma_store_4d(&tm_o, base + kOffOut + blk * kBlk, kDvHalf * half + 32 * blk, h, t0, b);
                 tma_store_commit();
             }
         }
-        if (mt == 0) tma_store_wait_all();
+        if (gt == 0) tma_store_wait_all();
     }
 
     tc_fence_before();
