@@ -17,33 +17,39 @@
 // TMEM for the whole sequence. Sibling CTAs (the two dv halves of one head)
 // are adjacent in the grid, so the second read of q and k hits L2.
 //
-// Warp roles (320 threads):
+// Warp roles (448 threads):
 //   warp 0      TMA producer: Q, K, V tiles of chunk c into stage c%2
-//   warp 1      TMEM owner and MMA issuer
-//   warps 2-5   "P group": A -> P = bf16(A .* D) into TMEM; Q and K scaled
-//               in place by lambda^(i+1) and lambda^(Cc-1-j)
-//   warps 6-9   "E group": the state hand-off (bf16 copy of S for the next
+//   warp 1      TMEM owner and MMA issuer (a non-blocking event loop)
+//   warps 2-9   "P group", two warps per TMEM lane quadrant:
+//                 sub-group 0 (warps 2-5) scales K in place by lambda^(Cc-1-j)
+//                 and signals it at once, then builds the even 32-column
+//                 blocks of P = bf16(A .* D);
+//                 sub-group 1 (warps 6-9) scales Q in place by lambda^(i+1)
+//                 and builds the odd blocks of P.
+//               Blocks of P above the diagonal are zero and are written once;
+//               only the diagonal block is masked.
+//   warps 10-13 "E group": the state hand-off (bf16 copy of S for the next
 //               chunk's Q~ S, S <- lambda^C' S in TMEM, hT at the end) and the
 //               output epilogue (O * scale -> bf16 -> smem -> TMA store)
-// Each element-wise group has one thread per TMEM lane (= tile row).
 //
 // TMEM (512 columns): R0, R1 = [0,128), [128,256) hold A = Q K^T of chunk c
 // in R[c%2], then that chunk's O (first 96 columns); S = [256,352) fp32;
 // P0, P1 = [352,416), [416,480) bf16 pairs, the A operand of P V.
-// MMA issue order per chunk c (one thread):
-//   MMA1(c+1) into R[(c+1)%2]            -- before waiting on chunk c's P,
-//   MMA2(c)  R[c%2]  = Q~ S_prev          so the next Q K^T overlaps it
-//   MMA4(c)  S      += K~^T V      -> state ready (E group)
-//   MMA3(c)  R[c%2] += P V          -> output ready (E group)
-// The serial chain per chunk is MMA2 + MMA4 + the state hand-off; the P
-// computation of the next chunk runs beside the hand-off.
+// The issuer runs three kinds of events per chunk c as soon as their inputs
+// are ready (in chunk order within each kind):
+//   QK(c)    MMA1  R[c%2]  = Q K^T                (tiles landed, R[c%2] free)
+//   ST(c)    MMA4  S      += K~^T V   -> state    (K~ scaled, S rescaled)
+//   OUT(c)   MMA2  R[c%2]  = Q~ S_prev
+//            MMA3  R[c%2] += P V      -> output   (P built, Q~ scaled)
+// with ST(c) before OUT(c) before ST(c+1). The serial chain per chunk is
+// ST + the state hand-off; P and the output run beside it.
 //
 // Shared-memory operand layouts (64-byte swizzle, 32-column blocks of
 // 128 rows x 64 B): Q, K, V tiles [token][d] are K-major for Q K^T and
 // Q~ S and MN-major for the state update (K~^T as A; the fourth dk block of
 // K is a zero block, padding dk = 96 to M = 128) and for P V (V as B); the
 // bf16 S_prev copy [dk][dv] is an MN-major B operand (96-row blocks,
-// double-buffered so the hand-off of chunk c can run while MMA2(c+1) still
+// double-buffered so the hand-off of chunk c can run while MMA2(c) still
 // waits for P).
 #include <cuda.h>
 
@@ -58,9 +64,9 @@ namespace {
 using namespace ptx;
 
 constexpr int kDk = 96, kDv = 192, kDvHalf = 96;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr uint32_t kGroupThreads = 128;
-constexpr uint32_t kBarP = 1, kBarE = 2;             // named barriers of the two groups
+constexpr uint32_t kBarP0 = 1, kBarP1 = 2, kBarE = 3;  // named barriers of the three 128-thread groups
 
 constexpr uint32_t kBlk = 128 * 64;                  // [128 rows][32 bf16] block = 8 KB
 constexpr uint32_t kStageQ = 0;                      // 3 blocks
@@ -72,11 +78,12 @@ constexpr uint32_t kSbBytes = 3 * kSbBlk;
 constexpr uint32_t kOffSb = 2 * kStageBytes;         // two S_prev copies
 constexpr uint32_t kOffOut = kOffSb + 2 * kSbBytes;  // output staging, 3 blocks
 constexpr uint32_t kOffPw = kOffOut + 3 * kBlk;      // lambda^n, n = 0..128 (+pad)
-enum { BAR_FULL0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_MMA1_0, BAR_MMA1_1, BAR_PREADY0, BAR_PREADY1, BAR_SBREADY,
-       BAR_SFULL, BAR_OFULL0, BAR_OFULL1, BAR_OEMPTY, BAR_DONE, kNumBars };
+enum { BAR_FULL0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_QK0, BAR_QK1, BAR_KREADY0, BAR_KREADY1,
+       BAR_PREADY0, BAR_PREADY1, BAR_SBREADY, BAR_SFULL, BAR_OFULL0, BAR_OFULL1, BAR_OEMPTY0, BAR_OEMPTY1,
+       BAR_DONE, kNumBars };
 constexpr uint32_t kOffBar = kOffPw + 132 * 4;
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, 2+2 decision slots
-constexpr uint32_t kSmemUsed = kOffMisc + 24;
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, 3 x 2 decision slots
+constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
@@ -91,19 +98,21 @@ struct FwdTcArgs {
     unsigned int *status;
 };
 
-// Multiply the 32 bf16 values of one 64-byte row in place by w. The 64-byte
-// swizzle only permutes the row's 16-byte chunks, so the row is scaled as is.
-__device__ __forceinline__ void scale_row64(uint32_t row_addr, float w) {
+// Multiply the 32 bf16 values of row `row` of a 64-byte-swizzled block in
+// place by w. The chunks are visited in swizzled order so that the 32 rows a
+// warp touches at once fall in distinct banks.
+__device__ __forceinline__ void scale_row64(uint32_t blk_addr, uint32_t row, float w) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        uint4 v = ld_shared_v4(row_addr + 16 * c);
+        const uint32_t addr = blk_addr + sw64_offset(row, (uint32_t)c);
+        uint4 v = ld_shared_v4(addr);
         uint32_t *u = reinterpret_cast<uint32_t *>(&v);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             float2 f = unpack_bf16x2(u[e]);
             u[e] = pack_bf16x2(f.x * w, f.y * w);
         }
-        st_shared_v4(row_addr + 16 * c, v.x, v.y, v.z, v.w);
+        st_shared_v4(addr, v.x, v.y, v.z, v.w);
     }
 }
 
@@ -150,15 +159,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
-    volatile int *decP = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);
-    volatile int *decE = reinterpret_cast<volatile int *>(sm + kOffMisc + 16);
+    volatile int *dec = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);   // [3][2]
     const WaitCtl ctl{abort_flag, a.status};
     auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        decP[0] = decP[1] = decE[0] = decE[1] = 0;
-        for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < 6; ++i) dec[i] = 0;
+        for (int i = 0; i < kNumBars; ++i)
+            mbar_init(bar(i), (i == BAR_PREADY0 || i == BAR_PREADY1) ? 2u : 1u);
         fence_mbar_init();
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
@@ -218,118 +227,166 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c)
             lane0_wait(bar(BAR_FULL0 + (c & 1)), (c >> 1) & 1, ctl, lane);
     } else if (warp == 1) {
-        // --------------------------------------------------------- MMA issuer
-        const uint32_t idA = idesc_bf16(128, C, false, false);
-        const uint32_t idO = idesc_bf16(128, kDvHalf, false, true);
-        const uint32_t idS = idesc_bf16(128, kDvHalf, true, true);
-        // MMA1(c): A = Q K^T into R[c%2], once its tiles landed and R[c%2]
-        // is free (the epilogue of chunk c-2 read its output).
-        auto issue_qk = [&](int c) -> bool {
-            const int s = c & 1;
-            if (!lane0_wait(bar(BAR_FULL0 + s), (c >> 1) & 1, ctl, lane)) return false;
-            if (c >= 2 && !lane0_wait(bar(BAR_OEMPTY), (c - 2) & 1, ctl, lane)) return false;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t st = base + (uint32_t)s * kStageBytes;
+        // ----------------------------------------------- MMA issuer (event loop)
+        if (lane == 0) {
+            const uint32_t idA = idesc_bf16(128, C, false, false);
+            const uint32_t idO = idesc_bf16(128, kDvHalf, false, true);
+            const uint32_t idS = idesc_bf16(128, kDvHalf, true, true);
+            int q1 = 0, q4 = 0, q23 = 0;   // next chunk of each event kind
+            uint64_t t_idle = globaltimer_ns();
+            uint32_t spins = 0;
+            while (q23 < nck) {
+                bool progress = false;
+                // QK(c): tiles landed and R[c%2] released by the epilogue of chunk c-2
+                if (q1 < nck) {
+                    const int c = q1, s = c & 1;
+                    if (mbar_test(bar(BAR_FULL0 + s), (c >> 1) & 1) &&
+                        (c < 2 || mbar_test(bar(BAR_OEMPTY0 + s), ((c - 2) >> 1) & 1))) {
+                        tc_fence_after();
+                        const uint32_t st = base + (uint32_t)s * kStageBytes;
 #pragma unroll
-                for (int ks = 0; ks < 6; ++ks) {
-                    const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
-                    mma_bf16_ss(tmem + kColR + 128u * s, smem_desc(st + kStageQ + off, 16, 512, 4),
-                                smem_desc(st + kStageK + off, 16, 512, 4), idA, ks > 0);
+                        for (int ks = 0; ks < 6; ++ks) {
+                            const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
+                            mma_bf16_ss(tmem + kColR + 128u * s, smem_desc(st + kStageQ + off, 16, 512, 4),
+                                        smem_desc(st + kStageK + off, 16, 512, 4), idA, ks > 0);
+                        }
+                        mma_commit(bar(BAR_QK0 + s));
+                        ++q1;
+                        progress = true;
+                    }
                 }
-                mma_commit(bar(BAR_MMA1_0 + s));
-            }
-            __syncwarp();
-            return true;
-        };
-        bool ok = issue_qk(0);
-        for (int c = 0; ok && c < nck; ++c) {
-            const int s = c & 1;
-            const uint32_t st = base + (uint32_t)s * kStageBytes;
-            if (c + 1 < nck && !issue_qk(c + 1)) break;
-            if (!lane0_wait(bar(BAR_PREADY0 + s), (c >> 1) & 1, ctl, lane)) break;
-            if (!lane0_wait(bar(BAR_SBREADY), c & 1, ctl, lane)) break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t dR = tmem + kColR + 128u * s;
-                const uint32_t sb = base + kOffSb + (uint32_t)s * kSbBytes;
-                // MMA2: O = Q~ S_prev over dk
+                // ST(c): S += K~^T V once K~ is scaled and S rescaled; after OUT(c-1)
+                if (q4 < q1 && q4 <= q23) {
+                    const int c = q4, s = c & 1;
+                    if (mbar_test(bar(BAR_KREADY0 + s), (c >> 1) & 1) && mbar_test(bar(BAR_SBREADY), c & 1)) {
+                        tc_fence_after();
+                        const uint32_t st = base + (uint32_t)s * kStageBytes;
+                        for (int ks = 0; ks < ksteps_tok; ++ks)
+                            mma_bf16_ss(tmem + kColS, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
+                                        smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
+                        mma_commit(bar(BAR_SFULL));
+                        ++q4;
+                        progress = true;
+                    }
+                }
+                // OUT(c): O = Q~ S_prev + P V once P is built and Q~ scaled
+                if (q23 < q4) {
+                    const int c = q23, s = c & 1;
+                    if (mbar_test(bar(BAR_PREADY0 + s), (c >> 1) & 1)) {
+                        tc_fence_after();
+                        const uint32_t st = base + (uint32_t)s * kStageBytes;
+                        const uint32_t dR = tmem + kColR + 128u * s;
+                        const uint32_t sb = base + kOffSb + (uint32_t)s * kSbBytes;
 #pragma unroll
-                for (int ks = 0; ks < 6; ++ks) {
-                    const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
-                    mma_bf16_ss(dR, smem_desc(st + kStageQ + off, 16, 512, 4),
-                                smem_desc(sb + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
+                        for (int ks = 0; ks < 6; ++ks) {
+                            const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
+                            mma_bf16_ss(dR, smem_desc(st + kStageQ + off, 16, 512, 4),
+                                        smem_desc(sb + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
+                        }
+                        for (int ks = 0; ks < ksteps_tok; ++ks)
+                            mma_bf16_ts(dR, tmem + kColP + 64u * s + 8u * (uint32_t)ks,
+                                        smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idO, 1);
+                        mma_commit(bar(BAR_OFULL0 + s));
+                        mma_commit(bar(BAR_EMPTY0 + s));
+                        ++q23;
+                        progress = true;
+                    }
                 }
-                // MMA4: S += K~^T V over the chunk's tokens
-                for (int ks = 0; ks < ksteps_tok; ++ks)
-                    mma_bf16_ss(tmem + kColS, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
-                                smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
-                mma_commit(bar(BAR_SFULL));
-                // MMA3: O += P V (P from TMEM)
-                for (int ks = 0; ks < ksteps_tok; ++ks)
-                    mma_bf16_ts(dR, tmem + kColP + 64u * s + 8u * (uint32_t)ks,
-                                smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idO, 1);
-                mma_commit(bar(BAR_OFULL0 + s));
-                mma_commit(bar(BAR_EMPTY0 + s));
+                if (progress) {
+                    t_idle = globaltimer_ns();
+                    spins = 0;
+                } else if ((++spins & 255u) == 0) {
+                    if (*abort_flag) break;
+                    if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        atomicOr(a.status, kDevTimeout);
+                        break;
+                    }
+                }
             }
-            __syncwarp();
+            // Every MMA issued must be complete before TMEM is released.
+            mma_commit(bar(BAR_DONE));
         }
-        // Every MMA issued must be complete before TMEM is released.
-        if (lane == 0) mma_commit(bar(BAR_DONE));
         __syncwarp();
         lane0_wait(bar(BAR_DONE), 0, ctl, lane);
-    } else if (warp < 6) {
-        // ------------------------------------------------- P group (2..5)
+    } else if (warp < 10) {
+        // ------------------------------------------------- P group (2..9)
         const uint32_t quad = (uint32_t)(warp & 3);
+        const uint32_t sub = (uint32_t)(warp - 2) >> 2;            // 0: K + even blocks, 1: Q + odd blocks
         const uint32_t row = quad * 32 + (uint32_t)lane;          // TMEM lane = token row
-        const uint32_t gt = (uint32_t)threadIdx.x - 64;            // 0..127
+        const uint32_t gt = (uint32_t)threadIdx.x - 64 - 128 * sub;  // 0..127 within the sub-group
+        const uint32_t named = sub ? kBarP1 : kBarP0;
+        volatile int *mydec = dec + 2 * sub;
         const uint32_t tl = tmem + ((quad * 32) << 16);
+        const int nblk = C / 32;
+        const int diag = (int)quad;                               // block holding this warp's diagonal
         uint32_t kw = 0;
+        // P blocks above the diagonal are zero for every chunk: write them once.
+        {
+            uint32_t z[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) z[e] = 0u;
+            for (int blk = diag + 1 + (int)sub; blk < 4; blk += 2) {
+                tmem_st_16cols(tl + kColP + 16u * blk, z);
+                tmem_st_16cols(tl + kColP + 64u + 16u * blk, z);
+            }
+            tmem_st_wait();
+        }
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
             const uint32_t st = base + (uint32_t)s * kStageBytes;
             const int Cc = min(C, T - c * C);
-            if (!group_wait(bar(BAR_MMA1_0 + s), (c >> 1) & 1, ctl, decP, gt, kBarP, kw)) break;
+            if (!group_wait(bar(BAR_QK0 + s), (c >> 1) & 1, ctl, mydec, gt, named, kw)) break;
             tc_fence_after();
-            // P = bf16((Q K^T) .* D), row i = row, packed pairs into TMEM P[c%2].
-            for (int blk = 0; blk < C / 32; ++blk) {
+            if (sub == 0) {
+                // K~ = diag(lambda^(Cc-1-j)) K (zero past the end of the sequence); signalled at once.
+                const float wk = row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f;
+#pragma unroll
+                for (int blk = 0; blk < 3; ++blk) scale_row64(st + kStageK + blk * kBlk, row, wk);
+                fence_proxy_async_smem();
+                named_sync(named, kGroupThreads);
+                if (gt == 0) mbar_arrive(bar(BAR_KREADY0 + s));
+            } else {
+                // Q~ = diag(lambda^(i+1)) Q
+                const float wq = pw[row + 1];
+#pragma unroll
+                for (int blk = 0; blk < 3; ++blk) scale_row64(st + kStageQ + blk * kBlk, row, wq);
+            }
+            // P = bf16((Q K^T) .* D) for this sub-group's blocks at or below the diagonal.
+            // Tokens past the end of a ragged chunk have zero q and k, so A is zero there.
+            for (int blk = (int)sub; blk < nblk && blk <= diag; blk += 2) {
                 uint32_t r[32];
+                uint32_t pk[16];
                 tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, r);
                 tmem_ld_wait();
-                uint32_t pk[16];
+                const int n0 = (int)row - 32 * blk;    // lambda exponent of column 0 of the block
+                if (blk < diag) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int j = blk * 32 + e;
-                    const int n = (int)row - j;
-                    const float x0 = (n >= 0 && j < Cc) ? __uint_as_float(r[e]) * pw[n] : 0.f;
-                    const float x1 = (n >= 1 && j + 1 < Cc) ? __uint_as_float(r[e + 1]) * pw[n - 1] : 0.f;
-                    pk[e >> 1] = pack_bf16x2(x0, x1);
+                    for (int e = 0; e < 32; e += 2)
+                        pk[e >> 1] = pack_bf16x2(__uint_as_float(r[e]) * pw[n0 - e],
+                                                 __uint_as_float(r[e + 1]) * pw[n0 - e - 1]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const float x0 = (n0 - e >= 0) ? __uint_as_float(r[e]) * pw[max(n0 - e, 0)] : 0.f;
+                        const float x1 = (n0 - e - 1 >= 0) ? __uint_as_float(r[e + 1]) * pw[max(n0 - e - 1, 0)] : 0.f;
+                        pk[e >> 1] = pack_bf16x2(x0, x1);
+                    }
                 }
-                // 32 tokens = 16 packed columns of P[c%2]
                 tmem_st_16cols(tl + kColP + 64u * s + 16u * blk, pk);
             }
             tmem_st_wait();
-            // In-place decay scaling of this row of Q (lambda^(i+1)) and K
-            // (lambda^(Cc-1-j), zero past the end of the sequence).
-            {
-                const float wq = pw[row + 1];
-                const float wk = row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f;
-#pragma unroll
-                for (int blk = 0; blk < 3; ++blk) {
-                    scale_row64(st + kStageQ + blk * kBlk + row * 64, wq);
-                    scale_row64(st + kStageK + blk * kBlk + row * 64, wk);
-                }
-            }
             fence_proxy_async_smem();
             tc_fence_before();
-            named_sync(kBarP, kGroupThreads);
+            named_sync(named, kGroupThreads);
             if (gt == 0) mbar_arrive(bar(BAR_PREADY0 + s));
         }
     } else {
-        // ------------------------------------------------- E group (6..9)
+        // ------------------------------------------------- E group (10..13)
         const uint32_t quad = (uint32_t)(warp & 3);
         const uint32_t row = quad * 32 + (uint32_t)lane;
-        const uint32_t gt = (uint32_t)threadIdx.x - 192;           // 0..127
+        const uint32_t gt = (uint32_t)threadIdx.x - 320;           // 0..127
+        volatile int *mydec = dec + 4;
         const uint32_t tl = tmem + ((quad * 32) << 16);
         uint32_t kw = 0;
         // Initial state: S_prev copy 0 = bf16(h0 slice), TMEM S = lambda^C0 * h0.
@@ -364,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = c & 1;
             const int t0 = c * C;
             // State hand-off (rows 0..95 = quadrants 0..2).
-            if (!group_wait(bar(BAR_SFULL), c & 1, ctl, decE, gt, kBarE, kw)) break;
+            if (!group_wait(bar(BAR_SFULL), c & 1, ctl, mydec, gt, kBarE, kw)) break;
             tc_fence_after();
             const bool last = (c == nck - 1);
             if (quad < 3) {
@@ -402,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (gt == 0 && !last) mbar_arrive(bar(BAR_SBREADY));
 
             // Output tile: O * scale -> bf16 -> staging -> TMA store.
-            if (!group_wait(bar(BAR_OFULL0 + s), (c >> 1) & 1, ctl, decE, gt, kBarE, kw)) break;
+            if (!group_wait(bar(BAR_OFULL0 + s), (c >> 1) & 1, ctl, mydec, gt, kBarE, kw)) break;
             tc_fence_after();
             if (gt == 0) tma_store_wait_read_all();   // staging free (store of chunk c-1 read it)
             named_sync(kBarE, kGroupThreads);
@@ -420,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             named_sync(kBarE, kGroupThreads);
             if (gt == 0) {
-                mbar_arrive(bar(BAR_OEMPTY));
+                mbar_arrive(bar(BAR_OEMPTY0 + s));
 #pragma unroll
                 for (int blk = 0; blk < 3; ++blk)
                     tma_store_4d(&tm_o, base + kOffOut + blk * kBlk, kDvHalf * half + 32 * blk, h, t0, b);
