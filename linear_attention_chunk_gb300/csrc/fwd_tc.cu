@@ -78,7 +78,7 @@ constexpr uint32_t kSbBytes = 3 * kSbBlk;
 constexpr uint32_t kOffSb = 2 * kStageBytes;         // two S_prev copies
 constexpr uint32_t kOffOut = kOffSb + 2 * kSbBytes;  // output staging, 3 blocks
 constexpr uint32_t kOffPw = kOffOut + 3 * kBlk;      // lambda^n, n = 0..128 (+pad)
-enum { BAR_FULL0, BAR_FULL1, BAR_EMPTY0, BAR_EMPTY1, BAR_QK0, BAR_QK1, BAR_KREADY0, BAR_KREADY1,
+enum { BAR_FULL0, BAR_FULL1, BAR_FULLV0, BAR_FULLV1, BAR_EMPTY0, BAR_EMPTY1, BAR_QK0, BAR_QK1, BAR_KREADY0, BAR_KREADY1,
        BAR_PREADY0, BAR_PREADY1, BAR_SBREADY, BAR_SFULL, BAR_OFULL0, BAR_OFULL1, BAR_OEMPTY0, BAR_OEMPTY1,
        BAR_DONE, kNumBars };
 constexpr uint32_t kOffBar = kOffPw + 132 * 4;
@@ -98,31 +98,78 @@ struct FwdTcArgs {
     unsigned int *status;
 };
 
-// Multiply the 32 bf16 values of row `row` of a 64-byte-swizzled block in
-// place by w. The chunks are visited in swizzled order so that the 32 rows a
-// warp touches at once fall in distinct banks.
-__device__ __forceinline__ void scale_row64(uint32_t blk_addr, uint32_t row, float w) {
+// Multiply row `row` of the three 64-byte-swizzled blocks at blk0 (stride
+// kBlk) in place by w: 12 16-byte loads first, then 12 stores, so the loads
+// overlap. The 64-byte swizzle only permutes a row's chunks, so a row is
+// scaled as it lies; chunks are visited in swizzled order so that the 32 rows
+// a warp touches at once fall in distinct banks.
+__device__ __forceinline__ void scale_rows3(unsigned char *blk0, uint32_t row, float w) {
+#pragma unroll
+    for (int h6 = 0; h6 < 12; h6 += 6) {
+        uint4 v[6];
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            const int k = h6 + i;
+            v[i] = *reinterpret_cast<const uint4 *>(blk0 + (k >> 2) * kBlk + sw64_offset(row, (uint32_t)(k & 3)));
+        }
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            uint32_t *u = reinterpret_cast<uint32_t *>(&v[i]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float2 f = unpack_bf16x2(u[e]);
+                u[e] = pack_bf16x2(f.x * w, f.y * w);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            const int k = h6 + i;
+            *reinterpret_cast<uint4 *>(blk0 + (k >> 2) * kBlk + sw64_offset(row, (uint32_t)(k & 3))) = v[i];
+        }
+    }
+}
+
+// Write 32 fp32 values (raw bits, times mul) as bf16 into row `row` of a
+// 64-byte-swizzled block.
+__device__ __forceinline__ void write_row_sw64_bits(unsigned char *blk, uint32_t row, const uint32_t (&r)[32],
+                                                    float mul) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint32_t addr = blk_addr + sw64_offset(row, (uint32_t)c);
-        uint4 v = ld_shared_v4(addr);
-        uint32_t *u = reinterpret_cast<uint32_t *>(&v);
+        uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float2 f = unpack_bf16x2(u[e]);
-            u[e] = pack_bf16x2(f.x * w, f.y * w);
-        }
-        st_shared_v4(addr, v.x, v.y, v.z, v.w);
+        for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(r[8 * c + 2 * e]) * mul, __uint_as_float(r[8 * c + 2 * e + 1]) * mul);
+        *reinterpret_cast<uint4 *>(blk + sw64_offset(row, c)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
 // Write 32 fp32 values as bf16 into row `row` of a 64-byte-swizzled block.
-__device__ __forceinline__ void write_row_sw64(uint32_t blk_addr, uint32_t row, const float (&x)[32]) {
+__device__ __forceinline__ void write_row_sw64(unsigned char *blk, uint32_t row, const float (&x)[32]) {
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-        st_shared_v4(blk_addr + sw64_offset(row, c), pack_bf16x2(x[8 * c + 0], x[8 * c + 1]),
-                     pack_bf16x2(x[8 * c + 2], x[8 * c + 3]), pack_bf16x2(x[8 * c + 4], x[8 * c + 5]),
-                     pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+        *reinterpret_cast<uint4 *>(blk + sw64_offset(row, c)) =
+            make_uint4(pack_bf16x2(x[8 * c + 0], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
+                       pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+}
+
+// One 32-column block of P for one row: x_j * lambda^(n0 - j) (n0 = i - j0),
+// masked to j <= i on the diagonal block, packed to bf16 pairs in TMEM.
+__device__ __forceinline__ void build_p_block(const uint32_t (&r)[32], int n0, bool diagonal, uint32_t taddr,
+                                              const float *pw) {
+    uint32_t pk[16];
+    if (!diagonal) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+            pk[e >> 1] = pack_bf16x2(__uint_as_float(r[e]) * pw[n0 - e], __uint_as_float(r[e + 1]) * pw[n0 - e - 1]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const float x0 = (n0 - e >= 0) ? __uint_as_float(r[e]) * pw[max(n0 - e, 0)] : 0.f;
+            const float x1 = (n0 - e - 1 >= 0) ? __uint_as_float(r[e + 1]) * pw[max(n0 - e - 1, 0)] : 0.f;
+            pk[e >> 1] = pack_bf16x2(x0, x1);
+        }
+    }
+    tmem_st_16cols(taddr, pk);
 }
 
 // One elected thread of a 128-thread group waits on an mbarrier; the verdict
@@ -146,8 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                       const FwdTcArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                          ~static_cast<uintptr_t>(1023));
+    // 1024-byte aligned base, derived from the shared array by pointer
+    // arithmetic so that accesses through it stay shared-memory accesses.
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = smem_u32(sm);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int half = blockIdx.x & 1;
@@ -203,29 +251,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
-        const uint32_t tx_bytes = 9u * (uint32_t)C * 64u;
+        const uint32_t tx_qk = 6u * (uint32_t)C * 64u, tx_v = 3u * (uint32_t)C * 64u;
         int issued = 0;
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
             if (c >= 2 && !lane0_wait(bar(BAR_EMPTY0 + s), ((c >> 1) - 1) & 1, ctl, lane)) break;
             if (lane == 0) {
                 const uint32_t st = base + (uint32_t)s * kStageBytes;
-                const uint32_t fb = bar(BAR_FULL0 + s);
-                mbar_arrive_expect_tx(fb, tx_bytes);
+                const uint32_t fb = bar(BAR_FULL0 + s), fv = bar(BAR_FULLV0 + s);
+                mbar_arrive_expect_tx(fb, tx_qk);
+                mbar_arrive_expect_tx(fv, tx_v);
                 const int t0 = c * C;
+                // Q and K first: Q K^T can start before V has landed.
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {
                     tma_load_4d(st + kStageQ + j * kBlk, &tm_q, fb, 32 * j, h, t0, b);
                     tma_load_4d(st + kStageK + j * kBlk, &tm_k, fb, 32 * j, h, t0, b);
-                    tma_load_4d(st + kStageV + j * kBlk, &tm_v, fb, kDvHalf * half + 32 * j, h, t0, b);
                 }
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    tma_load_4d(st + kStageV + j * kBlk, &tm_v, fv, kDvHalf * half + 32 * j, h, t0, b);
             }
             __syncwarp();
             issued = c + 1;
         }
         // Drain: every load issued must have landed before the CTA exits.
-        for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c)
+        for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c) {
             lane0_wait(bar(BAR_FULL0 + (c & 1)), (c >> 1) & 1, ctl, lane);
+            lane0_wait(bar(BAR_FULLV0 + (c & 1)), (c >> 1) & 1, ctl, lane);
+        }
     } else if (warp == 1) {
         // ----------------------------------------------- MMA issuer (event loop)
         if (lane == 0) {
@@ -258,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ST(c): S += K~^T V once K~ is scaled and S rescaled; after OUT(c-1)
                 if (q4 < q1 && q4 <= q23) {
                     const int c = q4, s = c & 1;
-                    if (mbar_test(bar(BAR_KREADY0 + s), (c >> 1) & 1) && mbar_test(bar(BAR_SBREADY), c & 1)) {
+                    if (mbar_test(bar(BAR_KREADY0 + s), (c >> 1) & 1) && mbar_test(bar(BAR_SBREADY), c & 1) &&
+                        mbar_test(bar(BAR_FULLV0 + s), (c >> 1) & 1)) {
                         tc_fence_after();
                         const uint32_t st = base + (uint32_t)s * kStageBytes;
                         for (int ks = 0; ks < ksteps_tok; ++ks)
@@ -341,39 +396,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (sub == 0) {
                 // K~ = diag(lambda^(Cc-1-j)) K (zero past the end of the sequence); signalled at once.
                 const float wk = row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f;
-#pragma unroll
-                for (int blk = 0; blk < 3; ++blk) scale_row64(st + kStageK + blk * kBlk, row, wk);
+                scale_rows3(sm + (uint32_t)s * kStageBytes + kStageK, row, wk);
                 fence_proxy_async_smem();
                 named_sync(named, kGroupThreads);
                 if (gt == 0) mbar_arrive(bar(BAR_KREADY0 + s));
             } else {
                 // Q~ = diag(lambda^(i+1)) Q
                 const float wq = pw[row + 1];
-#pragma unroll
-                for (int blk = 0; blk < 3; ++blk) scale_row64(st + kStageQ + blk * kBlk, row, wq);
+                scale_rows3(sm + (uint32_t)s * kStageBytes + kStageQ, row, wq);
             }
-            // P = bf16((Q K^T) .* D) for this sub-group's blocks at or below the diagonal.
+            // P = bf16((Q K^T) .* D) for this sub-group's blocks at or below the diagonal
+            // (at most two per warp; both TMEM loads are issued before one wait).
             // Tokens past the end of a ragged chunk have zero q and k, so A is zero there.
-            for (int blk = (int)sub; blk < nblk && blk <= diag; blk += 2) {
-                uint32_t r[32];
-                uint32_t pk[16];
-                tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, r);
+            {
+                const int b0 = (int)sub, b1 = (int)sub + 2;
+                const bool has0 = b0 < nblk && b0 <= diag, has1 = b1 < nblk && b1 <= diag;
+                uint32_t r0[32], r1[32];
+                if (has0) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b0, r0);
+                if (has1) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b1, r1);
                 tmem_ld_wait();
-                const int n0 = (int)row - 32 * blk;    // lambda exponent of column 0 of the block
-                if (blk < diag) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2)
-                        pk[e >> 1] = pack_bf16x2(__uint_as_float(r[e]) * pw[n0 - e],
-                                                 __uint_as_float(r[e + 1]) * pw[n0 - e - 1]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float x0 = (n0 - e >= 0) ? __uint_as_float(r[e]) * pw[max(n0 - e, 0)] : 0.f;
-                        const float x1 = (n0 - e - 1 >= 0) ? __uint_as_float(r[e + 1]) * pw[max(n0 - e - 1, 0)] : 0.f;
-                        pk[e >> 1] = pack_bf16x2(x0, x1);
-                    }
-                }
-                tmem_st_16cols(tl + kColP + 64u * s + 16u * blk, pk);
+                if (has0) build_p_block(r0, (int)row - 32 * b0, b0 == diag, tl + kColP + 64u * s + 16u * b0, pw);
+                if (has1) build_p_block(r1, (int)row - 32 * b1, b1 == diag, tl + kColP + 64u * s + 16u * b1, pw);
             }
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -405,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                         x[e] = v4.x; x[e + 1] = v4.y; x[e + 2] = v4.z; x[e + 3] = v4.w;
                     }
-                    write_row_sw64(base + kOffSb + blk * kSbBlk, row, x);
+                    write_row_sw64(sm + kOffSb + blk * kSbBlk, row, x);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(x[e] * w0);
                     tmem_st_32cols(tl + kColS + blk * 32, r);
@@ -426,31 +469,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool last = (c == nck - 1);
             if (quad < 3) {
                 const float wn = last ? 1.f : pw[min(C, T - t0 - C)];
-                const uint32_t sb_next = base + kOffSb + (uint32_t)(s ^ 1) * kSbBytes;
+                unsigned char *sb_next = sm + kOffSb + (uint32_t)(s ^ 1) * kSbBytes;
                 float *dst = (last && a.hT) ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
                                             : nullptr;
-#pragma unroll
-                for (int blk = 0; blk < 3; ++blk) {
-                    uint32_t r[32];
-                    float x[32];
-                    tmem_ld_32cols(tl + kColS + blk * 32, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]);
+                // Three 32-column blocks; the next block's TMEM load overlaps this one's work.
+                auto handle = [&](uint32_t (&r)[32], int blk) {
                     if (last) {
                         if (dst) {
 #pragma unroll
                             for (int e = 0; e < 32; e += 4)
                                 *reinterpret_cast<float4 *>(dst + blk * 32 + e) =
-                                    make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                                    make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                                __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
                         }
                     } else {
-                        write_row_sw64(sb_next + blk * kSbBlk, row, x);
+                        write_row_sw64_bits(sb_next + blk * kSbBlk, row, r, 1.f);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(x[e] * wn);
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * wn);
                         tmem_st_32cols(tl + kColS + blk * 32, r);
                     }
-                }
+                };
+                uint32_t ra[32], rb[32];
+                tmem_ld_32cols(tl + kColS, ra);
+                tmem_ld_wait();
+                tmem_ld_32cols(tl + kColS + 32, rb);
+                handle(ra, 0);
+                tmem_ld_wait();
+                tmem_ld_32cols(tl + kColS + 64, ra);
+                handle(rb, 1);
+                tmem_ld_wait();
+                handle(ra, 2);
                 tmem_st_wait();
             }
             fence_proxy_async_smem();
@@ -463,15 +511,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (gt == 0) tma_store_wait_read_all();   // staging free (store of chunk c-1 read it)
             named_sync(kBarE, kGroupThreads);
-#pragma unroll
-            for (int blk = 0; blk < 3; ++blk) {
-                uint32_t r[32];
-                float x[32];
-                tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, r);
+            {
+                const uint32_t src = tl + kColR + 128u * s;
+                auto handle = [&](const uint32_t (&r)[32], int blk) {
+                    write_row_sw64_bits(sm + kOffOut + blk * kBlk, row, r, a.scale);
+                };
+                uint32_t ra[32], rb[32];
+                tmem_ld_32cols(src, ra);
                 tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(r[e]) * a.scale;
-                write_row_sw64(base + kOffOut + blk * kBlk, row, x);
+                tmem_ld_32cols(src + 32, rb);
+                handle(ra, 0);
+                tmem_ld_wait();
+                tmem_ld_32cols(src + 64, ra);
+                handle(rb, 1);
+                tmem_ld_wait();
+                handle(ra, 2);
             }
             tc_fence_before();
             fence_proxy_async_smem();
