@@ -91,9 +91,10 @@ constexpr uint32_t kTmemCols = 512, kColR = 0, kColS = 256, kColP = 352;
 
 struct FwdTcArgs {
     const float *log_lambda;
-    const float *h0;
-    float *hT;
+    const float *h0;       // initial state (times init_mul), or NULL
+    float *hT;             // final state (times final_mul), or NULL
     float scale;
+    float init_mul, final_mul;
     int T, H, C, nck;
     unsigned int *status;
 };
@@ -152,22 +153,27 @@ __device__ __forceinline__ void write_row_sw64(unsigned char *blk, uint32_t row,
                        pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
 }
 
-// One 32-column block of P for one row: x_j * lambda^(n0 - j) (n0 = i - j0),
-// masked to j <= i on the diagonal block, packed to bf16 pairs in TMEM.
+// One 32-column block of P for one row, packed to bf16 pairs in TMEM.
+// Forward: x_j * lambda^(i - j), kept for j <= i; n0 = i - j0.
+// Reverse: x_j * lambda^(j - i), kept for j >= i; n0 = i - j0 as well.
+// Only the diagonal block needs the mask.
+template <bool kRev>
 __device__ __forceinline__ void build_p_block(const uint32_t (&r)[32], int n0, bool diagonal, uint32_t taddr,
                                               const float *pw) {
     uint32_t pk[16];
-    if (!diagonal) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2)
-            pk[e >> 1] = pack_bf16x2(__uint_as_float(r[e]) * pw[n0 - e], __uint_as_float(r[e + 1]) * pw[n0 - e - 1]);
-    } else {
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-            const float x0 = (n0 - e >= 0) ? __uint_as_float(r[e]) * pw[max(n0 - e, 0)] : 0.f;
-            const float x1 = (n0 - e - 1 >= 0) ? __uint_as_float(r[e + 1]) * pw[max(n0 - e - 1, 0)] : 0.f;
-            pk[e >> 1] = pack_bf16x2(x0, x1);
+    for (int e = 0; e < 32; e += 2) {
+        const int d0 = kRev ? e - n0 : n0 - e;          // exponent of column e
+        const int d1 = kRev ? e + 1 - n0 : n0 - e - 1;  // exponent of column e + 1
+        float x0, x1;
+        if (!diagonal) {
+            x0 = __uint_as_float(r[e]) * pw[d0];
+            x1 = __uint_as_float(r[e + 1]) * pw[d1];
+        } else {
+            x0 = d0 >= 0 ? __uint_as_float(r[e]) * pw[max(d0, 0)] : 0.f;
+            x1 = d1 >= 0 ? __uint_as_float(r[e + 1]) * pw[max(d1, 0)] : 0.f;
         }
+        pk[e >> 1] = pack_bf16x2(x0, x1);
     }
     tmem_st_16cols(taddr, pk);
 }
@@ -188,6 +194,13 @@ __device__ __forceinline__ bool lane0_wait(uint32_t bar, uint32_t parity, const 
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// kRev = false: the forward pass. kRev = true: the same chunked recurrence
+// run backwards in time, which is how the backward pass obtains dv and dh0:
+// rows are k tokens, columns q tokens, values dO, the mask keeps col >= row
+// with lambda^(col-row), the row weights swap (lambda^(Cc-1-j) on the
+// readout, lambda^(i+1) on the state update), chunks run last to first, and
+// the state is the state gradient divided by the scale.
+template <bool kRev>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t fb = bar(BAR_FULL0 + s), fv = bar(BAR_FULLV0 + s);
                 mbar_arrive_expect_tx(fb, tx_qk);
                 mbar_arrive_expect_tx(fv, tx_v);
-                const int t0 = c * C;
+                const int t0 = (kRev ? nck - 1 - c : c) * C;
                 // Q and K first: Q K^T can start before V has landed.
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {
@@ -376,12 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nblk = C / 32;
         const int diag = (int)quad;                               // block holding this warp's diagonal
         uint32_t kw = 0;
-        // P blocks above the diagonal are zero for every chunk: write them once.
+        // P blocks on the masked side of the diagonal (above it forward, below
+        // it in reverse) are zero for every chunk: write them once.
         {
             uint32_t z[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) z[e] = 0u;
-            for (int blk = diag + 1 + (int)sub; blk < 4; blk += 2) {
+            for (int blk = (int)sub; blk < 4; blk += 2) {
+                if (kRev ? (blk >= diag) : (blk <= diag)) continue;
                 tmem_st_16cols(tl + kColP + 16u * blk, z);
                 tmem_st_16cols(tl + kColP + 64u + 16u * blk, z);
             }
@@ -390,19 +405,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
             const uint32_t st = base + (uint32_t)s * kStageBytes;
-            const int Cc = min(C, T - c * C);
+            const int Cc = min(C, T - (kRev ? nck - 1 - c : c) * C);
             if (!group_wait(bar(BAR_QK0 + s), (c >> 1) & 1, ctl, mydec, gt, named, kw)) break;
             tc_fence_after();
             if (sub == 0) {
-                // K~ = diag(lambda^(Cc-1-j)) K (zero past the end of the sequence); signalled at once.
-                const float wk = row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f;
+                // K~ = diag(w) K with w = lambda^(Cc-1-j) (zero past the end of the
+                // sequence), or lambda^(i+1) in reverse; signalled at once.
+                const float wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
                 scale_rows3(sm + (uint32_t)s * kStageBytes + kStageK, row, wk);
                 fence_proxy_async_smem();
                 named_sync(named, kGroupThreads);
                 if (gt == 0) mbar_arrive(bar(BAR_KREADY0 + s));
             } else {
-                // Q~ = diag(lambda^(i+1)) Q
-                const float wq = pw[row + 1];
+                // Q~ = diag(lambda^(i+1)) Q, or diag(lambda^(Cc-1-j)) in reverse
+                const float wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
                 scale_rows3(sm + (uint32_t)s * kStageBytes + kStageQ, row, wq);
             }
             // P = bf16((Q K^T) .* D) for this sub-group's blocks at or below the diagonal
@@ -410,13 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Tokens past the end of a ragged chunk have zero q and k, so A is zero there.
             {
                 const int b0 = (int)sub, b1 = (int)sub + 2;
-                const bool has0 = b0 < nblk && b0 <= diag, has1 = b1 < nblk && b1 <= diag;
+                const bool has0 = b0 < nblk && (kRev ? b0 >= diag : b0 <= diag);
+                const bool has1 = b1 < nblk && (kRev ? b1 >= diag : b1 <= diag);
                 uint32_t r0[32], r1[32];
                 if (has0) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b0, r0);
                 if (has1) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b1, r1);
                 tmem_ld_wait();
-                if (has0) build_p_block(r0, (int)row - 32 * b0, b0 == diag, tl + kColP + 64u * s + 16u * b0, pw);
-                if (has1) build_p_block(r1, (int)row - 32 * b1, b1 == diag, tl + kColP + 64u * s + 16u * b1, pw);
+                if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, b0 == diag, tl + kColP + 64u * s + 16u * b0, pw);
+                if (has1) build_p_block<kRev>(r1, (int)row - 32 * b1, b1 == diag, tl + kColP + 64u * s + 16u * b1, pw);
             }
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -432,9 +449,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         volatile int *mydec = dec + 4;
         const uint32_t tl = tmem + ((quad * 32) << 16);
         uint32_t kw = 0;
-        // Initial state: S_prev copy 0 = bf16(h0 slice), TMEM S = lambda^C0 * h0.
+        // Initial state: S_prev copy 0 = bf16(h0 slice), TMEM S = lambda^C0 * h0,
+        // with C0 the length of the first chunk processed.
         {
-            const float w0 = pw[min(C, T)];
+            const float w0 = pw[kRev ? T - (nck - 1) * C : min(C, T)];
             if (quad < 3) {
                 const float *src =
                     a.h0 ? a.h0 + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half : nullptr;
@@ -446,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; e += 4) {
                         float4 v4 = src ? *reinterpret_cast<const float4 *>(src + blk * 32 + e)
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-                        x[e] = v4.x; x[e + 1] = v4.y; x[e + 2] = v4.z; x[e + 3] = v4.w;
+                        x[e] = v4.x * a.init_mul; x[e + 1] = v4.y * a.init_mul;
+                        x[e + 2] = v4.z * a.init_mul; x[e + 3] = v4.w * a.init_mul;
                     }
                     write_row_sw64(sm + kOffSb + blk * kSbBlk, row, x);
 #pragma unroll
@@ -462,13 +481,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
-            const int t0 = c * C;
+            const int t0 = (kRev ? nck - 1 - c : c) * C;
             // State hand-off (rows 0..95 = quadrants 0..2).
             if (!group_wait(bar(BAR_SFULL), c & 1, ctl, mydec, gt, kBarE, kw)) break;
             tc_fence_after();
             const bool last = (c == nck - 1);
             if (quad < 3) {
-                const float wn = last ? 1.f : pw[min(C, T - t0 - C)];
+                // rescale by lambda^(length of the next chunk processed)
+                const float wn = last ? 1.f : (kRev ? pw[C] : pw[min(C, T - t0 - C)]);
                 unsigned char *sb_next = sm + kOffSb + (uint32_t)(s ^ 1) * kSbBytes;
                 float *dst = (last && a.hT) ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
                                             : nullptr;
@@ -478,9 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (dst) {
 #pragma unroll
                             for (int e = 0; e < 32; e += 4)
-                                *reinterpret_cast<float4 *>(dst + blk * 32 + e) =
-                                    make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                                                __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                                *reinterpret_cast<float4 *>(dst + blk * 32 + e) = make_float4(
+                                    __uint_as_float(r[e]) * a.final_mul, __uint_as_float(r[e + 1]) * a.final_mul,
+                                    __uint_as_float(r[e + 2]) * a.final_mul, __uint_as_float(r[e + 3]) * a.final_mul);
                         }
                     } else {
                         write_row_sw64_bits(sb_next + blk * kSbBlk, row, r, 1.f);
@@ -547,6 +567,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// One launch of the chunk kernel: `qm`, `km` are [B,T,H,96] maps, `vm` and
+// `om` [B,T,H,192] maps (box height = chunk).
+template <bool kRev>
+cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
+                                const CUtensorMap &om, const FwdTcArgs &a, int B, cudaStream_t s, int *launches) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gla_fwd_tc_kernel<kRev>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(B * a.H * 2);
+    gla_fwd_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, om, a);
+    if (launches) ++*launches;
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t fwd_tc_workspace_size(int, int, int, int) { return 0; }
@@ -559,13 +593,25 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     if ((e = make_token_map(&mk, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mo, p.o, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gla_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, p.T, p.H, p.chunk, (p.T + p.chunk - 1) / p.chunk, p.status};
-    const unsigned grid = (unsigned)(p.B * p.H * 2);
-    gla_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, a);
-    if (launches) ++*launches;
-    return cudaGetLastError();
+    FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, (p.T + p.chunk - 1) / p.chunk,
+                p.status};
+    return launch_chunk_kernel<false>(mq, mk, mv, mo, a, p.B, s, launches);
+}
+
+// dv and dh0 of the backward pass: the chunk recurrence in reverse time with
+// rows = k, columns = q, values = dO; state = (state gradient) / scale,
+// seeded by dhT / scale.
+cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches) {
+    if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
+    CUtensorMap mrow, mcol, mval, mout;
+    cudaError_t e;
+    if ((e = make_token_map(&mrow, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mcol, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mval, p.do_, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mout, p.dv_out, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    FwdTcArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, p.chunk,
+                (p.T + p.chunk - 1) / p.chunk, p.status};
+    return launch_chunk_kernel<true>(mrow, mcol, mval, mout, a, p.B, s, launches);
 }
 
 }  // namespace gla

@@ -59,6 +59,8 @@ cudaError_t launch_copy_state(const float *src, float *dst, size_t n, cudaStream
 // tcgen05 / TMA tensor-core kernels (bf16, dk = 96, dv = 192).
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
+// dv and dh0 of the backward pass: the chunk kernel run in reverse time.
+cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches);
 size_t fwd_tc_workspace_size(int B, int T, int H, int chunk);
 size_t bwd_tc_workspace_size(int B, int T, int H, int chunk);
 

@@ -1,10 +1,16 @@
-// tc_interim.cu -- bf16 backward routed to the SIMT kernels until the
-// tcgen05 backward kernel is in place.
+// tc_interim.cu -- bf16 backward: dv and dh0 from the reverse-time tensor-core
+// chunk kernel; dq and dk from the SIMT kernels until their tensor-core
+// kernel is in place.
 #include "kernels.h"
 
 namespace gla {
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches) {
-    return launch_bwd_simt(p, true, s, launches);
+    cudaError_t e = launch_bwd_dv_tc(p, s, launches);
+    if (e != cudaSuccess) return e;
+    BwdParams rest = p;
+    rest.dv_out = nullptr;
+    rest.dh0 = nullptr;
+    return launch_bwd_simt(rest, true, s, launches);
 }
 size_t bwd_tc_workspace_size(int, int, int, int) { return 0; }
 }  // namespace gla
