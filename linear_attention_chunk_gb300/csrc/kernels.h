@@ -61,6 +61,9 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // dv and dh0 of the backward pass: the chunk kernel run in reverse time.
 cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches);
+// dq and dk: the transposed-shape chunk kernel (192-wide scores, 96-wide outputs).
+cudaError_t launch_bwd_dq_tc(const BwdParams &p, cudaStream_t s, int *launches);
+cudaError_t launch_bwd_dk_tc(const BwdParams &p, cudaStream_t s, int *launches);
 size_t fwd_tc_workspace_size(int B, int T, int H, int chunk);
 size_t bwd_tc_workspace_size(int B, int T, int H, int chunk);
 
