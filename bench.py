@@ -78,11 +78,14 @@ def committed_traffic(kernel: str):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    src = fields.get("source_file")
-    if not src or "traffic_bytes_per_launch" not in fields:
+    srcs = [x.strip() for x in fields.get("source_files", "").split(",") if x.strip()]
+    if not srcs or "traffic_bytes_per_launch" not in fields:
         return None, None
     try:
-        digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+        h = hashlib.sha256()
+        for src in srcs:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+        digest = h.hexdigest()[:16]
     except OSError:
         return None, None
     if digest != fields.get("source_sha256_16"):
@@ -326,7 +329,7 @@ def e2e_fwd(args, dist, device, stream, c, ll):
 def bench_fwd_bwd(args, dist, device, stream, peaks, sampler):
     import torch
     import linear_attention_chunk_gb300 as gla
-    B, T = 16, 2048
+    B, T = args.batch or 16, 2048
     c = gen.train_fwd_bwd(seed=2, B=B, T=T)
     q, k, v, do = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v, c.do))
     ll = torch.from_numpy(c.log_lambda).to(device)
@@ -372,7 +375,7 @@ def bench_fwd_bwd(args, dist, device, stream, peaks, sampler):
 def bench_decode(args, dist, device, stream, peaks, sampler):
     import torch
     import linear_attention_chunk_gb300 as gla
-    N, L = 1280, 24
+    N, L = 1280, args.layers or 24
     g = torch.Generator(device=device)
     g.manual_seed(3)
     states = []
@@ -406,8 +409,8 @@ def bench_decode(args, dist, device, stream, peaks, sampler):
         "value": N * dist.world * args.steps / (total * 1e-3), "unit": "seq-steps/s",
         "ms_per_step": total / args.steps, "ms_per_layer_step": total / args.steps / L,
         "config": {"workload": f"serving_decode_bf16_N{N}_H16_L{L}", "N": N, "H": H, "layers": L,
-                   "state": "fp32 N(0,0.1), 24 distinct buffers, 36.2 GB",
-                   "l2": "24 distinct 1.5 GB states per step, larger than L2, no flush"},
+                   "state": f"fp32 N(0,0.1), {L} distinct buffers, {L * N * H * STATE_BYTES / 1e9:.1f} GB",
+                   "l2": f"{L} distinct 1.5 GB states per step, larger than L2, no flush"},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ach / peaks["hbm_gbs"], "traffic": committed_traffic("gla_decode")[0],
                      "algorithmic_bytes_per_launch": bytes_, "avg_launch_ms": avg_launch_ms,
@@ -551,7 +554,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gla", "reference"), default="gla")
     ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode"), default="all")
-    ap.add_argument("--batch", type=int, default=0, help="override the forward workload's B (profiling)")
+    ap.add_argument("--batch", type=int, default=0, help="override B of the fwd / fwd_bwd workloads (profiling)")
+    ap.add_argument("--layers", type=int, default=0, help="override the decode layer count (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
