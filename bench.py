@@ -372,6 +372,53 @@ def bench_fwd_bwd(args, dist, device, stream, peaks, sampler):
     return res
 
 
+def bench_long(args, dist, device, stream, peaks, sampler):
+    """Long-context prefill: B=1, H=16, T=65,536, nonzero h0, decay
+    log-uniform in [0.9, 0.9999]; chunk 128 (value) and 64 (reported beside)."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    T = args.long_T or 65536
+    c = gen.long_prefill(seed=4, T=T, chunk=CHUNK)
+    q, k, v = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v))
+    ll = torch.from_numpy(c.log_lambda).to(device)
+    h0 = torch.from_numpy(c.h0).to(device)
+    o = torch.empty((1, T, H, DV), dtype=torch.bfloat16, device=device)
+    hT = torch.empty((1, H, DK, DV), dtype=torch.float32, device=device)
+    out = {}
+    for C in (128, 64):
+        ws = torch.empty(max(gla.gla_chunk_fwd_workspace_size(1, T, H, DK, DV, C), 16), dtype=torch.uint8,
+                         device=device)
+
+        def step():
+            gla.gla_chunk_fwd(q, k, v, ll, h0, c.scale, C, o=o, hT=hT, workspace=ws, stream=stream)
+            return gla.gla_last_launch_count()
+
+        total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+        total = dist.max(total)
+        bytes_, fl_full, _ = fwd_work(1, T, True, True, C=C)
+        avg_ms = statistics.mean(per)
+        ach = bytes_ / (avg_ms * 1e-3) / 1e9
+        out[C] = {
+            "value": T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+            "ms_per_step": total / args.steps,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes_per_call": bytes_, "avg_call_ms": avg_ms,
+                         "launches_per_call": launches // max(args.steps, 1),
+                         "note": "one call = segment-state pass + scan + forward", "peak_source": peaks["source"]},
+            "tensor": {"achieved": fl_full / (avg_ms * 1e-3) / 1e12, "peak": peaks["bf16_tflops"],
+                       "unit": "TFLOP/s", "frac": fl_full / (avg_ms * 1e-3) / 1e12 / peaks["bf16_tflops"]},
+            "gpu_launches": launches,
+            "clocks": sampler.summary(*win) if sampler else None,
+        }
+    res = dict(out[128])
+    res["config"] = {"workload": c.name, "B": 1, "T": T, "H": H, "chunk": 128, "h0": "N(0,0.1)",
+                     "decay": "log-uniform [0.9, 0.9999]",
+                     "l2": f"inputs larger than L2 ({fwd_work(1, T, True, True)[0] / 1e6:.0f} MB per step), no flush"}
+    res["chunk64"] = out[64]
+    return res
+
+
 def bench_decode(args, dist, device, stream, peaks, sampler):
     import torch
     import linear_attention_chunk_gb300 as gla
@@ -553,9 +600,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gla", "reference"), default="gla")
-    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode"), default="all")
+    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long"), default="all")
     ap.add_argument("--batch", type=int, default=0, help="override B of the fwd / fwd_bwd workloads (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the decode layer count (profiling)")
+    ap.add_argument("--long-T", dest="long_T", type=int, default=0, help="override T of the long workload (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -589,6 +637,8 @@ def main(argv=None):
             results["fwd_bwd"] = bench_fwd_bwd(args, dist, device, stream, peaks, sampler)
         if args.mode in ("all", "decode"):
             results["decode"] = bench_decode(args, dist, device, stream, peaks, sampler)
+        if args.mode in ("all", "long"):
+            results["long"] = bench_long(args, dist, device, stream, peaks, sampler)
     finally:
         sampler.stop()
 

@@ -96,6 +96,11 @@ struct FwdTcArgs {
     float scale;
     float init_mul, final_mul;
     int T, H, C, nck;
+    // Sequence segmentation (forward only): the grid covers nseg segments of
+    // seg_chunks chunks; segment g starts from h0 + g * h0_seg_stride and only
+    // the last segment writes hT. nseg = 1 means one chain per (b, h).
+    int nseg, seg_chunks, BH;
+    size_t h0_seg_stride;
     unsigned int *status;
 };
 
@@ -117,9 +122,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = smem_u32(sm);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int half = blockIdx.x & 1;
-    const int bh = blockIdx.x >> 1;
+    const int seg = (blockIdx.x >> 1) / a.BH;
+    const int bh = (blockIdx.x >> 1) % a.BH;
     const int b = bh / a.H, h = bh % a.H;
-    const int C = a.C, T = a.T, nck = a.nck;
+    const int C = a.C, T = a.T;
+    const int cbeg = seg * a.seg_chunks;                          // first chunk of this segment
+    const int nck = min(a.seg_chunks, a.nck - cbeg);              // chunks of this CTA
+    const bool last_seg = seg == a.nseg - 1;
+    const float *h0 = a.h0 ? a.h0 + (size_t)seg * a.h0_seg_stride : nullptr;
     const int ksteps_tok = C / 16;
 
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
@@ -179,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t fb = bar(BAR_FULL0 + s), fv = bar(BAR_FULLV0 + s);
                 mbar_arrive_expect_tx(fb, tx_qk);
                 mbar_arrive_expect_tx(fv, tx_v);
-                const int t0 = (kRev ? nck - 1 - c : c) * C;
+                const int t0 = (kRev ? nck - 1 - c : cbeg + c) * C;
                 // Q and K first: Q K^T can start before V has landed.
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {
@@ -309,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
-            const int Cc = min(C, T - (kRev ? nck - 1 - c : c) * C);
+            const int Cc = min(C, T - (kRev ? nck - 1 - c : cbeg + c) * C);
             if (!group_wait(bar(BAR_QK0 + s), (c >> 1) & 1, ctl, mydec, gt, named, kw)) break;
             tc_fence_after();
             if (sub == 0) {
@@ -356,10 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Initial state: S_prev copy 0 = bf16(h0 slice), TMEM S = lambda^C0 * h0,
         // with C0 the length of the first chunk processed.
         {
-            const float w0 = pw[kRev ? T - (nck - 1) * C : min(C, T)];
+            const float w0 = pw[kRev ? T - (nck - 1) * C : min(C, T - cbeg * C)];
             if (quad < 3) {
                 const float *src =
-                    a.h0 ? a.h0 + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half : nullptr;
+                    h0 ? h0 + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half : nullptr;
 #pragma unroll
                 for (int blk = 0; blk < 3; ++blk) {
                     float x[32];
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
-            const int t0 = (kRev ? nck - 1 - c : c) * C;
+            const int t0 = (kRev ? nck - 1 - c : cbeg + c) * C;
             // State hand-off (rows 0..95 = quadrants 0..2).
             if (!group_wait(bar(BAR_SFULL), c & 1, ctl, mydec, gt, kBarE, kw)) break;
             tc_fence_after();
@@ -394,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // rescale by lambda^(length of the next chunk processed)
                 const float wn = last ? 1.f : (kRev ? pw[C] : pw[min(C, T - t0 - C)]);
                 unsigned char *sb_next = sm + kOffSb + (uint32_t)(s ^ 1) * kSbBytes;
-                float *dst = (last && a.hT) ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
-                                            : nullptr;
+                float *dst = (last && last_seg && a.hT)
+                                 ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
+                                 : nullptr;
                 // Three 32-column blocks; the next block's TMEM load overlaps this one's work.
                 auto handle = [&](uint32_t (&r)[32], int blk) {
                     if (last) {
@@ -479,7 +490,7 @@ cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, co
     cudaError_t e =
         cudaFuncSetAttribute(gla_fwd_tc_kernel<kRev>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(B * a.H * 2);
+    const unsigned grid = (unsigned)(B * a.H * 2 * a.nseg);
     gla_fwd_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, om, a);
     if (launches) ++*launches;
     return cudaGetLastError();
@@ -487,7 +498,9 @@ cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, co
 
 }  // namespace
 
-size_t fwd_tc_workspace_size(int, int, int, int) { return 0; }
+size_t fwd_tc_workspace_size(int B, int T, int H, int chunk) {
+    return seg_workspace_bytes(B, H, plan_segments(B, T, H, chunk));
+}
 
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
@@ -497,8 +510,19 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     if ((e = make_token_map(&mk, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mo, p.o, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
-    FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, (p.T + p.chunk - 1) / p.chunk,
-                p.status};
+    const int nck = (p.T + p.chunk - 1) / p.chunk;
+    FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, nck, 1, nck, p.B * p.H, 0, p.status};
+    // Few (b, h) pairs and a long sequence: split each sequence into segments
+    // that run in parallel, when the caller gave the workspace for it.
+    const SegPlan plan = plan_segments(p.B, p.T, p.H, p.chunk);
+    if (plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan)) {
+        float *S_in = nullptr;
+        if ((e = launch_seg_prologue(p, plan, &S_in, s, launches)) != cudaSuccess) return e;
+        a.h0 = S_in;
+        a.nseg = plan.nseg;
+        a.seg_chunks = plan.seg_chunks;
+        a.h0_seg_stride = (size_t)p.B * p.H * kDk * kDv;
+    }
     return launch_chunk_kernel<false>(mq, mk, mv, mo, a, p.B, s, launches);
 }
 
@@ -513,8 +537,9 @@ cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches) 
     if ((e = make_token_map(&mcol, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mval, p.do_, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mout, p.dv_out, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
-    FwdTcArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, p.chunk,
-                (p.T + p.chunk - 1) / p.chunk, p.status};
+    const int nck = (p.T + p.chunk - 1) / p.chunk;
+    FwdTcArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, p.chunk, nck, 1, nck,
+                p.B * p.H, 0, p.status};
     return launch_chunk_kernel<true>(mrow, mcol, mval, mout, a, p.B, s, launches);
 }
 

@@ -199,3 +199,27 @@ def test_prefill_then_decode_matches_longer_prefill(gla):
         assert relerr(to_host(o), ro[:, t]) <= TOL["bf16"]
     gla.gla_check()
     assert relerr(to_host(S), rhT) <= TOL["bf16"]
+
+
+# ------------------------------------------------ long sequences, segmented
+@pytest.mark.parametrize("T,C", [(5120, 128), (5000, 128), (2600, 64)])
+def test_fwd_segmented_matches_oracle_and_single_chain(gla, T, C):
+    """Few (b, h) pairs and a long sequence: the forward splits each sequence
+    into segments (state-only pass, scan, then all segments at once). The
+    result must match the oracle and the one-chain-per-(b, h) path."""
+    import torch
+    c = gen.make_case(1, T, 2, 96, 192, seed=91 + T, dtype="bf16", lam_random=True, h0_std=0.1, chunk=C)
+    assert gla.gla_chunk_fwd_workspace_size(1, T, 2, 96, 192, C) > 0
+    d = case_to_dev(c)
+    o, hT = gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["ll"], d["h0"], c.scale, C)
+    launches_seg = gla.gla_last_launch_count()
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")
+    o1, hT1 = gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["ll"], d["h0"], c.scale, C, workspace=empty)
+    launches_one = gla.gla_last_launch_count()
+    gla.gla_check()
+    assert launches_seg == 3 and launches_one == 1
+    ro, rh = oracle.fwd_recurrent(c.q, c.k, c.v, c.log_lambda, c.h0, c.scale)
+    assert relerr(to_host(o), ro) <= TOL["bf16"]
+    assert relerr(to_host(hT), rh) <= TOL["bf16"]
+    assert relerr(to_host(o), to_host(o1)) <= TOL["bf16"]
+    assert relerr(to_host(hT), to_host(hT1)) <= TOL["bf16"]
