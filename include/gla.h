@@ -105,6 +105,41 @@ size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chu
                                     gla_dtype dtype);
 
 /*
+ * gla_chunk_fwd_noalloc -- gla_chunk_fwd for callers that cannot allocate
+ * device memory. The method's description has no counterpart to this entry
+ * point: it exists for the library's users, not for the mixer's math.
+ *
+ * Who needs it: code that runs the forward where a cudaMalloc is not
+ * allowed -- a plugin whose host framework owns all device memory through
+ * its own pool, or a serving loop that must neither stall the device
+ * (cudaMalloc can synchronise it) nor fail with out-of-memory mid-step.
+ * gla_chunk_fwd asks for a workspace when it splits long sequences into
+ * segments; this entry point instead uses a fixed scratch array of
+ * GLA_NOALLOC_SCRATCH_BYTES (24 MiB) that the library reserves in each
+ * device's memory when it is loaded there, and holds until the process
+ * exits. It never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Arguments, layouts and results are those of gla_chunk_fwd (without the
+ * workspace). A shape whose segmentation would need more scratch than the
+ * array holds is rejected with GLA_ERR_WORKSPACE (see gla_last_error); no
+ * launch happens then.
+ *
+ * - The first call on a device that needs scratch looks up the array's
+ *   device address (cudaGetSymbolAddress). Make that first call before any
+ *   stream capture.
+ * - Every call on a device shares the one array and leaves the last call's
+ *   contents in it; each call writes every scratch byte it reads, so nothing
+ *   has to be cleared between calls.
+ * - Calls that overlap on the GPU (on different streams, or from different
+ *   host threads without ordering) race on the array: order them.
+ */
+#define GLA_NOALLOC_SCRATCH_BYTES (24u << 20)
+gla_status gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const float *log_lambda, const float *h0, float scale,
+                                 int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype,
+                                 void *o, float *hT, void *stream);
+
+/*
  * gla_chunk_bwd -- gradients of L = sum_t <do_t, o_t> + <dhT, hT> through
  * the chunked forward ("Challenge 3": through every serial state update).
  * lambda is fixed (not learned), so there is no gradient for log_lambda.

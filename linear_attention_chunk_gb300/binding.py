@@ -28,7 +28,7 @@ GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_CUDA, GLA_ERR_TIMEOUT,
 GLA_BF16, GLA_FP32 = 0, 1
 
 # The public entry points declared in include/gla.h.
-ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_bwd",
+ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_bwd",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
 
@@ -60,6 +60,9 @@ def lib():
             L.gla_chunk_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i,
                                         _vp, _vp, _vp, _sz, _vp]
             L.gla_chunk_fwd.restype = _i
+            L.gla_chunk_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i,
+                                                _vp, _vp, _vp]
+            L.gla_chunk_fwd_noalloc.restype = _i
             L.gla_chunk_fwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
             L.gla_chunk_fwd_workspace_size.restype = _sz
             L.gla_chunk_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
@@ -171,6 +174,22 @@ def gla_chunk_fwd(q, k, v, log_lambda, h0=None, scale=None, chunk=128, *, o=None
                              B, T, H, dk, dv, int(chunk), dt, _ptr(o), _ptr(hT),
                              _ptr(workspace), ws_bytes, _stream(stream))
     _raise_on(st, "gla_chunk_fwd")
+    return o, hT
+
+
+def gla_chunk_fwd_noalloc(q, k, v, log_lambda, h0=None, scale=None, chunk=128, *, o, hT=None, stream=None):
+    """The forward without any device allocation by the library: for callers
+    that may not allocate device memory, the segmentation scratch comes from
+    a fixed array inside the library. The caller passes the output tensors.
+    Returns (o, hT)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    st = lib().gla_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), float(scale),
+                                     B, T, H, dk, dv, int(chunk), _dtype_code(q), _ptr(o), _ptr(hT),
+                                     _stream(stream))
+    _raise_on(st, "gla_chunk_fwd_noalloc")
     return o, hT
 
 
