@@ -87,7 +87,7 @@ constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-constexpr uint32_t kTmemCols = 512, kColR = 0, kColS = 256, kColP = 352;
+constexpr uint32_t kTmemCols = 512, kColR = 0, kColS = 256, kColP = 352, kColQ = 416;
 
 struct FwdTcArgs {
     const float *log_lambda;
@@ -219,6 +219,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t spins = 0;
             while (q23 < nck) {
                 bool progress = false;
+                // ST(c): S += K~^T V once K~ is scaled and S rescaled; after OUT(c-1)
+                if (q4 < q1 && q4 <= q23) {
+                    const int c = q4, s = c & 1;
+                    if (mbar_test(bar(BAR_KREADY0 + s), (c >> 1) & 1) && mbar_test(bar(BAR_SBREADY), c & 1) &&
+                        mbar_test(bar(BAR_FULLV0 + s), (c >> 1) & 1)) {
+                        tc_fence_after();
+                        const uint32_t st = base + (uint32_t)s * kStageBytes;
+                        for (int ks = 0; ks < ksteps_tok; ++ks)
+                            mma_bf16_ss(tmem + kColS, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
+                                        smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
+                        mma_commit(bar(BAR_SFULL));
+                        ++q4;
+                        progress = true;
+                    }
+                }
                 // QK(c): tiles landed and R[c%2] released by the epilogue of chunk c-2
                 if (q1 < nck) {
                     const int c = q1, s = c & 1;
@@ -237,21 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         progress = true;
                     }
                 }
-                // ST(c): S += K~^T V once K~ is scaled and S rescaled; after OUT(c-1)
-                if (q4 < q1 && q4 <= q23) {
-                    const int c = q4, s = c & 1;
-                    if (mbar_test(bar(BAR_KREADY0 + s), (c >> 1) & 1) && mbar_test(bar(BAR_SBREADY), c & 1) &&
-                        mbar_test(bar(BAR_FULLV0 + s), (c >> 1) & 1)) {
-                        tc_fence_after();
-                        const uint32_t st = base + (uint32_t)s * kStageBytes;
-                        for (int ks = 0; ks < ksteps_tok; ++ks)
-                            mma_bf16_ss(tmem + kColS, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
-                                        smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
-                        mma_commit(bar(BAR_SFULL));
-                        ++q4;
-                        progress = true;
-                    }
-                }
                 // OUT(c): O = Q~ S_prev + P V once P is built and Q~ scaled
                 if (q23 < q4) {
                     const int c = q23, s = c & 1;
@@ -261,13 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t dR = tmem + kColR + 128u * s;
                         const uint32_t sb = base + kOffSb + (uint32_t)s * kSbBytes;
 #pragma unroll
-                        for (int ks = 0; ks < 6; ++ks) {
-                            const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
-                            mma_bf16_ss(dR, smem_desc(st + kStageQ + off, 16, 512, 4),
+                        for (int ks = 0; ks < 6; ++ks)
+                            mma_bf16_ts(dR, tmem + kColQ + 8u * (uint32_t)ks,
                                         smem_desc(sb + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
-                        }
                         for (int ks = 0; ks < ksteps_tok; ++ks)
-                            mma_bf16_ts(dR, tmem + kColP + 64u * s + 8u * (uint32_t)ks,
+                            mma_bf16_ts(dR, tmem + kColP + 8u * (uint32_t)ks,
                                         smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idO, 1);
                         mma_commit(bar(BAR_OFULL0 + s));
                         mma_commit(bar(BAR_EMPTY0 + s));
@@ -313,7 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int blk = (int)sub; blk < 4; blk += 2) {
                 if (kRev ? (blk >= diag) : (blk <= diag)) continue;
                 tmem_st_16cols(tl + kColP + 16u * blk, z);
-                tmem_st_16cols(tl + kColP + 64u + 16u * blk, z);
             }
             tmem_st_wait();
         }
@@ -330,13 +327,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 named_sync(named, kGroupThreads);
                 if (gt == 0) mbar_arrive(bar(BAR_KREADY0 + s));
-            } else {
-                // Q~ = diag(lambda^(i+1)) Q, or diag(lambda^(Cc-1-j)) in reverse
-                const float wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
-                scale_rows<3>(sm + (uint32_t)s * kStageBytes + kStageQ, row, wq);
             }
-            // P = bf16((Q K^T) .* D) for this sub-group's blocks at or below the diagonal
-            // (at most two per warp; both TMEM loads are issued before one wait).
+            // P and Q~ live in single TMEM buffers: the previous chunk's output
+            // MMAs (their only readers) must have completed before they change.
+            if (c >= 1 && !group_wait(bar(BAR_OFULL0 + (s ^ 1)), ((c - 1) >> 1) & 1, ctl, mydec, gt, named, kw))
+                break;
+            tc_fence_after();
+            if (sub == 1) {
+                // Q~ = diag(lambda^(i+1)) Q (diag(lambda^(Cc-1-j)) in reverse) into TMEM as the
+                // A operand of Q~ S_prev: lane = token row, column c = dk pair (2c, 2c+1).
+                const float wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+                const unsigned char *qt = sm + (uint32_t)s * kStageBytes + kStageQ;
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(qt + j * kBlk + sw64_offset(row, cc));
+                        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_bf16x2(u[e]);
+                            pk[4 * cc + e] = pack_bf16x2(f.x * wq, f.y * wq);
+                        }
+                    }
+                    tmem_st_16cols(tl + kColQ + 16u * j, pk);
+                }
+            }
+            // P = bf16((Q K^T) .* D) for this sub-group's blocks on the kept side of the
+            // diagonal (at most two per warp; both TMEM loads are issued before one wait).
             // Tokens past the end of a ragged chunk have zero q and k, so A is zero there.
             {
                 const int b0 = (int)sub, b1 = (int)sub + 2;
@@ -346,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (has0) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b0, r0);
                 if (has1) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b1, r1);
                 tmem_ld_wait();
-                if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, b0 == diag, tl + kColP + 64u * s + 16u * b0, pw);
-                if (has1) build_p_block<kRev>(r1, (int)row - 32 * b1, b1 == diag, tl + kColP + 64u * s + 16u * b1, pw);
+                if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, b0 == diag, tl + kColP + 16u * b0, pw);
+                if (has1) build_p_block<kRev>(r1, (int)row - 32 * b1, b1 == diag, tl + kColP + 16u * b1, pw);
             }
             tmem_st_wait();
             fence_proxy_async_smem();
