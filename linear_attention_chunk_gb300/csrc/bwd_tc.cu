@@ -59,7 +59,9 @@ constexpr uint32_t kOffOut = kOffSb + 6 * kSbBlk;   // output staging: 3 blocks
 constexpr uint32_t kOffPw = kOffOut + 3 * kBlk;
 enum { BAR_FULL, BAR_EMPTY, BAR_SCORE, BAR_KREADY, BAR_PREADY, BAR_SBREADY, BAR_SFULL, BAR_OFULL, BAR_OEMPTY,
        BAR_DONE, kNumBars };
-constexpr uint32_t kOffBar = kOffPw + 132 * 4;
+constexpr uint32_t kOffPair = kOffPw + 132 * 4;     // pp, pr: packed decay pairs
+constexpr uint32_t kOffBar = kOffPair + 2 * 164 * 4;
+static_assert(kPairLen <= 164, "pair table stride");
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
@@ -89,6 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ksteps_tok = C / 16;
 
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
+    uint32_t *pp = reinterpret_cast<uint32_t *>(sm + kOffPair);
+    uint32_t *pr = pp + 164;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
     volatile int *dec = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);   // [3][2]
@@ -109,6 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         const float l2 = log2_of_decay(a.log_lambda[h]);
         for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
+        fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
     }
     // Zero what TMA never writes: the M-padding block of C, and for C = 64 the
     // rows 64..127 of every tile block.
@@ -245,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     tmem_ld_32cols(tl + kColX + 32u * bk, r);
                     tmem_ld_wait();
-                    build_p_block<kRev>(r, (int)row - 32 * bk, bk == diag, tl + kColX + 16u * bk, pw);
+                    pack_scores(r);
+                    build_p_block<kRev>(r, (int)row - 32 * bk, tl + kColX + 16u * bk, pp, pr);
                 } else {
                     uint32_t z[16];
 #pragma unroll

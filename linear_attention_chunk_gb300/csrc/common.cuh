@@ -49,6 +49,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Two bf16 products in one instruction (round to nearest).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a);
+    __nv_bfloat162 y = *reinterpret_cast<__nv_bfloat162 *>(&b);
+    __nv_bfloat162 z = __hmul2(x, y);
+    return *reinterpret_cast<uint32_t *>(&z);
+}
+
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
     __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
     return __bfloat1622float2(v);

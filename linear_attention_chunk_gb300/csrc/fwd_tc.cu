@@ -24,17 +24,20 @@
 //                 sub-group 0 (warps 2-5) scales K in place by lambda^(Cc-1-j)
 //                 and signals it at once, then builds the even 32-column
 //                 blocks of P = bf16(A .* D);
-//                 sub-group 1 (warps 6-9) scales Q in place by lambda^(i+1)
-//                 and builds the odd blocks of P.
-//               Blocks of P above the diagonal are zero and are written once;
-//               only the diagonal block is masked.
+//                 sub-group 1 (warps 6-9) writes Q~ = diag(lambda^(i+1)) Q into
+//                 TMEM and builds the odd blocks of P.
+//               P is built with packed bf16x2 multiplies by a table of decay
+//               pairs whose zero entries mask the diagonal block. Blocks of P
+//               on the masked side of the diagonal are zero and written once.
 //   warps 10-13 "E group": the state hand-off (bf16 copy of S for the next
 //               chunk's Q~ S, S <- lambda^C' S in TMEM, hT at the end) and the
 //               output epilogue (O * scale -> bf16 -> smem -> TMA store)
 //
 // TMEM (512 columns): R0, R1 = [0,128), [128,256) hold A = Q K^T of chunk c
 // in R[c%2], then that chunk's O (first 96 columns); S = [256,352) fp32;
-// P0, P1 = [352,416), [416,480) bf16 pairs, the A operand of P V.
+// P = [352,416) bf16 pairs (A operand of P V); Q~ = [416,464) bf16 pairs (A
+// operand of Q~ S_prev). P and Q~ are single buffers, rewritten only after
+// the previous chunk's output MMAs have completed.
 // The issuer runs three kinds of events per chunk c as soon as their inputs
 // are ready (in chunk order within each kind):
 //   QK(c)    MMA1  R[c%2]  = Q K^T                (tiles landed, R[c%2] free)
@@ -81,7 +84,9 @@ constexpr uint32_t kOffPw = kOffOut + 3 * kBlk;      // lambda^n, n = 0..128 (+p
 enum { BAR_FULL0, BAR_FULL1, BAR_FULLV0, BAR_FULLV1, BAR_EMPTY0, BAR_EMPTY1, BAR_QK0, BAR_QK1, BAR_KREADY0, BAR_KREADY1,
        BAR_PREADY0, BAR_PREADY1, BAR_SBREADY, BAR_SFULL, BAR_OFULL0, BAR_OFULL1, BAR_OEMPTY0, BAR_OEMPTY1,
        BAR_DONE, kNumBars };
-constexpr uint32_t kOffBar = kOffPw + 132 * 4;
+constexpr uint32_t kOffPair = kOffPw + 132 * 4;     // pp, pr: packed decay pairs
+constexpr uint32_t kOffBar = kOffPair + 2 * 164 * 4;
+static_assert(kPairLen <= 164, "pair table stride");
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, 3 x 2 decision slots
 constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
@@ -133,6 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ksteps_tok = C / 16;
 
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
+    uint32_t *pp = reinterpret_cast<uint32_t *>(sm + kOffPair);
+    uint32_t *pr = pp + 164;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
     volatile int *dec = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);   // [3][2]
@@ -153,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
         const float l2 = log2_of_decay(a.log_lambda[h]);
         for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
+        fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
     }
     // Zero what TMA never writes: the dk padding block of K (both stages),
     // and for C = 64 the rows 64..127 of every Q, K, V block.
@@ -337,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Q~ = diag(lambda^(i+1)) Q (diag(lambda^(Cc-1-j)) in reverse) into TMEM as the
                 // A operand of Q~ S_prev: lane = token row, column c = dk pair (2c, 2c+1).
                 const float wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+                const uint32_t wq2 = pack_bf16x2(wq, wq);
                 const unsigned char *qt = sm + (uint32_t)s * kStageBytes + kStageQ;
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {
@@ -344,12 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         const uint4 v = *reinterpret_cast<const uint4 *>(qt + j * kBlk + sw64_offset(row, cc));
-                        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 f = unpack_bf16x2(u[e]);
-                            pk[4 * cc + e] = pack_bf16x2(f.x * wq, f.y * wq);
-                        }
+                        pk[4 * cc + 0] = mul_bf16x2(v.x, wq2);
+                        pk[4 * cc + 1] = mul_bf16x2(v.y, wq2);
+                        pk[4 * cc + 2] = mul_bf16x2(v.z, wq2);
+                        pk[4 * cc + 3] = mul_bf16x2(v.w, wq2);
                     }
                     tmem_st_16cols(tl + kColQ + 16u * j, pk);
                 }
@@ -365,8 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (has0) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b0, r0);
                 if (has1) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b1, r1);
                 tmem_ld_wait();
-                if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, b0 == diag, tl + kColP + 16u * b0, pw);
-                if (has1) build_p_block<kRev>(r1, (int)row - 32 * b1, b1 == diag, tl + kColP + 16u * b1, pw);
+                pack_scores(r0);
+                pack_scores(r1);
+                if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, tl + kColP + 16u * b0, pp, pr);
+                if (has1) build_p_block<kRev>(r1, (int)row - 32 * b1, tl + kColP + 16u * b1, pp, pr);
             }
             tmem_st_wait();
             fence_proxy_async_smem();

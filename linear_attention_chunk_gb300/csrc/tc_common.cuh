@@ -21,6 +21,7 @@ constexpr uint32_t kGroupThreads = 128;
 // order so that the 32 rows a warp touches at once fall in distinct banks.
 template <int NB>
 __device__ __forceinline__ void scale_rows(unsigned char *blk0, uint32_t row, float w) {
+    const uint32_t w2 = pack_bf16x2(w, w);
 #pragma unroll
     for (int h6 = 0; h6 < 4 * NB; h6 += 6) {
         uint4 v[6];
@@ -31,12 +32,10 @@ __device__ __forceinline__ void scale_rows(unsigned char *blk0, uint32_t row, fl
         }
 #pragma unroll
         for (int i = 0; i < 6; ++i) {
-            uint32_t *u = reinterpret_cast<uint32_t *>(&v[i]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float2 f = unpack_bf16x2(u[e]);
-                u[e] = pack_bf16x2(f.x * w, f.y * w);
-            }
+            v[i].x = mul_bf16x2(v[i].x, w2);
+            v[i].y = mul_bf16x2(v[i].y, w2);
+            v[i].z = mul_bf16x2(v[i].z, w2);
+            v[i].w = mul_bf16x2(v[i].w, w2);
         }
 #pragma unroll
         for (int i = 0; i < 6; ++i) {
@@ -69,29 +68,46 @@ __device__ __forceinline__ void write_row_sw64(unsigned char *blk, uint32_t row,
                        pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
 }
 
-// One 32-column block of P for one row, packed to bf16 pairs in TMEM.
-// Forward: x_j * lambda^(i - j), kept for j <= i; n0 = i - j0.
-// Reverse: x_j * lambda^(j - i), kept for j >= i; n0 = i - j0 as well.
-// Only the diagonal block needs the mask.
+// Packed decay pairs for P, as bf16x2 (low half = column j, high half =
+// column j+1), stored at index u + kPairBias for u = -kPairBias..128:
+//   forward  pp[u] = (lambda^u, lambda^(u-1)),  u = i - j: columns j, j+1 sit
+//            at exponents u, u-1;
+//   reverse  pr[u] = (lambda^(u-1), lambda^u),  u = j - i + 1: columns j, j+1
+//            sit at exponents u-1, u.
+// A negative exponent is the masked side of the diagonal and holds zero, so
+// the diagonal block needs no separate mask.
+constexpr int kPairBias = 32, kPairLen = 128 + kPairBias + 1;
+
+__device__ __forceinline__ void fill_pair_tables(uint32_t *pp, uint32_t *pr, float l2, int tid, int nthr) {
+    for (int i = tid; i < kPairLen; i += nthr) {
+        const int u = i - kPairBias;
+        const float w = u >= 0 ? decay_pow(l2, u) : 0.f, w1 = u >= 1 ? decay_pow(l2, u - 1) : 0.f;
+        pp[i] = pack_bf16x2(w, w1);
+        pr[i] = pack_bf16x2(w1, w);
+    }
+}
+
+// 32 fp32 scores (raw bits, as loaded from TMEM) rounded to 16 bf16 pairs,
+// in place in the first 16 entries.
+__device__ __forceinline__ void pack_scores(uint32_t (&r)[32]) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) r[e >> 1] = pack_bf16x2(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+}
+
+// One 32-column block of P for TMEM lane row i, block columns j0..j0+31
+// (n0 = i - j0 in both directions), from the scores packed by pack_scores
+// (x[0..15]), written as 16 bf16 pairs at taddr: each pair is multiplied by
+// its bf16 decay pair in one packed instruction. Only blocks on the kept side
+// of the diagonal come here, so every index stays inside the table.
 template <bool kRev>
-__device__ __forceinline__ void build_p_block(const uint32_t (&r)[32], int n0, bool diagonal, uint32_t taddr,
-                                              const float *pw) {
-    uint32_t pk[16];
+__device__ __forceinline__ void build_p_block(uint32_t (&x)[32], int n0, uint32_t taddr, const uint32_t *pp,
+                                              const uint32_t *pr) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-        const int d0 = kRev ? e - n0 : n0 - e;          // exponent of column e
-        const int d1 = kRev ? e + 1 - n0 : n0 - e - 1;  // exponent of column e + 1
-        float x0, x1;
-        if (!diagonal) {
-            x0 = __uint_as_float(r[e]) * pw[d0];
-            x1 = __uint_as_float(r[e + 1]) * pw[d1];
-        } else {
-            x0 = d0 >= 0 ? __uint_as_float(r[e]) * pw[max(d0, 0)] : 0.f;
-            x1 = d1 >= 0 ? __uint_as_float(r[e + 1]) * pw[max(d1, 0)] : 0.f;
-        }
-        pk[e >> 1] = pack_bf16x2(x0, x1);
+        const int u = kRev ? e - n0 + 1 : n0 - e;       // table index of columns (e, e+1)
+        x[e >> 1] = mul_bf16x2(x[e >> 1], kRev ? pr[u + kPairBias] : pp[u + kPairBias]);
     }
-    tmem_st_16cols(taddr, pk);
+    tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
 }
 
 // One elected thread of a 128-thread group waits on an mbarrier; the verdict
