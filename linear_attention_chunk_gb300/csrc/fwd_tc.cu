@@ -83,7 +83,7 @@ constexpr uint32_t kOffOut = kOffSb + 2 * kSbBytes;  // output staging, 3 blocks
 constexpr uint32_t kOffPw = kOffOut + 3 * kBlk;      // lambda^n, n = 0..128 (+pad)
 enum { BAR_FULL0, BAR_FULL1, BAR_FULLV0, BAR_FULLV1, BAR_EMPTY0, BAR_EMPTY1, BAR_QK0, BAR_QK1, BAR_KREADY0, BAR_KREADY1,
        BAR_PREADY0, BAR_PREADY1, BAR_SBREADY, BAR_SFULL, BAR_OFULL0, BAR_OFULL1, BAR_OEMPTY0, BAR_OEMPTY1,
-       BAR_DONE, kNumBars };
+       BAR_KFREE0, BAR_KFREE1, BAR_DONE, kNumBars };
 constexpr uint32_t kOffPair = kOffPw + 132 * 4;     // pp, pr: packed decay pairs
 constexpr uint32_t kOffBar = kOffPair + 2 * 164 * 4;
 static_assert(kPairLen <= 164, "pair table stride");
@@ -187,35 +187,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
+        // Each tile of stage s is refilled as soon as chunk c-2 is done with it:
+        // Q once Q~(c-2) is in TMEM (P ready), K once the state update of c-2
+        // has completed, V once the output MMAs of c-2 have completed.
         const uint32_t tx_qk = 6u * (uint32_t)C * 64u, tx_v = 3u * (uint32_t)C * 64u;
-        int issued = 0;
+        int nq = 0, nv = 0;   // chunks whose Q (and K) / V loads were issued
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
-            if (c >= 2 && !lane0_wait(bar(BAR_EMPTY0 + s), ((c >> 1) - 1) & 1, ctl, lane)) break;
+            const uint32_t ph = ((c >> 1) - 1) & 1;   // phase parity of chunk c-2
+            const uint32_t st = base + (uint32_t)s * kStageBytes;
+            const uint32_t fb = bar(BAR_FULL0 + s), fv = bar(BAR_FULLV0 + s);
+            const int t0 = (kRev ? nck - 1 - c : cbeg + c) * C;
+            if (c >= 2 && !lane0_wait(bar(BAR_PREADY0 + s), ph, ctl, lane)) break;
             if (lane == 0) {
-                const uint32_t st = base + (uint32_t)s * kStageBytes;
-                const uint32_t fb = bar(BAR_FULL0 + s), fv = bar(BAR_FULLV0 + s);
                 mbar_arrive_expect_tx(fb, tx_qk);
-                mbar_arrive_expect_tx(fv, tx_v);
-                const int t0 = (kRev ? nck - 1 - c : cbeg + c) * C;
-                // Q and K first: Q K^T can start before V has landed.
 #pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    tma_load_4d(st + kStageQ + j * kBlk, &tm_q, fb, 32 * j, h, t0, b);
-                    tma_load_4d(st + kStageK + j * kBlk, &tm_k, fb, 32 * j, h, t0, b);
-                }
+                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStageQ + j * kBlk, &tm_q, fb, 32 * j, h, t0, b);
+            }
+            __syncwarp();
+            nq = c + 1;
+            if (c >= 2 && !lane0_wait(bar(BAR_KFREE0 + s), ph, ctl, lane)) break;
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStageK + j * kBlk, &tm_k, fb, 32 * j, h, t0, b);
+            }
+            __syncwarp();
+            if (c >= 2 && !lane0_wait(bar(BAR_EMPTY0 + s), ph, ctl, lane)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(fv, tx_v);
 #pragma unroll
                 for (int j = 0; j < 3; ++j)
                     tma_load_4d(st + kStageV + j * kBlk, &tm_v, fv, kDvHalf * half + 32 * j, h, t0, b);
             }
             __syncwarp();
-            issued = c + 1;
+            nv = c + 1;
         }
-        // Drain: every load issued must have landed before the CTA exits.
-        for (int c = (issued >= 2 ? issued - 2 : 0); c < issued; ++c) {
-            lane0_wait(bar(BAR_FULL0 + (c & 1)), (c >> 1) & 1, ctl, lane);
-            lane0_wait(bar(BAR_FULLV0 + (c & 1)), (c >> 1) & 1, ctl, lane);
+        // Drain: every load issued must have landed before the CTA exits (a
+        // chunk left half-issued by an abort waits out the 1 ms limit).
+        if (lane == 0) {
+            for (int c = (nq >= 2 ? nq - 2 : 0); c < nq; ++c)
+                mbar_wait_drain(bar(BAR_FULL0 + (c & 1)), (c >> 1) & 1, 1000000ull);
+            for (int c = (nv >= 2 ? nv - 2 : 0); c < nv; ++c)
+                mbar_wait_drain(bar(BAR_FULLV0 + (c & 1)), (c >> 1) & 1, 1000000ull);
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ----------------------------------------------- MMA issuer (event loop)
         if (lane == 0) {
@@ -238,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_bf16_ss(tmem + kColS, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
                                         smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
                         mma_commit(bar(BAR_SFULL));
+                        mma_commit(bar(BAR_KFREE0 + s));
                         ++q4;
                         progress = true;
                     }
