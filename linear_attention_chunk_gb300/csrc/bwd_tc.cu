@@ -24,13 +24,16 @@
 //   score  X  = A B^T                 (K = 192; TMEM [0,128))
 //   P      = bf16(X .* D) in place over X (columns [0,64))
 //   inter  O1 = A S_prev^T            (K = 192, N = 96; S_prev as a bf16 smem copy)
-//   state  S += C^T (w .* B)          (M = 96 padded to 128, N = 192)
+//   state  S += (w .* C)^T B          (M = 96 padded to 128, N = 192)
 //   intra  O2 = P C                   (K = C tokens, N = 96)
 //   out    = s (O2 + w_row O1)        -> bf16 -> TMA store
 // The row weight of the state update (lambda^(Cc-1-j) forward, lambda^(i+1)
-// reverse) is applied by scaling the B tile in place after the score
-// contraction has read it. One CTA per (b, h); one tile stage.
-// Warps: 0 TMA, 1 TMEM + MMA, 2-5 scale B, 6-9 build P, 10-13 state hand-off
+// reverse) goes on the small C tile: a scaled copy C~ = w .* C is made as soon
+// as C lands, so A and B are read only by the tensor core.
+// One CTA per (b, h), one buffer per tile, each refilled as soon as its
+// readers are done: A after the inter MMA, B after the state MMA, C after the
+// intra MMA (and the copy). The MMA issuer is a non-blocking event loop.
+// Warps: 0 TMA, 1 TMEM + MMA, 2-5 make C~, 6-9 build P, 10-13 state hand-off
 // and output epilogue.
 #include <cuda.h>
 
@@ -52,13 +55,14 @@ constexpr uint32_t kBarScale = 1, kBarP = 2, kBarE = 3;
 
 constexpr uint32_t kOffA = 0;                       // [C][192]: 6 blocks
 constexpr uint32_t kOffB = 6 * kBlk;                // [C][192]: 6 blocks
-constexpr uint32_t kOffC = 12 * kBlk;               // [C][96]: 3 blocks + 1 zero block (M pad)
+constexpr uint32_t kOffC = 12 * kBlk;               // [C][96]: 3 blocks
+constexpr uint32_t kOffCt = 15 * kBlk;              // C~ = w .* C: 3 blocks + 1 zero block (M pad)
 constexpr uint32_t kSbBlk = kDk * 64;               // [96 rows][32 bf16] = 6 KB
-constexpr uint32_t kOffSb = 16 * kBlk;              // S_prev copy: 6 blocks of 96 rows
+constexpr uint32_t kOffSb = 19 * kBlk;              // S_prev copy: 6 blocks of 96 rows
 constexpr uint32_t kOffOut = kOffSb + 6 * kSbBlk;   // output staging: 3 blocks
 constexpr uint32_t kOffPw = kOffOut + 3 * kBlk;
-enum { BAR_FULL, BAR_EMPTY, BAR_SCORE, BAR_KREADY, BAR_PREADY, BAR_SBREADY, BAR_SFULL, BAR_OFULL, BAR_OEMPTY,
-       BAR_DONE, kNumBars };
+enum { BAR_FULLAB, BAR_FULLC, BAR_AFREE, BAR_BFREE, BAR_CFREE, BAR_SCORE, BAR_CTREADY, BAR_PREADY, BAR_SBREADY,
+       BAR_SFULL, BAR_OFULL, BAR_OEMPTY, BAR_DONE, kNumBars };
 constexpr uint32_t kOffPair = kOffPw + 132 * 4;     // pp, pr: packed decay pairs
 constexpr uint32_t kOffBar = kOffPair + 2 * 164 * 4;
 static_assert(kPairLen <= 164, "pair table stride");
@@ -115,10 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
         fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
     }
-    // Zero what TMA never writes: the M-padding block of C, and for C = 64 the
-    // rows 64..127 of every tile block.
+    // Zero what TMA never writes: the M-padding block of C~, and for C = 64 the
+    // rows 64..127 of every tile block (C~ rows there are made from zero C rows).
     for (uint32_t i = threadIdx.x; i < kBlk / 16; i += kThreads)
-        *reinterpret_cast<uint4 *>(sm + kOffC + 3 * kBlk + i * 16) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sm + kOffCt + 3 * kBlk + i * 16) = make_uint4(0, 0, 0, 0);
     if (C < 128) {
         const uint32_t lo = (uint32_t)C * 64, per_blk = (kBlk - lo) / 16;
         for (uint32_t i = threadIdx.x; i < 15 * per_blk; i += kThreads) {
@@ -138,97 +142,140 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
-        const uint32_t tx = 15u * (uint32_t)C * 64u;
-        int issued = 0;
+        // A of chunk c once the inter MMA of c-1 has completed, B once the state
+        // MMA of c-1 has (it follows the score and inter MMAs), C once the intra
+        // MMA of c-1 (and the copy C~) has.
+        const uint32_t tx_ab = 12u * (uint32_t)C * 64u, tx_c = 3u * (uint32_t)C * 64u;
+        int nab = 0, nc = 0;   // chunks whose A and B / C loads were issued
         for (int c = 0; c < nck; ++c) {
-            if (c >= 1 && !lane0_wait(bar(BAR_EMPTY), (c - 1) & 1, ctl, lane)) break;
+            const uint32_t ph = (uint32_t)(c - 1) & 1u;   // phase parity of chunk c-1
+            const int t0 = natural(c) * C;
+            if (c >= 1 && !lane0_wait(bar(BAR_AFREE), ph, ctl, lane)) break;
             if (lane == 0) {
-                const uint32_t fb = bar(BAR_FULL);
-                mbar_arrive_expect_tx(fb, tx);
-                const int t0 = natural(c) * C;
+                mbar_arrive_expect_tx(bar(BAR_FULLAB), tx_ab);
 #pragma unroll
-                for (int j = 0; j < 6; ++j) {
-                    tma_load_4d(base + kOffA + j * kBlk, &tm_a, fb, 32 * j, h, t0, b);
-                    tma_load_4d(base + kOffB + j * kBlk, &tm_b, fb, 32 * j, h, t0, b);
-                }
-#pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffC + j * kBlk, &tm_c, fb, 32 * j, h, t0, b);
+                for (int j = 0; j < 6; ++j) tma_load_4d(base + kOffA + j * kBlk, &tm_a, bar(BAR_FULLAB), 32 * j, h, t0, b);
             }
             __syncwarp();
-            issued = c + 1;
+            nab = c + 1;
+            if (c >= 1 && !lane0_wait(bar(BAR_BFREE), ph, ctl, lane)) break;
+            if (lane == 0) {
+#pragma unroll
+                for (int j = 0; j < 6; ++j) tma_load_4d(base + kOffB + j * kBlk, &tm_b, bar(BAR_FULLAB), 32 * j, h, t0, b);
+            }
+            __syncwarp();
+            if (c >= 1 && !lane0_wait(bar(BAR_CFREE), ph, ctl, lane)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(BAR_FULLC), tx_c);
+#pragma unroll
+                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffC + j * kBlk, &tm_c, bar(BAR_FULLC), 32 * j, h, t0, b);
+            }
+            __syncwarp();
+            nc = c + 1;
         }
-        if (issued >= 1) lane0_wait(bar(BAR_FULL), (issued - 1) & 1, ctl, lane);
+        // Drain: the last loads issued must have landed before the CTA exits (a
+        // chunk left half-issued by an abort waits out the 1 ms limit).
+        if (lane == 0) {
+            if (nab >= 1) mbar_wait_drain(bar(BAR_FULLAB), (uint32_t)(nab - 1) & 1u, 1000000ull);
+            if (nc >= 1) mbar_wait_drain(bar(BAR_FULLC), (uint32_t)(nc - 1) & 1u, 1000000ull);
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
-        const uint32_t idX = idesc_bf16(128, C, false, false);
-        const uint32_t id96 = idesc_bf16(128, kDk, false, false);     // O1: A K-major, S_prev^T K-major
-        const uint32_t idO2 = idesc_bf16(128, kDk, false, true);      // O2: P (TMEM), C MN-major
-        const uint32_t idS = idesc_bf16(128, kDv, true, true);        // S: C^T MN-major, B MN-major
-        for (int c = 0; c < nck; ++c) {
-            if (!lane0_wait(bar(BAR_FULL), c & 1, ctl, lane)) break;
-            tc_fence_after();
-            if (lane == 0) {
-                // score X = A B^T over 192 (12 steps)
-                for (int ks = 0; ks < 12; ++ks) {
-                    const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
-                    mma_bf16_ss(tmem + kColX, smem_desc(base + kOffA + off, 16, 512, 4),
-                                smem_desc(base + kOffB + off, 16, 512, 4), idX, ks > 0);
+        // Four events per chunk c, each in chunk order, issued as soon as ready:
+        //   X(c)   score       tiles A, B landed; O2(c-1) complete (P(c-1) read)
+        //   O1(c)  inter       after X(c); S_prev copy ready; O1/O2 drained
+        //   ST(c)  state       after O1(c) (so the hand-off that rewrites the
+        //                      S_prev copy follows O1's completion); C~ ready
+        //   O2(c)  intra       after ST(c); P built
+        if (lane == 0) {
+            const uint32_t idX = idesc_bf16(128, C, false, false);
+            const uint32_t id96 = idesc_bf16(128, kDk, false, false);     // O1: A K-major, S_prev^T K-major
+            const uint32_t idO2 = idesc_bf16(128, kDk, false, true);      // O2: P (TMEM), C MN-major
+            const uint32_t idS = idesc_bf16(128, kDv, true, true);        // S: C~^T MN-major, B MN-major
+            int qx = 0, q1 = 0, qs = 0, q2 = 0;
+            uint64_t t_idle = globaltimer_ns();
+            uint32_t spins = 0;
+            while (q2 < nck) {
+                bool progress = false;
+                if (qx < nck && qx == q2 && mbar_test(bar(BAR_FULLAB), (uint32_t)qx & 1u) &&
+                    (qx == 0 || mbar_test(bar(BAR_OFULL), (uint32_t)(qx - 1) & 1u))) {
+                    tc_fence_after();
+                    for (int ks = 0; ks < 12; ++ks) {
+                        const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
+                        mma_bf16_ss(tmem + kColX, smem_desc(base + kOffA + off, 16, 512, 4),
+                                    smem_desc(base + kOffB + off, 16, 512, 4), idX, ks > 0);
+                    }
+                    mma_commit(bar(BAR_SCORE));
+                    ++qx;
+                    progress = true;
                 }
-                mma_commit(bar(BAR_SCORE));
-            }
-            __syncwarp();
-            if (!lane0_wait(bar(BAR_SBREADY), c & 1, ctl, lane)) break;
-            if (c >= 1 && !lane0_wait(bar(BAR_OEMPTY), (c - 1) & 1, ctl, lane)) break;
-            tc_fence_after();
-            if (lane == 0) {
-                // inter O1 = A S_prev^T over 192
-                for (int ks = 0; ks < 12; ++ks) {
-                    const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
-                    const uint32_t soff = (uint32_t)(ks >> 1) * kSbBlk + (uint32_t)(ks & 1) * 32;
-                    mma_bf16_ss(tmem + kColO1, smem_desc(base + kOffA + off, 16, 512, 4),
-                                smem_desc(base + kOffSb + soff, 16, 512, 4), id96, ks > 0);
+                if (q1 < qx && mbar_test(bar(BAR_SBREADY), (uint32_t)q1 & 1u) &&
+                    (q1 == 0 || mbar_test(bar(BAR_OEMPTY), (uint32_t)(q1 - 1) & 1u))) {
+                    tc_fence_after();
+                    for (int ks = 0; ks < 12; ++ks) {
+                        const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
+                        const uint32_t soff = (uint32_t)(ks >> 1) * kSbBlk + (uint32_t)(ks & 1) * 32;
+                        mma_bf16_ss(tmem + kColO1, smem_desc(base + kOffA + off, 16, 512, 4),
+                                    smem_desc(base + kOffSb + soff, 16, 512, 4), id96, ks > 0);
+                    }
+                    mma_commit(bar(BAR_AFREE));
+                    ++q1;
+                    progress = true;
+                }
+                if (qs < q1 && mbar_test(bar(BAR_CTREADY), (uint32_t)qs & 1u)) {
+                    tc_fence_after();
+                    for (int ks = 0; ks < ksteps_tok; ++ks)
+                        mma_bf16_ss(tmem + kColS, smem_desc(base + kOffCt + (uint32_t)ks * 1024, kBlk, 512, 4),
+                                    smem_desc(base + kOffB + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
+                    mma_commit(bar(BAR_SFULL));
+                    mma_commit(bar(BAR_BFREE));   // B is read by the score and the state MMAs
+                    ++qs;
+                    progress = true;
+                }
+                if (q2 < qs && mbar_test(bar(BAR_PREADY), (uint32_t)q2 & 1u)) {
+                    tc_fence_after();
+                    for (int ks = 0; ks < ksteps_tok; ++ks)
+                        mma_bf16_ts(tmem + kColO2, tmem + kColX + 8u * (uint32_t)ks,
+                                    smem_desc(base + kOffC + (uint32_t)ks * 1024, kBlk, 512, 4), idO2, ks > 0);
+                    mma_commit(bar(BAR_OFULL));
+                    mma_commit(bar(BAR_CFREE));
+                    ++q2;
+                    progress = true;
+                }
+                if (progress) {
+                    t_idle = globaltimer_ns();
+                    spins = 0;
+                } else if ((++spins & 255u) == 0) {
+                    if (*abort_flag) break;
+                    if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        atomicOr(a.status, kDevTimeout);
+                        break;
+                    }
                 }
             }
-            __syncwarp();
-            if (!lane0_wait(bar(BAR_KREADY), c & 1, ctl, lane)) break;
-            tc_fence_after();
-            if (lane == 0) {
-                // state S += C^T (w .* B) over the chunk's tokens
-                for (int ks = 0; ks < ksteps_tok; ++ks)
-                    mma_bf16_ss(tmem + kColS, smem_desc(base + kOffC + (uint32_t)ks * 1024, kBlk, 512, 4),
-                                smem_desc(base + kOffB + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
-                mma_commit(bar(BAR_SFULL));
-            }
-            __syncwarp();
-            if (!lane0_wait(bar(BAR_PREADY), c & 1, ctl, lane)) break;
-            tc_fence_after();
-            if (lane == 0) {
-                // intra O2 = P C
-                for (int ks = 0; ks < ksteps_tok; ++ks)
-                    mma_bf16_ts(tmem + kColO2, tmem + kColX + 8u * (uint32_t)ks,
-                                smem_desc(base + kOffC + (uint32_t)ks * 1024, kBlk, 512, 4), idO2, ks > 0);
-                mma_commit(bar(BAR_OFULL));
-                mma_commit(bar(BAR_EMPTY));
-            }
-            __syncwarp();
+            // Every MMA issued must be complete before TMEM is released.
+            mma_commit(bar(BAR_DONE));
         }
-        if (lane == 0) mma_commit(bar(BAR_DONE));
         __syncwarp();
         lane0_wait(bar(BAR_DONE), 0, ctl, lane);
     } else if (warp < 6) {
-        // ------------------------------- warps 2-5: state-update row weight on B
+        // ------------------------ warps 2-5: C~ = w .* C, the state-update operand
         const uint32_t quad = (uint32_t)(warp & 3);
         const uint32_t row = quad * 32 + (uint32_t)lane;
         const uint32_t gt = (uint32_t)threadIdx.x - 64;
         uint32_t kw = 0;
         for (int c = 0; c < nck; ++c) {
             const int Cc = min(C, T - natural(c) * C);
-            if (!group_wait(bar(BAR_SCORE), c & 1, ctl, dec, gt, kBarScale, kw)) break;
+            if (!group_wait(bar(BAR_FULLC), (uint32_t)c & 1u, ctl, dec, gt, kBarScale, kw)) break;
+            // C~ is a single buffer: the state MMA of chunk c-1 must have read it.
+            if (c >= 1 && !group_wait(bar(BAR_SFULL), (uint32_t)(c - 1) & 1u, ctl, dec, gt, kBarScale, kw)) break;
             const float w = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
-            scale_rows<6>(sm + kOffB, row, w);
+            scale_rows_to<3>(sm + kOffC, sm + kOffCt, row, w);
             fence_proxy_async_smem();
             named_sync(kBarScale, kGroupThreads);
-            if (gt == 0) mbar_arrive(bar(BAR_KREADY));
+            if (gt == 0) mbar_arrive(bar(BAR_CTREADY));
         }
     } else if (warp < 10) {
         // --------------------------------------- warps 6-9: P in place over X

@@ -45,6 +45,34 @@ __device__ __forceinline__ void scale_rows(unsigned char *blk0, uint32_t row, fl
     }
 }
 
+// Row `row` of NB 64-byte-swizzled blocks at src, times w, into the same row
+// of the blocks at dst (both with stride kBlk).
+template <int NB>
+__device__ __forceinline__ void scale_rows_to(const unsigned char *src, unsigned char *dst, uint32_t row, float w) {
+    const uint32_t w2 = pack_bf16x2(w, w);
+#pragma unroll
+    for (int h6 = 0; h6 < 4 * NB; h6 += 6) {
+        uint4 v[6];
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            const int k = h6 + i;
+            v[i] = *reinterpret_cast<const uint4 *>(src + (k >> 2) * kBlk + sw64_offset(row, (uint32_t)(k & 3)));
+        }
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            v[i].x = mul_bf16x2(v[i].x, w2);
+            v[i].y = mul_bf16x2(v[i].y, w2);
+            v[i].z = mul_bf16x2(v[i].z, w2);
+            v[i].w = mul_bf16x2(v[i].w, w2);
+        }
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            const int k = h6 + i;
+            *reinterpret_cast<uint4 *>(dst + (k >> 2) * kBlk + sw64_offset(row, (uint32_t)(k & 3))) = v[i];
+        }
+    }
+}
+
 // Write 32 fp32 values (raw bits, times mul) as bf16 into row `row` of a
 // 64-byte-swizzled block.
 __device__ __forceinline__ void write_row_sw64_bits(unsigned char *blk, uint32_t row, const uint32_t (&r)[32],
