@@ -44,8 +44,8 @@
 //   ST(c)    MMA4  S      += K~^T V   -> state    (K~ scaled, S rescaled)
 //   OUT(c)   MMA2  R[c%2]  = Q~ S_prev
 //            MMA3  R[c%2] += P V      -> output   (P built, Q~ scaled)
-// with ST(c) before OUT(c) before ST(c+1). The serial chain per chunk is
-// ST + the state hand-off; P and the output run beside it.
+// with ST(c) before OUT(c); ST(c+1) may run ahead of OUT(c). The serial
+// chain per chunk is ST + the state hand-off; P and the output run beside it.
 //
 // Shared-memory operand layouts (64-byte swizzle, 32-column blocks of
 // 128 rows x 64 B): Q, K, V tiles [token][d] are K-major for Q K^T and
@@ -242,8 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t spins = 0;
             while (q23 < nck) {
                 bool progress = false;
-                // ST(c): S += K~^T V once K~ is scaled and S rescaled; after OUT(c-1)
-                if (q4 < q1 && q4 <= q23) {
+                // ST(c): S += K~^T V once K~ is scaled and S rescaled. It may run ahead
+                // of OUT(c-1): the hand-off that follows it rewrites the S_prev copy
+                // OUT(c-1) reads only after the epilogue group has seen OUT(c-1) complete.
+                if (q4 < q1) {
                     const int c = q4, s = c & 1;
                     if (mbar_test(bar(BAR_KREADY0 + s), (c >> 1) & 1) && mbar_test(bar(BAR_SBREADY), c & 1) &&
                         mbar_test(bar(BAR_FULLV0 + s), (c >> 1) & 1)) {
