@@ -201,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (qx < nck && qx == q2 && mbar_test(bar(BAR_FULLAB), (uint32_t)qx & 1u) &&
                     (qx == 0 || mbar_test(bar(BAR_OFULL), (uint32_t)(qx - 1) & 1u))) {
                     tc_fence_after();
+#pragma unroll
                     for (int ks = 0; ks < 12; ++ks) {
                         const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
                         mma_bf16_ss(tmem + kColX, smem_desc(base + kOffA + off, 16, 512, 4),
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (q1 < qx && mbar_test(bar(BAR_SBREADY), (uint32_t)q1 & 1u) &&
                     (q1 == 0 || mbar_test(bar(BAR_OEMPTY), (uint32_t)(q1 - 1) & 1u))) {
                     tc_fence_after();
+#pragma unroll
                     for (int ks = 0; ks < 12; ++ks) {
                         const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
                         const uint32_t soff = (uint32_t)(ks >> 1) * kSbBlk + (uint32_t)(ks & 1) * 32;
@@ -225,9 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (qs < q1 && mbar_test(bar(BAR_CTREADY), (uint32_t)qs & 1u)) {
                     tc_fence_after();
-                    for (int ks = 0; ks < ksteps_tok; ++ks)
+                    for_token_steps(ksteps_tok, [&](int ks) {
                         mma_bf16_ss(tmem + kColS, smem_desc(base + kOffCt + (uint32_t)ks * 1024, kBlk, 512, 4),
                                     smem_desc(base + kOffB + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
+                    });
                     mma_commit(bar(BAR_SFULL));
                     mma_commit(bar(BAR_BFREE));   // B is read by the score and the state MMAs
                     ++qs;
@@ -235,9 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (q2 < qs && mbar_test(bar(BAR_PREADY), (uint32_t)q2 & 1u)) {
                     tc_fence_after();
-                    for (int ks = 0; ks < ksteps_tok; ++ks)
+                    for_token_steps(ksteps_tok, [&](int ks) {
                         mma_bf16_ts(tmem + kColO2, tmem + kColX + 8u * (uint32_t)ks,
                                     smem_desc(base + kOffC + (uint32_t)ks * 1024, kBlk, 512, 4), idO2, ks > 0);
+                    });
                     mma_commit(bar(BAR_OFULL));
                     mma_commit(bar(BAR_CFREE));
                     ++q2;

@@ -141,10 +141,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t st = base + (uint32_t)s * kStageBytes;
-                for (int ks = 0; ks < ksteps_tok; ++ks)
+                for_token_steps(ksteps_tok, [&](int ks) {
                     mma_bf16_ss(tmem, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
                                 smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS,
                                 (c > 0 || ks > 0) ? 1u : 0u);
+                });
                 mma_commit(bar(BAR_SFULL));
                 mma_commit(bar(BAR_EMPTY0 + s));
             }

@@ -138,6 +138,20 @@ __device__ __forceinline__ void build_p_block(uint32_t (&x)[32], int n0, uint32_
     tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
 }
 
+// Calls f(ks) for the n = C / 16 token steps of a chunk (4 or 8), fully
+// unrolled: an MMA issued from a loop with a run-time trip count costs about
+// twice the issue time of one whose descriptors are formed from constants.
+template <typename F>
+__device__ __forceinline__ void for_token_steps(int n, F &&f) {
+    if (n == 8) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) f(ks);
+    } else {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) f(ks);
+    }
+}
+
 // One elected thread of a 128-thread group waits on an mbarrier; the verdict
 // is published through a two-slot flag so every thread of the group takes
 // the same branch after the group's named barrier.
