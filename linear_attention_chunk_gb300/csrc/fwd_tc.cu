@@ -115,7 +115,7 @@ struct FwdTcArgs {
 // with lambda^(col-row), the row weights swap (lambda^(Cc-1-j) on the
 // readout, lambda^(i+1) on the state update), chunks run last to first, and
 // the state is the state gradient divided by the scale.
-template <bool kRev>
+template <bool kRev, int kC>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -130,12 +130,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seg = (blockIdx.x >> 1) / a.BH;
     const int bh = (blockIdx.x >> 1) % a.BH;
     const int b = bh / a.H, h = bh % a.H;
-    const int C = a.C, T = a.T;
+    constexpr int C = kC;   // chunk length, 64 or 128: token loops are unrolled
+    const int T = a.T;
     const int cbeg = seg * a.seg_chunks;                          // first chunk of this segment
     const int nck = min(a.seg_chunks, a.nck - cbeg);              // chunks of this CTA
     const bool last_seg = seg == a.nseg - 1;
     const float *h0 = a.h0 ? a.h0 + (size_t)seg * a.h0_seg_stride : nullptr;
-    const int ksteps_tok = C / 16;
+    constexpr int ksteps_tok = C / 16;
 
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
     uint32_t *pp = reinterpret_cast<uint32_t *>(sm + kOffPair);
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s = i / (kBlk / 16), o = (i % (kBlk / 16)) * 16;
         st_shared_v4(base + s * kStageBytes + kStageK + 3 * kBlk + o, 0, 0, 0, 0);
     }
-    if (C < 128) {
+    if constexpr (C < 128) {
         const uint32_t lo = (uint32_t)C * 64, per_blk = (kBlk - lo) / 16;
         for (uint32_t i = threadIdx.x; i < 2 * 10 * per_blk; i += kThreads) {
             const uint32_t blk = i / per_blk, o = lo + (i % per_blk) * 16;
@@ -251,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_test(bar(BAR_FULLV0 + s), (c >> 1) & 1)) {
                         tc_fence_after();
                         const uint32_t st = base + (uint32_t)s * kStageBytes;
+#pragma unroll
                         for (int ks = 0; ks < ksteps_tok; ++ks)
                             mma_bf16_ss(tmem + kColS, smem_desc(st + kStageK + (uint32_t)ks * 1024, kBlk, 512, 4),
                                         smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
@@ -290,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int ks = 0; ks < 6; ++ks)
                             mma_bf16_ts(dR, tmem + kColQ + 8u * (uint32_t)ks,
                                         smem_desc(sb + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
+#pragma unroll
                         for (int ks = 0; ks < ksteps_tok; ++ks)
                             mma_bf16_ts(dR, tmem + kColP + 8u * (uint32_t)ks,
                                         smem_desc(st + kStageV + (uint32_t)ks * 1024, kBlk, 512, 4), idO, 1);
@@ -533,11 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kRev>
 cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
                                 const CUtensorMap &om, const FwdTcArgs &a, int B, cudaStream_t s, int *launches) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gla_fwd_tc_kernel<kRev>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<kRev, 128> : gla_fwd_tc_kernel<kRev, 64>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(B * a.H * 2 * a.nseg);
-    gla_fwd_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, om, a);
+    kernel<<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, om, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }
