@@ -261,3 +261,51 @@ def decode_tokens(N: int, H: int, dk: int, dv: int, *, seed: int, dtype: str = B
     k = _store(_normal(rng, (N, H, dk)), dtype)
     v = _store(_normal(rng, (N, H, dv)), dtype)
     return {"q": q, "k": k, "v": v}
+
+
+# ------------------------------------------------- variable-length prefill
+@dataclass
+class VarlenCase:
+    """Sequences of different lengths packed token-major ([total_T, H, d]),
+    with their states in a pool of n_slots fp32 states [n_slots, H, dk, dv]."""
+    lengths: np.ndarray      # [nseq] int
+    cu_seqlens: np.ndarray   # [nseq + 1] int32
+    slots: np.ndarray        # [nseq] int32, distinct
+    H: int
+    dk: int
+    dv: int
+    scale: float
+    log_lambda: np.ndarray   # [H] fp32
+    q: np.ndarray            # [total_T, H, dk]
+    k: np.ndarray
+    v: np.ndarray            # [total_T, H, dv]
+    pool: np.ndarray         # [n_slots, H, dk, dv] fp32
+
+
+def make_varlen_case(lengths, H: int, *, seed: int, n_slots: Optional[int] = None, dk: int = 96, dv: int = 192,
+                     pool_std: float = 0.1, lam_range=(0.9, 0.9999), dtype: str = BF16) -> VarlenCase:
+    """Given lengths, draw packed q, k, v ~ N(0, 1), a pool of states
+    ~ N(0, pool_std), distinct slots (a random subset of the pool, in random
+    order) and log-uniform per-head decays, in that order."""
+    rng = np.random.default_rng(seed)
+    lengths = np.asarray(lengths, dtype=np.int64)
+    nseq = len(lengths)
+    n_slots = nseq if n_slots is None else n_slots
+    cu = np.zeros(nseq + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lengths)
+    total = int(cu[-1])
+    q = _normal(rng, (total, H, dk))
+    k = _normal(rng, (total, H, dk))
+    v = _normal(rng, (total, H, dv))
+    pool = _normal(rng, (n_slots, H, dk, dv), pool_std)
+    slots = rng.permutation(n_slots)[:nseq].astype(np.int32)
+    lam = decay_log_uniform(rng, H, *lam_range)
+    return VarlenCase(lengths=lengths, cu_seqlens=cu, slots=slots, H=H, dk=dk, dv=dv,
+                      scale=float(np.float32(1.0 / math.sqrt(dk))), log_lambda=log_lambda_of(lam),
+                      q=_store(q, dtype), k=_store(k, dtype), v=_store(v, dtype), pool=pool)
+
+
+def serving_prefill_lengths(seed: int = 5, nseq: int = 64, lo: int = 64, hi: int = 4096) -> np.ndarray:
+    """Prompt lengths of a batch of staggered requests: log-uniform integers in [lo, hi]."""
+    rng = np.random.default_rng(seed)
+    return np.floor(np.exp(rng.uniform(math.log(lo), math.log(hi + 1), size=nseq))).astype(np.int64)

@@ -140,6 +140,39 @@ gla_status gla_chunk_fwd_noalloc(const void *q, const void *k, const void *v,
                                  void *o, float *hT, void *stream);
 
 /*
+ * gla_chunk_fwd_varlen -- the chunked forward over sequences of different
+ * lengths packed one after another, each entering from and leaving its state
+ * in a state pool shared with gla_decode_step. This is the prefill of a
+ * serving loop: requests arrive with prompts of any length, are prefilled
+ * together, and continue with decode steps on the same pool (the pages keep
+ * each sequence's state in a fixed-size page, "Inference optimization on
+ * Trainium2"). The recurrence is that of gla_chunk_fwd.
+ *
+ *   q, k [total_T, H, dk], v [total_T, H, dv] (bf16), packed: sequence n holds
+ *   tokens [cu_seqlens[n], cu_seqlens[n+1]); log_lambda [H] fp32; scale;
+ *   cu_seqlens [nseq + 1] int32 in device memory, cu_seqlens[0] = 0,
+ *   non-decreasing, cu_seqlens[nseq] <= total_T; slots [nseq] int32 in device
+ *   memory or NULL (sequence n uses slot n); state_pool [n_slots, H, dk, dv]
+ *   fp32, updated in place: slot slots[n] is read as the initial state of
+ *   sequence n and overwritten with its final state (a new sequence's slot
+ *   must hold zeros, or the state to continue from); o [total_T, H, dv] bf16
+ *   (written for every token of every sequence). chunk 64 or 128; dk = 96,
+ *   dv = 192, dtype GLA_BF16 only.
+ * - Slots of one call must be distinct. A sequence of length 0 leaves its
+ *   slot untouched.
+ * - cu_seqlens and slots are device data the host does not read: a bad entry
+ *   (a decreasing offset, an offset past total_T, a slot outside
+ *   [0, n_slots)) skips that sequence on the device and sets a bit that the
+ *   next gla_check() reports as GLA_ERR_INVALID_ARG.
+ * - Tokens of different sequences never mix: the last partial chunk of a
+ *   sequence masks the next sequence's rows and stores its outputs row by row.
+ */
+gla_status gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *log_lambda,
+                                float scale, const int *cu_seqlens, const int *slots, float *state_pool,
+                                int n_slots, int nseq, int total_T, int H, int dk, int dv, int chunk,
+                                gla_dtype dtype, void *o, void *stream);
+
+/*
  * gla_chunk_bwd -- gradients of L = sum_t <do_t, o_t> + <dhT, hT> through
  * the chunked forward ("Challenge 3": through every serial state update).
  * lambda is fixed (not learned), so there is no gradient for log_lambda.

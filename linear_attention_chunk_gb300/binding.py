@@ -28,7 +28,8 @@ GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_CUDA, GLA_ERR_TIMEOUT,
 GLA_BF16, GLA_FP32 = 0, 1
 
 # The public entry points declared in include/gla.h.
-ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_bwd",
+ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen",
+                 "gla_chunk_bwd",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
 
@@ -63,6 +64,9 @@ def lib():
             L.gla_chunk_fwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i,
                                                 _vp, _vp, _vp]
             L.gla_chunk_fwd_noalloc.restype = _i
+            L.gla_chunk_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                               _i, _i, _vp, _vp]
+            L.gla_chunk_fwd_varlen.restype = _i
             L.gla_chunk_fwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
             L.gla_chunk_fwd_workspace_size.restype = _sz
             L.gla_chunk_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
@@ -191,6 +195,27 @@ def gla_chunk_fwd_noalloc(q, k, v, log_lambda, h0=None, scale=None, chunk=128, *
                                      _stream(stream))
     _raise_on(st, "gla_chunk_fwd_noalloc")
     return o, hT
+
+
+def gla_chunk_fwd_varlen(q, k, v, log_lambda, cu_seqlens, state_pool, slots=None, scale=None, chunk=128, *,
+                         o=None, stream=None):
+    """Variable-length forward: q, k [total_T,H,dk], v [total_T,H,dv] bf16
+    packed, sequence n = tokens [cu_seqlens[n], cu_seqlens[n+1]) (int32 CUDA
+    tensor), state_pool [n_slots,H,dk,dv] fp32 updated in place at slots[n]
+    (int32 CUDA tensor, or None for slot n). Returns o [total_T,H,dv]."""
+    torch = _torch()
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if o is None:
+        o = torch.empty((total_T, H, dv), dtype=q.dtype, device=q.device)
+    nseq = cu_seqlens.numel() - 1
+    st = lib().gla_chunk_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), float(scale), _ptr(cu_seqlens),
+                                    _ptr(slots), _ptr(state_pool), int(state_pool.shape[0]), nseq, total_T, H,
+                                    dk, dv, int(chunk), _dtype_code(q), _ptr(o), _stream(stream))
+    _raise_on(st, "gla_chunk_fwd_varlen")
+    return o
 
 
 def gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, scale=None, chunk=128, *,

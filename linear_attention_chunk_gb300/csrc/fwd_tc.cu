@@ -107,6 +107,14 @@ struct FwdTcArgs {
     int nseg, seg_chunks, BH;
     size_t h0_seg_stride;
     unsigned int *status;
+    // Variable-length mode (kVar): BH = nseq * H; sequence n holds tokens
+    // [cu_seqlens[n], cu_seqlens[n+1]) of the packed [1, T, H, d] tensors, and
+    // its state lives in slot slots[n] (n if NULL) of h0 = hT, a [n_slots, H,
+    // dk, dv] pool, read at the start and overwritten at the end.
+    const int *cu_seqlens;
+    const int *slots;
+    int n_slots;
+    __nv_bfloat16 *o;      // the output, for the masked store of a sequence's last partial chunk
 };
 
 // kRev = false: the forward pass. kRev = true: the same chunked recurrence
@@ -115,7 +123,7 @@ struct FwdTcArgs {
 // with lambda^(col-row), the row weights swap (lambda^(Cc-1-j) on the
 // readout, lambda^(i+1) on the state update), chunks run last to first, and
 // the state is the state gradient divided by the scale.
-template <bool kRev, int kC>
+template <bool kRev, int kC, bool kVar>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -129,11 +137,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = blockIdx.x & 1;
     const int seg = (blockIdx.x >> 1) / a.BH;
     const int bh = (blockIdx.x >> 1) % a.BH;
-    const int b = bh / a.H, h = bh % a.H;
     constexpr int C = kC;   // chunk length, 64 or 128: token loops are unrolled
-    const int T = a.T;
+    const int h = bh % a.H;
+    // b: batch index of the states; bt, tok0: token coordinates of the sequence
+    int b = bh / a.H, bt = b, tok0 = 0, T = a.T, nck_seq = a.nck;
+    if constexpr (kVar) {
+        const int n = b, beg = a.cu_seqlens[n], end = a.cu_seqlens[n + 1];
+        const int slot = a.slots ? a.slots[n] : n;
+        if (beg < 0 || end < beg || end > a.T || slot < 0 || slot >= a.n_slots) {
+            if (threadIdx.x == 0) atomicOr(a.status, kDevBadState);
+            return;
+        }
+        if (end == beg) return;   // empty sequence: its state stays as it is
+        b = slot;
+        bt = 0;
+        tok0 = beg;
+        T = end - beg;
+        nck_seq = (T + C - 1) / C;
+    }
     const int cbeg = seg * a.seg_chunks;                          // first chunk of this segment
-    const int nck = min(a.seg_chunks, a.nck - cbeg);              // chunks of this CTA
+    const int nck = min(kVar ? nck_seq : a.seg_chunks, nck_seq - cbeg);   // chunks of this CTA
     const bool last_seg = seg == a.nseg - 1;
     const float *h0 = a.h0 ? a.h0 + (size_t)seg * a.h0_seg_stride : nullptr;
     constexpr int ksteps_tok = C / 16;
@@ -203,14 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, tx_qk);
 #pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStageQ + j * kBlk, &tm_q, fb, 32 * j, h, t0, b);
+                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStageQ + j * kBlk, &tm_q, fb, 32 * j, h, tok0 + t0, bt);
             }
             __syncwarp();
             nq = c + 1;
             if (c >= 2 && !lane0_wait(bar(BAR_KFREE0 + s), ph, ctl, lane)) break;
             if (lane == 0) {
 #pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStageK + j * kBlk, &tm_k, fb, 32 * j, h, t0, b);
+                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStageK + j * kBlk, &tm_k, fb, 32 * j, h, tok0 + t0, bt);
             }
             __syncwarp();
             if (c >= 2 && !lane0_wait(bar(BAR_EMPTY0 + s), ph, ctl, lane)) break;
@@ -218,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(fv, tx_v);
 #pragma unroll
                 for (int j = 0; j < 3; ++j)
-                    tma_load_4d(st + kStageV + j * kBlk, &tm_v, fv, kDvHalf * half + 32 * j, h, t0, b);
+                    tma_load_4d(st + kStageV + j * kBlk, &tm_v, fv, kDvHalf * half + 32 * j, h, tok0 + t0, bt);
             }
             __syncwarp();
             nv = c + 1;
@@ -490,15 +513,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(kBarE, kGroupThreads);
             if (gt == 0 && !last) mbar_arrive(bar(BAR_SBREADY));
 
-            // Output tile: O * scale -> bf16 -> staging -> TMA store.
+            // Output tile: O * scale -> bf16 -> staging -> TMA store. A partial last
+            // chunk of a packed variable-length sequence is stored row by row
+            // instead: its tile would overlap the next sequence's rows.
             if (!group_wait(bar(BAR_OFULL0 + s), (c >> 1) & 1, ctl, mydec, gt, kBarE, kw)) break;
             tc_fence_after();
-            if (gt == 0) tma_store_wait_read_all();   // staging free (store of chunk c-1 read it)
-            named_sync(kBarE, kGroupThreads);
+            const bool rowwise = kVar && T - t0 < C;
+            if (!rowwise) {
+                if (gt == 0) tma_store_wait_read_all();   // staging free (store of chunk c-1 read it)
+                named_sync(kBarE, kGroupThreads);
+            }
             {
                 const uint32_t src = tl + kColR + 128u * s;
+                __nv_bfloat16 *orow =
+                    kVar ? a.o + ((size_t)(tok0 + t0 + (int)row) * a.H + h) * kDv + kDvHalf * half : nullptr;
+                const bool row_in = (int)row < T - t0;
                 auto handle = [&](const uint32_t (&r)[32], int blk) {
-                    write_row_sw64_bits(sm + kOffOut + blk * kBlk, row, r, a.scale);
+                    if (!rowwise) {
+                        write_row_sw64_bits(sm + kOffOut + blk * kBlk, row, r, a.scale);
+                    } else if (row_in) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 8)
+                            *reinterpret_cast<uint4 *>(orow + 32 * blk + e) = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale),
+                                pack_bf16x2(__uint_as_float(r[e + 2]) * a.scale, __uint_as_float(r[e + 3]) * a.scale),
+                                pack_bf16x2(__uint_as_float(r[e + 4]) * a.scale, __uint_as_float(r[e + 5]) * a.scale),
+                                pack_bf16x2(__uint_as_float(r[e + 6]) * a.scale, __uint_as_float(r[e + 7]) * a.scale));
+                    }
                 };
                 uint32_t ra[32], rb[32];
                 tmem_ld_32cols(src, ra);
@@ -516,10 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(kBarE, kGroupThreads);
             if (gt == 0) {
                 mbar_arrive(bar(BAR_OEMPTY0 + s));
+                if (!rowwise) {
 #pragma unroll
-                for (int blk = 0; blk < 3; ++blk)
-                    tma_store_4d(&tm_o, base + kOffOut + blk * kBlk, kDvHalf * half + 32 * blk, h, t0, b);
-                tma_store_commit();
+                    for (int blk = 0; blk < 3; ++blk)
+                        tma_store_4d(&tm_o, base + kOffOut + blk * kBlk, kDvHalf * half + 32 * blk, h, tok0 + t0, bt);
+                    tma_store_commit();
+                }
             }
         }
         if (gt == 0) tma_store_wait_all();
@@ -536,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kRev>
 cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
                                 const CUtensorMap &om, const FwdTcArgs &a, int B, cudaStream_t s, int *launches) {
-    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<kRev, 128> : gla_fwd_tc_kernel<kRev, 64>;
+    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<kRev, 128, false> : gla_fwd_tc_kernel<kRev, 64, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(B * a.H * 2 * a.nseg);
@@ -560,7 +603,8 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mo, p.o, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     const int nck = (p.T + p.chunk - 1) / p.chunk;
-    FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, nck, 1, nck, p.B * p.H, 0, p.status};
+    FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, nck, 1, nck, p.B * p.H, 0, p.status,
+                nullptr, nullptr, 0, nullptr};
     // Few (b, h) pairs and a long sequence: split each sequence into segments
     // that run in parallel, when the caller gave the workspace for it.
     const SegPlan plan = plan_segments(p.B, p.T, p.H, p.chunk);
@@ -573,6 +617,27 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
         a.h0_seg_stride = (size_t)p.B * p.H * kDk * kDv;
     }
     return launch_chunk_kernel<false>(mq, mk, mv, mo, a, p.B, s, launches);
+}
+
+// Variable-length forward: one CTA per (sequence, head, dv half) over the
+// packed [1, total_T, H, d] tensors; states in the pool.
+cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *launches) {
+    if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
+    CUtensorMap mq, mk, mv, mo;
+    cudaError_t e;
+    if ((e = make_token_map(&mq, p.q, 1, p.total_T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mk, p.k, 1, p.total_T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mv, p.v, 1, p.total_T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mo, p.o, 1, p.total_T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    FwdTcArgs a{p.log_lambda, p.pool, p.pool, p.scale, 1.f, 1.f, p.total_T, p.H, p.chunk, 0, 1, 0, p.nseq * p.H, 0,
+                p.status, p.cu_seqlens, p.slots, p.n_slots, static_cast<__nv_bfloat16 *>(p.o)};
+    auto kernel = p.chunk == 128 ? gla_fwd_tc_kernel<false, 128, true> : gla_fwd_tc_kernel<false, 64, true>;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
+        cudaSuccess)
+        return e;
+    kernel<<<(unsigned)(p.nseq * p.H * 2), kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, a);
+    if (launches) ++*launches;
+    return cudaGetLastError();
 }
 
 // dv and dh0 of the backward pass: the chunk recurrence in reverse time with
@@ -588,7 +653,7 @@ cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches) 
     if ((e = make_token_map(&mout, p.dv_out, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     const int nck = (p.T + p.chunk - 1) / p.chunk;
     FwdTcArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, p.chunk, nck, 1, nck,
-                p.B * p.H, 0, p.status};
+                p.B * p.H, 0, p.status, nullptr, nullptr, 0, nullptr};
     return launch_chunk_kernel<true>(mrow, mcol, mval, mout, a, p.B, s, launches);
 }
 

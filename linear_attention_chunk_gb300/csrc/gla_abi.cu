@@ -199,6 +199,41 @@ gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const floa
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_bwd launch");
 }
 
+gla_status gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *log_lambda, float scale,
+                                const int *cu_seqlens, const int *slots, float *state_pool, int n_slots, int nseq,
+                                int total_T, int H, int dk, int dv, int chunk, gla_dtype dtype, void *o,
+                                void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_chunk_shape(1, total_T, H, dk, dv, chunk, dtype);
+    if (st != GLA_OK) return st;
+    if (dtype != GLA_BF16) return fail(GLA_ERR_UNSUPPORTED, "gla_chunk_fwd_varlen supports GLA_BF16 only");
+    if (nseq < 0 || n_slots < 0) return fail(GLA_ERR_INVALID_ARG, "negative nseq=%d or n_slots=%d", nseq, n_slots);
+    if ((long double)nseq * H * 2 > 2147483647.0L) return fail(GLA_ERR_INVALID_ARG, "nseq*H too large");
+    OPTIONAL_PTR(slots, "slots");
+    if (nseq == 0 || H == 0) return GLA_OK;
+    REQUIRE_PTR(log_lambda, "log_lambda");
+    REQUIRE_PTR(cu_seqlens, "cu_seqlens");
+    REQUIRE_PTR(state_pool, "state_pool");
+    if (!slots && n_slots < nseq)
+        return fail(GLA_ERR_INVALID_ARG, "without slots the pool needs nseq=%d slots, has %d", nseq, n_slots);
+    if (total_T > 0) {
+        REQUIRE_PTR(q, "q");
+        REQUIRE_PTR(k, "k");
+        REQUIRE_PTR(v, "v");
+        REQUIRE_PTR(o, "o");
+    }
+    unsigned int *status = nullptr;
+    if ((st = status_word(&status)) != GLA_OK) return st;
+    if (total_T == 0) return GLA_OK;   // every sequence is empty: no state changes
+    VarlenParams p{q, k, v, log_lambda, scale, cu_seqlens, slots, state_pool, n_slots, nseq, total_T, H, dk, dv,
+                   chunk, o, status};
+    int launches = 0;
+    const cudaError_t e = launch_fwd_varlen_tc(p, static_cast<cudaStream_t>(stream), &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_varlen launch");
+}
+
 size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype) {
     if (check_chunk_shape(B, T, H, dk, dv, chunk, dtype) != GLA_OK) return 0;
     if (dtype != GLA_BF16) return 0;
@@ -249,6 +284,9 @@ gla_status gla_check(void *stream) {
         e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail(e, "clear status word");
         if (word & kDevTimeout) return fail(GLA_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", word);
+        if (word & kDevBadState)
+            return fail(GLA_ERR_INVALID_ARG, "a sequence had a bad cu_seqlens or slots entry and was skipped "
+                                             "(status 0x%x)", word);
         return fail(GLA_ERR_CUDA, "device reported an internal error (status 0x%x)", word);
     }
     return GLA_OK;

@@ -36,6 +36,18 @@ struct BwdParams {
     unsigned int *status;
 };
 
+struct VarlenParams {
+    const void *q, *k, *v;      // packed [total_T, H, d]
+    const float *log_lambda;
+    float scale;
+    const int *cu_seqlens;      // [nseq + 1], device
+    const int *slots;           // [nseq], device, or NULL
+    float *pool;                // [n_slots, H, dk, dv] fp32 states
+    int n_slots, nseq, total_T, H, dk, dv, chunk;
+    void *o;                    // packed [total_T, H, dv]
+    unsigned int *status;
+};
+
 struct DecodeParams {
     const void *q, *k, *v;
     const float *log_lambda;
@@ -58,6 +70,8 @@ cudaError_t launch_copy_state(const float *src, float *dst, size_t n, cudaStream
 
 // tcgen05 / TMA tensor-core kernels (bf16, dk = 96, dv = 192).
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
+// Variable-length forward with the states in a pool (bf16, dk = 96, dv = 192).
+cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // dv and dh0 of the backward pass: the chunk kernel run in reverse time.
 cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches);

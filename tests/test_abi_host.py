@@ -125,3 +125,24 @@ def test_workspace_queries_are_host_only(L):
             assert binding.gla_chunk_bwd_workspace_size(B, T, 16, 96, 192, C) >= 0
     assert binding.gla_chunk_fwd_workspace_size(1, 100, 1, 5, 7, 64, binding.GLA_FP32) == 0
     assert binding.gla_chunk_fwd_workspace_size(1, 100, 1, 96, 192, 100) == 0   # invalid chunk
+
+
+def test_varlen_rejects_bad_arguments(L):
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, ll=FAKE, cu=FAKE, slots=None, pool=FAKE, n_slots=8, nseq=4, T=100, H=16,
+                 dk=96, dv=192, C=128, dt=0, o=FAKE)
+        a.update(kw)
+        return L.gla_chunk_fwd_varlen(a["q"], a["k"], a["v"], a["ll"], 0.1, a["cu"], a["slots"], a["pool"],
+                                      a["n_slots"], a["nseq"], a["T"], a["H"], a["dk"], a["dv"], a["C"], a["dt"],
+                                      a["o"], None)
+    assert call(dt=1) == binding.GLA_ERR_UNSUPPORTED          # bf16 only
+    assert call(C=32) == binding.GLA_ERR_UNSUPPORTED
+    assert call(dk=64) == binding.GLA_ERR_UNSUPPORTED
+    assert call(nseq=-1) == binding.GLA_ERR_INVALID_ARG
+    assert call(cu=None) == binding.GLA_ERR_INVALID_ARG
+    assert call(pool=None) == binding.GLA_ERR_INVALID_ARG
+    assert call(cu=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert call(slots=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert call(n_slots=3) == binding.GLA_ERR_INVALID_ARG      # no slots array: slot n for n < nseq
+    assert call(o=None) == binding.GLA_ERR_INVALID_ARG
+    assert call(nseq=0) == binding.GLA_OK                      # nothing to do, no device touched
