@@ -2,14 +2,16 @@
 """Benchmark of libgla, the Simple GLA mixer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
-                    [--mode all|fwd|fwd_bwd|decode] [--batch B] [--no-e2e] [--no-cpu-baseline]
+                    [--mode all|fwd|fwd_bwd|decode|long|varlen] [--batch B] [--no-e2e] [--no-cpu-baseline]
 
 Prints ONE JSON line (rank 0). The headline `value` is the chunked forward
 over the Laplace-layer workload (bf16, B=8, H=16, T=2048, dk=96, dv=192,
 C=128: tokens/s = B*T per call over all heads). `modes` carries the same
-measurement for the training forward+backward workload (B=16, tokens/s)
-and for the serving decode workload (1,280 sequences x 16 heads x 24
-distinct layer states per step, seq-steps/s), each with its own roofline.
+measurement for the training forward+backward workload (B=16, tokens/s),
+the serving decode workload (1,280 sequences x 16 heads x 24 distinct layer
+states per step, seq-steps/s), the long-context prefill (T=65,536, chunk 128
+and 64) and the variable-length serving prefill into the decode state pool
+(64 prompts of 64..4,096 tokens), each with its own roofline.
 
 Timing: W untimed warm-up steps, then exactly K steps between two
 barrier + synchronize pairs, on the device with CUDA events recorded on the
@@ -419,6 +421,53 @@ def bench_long(args, dist, device, stream, peaks, sampler):
     return res
 
 
+VARLEN_NSEQ, VARLEN_SLOTS = 64, 128
+
+
+def varlen_case():
+    """Serving prefill mix: 64 prompts, lengths log-uniform in [64, 4096]
+    (seed 5), H = 16, states in a pool of 128 slots."""
+    lengths = gen.serving_prefill_lengths(seed=5, nseq=VARLEN_NSEQ)
+    return gen.make_varlen_case(lengths, H, seed=5, n_slots=VARLEN_SLOTS)
+
+
+def bench_varlen(args, dist, device, stream, peaks, sampler):
+    """Variable-length prefill into the decode state pool (gla_chunk_fwd_varlen)."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    c = varlen_case()
+    q, k, v = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v))
+    ll = torch.from_numpy(c.log_lambda).to(device)
+    cu = torch.from_numpy(c.cu_seqlens).to(device)
+    slots = torch.from_numpy(c.slots).to(device)
+    pool = torch.from_numpy(c.pool.astype(np.float32)).to(device)
+    total = int(c.cu_seqlens[-1])
+    o = torch.empty((total, H, DV), dtype=torch.bfloat16, device=device)
+
+    def step():
+        gla.gla_chunk_fwd_varlen(q, k, v, ll, cu, pool, slots, c.scale, CHUNK, o=o, stream=stream)
+        return gla.gla_last_launch_count()
+
+    tot, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+    tot = dist.max(tot)
+    bytes_ = total * H * (2 * DK * 2 + 2 * DV * 2) + VARLEN_NSEQ * H * STATE_BYTES * 2
+    avg_ms = statistics.mean(per)
+    ach = bytes_ / (avg_ms * 1e-3) / 1e9
+    return {
+        "value": total * dist.world * args.steps / (tot * 1e-3), "unit": "tokens/s",
+        "ms_per_step": tot / args.steps,
+        "config": {"workload": f"serving_prefill_varlen_bf16_N{VARLEN_NSEQ}_H{H}", "sequences": VARLEN_NSEQ,
+                   "tokens": total, "lengths": "log-uniform [64, 4096], seed 5", "pool_slots": VARLEN_SLOTS,
+                   "chunk": CHUNK,
+                   "l2": f"inputs larger than L2 ({bytes_ / 1e6:.0f} MB per step), no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": bytes_,
+                     "avg_launch_ms": avg_ms, "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+
+
 def bench_decode(args, dist, device, stream, peaks, sampler):
     import torch
     import linear_attention_chunk_gb300 as gla
@@ -562,7 +611,25 @@ def cpu_baseline():
     dt, ss, nt, sample = oracle_decode_sample(1)
     modes["decode"] = {"value": ss / dt, "unit": "seq-steps/s", "cores": nt, "kind": "oracle",
                        "sample": sample, "seconds": dt}
+    dt, toks, nt, sample = oracle_varlen_sample(8)
+    modes["varlen"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                       "sample": sample, "seconds": dt}
     return base, modes
+
+
+def oracle_varlen_sample(nseq):
+    """The oracle on the first nseq prompts of the serving prefill mix, all heads."""
+    import oracle
+    c = varlen_case()
+    n = min(nseq, VARLEN_NSEQ)
+    t0 = time.perf_counter()
+    for i in range(n):
+        a, b = int(c.cu_seqlens[i]), int(c.cu_seqlens[i + 1])
+        oracle.fwd_recurrent(c.q[None, a:b], c.k[None, a:b], c.v[None, a:b], c.log_lambda,
+                             c.pool[c.slots[i]][None].astype(np.float32), c.scale)
+    dt = time.perf_counter() - t0
+    toks = int(c.cu_seqlens[n])
+    return dt, toks, os.cpu_count() or 1, f"{n} of {VARLEN_NSEQ} prompts ({toks} tokens) x {H} heads"
 
 
 def run_reference(args, dist):
@@ -600,7 +667,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gla", "reference"), default="gla")
-    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long"), default="all")
+    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long", "varlen"), default="all")
     ap.add_argument("--batch", type=int, default=0, help="override B of the fwd / fwd_bwd workloads (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the decode layer count (profiling)")
     ap.add_argument("--long-T", dest="long_T", type=int, default=0, help="override T of the long workload (profiling)")
@@ -639,6 +706,8 @@ def main(argv=None):
             results["decode"] = bench_decode(args, dist, device, stream, peaks, sampler)
         if args.mode in ("all", "long"):
             results["long"] = bench_long(args, dist, device, stream, peaks, sampler)
+        if args.mode in ("all", "varlen"):
+            results["varlen"] = bench_varlen(args, dist, device, stream, peaks, sampler)
     finally:
         sampler.stop()
 
