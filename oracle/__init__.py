@@ -16,6 +16,7 @@ Functions (all layouts token-major, see gla_oracle.c):
   bwd            -- analytic two-pass backward (O3)
   bwd_chunked    -- the chunk-level backward equations in double (O6)
   decode         -- one recurrent step per (sequence, head) (O4)
+  mixer_epilogue -- self-augmentation, Head RMSNorm and the SiLU(g) gate (O7)
 """
 from __future__ import annotations
 
@@ -65,9 +66,11 @@ def _load():
             lib.gla_oracle_decode.argtypes = [_D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L, _L,
                                               _D, ctypes.c_int]
             lib.gla_oracle_threads.argtypes = [ctypes.c_int]
+            lib.gla_oracle_mixer_epilogue.argtypes = [_D, _D, _D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L,
+                                                      _L, _D, ctypes.c_int]
             for f in ("gla_oracle_fwd_recurrent", "gla_oracle_fwd_quadratic", "gla_oracle_fwd_chunked",
                       "gla_oracle_bwd", "gla_oracle_bwd_chunked", "gla_oracle_decode",
-                      "gla_oracle_threads"):
+                      "gla_oracle_threads", "gla_oracle_mixer_epilogue"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -166,3 +169,20 @@ def decode(q, k, v, log_lambda, S, scale=1.0, nthreads=0):
     _check(lib.gla_oracle_decode(_p(q), _p(k), _p(v), _p(ll), _p(S_new), float(scale), N, H, dk, dv,
                                  _p(o), int(nthreads)), "decode")
     return o, S_new
+
+
+def mixer_epilogue(o, q, k, v, g, aug=None, norm_w=None, eps=1e-6, nthreads=0):
+    """O7: z = w * u / sqrt(mean(u^2) + eps) * SiLU(g) with u = o + sigmoid(q.(a*k)) v,
+    per (token, head). o, v, g [..., H, dv]; q, k [..., H, dk]; aug [H, dk] or None
+    (zero); norm_w [H, dv] or None (one). Returns z with o's shape."""
+    lib = _load()
+    o, q, k, v, g = map(_f64, (o, q, k, v, g))
+    H, dv = o.shape[-2], o.shape[-1]
+    dk = q.shape[-1]
+    NT = int(np.prod(o.shape[:-2]))
+    a = _f64(aug) if aug is not None else None
+    w = _f64(norm_w) if norm_w is not None else None
+    z = np.zeros_like(o)
+    _check(lib.gla_oracle_mixer_epilogue(_p(o), _p(q), _p(k), _p(v), _p(g), _p(a), _p(w), float(eps), NT, H, dk,
+                                         dv, _p(z), int(nthreads)), "mixer_epilogue")
+    return z

@@ -512,3 +512,59 @@ int gla_oracle_decode(const double *q, const double *k, const double *v,
     run_units(N * H, nthreads, decode_unit, &a);
     return 0;
 }
+
+/* ---------------------------------------------------------- mixer epilogue
+ * The per-head epilogue of the mixer, from the "GLA mixer" paragraph of the
+ * same page (its equations are images that did not survive extraction):
+ *   - self-augmentation: a gated copy of the value is added to the head's
+ *     output; the gate is the sigmoid of the query-key dot product with a
+ *     learned per-channel scaling a_h (aug_balance, zero at initialisation,
+ *     which makes the copy a half-strength skip):
+ *         u = o + sigmoid(sum_i q_i a_i k_i) v;
+ *   - Head RMSNorm over the head's dv channels with a per-channel weight w_h
+ *     (the grouping of heads into decay tiers is not given: each head is
+ *     normalised on its own):  y = w * u / sqrt(mean(u^2) + eps);
+ *   - the output gate SiLU(g) of the fused projection:  z = y * g * sigmoid(g).
+ * o, v, g, z [NT,H,dv]; q, k [NT,H,dk]; a [H,dk] (NULL: 0); w [H,dv] (NULL: 1).
+ */
+typedef struct {
+    const double *o, *q, *k, *v, *g, *a, *w;
+    double eps;
+    long H, dk, dv;
+    double *z;
+} epi_t;
+
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+static void epilogue_unit(void *ctx, long unit) {
+    const epi_t *e = (const epi_t *)ctx;
+    const long h = unit % e->H, dk = e->dk, dv = e->dv;
+    const double *q = e->q + unit * dk, *k = e->k + unit * dk;
+    const double *o = e->o + unit * dv, *v = e->v + unit * dv, *g = e->g + unit * dv;
+    double *z = e->z + unit * dv;
+    double dot = 0.0;
+    for (long i = 0; i < dk; ++i) dot += q[i] * (e->a ? e->a[h * dk + i] : 0.0) * k[i];
+    const double gate = sigmoid(dot);
+    double ss = 0.0;
+    for (long c = 0; c < dv; ++c) {
+        const double u = o[c] + gate * v[c];
+        z[c] = u;
+        ss += u * u;
+    }
+    const double r = 1.0 / sqrt(ss / (double)dv + e->eps);
+    for (long c = 0; c < dv; ++c) {
+        const double w = e->w ? e->w[h * dv + c] : 1.0;
+        z[c] = z[c] * r * w * (g[c] * sigmoid(g[c]));
+    }
+}
+
+int gla_oracle_mixer_epilogue(const double *o, const double *q, const double *k, const double *v,
+                              const double *g, const double *a, const double *w, double eps, long NT, long H,
+                              long dk, long dv, double *z, int nthreads) {
+    if (!o || !q || !k || !v || !g || !z || NT < 0 || H <= 0 || dk <= 0 || dv <= 0 || eps < 0.0) return 1;
+    epi_t e;
+    e.o = o; e.q = q; e.k = k; e.v = v; e.g = g; e.a = a; e.w = w; e.eps = eps;
+    e.H = H; e.dk = dk; e.dv = dv; e.z = z;
+    run_units(NT * H, nthreads, epilogue_unit, &e);
+    return 0;
+}
