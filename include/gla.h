@@ -208,6 +208,33 @@ gla_status gla_decode_step(const void *q, const void *k, const void *v,
                            int N, int H, int dk, int dv, gla_dtype dtype,
                            void *o, void *stream);
 
+/*
+ * The mixer epilogue, per (token or sequence, head): the reading of the
+ * "GLA mixer" paragraph, whose equations did not survive extraction:
+ *     u = o + sigmoid(q . (aug_h * k)) v     self-augmentation (aug_balance;
+ *                                            aug_h = 0 is a half-strength skip)
+ *     y = norm_w_h * u / sqrt(mean(u^2) + eps)   Head RMSNorm over the dv channels
+ *                                            (each head normalised on its own;
+ *                                            the pages group heads into decay
+ *                                            tiers without saying how)
+ *     z = y * g * sigmoid(g)                 the SiLU(g) gate of the fused projection
+ * aug [H, dk] fp32 or NULL (zero), norm_w [H, dv] fp32 or NULL (one), eps >= 0.
+ * W_out, the projection that follows, is a dense GEMM outside this library.
+ *
+ * gla_mixer_epilogue: over rows [NT, H, *] (NT = B*T tokens, or N sequences):
+ *   o, v, g, z [NT, H, dv], q, k [NT, H, dk], all of `dtype` (GLA_BF16 or
+ *   GLA_FP32); dk <= 1024, dv <= 256. z may not alias the inputs.
+ * gla_decode_step_mixer: gla_decode_step followed by the epilogue in the same
+ *   kernel (o never reaches memory); g [N, H, dv] of `dtype`, z [N, H, dv].
+ */
+gla_status gla_mixer_epilogue(const void *o, const void *q, const void *k, const void *v, const void *g,
+                              const float *aug, const float *norm_w, float eps, int NT, int H, int dk, int dv,
+                              gla_dtype dtype, void *z, void *stream);
+gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, const float *log_lambda,
+                                 float *S_inout, float scale, const void *g, const float *aug,
+                                 const float *norm_w, float eps, int N, int H, int dk, int dv, gla_dtype dtype,
+                                 void *z, void *stream);
+
 /* Synchronise `stream` and report: GLA_ERR_CUDA if the stream or an earlier
  * launch failed, GLA_ERR_TIMEOUT if a device-side wait gave up since the last
  * gla_check (the status word is cleared on read), else GLA_OK. */

@@ -24,7 +24,9 @@ from .binding import (  # noqa: F401
     gla_chunk_fwd_varlen,
     gla_chunk_fwd_workspace_size,
     gla_decode_step,
+    gla_decode_step_mixer,
     gla_last_launch_count,
+    gla_mixer_epilogue,
     gla_status_string,
     gla_version,
     lib,

@@ -30,7 +30,8 @@ GLA_BF16, GLA_FP32 = 0, 1
 # The public entry points declared in include/gla.h.
 ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen",
                  "gla_chunk_bwd",
-                 "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_check",
+                 "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
+                 "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
 
 
@@ -76,6 +77,11 @@ def lib():
             L.gla_chunk_bwd_workspace_size.restype = _sz
             L.gla_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _vp, _vp]
             L.gla_decode_step.restype = _i
+            L.gla_decode_step_mixer.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i,
+                                                _vp, _vp]
+            L.gla_decode_step_mixer.restype = _i
+            L.gla_mixer_epilogue.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _vp, _vp]
+            L.gla_mixer_epilogue.restype = _i
             L.gla_check.argtypes = [_vp]
             L.gla_check.restype = _i
             L.gla_status_string.argtypes = [_i]
@@ -259,6 +265,37 @@ def gla_decode_step(q, k, v, log_lambda, S, scale=None, *, o=None, stream=None):
                                N, H, dk, dv, dt, _ptr(o), _stream(stream))
     _raise_on(st, "gla_decode_step")
     return o
+
+
+def gla_decode_step_mixer(q, k, v, log_lambda, S, g, aug=None, norm_w=None, eps=1e-6, scale=None, *, z=None,
+                          stream=None):
+    """Decode step plus the mixer epilogue in one kernel. Returns z [N,H,dv]."""
+    torch = _torch()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if z is None:
+        z = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    st = lib().gla_decode_step_mixer(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(S), float(scale), _ptr(g),
+                                     _ptr(aug), _ptr(norm_w), float(eps), N, H, dk, dv, _dtype_code(q), _ptr(z),
+                                     _stream(stream))
+    _raise_on(st, "gla_decode_step_mixer")
+    return z
+
+
+def gla_mixer_epilogue(o, q, k, v, g, aug=None, norm_w=None, eps=1e-6, *, z=None, stream=None):
+    """The mixer epilogue over [..., H, d] rows (any leading dims). Returns z like o."""
+    torch = _torch()
+    H, dv = o.shape[-2], o.shape[-1]
+    dk = q.shape[-1]
+    NT = o.numel() // (H * dv)
+    if z is None:
+        z = torch.empty_like(o)
+    st = lib().gla_mixer_epilogue(_ptr(o), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(aug), _ptr(norm_w), float(eps),
+                                  NT, H, dk, dv, _dtype_code(o), _ptr(z), _stream(stream))
+    _raise_on(st, "gla_mixer_epilogue")
+    return z
 
 
 def gla_check(stream=None):

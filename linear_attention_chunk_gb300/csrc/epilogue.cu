@@ -1,0 +1,95 @@
+// epilogue.cu -- the per-head epilogue of the Simple GLA mixer, from the
+// "GLA mixer" paragraph of "Beyond the KV cache: Training and serving i14's
+// Laplace 3B linear attention model on AWS Trainium2 with native PyTorch"
+// (its equations did not survive extraction; the reading):
+//     u = o + sigmoid(q . (a * k)) v       self-augmentation, a = aug_balance of the head
+//     y = w * u / sqrt(mean(u^2) + eps)    Head RMSNorm over the head's dv channels
+//     z = y * g * sigmoid(g)               the SiLU(g) output gate
+// per (token, head). A stream over o, q, k, v, g in and z out (1,920 bytes
+// per head-token at bf16, dk = 96, dv = 192): one warp per (token, head),
+// lanes striding over channels so that every load instruction of a warp
+// reads consecutive bytes; the two reductions are warp shuffles.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gla {
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + __expf(-x)); }
+
+// DK, DV: compile-time channel counts (0: take them from the parameters).
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_kernel(EpilogueParams p) {
+    const size_t row = (size_t)blockIdx.x * kWarps + threadIdx.x / 32;   // token * H + head
+    const int lane = threadIdx.x % 32;
+    if (row >= (size_t)p.NT * p.H) return;
+    const int h = (int)(row % (size_t)p.H);
+    const int dk = DK ? DK : p.dk, dv = DV ? DV : p.dv;
+    const T *q = static_cast<const T *>(p.q) + row * dk;
+    const T *k = static_cast<const T *>(p.k) + row * dk;
+    const T *o = static_cast<const T *>(p.o) + row * dv;
+    const T *v = static_cast<const T *>(p.v) + row * dv;
+    const T *g = static_cast<const T *>(p.g) + row * dv;
+    T *z = static_cast<T *>(p.z) + row * dv;
+    const float *a = p.aug ? p.aug + (size_t)h * dk : nullptr;
+    const float *w = p.norm_w ? p.norm_w + (size_t)h * dv : nullptr;
+
+    float dot = 0.f;
+    if (a) {
+#pragma unroll 4
+        for (int i = lane; i < dk; i += 32) dot += Elem<T>::load(q + i) * a[i] * Elem<T>::load(k + i);
+    }
+    const float gate = sigmoidf_(warp_sum(dot));
+
+    constexpr int kMaxPer = 8;   // dv <= 256
+    float u[kMaxPer];
+    float ss = 0.f;
+#pragma unroll
+    for (int m = 0; m < kMaxPer; ++m) {
+        const int c = lane + 32 * m;
+        u[m] = 0.f;
+        if (c < dv) {
+            u[m] = fmaf(gate, Elem<T>::load(v + c), Elem<T>::load(o + c));
+            ss = fmaf(u[m], u[m], ss);
+        }
+    }
+    const float r = rsqrtf(warp_sum(ss) / (float)dv + p.eps);
+#pragma unroll
+    for (int m = 0; m < kMaxPer; ++m) {
+        const int c = lane + 32 * m;
+        if (c < dv) {
+            const float gc = Elem<T>::load(g + c);
+            Elem<T>::store(z + c, u[m] * r * (w ? w[c] : 1.f) * gc * sigmoidf_(gc));
+        }
+    }
+}
+
+template <typename T>
+cudaError_t epilogue_impl(const EpilogueParams &p, cudaStream_t s, int *launches) {
+    const size_t rows = (size_t)p.NT * p.H;
+    if (rows == 0) return cudaSuccess;
+    const size_t blocks = (rows + kWarps - 1) / kWarps;
+    if (blocks > 0x7fffffffull) return cudaErrorInvalidValue;
+    if (p.dk == 96 && p.dv == 192)
+        mixer_epilogue_kernel<T, 96, 192><<<(unsigned)blocks, 32 * kWarps, 0, s>>>(p);
+    else
+        mixer_epilogue_kernel<T, 0, 0><<<(unsigned)blocks, 32 * kWarps, 0, s>>>(p);
+    if (launches) ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mixer_epilogue(const EpilogueParams &p, bool bf16, cudaStream_t s, int *launches) {
+    return bf16 ? epilogue_impl<__nv_bfloat16>(p, s, launches) : epilogue_impl<float>(p, s, launches);
+}
+
+}  // namespace gla

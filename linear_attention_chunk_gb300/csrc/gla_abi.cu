@@ -91,6 +91,41 @@ gla_status check_chunk_shape(int B, int T, int H, int dk, int dv, int chunk, gla
         if ((p) && !aligned16(p)) return fail(GLA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
     } while (0)
 
+// The decode step with or without the mixer epilogue (g == NULL: plain o).
+gla_status decode_common(const void *q, const void *k, const void *v, const float *log_lambda, float *S_inout,
+                         float scale, const void *g, const float *aug, const float *norm_w, float eps, int N,
+                         int H, int dk, int dv, gla_dtype dtype, void *o, void *stream, const char *name) {
+    t_err[0] = 0;
+    t_launches = 0;
+    if (dtype != GLA_BF16 && dtype != GLA_FP32) return fail(GLA_ERR_INVALID_ARG, "dtype %d invalid", (int)dtype);
+    if (N < 0 || H < 0) return fail(GLA_ERR_INVALID_ARG, "negative size N=%d H=%d", N, H);
+    if (dk <= 0 || dv <= 0) return fail(GLA_ERR_INVALID_ARG, "dk=%d dv=%d must be positive", dk, dv);
+    if (dtype == GLA_BF16 && (dk != 96 || dv != 192))
+        return fail(GLA_ERR_UNSUPPORTED, "GLA_BF16 needs dk=96, dv=192 (got %d, %d)", dk, dv);
+    if (dtype == GLA_FP32 && (dk > 128 || dv > 256))
+        return fail(GLA_ERR_UNSUPPORTED, "GLA_FP32 needs dk <= 128, dv <= 256 (got %d, %d)", dk, dv);
+    if ((long double)N * H > 2147483647.0L) return fail(GLA_ERR_INVALID_ARG, "N*H too large");
+    if (!(eps >= 0.f)) return fail(GLA_ERR_INVALID_ARG, "eps must be >= 0");
+    OPTIONAL_PTR(aug, "aug");
+    OPTIONAL_PTR(norm_w, "norm_w");
+    if (N == 0 || H == 0) return GLA_OK;
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(log_lambda, "log_lambda");
+    REQUIRE_PTR(S_inout, "S_inout");
+    REQUIRE_PTR(o, name);
+    unsigned int *status = nullptr;
+    gla_status st = status_word(&status);
+    if (st != GLA_OK) return st;
+    DecodeParams p{q, k, v, log_lambda, S_inout, scale, N, H, dk, dv, o, status, g, aug, norm_w, eps};
+    int launches = 0;
+    cudaError_t e = launch_decode(p, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "decode launch");
+}
+
+
 }  // namespace
 
 void set_error_detail(const char *fmt, ...) {
@@ -243,31 +278,47 @@ size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int chu
 gla_status gla_decode_step(const void *q, const void *k, const void *v, const float *log_lambda,
                            float *S_inout, float scale, int N, int H, int dk, int dv, gla_dtype dtype,
                            void *o, void *stream) {
+    return decode_common(q, k, v, log_lambda, S_inout, scale, nullptr, nullptr, nullptr, 0.f, N, H, dk, dv, dtype,
+                         o, stream, "o");
+}
+
+gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, const float *log_lambda,
+                                 float *S_inout, float scale, const void *g, const float *aug,
+                                 const float *norm_w, float eps, int N, int H, int dk, int dv, gla_dtype dtype,
+                                 void *z, void *stream) {
+    if (N > 0 && H > 0) {
+        if (!g) return fail(GLA_ERR_INVALID_ARG, "g is NULL");
+        if (!aligned16(g)) return fail(GLA_ERR_INVALID_ARG, "g is not 16-byte aligned");
+    }
+    return decode_common(q, k, v, log_lambda, S_inout, scale, g, aug, norm_w, eps, N, H, dk, dv, dtype, z, stream,
+                         "z");
+}
+
+gla_status gla_mixer_epilogue(const void *o, const void *q, const void *k, const void *v, const void *g,
+                              const float *aug, const float *norm_w, float eps, int NT, int H, int dk, int dv,
+                              gla_dtype dtype, void *z, void *stream) {
     t_err[0] = 0;
     t_launches = 0;
     if (dtype != GLA_BF16 && dtype != GLA_FP32) return fail(GLA_ERR_INVALID_ARG, "dtype %d invalid", (int)dtype);
-    if (N < 0 || H < 0) return fail(GLA_ERR_INVALID_ARG, "negative size N=%d H=%d", N, H);
+    if (NT < 0 || H < 0) return fail(GLA_ERR_INVALID_ARG, "negative size NT=%d H=%d", NT, H);
     if (dk <= 0 || dv <= 0) return fail(GLA_ERR_INVALID_ARG, "dk=%d dv=%d must be positive", dk, dv);
-    if (dtype == GLA_BF16 && (dk != 96 || dv != 192))
-        return fail(GLA_ERR_UNSUPPORTED, "GLA_BF16 needs dk=96, dv=192 (got %d, %d)", dk, dv);
-    if (dtype == GLA_FP32 && (dk > 128 || dv > 256))
-        return fail(GLA_ERR_UNSUPPORTED, "GLA_FP32 needs dk <= 128, dv <= 256 (got %d, %d)", dk, dv);
-    if ((long double)N * H > 2147483647.0L) return fail(GLA_ERR_INVALID_ARG, "N*H too large");
-    if (N == 0 || H == 0) return GLA_OK;
+    if (dk > 1024 || dv > 256) return fail(GLA_ERR_UNSUPPORTED, "needs dk <= 1024, dv <= 256 (got %d, %d)", dk, dv);
+    if ((long double)NT * H > 2147483647.0L * 8.0L) return fail(GLA_ERR_INVALID_ARG, "NT*H too large");
+    if (!(eps >= 0.f)) return fail(GLA_ERR_INVALID_ARG, "eps must be >= 0");
+    OPTIONAL_PTR(aug, "aug");
+    OPTIONAL_PTR(norm_w, "norm_w");
+    if (NT == 0 || H == 0) return GLA_OK;
+    REQUIRE_PTR(o, "o");
     REQUIRE_PTR(q, "q");
     REQUIRE_PTR(k, "k");
     REQUIRE_PTR(v, "v");
-    REQUIRE_PTR(log_lambda, "log_lambda");
-    REQUIRE_PTR(S_inout, "S_inout");
-    REQUIRE_PTR(o, "o");
-    unsigned int *status = nullptr;
-    gla_status st = status_word(&status);
-    if (st != GLA_OK) return st;
-    DecodeParams p{q, k, v, log_lambda, S_inout, scale, N, H, dk, dv, o, status};
+    REQUIRE_PTR(g, "g");
+    REQUIRE_PTR(z, "z");
+    EpilogueParams p{o, q, k, v, g, aug, norm_w, eps, NT, H, dk, dv, z};
     int launches = 0;
-    cudaError_t e = launch_decode(p, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
+    cudaError_t e = launch_mixer_epilogue(p, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
     t_launches = launches;
-    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_decode_step launch");
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_mixer_epilogue launch");
 }
 
 gla_status gla_check(void *stream) {

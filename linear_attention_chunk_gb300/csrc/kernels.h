@@ -54,9 +54,23 @@ struct DecodeParams {
     float *S;
     float scale;
     int N, H, dk, dv;
-    void *o;
+    void *o;                 // o, or z when g is given
     unsigned int *status;
+    // mixer epilogue (g != NULL): aug [H, dk] (NULL: 0), norm_w [H, dv] (NULL: 1)
+    const void *g;
+    const float *aug, *norm_w;
+    float eps;
 };
+
+// The mixer epilogue over [NT, H, d] rows (epilogue.cu).
+struct EpilogueParams {
+    const void *o, *q, *k, *v, *g;
+    const float *aug, *norm_w;
+    float eps;
+    int NT, H, dk, dv;
+    void *z;
+};
+cudaError_t launch_mixer_epilogue(const EpilogueParams &p, bool bf16, cudaStream_t s, int *launches);
 
 // SIMT kernels (any dk <= 128, dv <= 256; fp32 or bf16 elements).
 cudaError_t launch_fwd_simt(const FwdParams &p, bool bf16, cudaStream_t s, int *launches);

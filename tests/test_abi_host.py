@@ -146,3 +146,31 @@ def test_varlen_rejects_bad_arguments(L):
     assert call(n_slots=3) == binding.GLA_ERR_INVALID_ARG      # no slots array: slot n for n < nseq
     assert call(o=None) == binding.GLA_ERR_INVALID_ARG
     assert call(nseq=0) == binding.GLA_OK                      # nothing to do, no device touched
+
+
+def test_epilogue_entry_points_reject_bad_arguments(L):
+    def epi(**kw):
+        a = dict(o=FAKE, q=FAKE, k=FAKE, v=FAKE, g=FAKE, aug=None, w=None, eps=1e-6, NT=10, H=4, dk=96, dv=192, dt=0,
+                 z=FAKE)
+        a.update(kw)
+        return L.gla_mixer_epilogue(a["o"], a["q"], a["k"], a["v"], a["g"], a["aug"], a["w"], a["eps"], a["NT"],
+                                    a["H"], a["dk"], a["dv"], a["dt"], a["z"], None)
+    assert epi(dt=5) == binding.GLA_ERR_INVALID_ARG
+    assert epi(NT=-1) == binding.GLA_ERR_INVALID_ARG
+    assert epi(dv=300) == binding.GLA_ERR_UNSUPPORTED
+    assert epi(eps=-1.0) == binding.GLA_ERR_INVALID_ARG
+    assert epi(g=None) == binding.GLA_ERR_INVALID_ARG
+    assert epi(aug=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert epi(NT=0) == binding.GLA_OK
+
+    def dec(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, ll=FAKE, S=FAKE, g=FAKE, aug=None, w=None, eps=1e-6, N=4, H=16, dk=96,
+                 dv=192, dt=0, z=FAKE)
+        a.update(kw)
+        return L.gla_decode_step_mixer(a["q"], a["k"], a["v"], a["ll"], a["S"], 0.1, a["g"], a["aug"], a["w"],
+                                       a["eps"], a["N"], a["H"], a["dk"], a["dv"], a["dt"], a["z"], None)
+    assert dec(g=None) == binding.GLA_ERR_INVALID_ARG
+    assert dec(g=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert dec(dk=64) == binding.GLA_ERR_UNSUPPORTED
+    assert dec(eps=-1.0) == binding.GLA_ERR_INVALID_ARG
+    assert dec(N=0) == binding.GLA_OK
