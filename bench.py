@@ -2,7 +2,8 @@
 """Benchmark of libgla, the Simple GLA mixer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
-                    [--mode all|fwd|fwd_bwd|decode|long|varlen] [--batch B] [--no-e2e] [--no-cpu-baseline]
+                    [--mode all|fwd|fwd_bwd|decode|long|varlen|mixer] [--batch B] [--no-e2e]
+                    [--no-cpu-baseline]
 
 Prints ONE JSON line (rank 0). The headline `value` is the chunked forward
 over the Laplace-layer workload (bf16, B=8, H=16, T=2048, dk=96, dv=192,
@@ -11,7 +12,9 @@ measurement for the training forward+backward workload (B=16, tokens/s),
 the serving decode workload (1,280 sequences x 16 heads x 24 distinct layer
 states per step, seq-steps/s), the long-context prefill (T=65,536, chunk 128
 and 64) and the variable-length serving prefill into the decode state pool
-(64 prompts of 64..4,096 tokens), each with its own roofline.
+(64 prompts of 64..4,096 tokens), and the mixer epilogue (fused into the
+decode step, and standalone over the layer-forward output), each with its
+own roofline.
 
 Timing: W untimed warm-up steps, then exactly K steps between two
 barrier + synchronize pairs, on the device with CUDA events recorded on the
@@ -520,6 +523,93 @@ def bench_decode(args, dist, device, stream, peaks, sampler):
     return res
 
 
+def bench_mixer(args, dist, device, stream, peaks, sampler):
+    """The mixer epilogue (self-augmentation, Head RMSNorm, SiLU(g) gate):
+    fused into the serving decode step (1,280 x 16 x 24 layer-steps), and the
+    standalone kernel over the layer-forward output (8 x 2048 x 16)."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    N, L = 1280, args.layers or 24
+    gen_t = torch.Generator(device=device)
+    gen_t.manual_seed(3)
+    states = []
+    for _ in range(L):
+        S = torch.randn((N, H, DK, DV), generator=gen_t, device=device, dtype=torch.float32)
+        S.mul_(0.1)
+        states.append(S)
+    toks, gates = [], []
+    for layer in range(L):
+        dc = gen.decode_tokens(N, H, DK, DV, seed=3 + 1000 * layer)
+        toks.append(tuple(dev_tensor(x, "bf16", device) for x in (dc["q"], dc["k"], dc["v"])))
+        gates.append(torch.randn((N, H, DV), generator=gen_t, device=device).to(torch.bfloat16))
+    ll = torch.from_numpy(gen.log_lambda_of(gen.decay_layer_schedule(H))).to(device)
+    aug = (0.3 * torch.randn((H, DK), generator=gen_t, device=device)).contiguous()
+    nw = (1.0 + 0.1 * torch.randn((H, DV), generator=gen_t, device=device)).contiguous()
+    outs = [torch.empty((N, H, DV), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    scale = 1.0 / math.sqrt(DK)
+
+    def step():
+        n = 0
+        for layer in range(L):
+            q, k, v = toks[layer]
+            gla.gla_decode_step_mixer(q, k, v, ll, states[layer], gates[layer], aug, nw, 1e-6, scale,
+                                      z=outs[layer], stream=stream)
+            n += gla.gla_last_launch_count()
+        return n
+
+    total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    bytes_, _ = decode_work(N)
+    bytes_ += N * H * DV * 2                      # g
+    avg_launch_ms = statistics.mean(per) / L
+    ach = bytes_ / (avg_launch_ms * 1e-3) / 1e9
+    dec = {
+        "value": N * dist.world * args.steps / (total * 1e-3), "unit": "seq-steps/s",
+        "ms_per_step": total / args.steps, "ms_per_layer_step": total / args.steps / L,
+        "config": {"workload": f"serving_decode_mixer_bf16_N{N}_H16_L{L}", "N": N, "H": H, "layers": L,
+                   "epilogue": "fused: self-augmentation, Head RMSNorm, SiLU(g)",
+                   "l2": f"{L} distinct 1.5 GB states per step, larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": bytes_,
+                     "avg_launch_ms": avg_launch_ms, "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    del states, toks, gates, outs
+
+    B, T = args.batch or 8, 2048
+    rows = B * T * H
+    shp = lambda d: (B, T, H, d)
+    o = torch.randn(shp(DV), generator=gen_t, device=device).to(torch.bfloat16)
+    v = torch.randn(shp(DV), generator=gen_t, device=device).to(torch.bfloat16)
+    g = torch.randn(shp(DV), generator=gen_t, device=device).to(torch.bfloat16)
+    q = torch.randn(shp(DK), generator=gen_t, device=device).to(torch.bfloat16)
+    k = torch.randn(shp(DK), generator=gen_t, device=device).to(torch.bfloat16)
+    z = torch.empty_like(o)
+
+    def step2():
+        gla.gla_mixer_epilogue(o, q, k, v, g, aug, nw, 1e-6, z=z, stream=stream)
+        return gla.gla_last_launch_count()
+
+    total, per, win, launches = time_steps(step2, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    bytes2 = rows * (3 * DV * 2 + 2 * DK * 2 + DV * 2)
+    avg_ms = statistics.mean(per)
+    ach2 = bytes2 / (avg_ms * 1e-3) / 1e9
+    dec["standalone"] = {
+        "value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+        "ms_per_step": total / args.steps,
+        "config": {"workload": f"mixer_epilogue_bf16_B{B}_H16_T{T}", "B": B, "T": T, "H": H,
+                   "l2": f"inputs larger than L2 ({bytes2 / 1e6:.0f} MB per step), no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach2, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach2 / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": bytes2,
+                     "avg_launch_ms": avg_ms, "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    return dec
+
+
 def e2e_decode(args, dist, device, stream, toks, states, ll, scale, N, L):
     """Decode through the public API with host token buffers: per step the 24
     layers' q, k, v come from pinned host memory and the 24 outputs go back;
@@ -667,7 +757,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gla", "reference"), default="gla")
-    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long", "varlen"), default="all")
+    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long", "varlen", "mixer"),
+                    default="all")
     ap.add_argument("--batch", type=int, default=0, help="override B of the fwd / fwd_bwd workloads (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the decode layer count (profiling)")
     ap.add_argument("--long-T", dest="long_T", type=int, default=0, help="override T of the long workload (profiling)")
@@ -708,6 +799,8 @@ def main(argv=None):
             results["long"] = bench_long(args, dist, device, stream, peaks, sampler)
         if args.mode in ("all", "varlen"):
             results["varlen"] = bench_varlen(args, dist, device, stream, peaks, sampler)
+        if args.mode in ("all", "mixer"):
+            results["mixer"] = bench_mixer(args, dist, device, stream, peaks, sampler)
     finally:
         sampler.stop()
 
@@ -725,6 +818,7 @@ def main(argv=None):
         "gpu_launches": head["gpu_launches"],
         "clocks": head["clocks"],
         "modes": {k: v for k, v in results.items() if k != head_key},
+        **{key: head[key] for key in ("standalone", "chunk64", "ms_per_layer_step") if key in head},
         "peaks": peaks,
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
