@@ -7,8 +7,10 @@
 //     z = y * g * sigmoid(g)               the SiLU(g) output gate
 // per (token, head). A stream over o, q, k, v, g in and z out (1,920 bytes
 // per head-token at bf16, dk = 96, dv = 192): one warp per (token, head),
-// lanes striding over channels so that every load instruction of a warp
-// reads consecutive bytes; the two reductions are warp shuffles.
+// 16-byte loads for the bf16 96 x 192 shape (lanes striding over channels
+// otherwise); the two reductions are warp shuffles.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -72,13 +74,70 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_kernel(EpiloguePar
     }
 }
 
+// bf16, dk = 96, dv = 192: one warp per row with 16-byte accesses; lane l < 24
+// owns channels 8l..8l+7 of o, v, g, z and lane l < 12 dims 8l..8l+7 of q, k.
+__global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(EpilogueParams p) {
+    const size_t row = (size_t)blockIdx.x * kWarps + threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    if (row >= (size_t)p.NT * p.H) return;
+    const int h = (int)(row % (size_t)p.H);
+    uint4 ov = make_uint4(0, 0, 0, 0), vv = ov, gv = ov, qv = ov, kv = ov;
+    if (lane < 24) {
+        ov = __ldcs(static_cast<const uint4 *>(p.o) + row * 24 + lane);
+        vv = __ldcs(static_cast<const uint4 *>(p.v) + row * 24 + lane);
+        gv = __ldcs(static_cast<const uint4 *>(p.g) + row * 24 + lane);
+    }
+    if (lane < 12 && p.aug) {
+        qv = __ldcs(static_cast<const uint4 *>(p.q) + row * 12 + lane);
+        kv = __ldcs(static_cast<const uint4 *>(p.k) + row * 12 + lane);
+    }
+    float dot = 0.f;
+    if (lane < 12 && p.aug) {
+        const float *a = p.aug + (size_t)h * 96 + 8 * lane;
+        const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 qf = unpack_bf16x2(qw[e]), kf = unpack_bf16x2(kw[e]);
+            dot = fmaf(qf.x * a[2 * e], kf.x, dot);
+            dot = fmaf(qf.y * a[2 * e + 1], kf.y, dot);
+        }
+    }
+    const float gate = sigmoidf_(warp_sum(dot));
+    float u[8];
+    float ss = 0.f;
+    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 of = unpack_bf16x2(ow[e]), vf = unpack_bf16x2(vw[e]);
+        u[2 * e] = fmaf(gate, vf.x, of.x);
+        u[2 * e + 1] = fmaf(gate, vf.y, of.y);
+        ss = fmaf(u[2 * e], u[2 * e], fmaf(u[2 * e + 1], u[2 * e + 1], ss));
+    }
+    const float r = rsqrtf(warp_sum(ss) / 192.f + p.eps);
+    if (lane < 24) {
+        const float *w = p.norm_w ? p.norm_w + (size_t)h * 192 + 8 * lane : nullptr;
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+        uint32_t zw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 gf = unpack_bf16x2(gw[e]);
+            const float z0 = u[2 * e] * r * (w ? w[2 * e] : 1.f) * gf.x * sigmoidf_(gf.x);
+            const float z1 = u[2 * e + 1] * r * (w ? w[2 * e + 1] : 1.f) * gf.y * sigmoidf_(gf.y);
+            zw[e] = pack_bf16x2(z0, z1);
+        }
+        __stcs(static_cast<uint4 *>(p.z) + row * 24 + lane, make_uint4(zw[0], zw[1], zw[2], zw[3]));
+    }
+}
+
 template <typename T>
 cudaError_t epilogue_impl(const EpilogueParams &p, cudaStream_t s, int *launches) {
     const size_t rows = (size_t)p.NT * p.H;
     if (rows == 0) return cudaSuccess;
     const size_t blocks = (rows + kWarps - 1) / kWarps;
     if (blocks > 0x7fffffffull) return cudaErrorInvalidValue;
-    if (p.dk == 96 && p.dv == 192)
+    if (std::is_same<T, __nv_bfloat16>::value && p.dk == 96 && p.dv == 192)
+        mixer_epilogue_bf16_kernel<<<(unsigned)blocks, 32 * kWarps, 0, s>>>(p);
+    else if (p.dk == 96 && p.dv == 192)
         mixer_epilogue_kernel<T, 96, 192><<<(unsigned)blocks, 32 * kWarps, 0, s>>>(p);
     else
         mixer_epilogue_kernel<T, 0, 0><<<(unsigned)blocks, 32 * kWarps, 0, s>>>(p);
