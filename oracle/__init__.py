@@ -17,6 +17,7 @@ Functions (all layouts token-major, see gla_oracle.c):
   bwd_chunked    -- the chunk-level backward equations in double (O6)
   decode         -- one recurrent step per (sequence, head) (O4)
   mixer_epilogue -- self-augmentation, Head RMSNorm and the SiLU(g) gate (O7)
+  conv1d         -- causal depthwise Conv1d (width 4) with SiLU and its window (O8)
 """
 from __future__ import annotations
 
@@ -68,9 +69,10 @@ def _load():
             lib.gla_oracle_threads.argtypes = [ctypes.c_int]
             lib.gla_oracle_mixer_epilogue.argtypes = [_D, _D, _D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L,
                                                       _L, _D, ctypes.c_int]
+            lib.gla_oracle_conv1d.argtypes = [_D, _D, _D, _D, _L, _L, _L, _D, _D, ctypes.c_int]
             for f in ("gla_oracle_fwd_recurrent", "gla_oracle_fwd_quadratic", "gla_oracle_fwd_chunked",
                       "gla_oracle_bwd", "gla_oracle_bwd_chunked", "gla_oracle_decode",
-                      "gla_oracle_threads", "gla_oracle_mixer_epilogue"):
+                      "gla_oracle_threads", "gla_oracle_mixer_epilogue", "gla_oracle_conv1d"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -186,3 +188,19 @@ def mixer_epilogue(o, q, k, v, g, aug=None, norm_w=None, eps=1e-6, nthreads=0):
     _check(lib.gla_oracle_mixer_epilogue(_p(o), _p(q), _p(k), _p(v), _p(g), _p(a), _p(w), float(eps), NT, H, dk,
                                          dv, _p(z), int(nthreads)), "mixer_epilogue")
     return z
+
+
+def conv1d(x, w, b=None, window=None, nthreads=0):
+    """O8: y_t = SiLU(sum_i w[:, i] x_{t-3+i} + b) per channel. x [B,T,D], w [D,4],
+    b [D] or None, window [B,4,D] (the sequence's last four inputs before x,
+    oldest first) or None (zeros). Returns (y, window_out)."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    b = _f64(b)
+    win = _f64(window)
+    B, T, D = x.shape
+    y = np.zeros_like(x)
+    win_out = np.zeros((B, 4, D))
+    _check(lib.gla_oracle_conv1d(_p(x), _p(w), _p(b), _p(win), B, T, D, _p(y), _p(win_out), int(nthreads)),
+           "conv1d")
+    return y, win_out

@@ -568,3 +568,52 @@ int gla_oracle_mixer_epilogue(const double *o, const double *q, const double *k,
     run_units(NT * H, nthreads, epilogue_unit, &e);
     return 0;
 }
+
+/* ------------------------------------------------- causal depthwise Conv1d
+ * The token filter in front of the mixer: "Beyond the KV cache: Training and
+ * serving i14's Laplace 3B linear attention model on AWS Trainium2 with
+ * native PyTorch", section "i14 and the Laplace 3B architecture", paragraph
+ * "Normalisation and convolution": after its LayerNorm, each token's residual
+ * vector passes a depthwise causal Conv1d of width 4 with SiLU, a 4-gram
+ * summary per position. No equation is printed; the reading, per channel c:
+ *     y_t[c] = SiLU( sum_{i=0..3} w[c][i] x_{t-3+i}[c] + b[c] ).
+ * Inputs before the call's first token come from the conv window: the last
+ * four inputs of the sequence so far, oldest first (zero for a new sequence;
+ * its oldest row is carried but never multiplied). The window after the call
+ * holds the sequence's last four inputs. A 4 x D window per layer in fp32 is
+ * what makes the per-sequence state add up to the 29.5 MB the page states.
+ * x, y [B,T,D]; w [D,4]; b [D] (NULL: 0); win_in, win_out [B,4,D] (win_in
+ * NULL: zeros; win_out NULL: not written).
+ */
+typedef struct {
+    const double *x, *w, *b, *win_in;
+    long T, D;
+    double *y, *win_out;
+} conv_t;
+
+/* Input at position p of sequence bi, channel c; p < 0 reads the window. */
+static double conv_input(const conv_t *a, long bi, long c, long p) {
+    if (p >= 0) return a->x[(bi * a->T + p) * a->D + c];
+    return a->win_in ? a->win_in[(bi * 4 + 4 + p) * a->D + c] : 0.0;   /* p = -1 is row 3 */
+}
+
+static void conv_unit(void *ctx, long unit) {   /* unit = b * D + c */
+    const conv_t *a = (const conv_t *)ctx;
+    const long bi = unit / a->D, c = unit % a->D, T = a->T, D = a->D;
+    for (long t = 0; t < T; ++t) {
+        double acc = a->b ? a->b[c] : 0.0;
+        for (int i = 0; i < 4; ++i) acc += a->w[c * 4 + i] * conv_input(a, bi, c, t - 3 + i);
+        a->y[(bi * T + t) * D + c] = acc * sigmoid(acc);
+    }
+    if (a->win_out)
+        for (int r = 0; r < 4; ++r) a->win_out[(bi * 4 + r) * D + c] = conv_input(a, bi, c, T - 4 + r);
+}
+
+int gla_oracle_conv1d(const double *x, const double *w, const double *b, const double *win_in, long B, long T,
+                      long D, double *y, double *win_out, int nthreads) {
+    if (!x || !w || !y || B < 0 || T < 0 || D <= 0) return 1;
+    conv_t a;
+    a.x = x; a.w = w; a.b = b; a.win_in = win_in; a.T = T; a.D = D; a.y = y; a.win_out = win_out;
+    run_units(B * D, nthreads, conv_unit, &a);
+    return 0;
+}
