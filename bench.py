@@ -2,7 +2,7 @@
 """Benchmark of libgla, the Simple GLA mixer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
-                    [--mode all|fwd|fwd_bwd|decode|long|varlen|mixer] [--batch B] [--no-e2e]
+                    [--mode all|fwd|fwd_bwd|decode|long|varlen|mixer|conv] [--batch B] [--no-e2e]
                     [--no-cpu-baseline]
 
 Prints ONE JSON line (rank 0). The headline `value` is the chunked forward
@@ -610,6 +610,85 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
     return dec
 
 
+def bench_conv(args, dist, device, stream, peaks, sampler):
+    """The causal depthwise Conv1d (width 4) + SiLU in front of the mixer over
+    the layer-forward token batch (8 x 2048 x 3072, four layers' distinct
+    inputs per step), and its serving step (1,280 sequences x 24 layers,
+    fp32 conv windows resident)."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    D = gen.D_MODEL
+    B, T, L = args.batch or 8, 2048, 4
+    xs, ws, bs, wins, ys = [], [], [], [], []
+    for layer in range(L):
+        c = gen.make_conv_case(B, T, D, seed=40 + layer)
+        xs.append(dev_tensor(c.x, "bf16", device))
+        ws.append(torch.from_numpy(c.w).to(device))
+        bs.append(torch.from_numpy(c.b).to(device))
+        wins.append(torch.from_numpy(c.window).to(device))
+        ys.append(torch.empty_like(xs[-1]))
+
+    def step():
+        n = 0
+        for layer in range(L):
+            gla.gla_conv1d_fwd(xs[layer], ws[layer], bs[layer], wins[layer], y=ys[layer], win_out=wins[layer],
+                               stream=stream)
+            n += gla.gla_last_launch_count()
+        return n
+
+    total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    # x in, y out, the 3 window rows the first tokens read, the 4 rows written
+    bytes_ = B * T * D * 2 * 2 + B * D * 4 * (3 + 4)
+    avg_ms = statistics.mean(per) / L
+    ach = bytes_ / (avg_ms * 1e-3) / 1e9
+    res = {
+        "value": B * T * L * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+        "ms_per_step": total / args.steps, "ms_per_layer_step": total / args.steps / L,
+        "config": {"workload": f"conv1d_k4_silu_bf16_B{B}_T{T}_D{D}_L{L}", "B": B, "T": T, "D": D, "layers": L,
+                   "window": "fp32 [B,4,D] per layer, in place",
+                   "l2": f"{L} distinct layer inputs per step ({L * B * T * D * 2 / 1e6:.0f} MB), larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": bytes_,
+                     "avg_launch_ms": avg_ms, "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    del xs, ys, wins
+
+    N, L2 = 1280, args.layers or 24
+    gen_t = torch.Generator(device=device)
+    gen_t.manual_seed(44)
+    wins = [torch.randn((N, 4, D), generator=gen_t, device=device) for _ in range(L2)]
+    xs = [torch.randn((N, D), generator=gen_t, device=device).to(torch.bfloat16) for _ in range(L2)]
+    ys = [torch.empty_like(x) for x in xs]
+
+    def step2():
+        n = 0
+        for layer in range(L2):
+            gla.gla_conv1d_step(xs[layer], ws[layer % L], bs[layer % L], wins[layer], y=ys[layer], stream=stream)
+            n += gla.gla_last_launch_count()
+        return n
+
+    total, per, win, launches = time_steps(step2, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    bytes2 = N * D * (2 + 2 + 4 * 3 + 4 * 4)      # x, y, 3 window rows read, 4 written
+    avg_ms = statistics.mean(per) / L2
+    ach2 = bytes2 / (avg_ms * 1e-3) / 1e9
+    res["step"] = {
+        "value": N * dist.world * args.steps / (total * 1e-3), "unit": "seq-steps/s",
+        "ms_per_step": total / args.steps, "ms_per_layer_step": total / args.steps / L2,
+        "config": {"workload": f"conv1d_step_bf16_N{N}_D{D}_L{L2}", "N": N, "D": D, "layers": L2,
+                   "l2": f"{L2} distinct {N * 4 * D * 4 / 1e6:.0f} MB windows per step, larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": ach2, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach2 / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": bytes2,
+                     "avg_launch_ms": avg_ms, "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    return res
+
+
 def e2e_decode(args, dist, device, stream, toks, states, ll, scale, N, L):
     """Decode through the public API with host token buffers: per step the 24
     layers' q, k, v come from pinned host memory and the 24 outputs go back;
@@ -704,7 +783,21 @@ def cpu_baseline():
     dt, toks, nt, sample = oracle_varlen_sample(8)
     modes["varlen"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
                        "sample": sample, "seconds": dt}
+    dt, toks, nt, sample = oracle_conv_sample(8)
+    modes["conv"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                     "sample": sample, "seconds": dt}
     return base, modes
+
+
+def oracle_conv_sample(B):
+    """The oracle's Conv1d over B of the 8 sequences of one layer input."""
+    import oracle
+    c = gen.make_conv_case(B, 2048, gen.D_MODEL, seed=40)
+    nthreads = oracle.threads(0)
+    t0 = time.perf_counter()
+    oracle.conv1d(c.x, c.w, c.b, c.window, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, B * 2048, nthreads, f"{B} of 8 sequences x 2048 tokens x {gen.D_MODEL} channels, one layer"
 
 
 def oracle_varlen_sample(nseq):
@@ -757,7 +850,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gla", "reference"), default="gla")
-    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long", "varlen", "mixer"),
+    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long", "varlen", "mixer", "conv"),
                     default="all")
     ap.add_argument("--batch", type=int, default=0, help="override B of the fwd / fwd_bwd workloads (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the decode layer count (profiling)")
@@ -801,6 +894,8 @@ def main(argv=None):
             results["varlen"] = bench_varlen(args, dist, device, stream, peaks, sampler)
         if args.mode in ("all", "mixer"):
             results["mixer"] = bench_mixer(args, dist, device, stream, peaks, sampler)
+        if args.mode in ("all", "conv"):
+            results["conv"] = bench_conv(args, dist, device, stream, peaks, sampler)
     finally:
         sampler.stop()
 
@@ -818,7 +913,7 @@ def main(argv=None):
         "gpu_launches": head["gpu_launches"],
         "clocks": head["clocks"],
         "modes": {k: v for k, v in results.items() if k != head_key},
-        **{key: head[key] for key in ("standalone", "chunk64", "ms_per_layer_step") if key in head},
+        **{key: head[key] for key in ("standalone", "chunk64", "step", "ms_per_layer_step") if key in head},
         "peaks": peaks,
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

@@ -309,3 +309,31 @@ def serving_prefill_lengths(seed: int = 5, nseq: int = 64, lo: int = 64, hi: int
     """Prompt lengths of a batch of staggered requests: log-uniform integers in [lo, hi]."""
     rng = np.random.default_rng(seed)
     return np.floor(np.exp(rng.uniform(math.log(lo), math.log(hi + 1), size=nseq))).astype(np.int64)
+
+
+# ------------------------------------------------------- the token Conv1d
+D_MODEL = 3072   # the residual width D of the Laplace 3B layer
+
+
+@dataclass
+class ConvCase:
+    """Inputs of the causal depthwise Conv1d: x [B, T, D] (LayerNorm output,
+    N(0, 1)), taps w [D, 4] and bias b [D] ~ U(-1/2, 1/2) (PyTorch's default
+    bound for a depthwise width-4 Conv1d, 1/sqrt(fan_in = 4)), and fp32 conv
+    windows [B, 4, D] ~ N(0, 1) (the previous inputs of each sequence)."""
+    x: np.ndarray
+    w: np.ndarray
+    b: np.ndarray
+    window: np.ndarray
+    dtype: str
+
+
+def make_conv_case(B: int, T: int, D: int = D_MODEL, *, seed: int, dtype: str = BF16) -> ConvCase:
+    """Draw x, w, b, window in that order. The window holds previous inputs,
+    so it is drawn on the same grid as x (bf16 values for bf16 x)."""
+    rng = np.random.default_rng(seed)
+    x = _store(_normal(rng, (B, T, D)), dtype)
+    w = rng.uniform(-0.5, 0.5, size=(D, 4)).astype(np.float32)
+    b = rng.uniform(-0.5, 0.5, size=D).astype(np.float32)
+    window = _store(_normal(rng, (B, 4, D)), dtype).astype(np.float32)
+    return ConvCase(x=x, w=w, b=b, window=window, dtype=dtype)

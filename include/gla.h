@@ -235,6 +235,46 @@ gla_status gla_decode_step_mixer(const void *q, const void *k, const void *v, co
                                  const float *norm_w, float eps, int N, int H, int dk, int dv, gla_dtype dtype,
                                  void *z, void *stream);
 
+/*
+ * The causal depthwise Conv1d of width 4 with SiLU that filters the token
+ * stream in front of the mixer ("i14 and the Laplace 3B architecture",
+ * paragraph "Normalisation and convolution"; no equation survives, the
+ * reading), per channel c:
+ *     y_t[c] = SiLU( sum_{i=0..3} w[c][i] x_{t-3+i}[c] + b[c] )
+ * Inputs before a call's first token come from the sequence's conv window:
+ * its last four inputs so far, fp32, [4, D] rows oldest first (zeros for a
+ * new sequence; the oldest row is carried, never multiplied). Four fp32 rows
+ * of D = 3072 per layer are the part of the 29.5 MB per-sequence state that
+ * is not the mixer's.
+ *   w [D, 4] fp32 (tap 3 multiplies the current token), b [D] fp32 or NULL
+ *   (zero); x, y rows of D channels of `dtype` (GLA_BF16 or GLA_FP32); D a
+ *   multiple of 8 (bf16) or 4 (fp32). y may not overlap x or a window.
+ *
+ * gla_conv1d_fwd: x, y [B, T, D]; win_in [B, 4, D] fp32 or NULL (zeros);
+ *   win_out [B, 4, D] fp32 or NULL (not wanted), the windows after the call.
+ *   win_in == win_out updates the windows in place (any other overlap is
+ *   undefined). T = 0 copies win_in to win_out.
+ * gla_conv1d_varlen: sequences packed as for gla_chunk_fwd_varlen (x, y
+ *   [total_T, D]; cu_seqlens [nseq + 1] and slots [nseq] or NULL in device
+ *   memory, with the same error behaviour: a bad entry skips the sequence and
+ *   the next gla_check() reports GLA_ERR_INVALID_ARG); win_pool
+ *   [n_slots, 4, D] fp32 holds each slot's window before the call and gets
+ *   the window after it (a sequence of length 0 leaves its slot untouched).
+ *   Tokens past cu_seqlens[nseq] get no output.
+ * gla_conv1d_step: one new token per sequence (the serving step): x, y
+ *   [N, D]; win [N, 4, D] fp32, read and updated in place (shifted by one
+ *   row, the new input last).
+ * Each call launches one kernel for y and, when a window is written by a
+ * call over several tokens, one small kernel after it for the windows.
+ */
+gla_status gla_conv1d_fwd(const void *x, const float *w, const float *b, const float *win_in, int B, int T, int D,
+                          gla_dtype dtype, void *y, float *win_out, void *stream);
+gla_status gla_conv1d_varlen(const void *x, const float *w, const float *b, const int *cu_seqlens,
+                             const int *slots, float *win_pool, int n_slots, int nseq, int total_T, int D,
+                             gla_dtype dtype, void *y, void *stream);
+gla_status gla_conv1d_step(const void *x, const float *w, const float *b, float *win, int N, int D,
+                           gla_dtype dtype, void *y, void *stream);
+
 /* Synchronise `stream` and report: GLA_ERR_CUDA if the stream or an earlier
  * launch failed, GLA_ERR_TIMEOUT if a device-side wait gave up since the last
  * gla_check (the status word is cleared on read), else GLA_OK. */

@@ -23,6 +23,9 @@ from .binding import (  # noqa: F401
     gla_chunk_fwd_noalloc,
     gla_chunk_fwd_varlen,
     gla_chunk_fwd_workspace_size,
+    gla_conv1d_fwd,
+    gla_conv1d_step,
+    gla_conv1d_varlen,
     gla_decode_step,
     gla_decode_step_mixer,
     gla_last_launch_count,

@@ -31,7 +31,7 @@ GLA_BF16, GLA_FP32 = 0, 1
 ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen",
                  "gla_chunk_bwd",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
-                 "gla_check",
+                 "gla_conv1d_fwd", "gla_conv1d_varlen", "gla_conv1d_step", "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
 
 
@@ -82,6 +82,12 @@ def lib():
             L.gla_decode_step_mixer.restype = _i
             L.gla_mixer_epilogue.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _vp, _vp]
             L.gla_mixer_epilogue.restype = _i
+            L.gla_conv1d_fwd.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]
+            L.gla_conv1d_fwd.restype = _i
+            L.gla_conv1d_varlen.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]
+            L.gla_conv1d_varlen.restype = _i
+            L.gla_conv1d_step.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]
+            L.gla_conv1d_step.restype = _i
             L.gla_check.argtypes = [_vp]
             L.gla_check.restype = _i
             L.gla_status_string.argtypes = [_i]
@@ -296,6 +302,49 @@ def gla_mixer_epilogue(o, q, k, v, g, aug=None, norm_w=None, eps=1e-6, *, z=None
                                   NT, H, dk, dv, _dtype_code(o), _ptr(z), _stream(stream))
     _raise_on(st, "gla_mixer_epilogue")
     return z
+
+
+def gla_conv1d_fwd(x, w, b=None, win_in=None, *, y=None, win_out=None, want_window=True, stream=None):
+    """Causal depthwise Conv1d (width 4) + SiLU over x [B,T,D]; w [D,4], b [D]
+    fp32; win_in [B,4,D] fp32 or None (zeros). Returns (y, win_out); win_out
+    may be win_in (in place), or None with want_window=False."""
+    torch = _torch()
+    B, T, D = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    if win_out is None and want_window:
+        win_out = torch.empty((B, 4, D), dtype=torch.float32, device=x.device)
+    st = lib().gla_conv1d_fwd(_ptr(x), _ptr(w), _ptr(b), _ptr(win_in), B, T, D, _dtype_code(x), _ptr(y),
+                              _ptr(win_out), _stream(stream))
+    _raise_on(st, "gla_conv1d_fwd")
+    return y, win_out
+
+
+def gla_conv1d_varlen(x, w, b, cu_seqlens, win_pool, slots=None, *, y=None, stream=None):
+    """The Conv1d over packed sequences x [total_T,D] (cu_seqlens int32 CUDA
+    tensor), windows in win_pool [n_slots,4,D] fp32 at slots[n] (int32 CUDA
+    tensor, or None for slot n), updated in place. Returns y [total_T,D]."""
+    torch = _torch()
+    total_T, D = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    nseq = cu_seqlens.numel() - 1
+    st = lib().gla_conv1d_varlen(_ptr(x), _ptr(w), _ptr(b), _ptr(cu_seqlens), _ptr(slots), _ptr(win_pool),
+                                 int(win_pool.shape[0]), nseq, total_T, D, _dtype_code(x), _ptr(y), _stream(stream))
+    _raise_on(st, "gla_conv1d_varlen")
+    return y
+
+
+def gla_conv1d_step(x, w, b, win, *, y=None, stream=None):
+    """One serving step of the Conv1d: x [N,D], win [N,4,D] fp32 updated in
+    place. Returns y [N,D]."""
+    torch = _torch()
+    N, D = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    st = lib().gla_conv1d_step(_ptr(x), _ptr(w), _ptr(b), _ptr(win), N, D, _dtype_code(x), _ptr(y), _stream(stream))
+    _raise_on(st, "gla_conv1d_step")
+    return y
 
 
 def gla_check(stream=None):

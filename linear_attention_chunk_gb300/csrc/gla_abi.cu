@@ -91,6 +91,16 @@ gla_status check_chunk_shape(int B, int T, int H, int dk, int dv, int chunk, gla
         if ((p) && !aligned16(p)) return fail(GLA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
     } while (0)
 
+// Shape checks of the Conv1d entry points (B sequences of T tokens of D channels).
+gla_status check_conv_shape(int B, int T, int D, gla_dtype dtype) {
+    if (dtype != GLA_BF16 && dtype != GLA_FP32) return fail(GLA_ERR_INVALID_ARG, "dtype %d is not GLA_BF16/GLA_FP32", (int)dtype);
+    if (B < 0 || T < 0) return fail(GLA_ERR_INVALID_ARG, "negative size B=%d T=%d", B, T);
+    const int vec = dtype == GLA_BF16 ? 8 : 4;
+    if (D <= 0 || D % vec != 0) return fail(GLA_ERR_UNSUPPORTED, "D=%d must be a positive multiple of %d", D, vec);
+    if ((long double)B * T * D > (long double)(1ull << 40)) return fail(GLA_ERR_INVALID_ARG, "tensor too large");
+    return GLA_OK;
+}
+
 // The decode step with or without the mixer epilogue (g == NULL: plain o).
 gla_status decode_common(const void *q, const void *k, const void *v, const float *log_lambda, float *S_inout,
                          float scale, const void *g, const float *aug, const float *norm_w, float eps, int N,
@@ -319,6 +329,80 @@ gla_status gla_mixer_epilogue(const void *o, const void *q, const void *k, const
     cudaError_t e = launch_mixer_epilogue(p, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
     t_launches = launches;
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_mixer_epilogue launch");
+}
+
+gla_status gla_conv1d_fwd(const void *x, const float *w, const float *b, const float *win_in, int B, int T, int D,
+                          gla_dtype dtype, void *y, float *win_out, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_conv_shape(B, T, D, dtype);
+    if (st != GLA_OK) return st;
+    OPTIONAL_PTR(b, "b");
+    OPTIONAL_PTR(win_in, "win_in");
+    OPTIONAL_PTR(win_out, "win_out");
+    if (B == 0 || (T == 0 && !win_out)) return GLA_OK;
+    REQUIRE_PTR(w, "w");
+    if (T > 0) {
+        REQUIRE_PTR(x, "x");
+        REQUIRE_PTR(y, "y");
+        if (x == y) return fail(GLA_ERR_INVALID_ARG, "y may not alias x");
+    }
+    unsigned int *status = nullptr;
+    if ((st = status_word(&status)) != GLA_OK) return st;
+    ConvParams p{x, w, b, nullptr, nullptr, win_in, win_out, B, B, (long)B * T, T, D, y, status};
+    int launches = 0;
+    const cudaError_t e = launch_conv_fwd(p, false, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_conv1d_fwd launch");
+}
+
+gla_status gla_conv1d_varlen(const void *x, const float *w, const float *b, const int *cu_seqlens,
+                             const int *slots, float *win_pool, int n_slots, int nseq, int total_T, int D,
+                             gla_dtype dtype, void *y, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_conv_shape(1, total_T, D, dtype);
+    if (st != GLA_OK) return st;
+    if (nseq < 0 || n_slots < 0) return fail(GLA_ERR_INVALID_ARG, "negative nseq=%d or n_slots=%d", nseq, n_slots);
+    OPTIONAL_PTR(b, "b");
+    OPTIONAL_PTR(slots, "slots");
+    if (nseq == 0) return GLA_OK;
+    if (!slots && n_slots < nseq)
+        return fail(GLA_ERR_INVALID_ARG, "without slots the pool needs nseq=%d slots, has %d", nseq, n_slots);
+    REQUIRE_PTR(w, "w");
+    REQUIRE_PTR(cu_seqlens, "cu_seqlens");
+    REQUIRE_PTR(win_pool, "win_pool");
+    if (total_T == 0) return GLA_OK;   // every sequence is empty: no window changes
+    REQUIRE_PTR(x, "x");
+    REQUIRE_PTR(y, "y");
+    if (x == y) return fail(GLA_ERR_INVALID_ARG, "y may not alias x");
+    unsigned int *status = nullptr;
+    if ((st = status_word(&status)) != GLA_OK) return st;
+    ConvParams p{x, w, b, cu_seqlens, slots, win_pool, win_pool, n_slots, nseq, (long)total_T, 0, D, y, status};
+    int launches = 0;
+    const cudaError_t e = launch_conv_fwd(p, true, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_conv1d_varlen launch");
+}
+
+gla_status gla_conv1d_step(const void *x, const float *w, const float *b, float *win, int N, int D,
+                           gla_dtype dtype, void *y, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_conv_shape(N, 1, D, dtype);
+    if (st != GLA_OK) return st;
+    OPTIONAL_PTR(b, "b");
+    if (N == 0) return GLA_OK;
+    REQUIRE_PTR(x, "x");
+    REQUIRE_PTR(w, "w");
+    REQUIRE_PTR(win, "win");
+    REQUIRE_PTR(y, "y");
+    if (x == y) return fail(GLA_ERR_INVALID_ARG, "y may not alias x");
+    ConvParams p{x, w, b, nullptr, nullptr, win, win, N, N, (long)N, 1, D, y, nullptr};
+    int launches = 0;
+    const cudaError_t e = launch_conv_step(p, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_conv1d_step launch");
 }
 
 gla_status gla_check(void *stream) {

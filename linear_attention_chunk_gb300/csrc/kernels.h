@@ -72,6 +72,26 @@ struct EpilogueParams {
 };
 cudaError_t launch_mixer_epilogue(const EpilogueParams &p, bool bf16, cudaStream_t s, int *launches);
 
+// The causal depthwise Conv1d (width 4) with SiLU (conv.cu). Batched: nseq
+// sequences of T tokens, window n at win_in / win_out + n*4*D (either may be
+// NULL). Varlen: cu_seqlens / slots on the device, the window pool
+// [n_slots, 4, D] at win_in == win_out. Step: one token per sequence,
+// window [nseq, 4, D] at win_out, in place.
+struct ConvParams {
+    const void *x;
+    const float *w, *b;          // [D, 4], [D] or NULL
+    const int *cu_seqlens, *slots;
+    const float *win_in;
+    float *win_out;
+    int n_slots, nseq;
+    long NT;                     // tokens in x
+    int T, D;
+    void *y;
+    unsigned int *status;
+};
+cudaError_t launch_conv_fwd(const ConvParams &p, bool varlen, bool bf16, cudaStream_t s, int *launches);
+cudaError_t launch_conv_step(const ConvParams &p, bool bf16, cudaStream_t s, int *launches);
+
 // SIMT kernels (any dk <= 128, dv <= 256; fp32 or bf16 elements).
 cudaError_t launch_fwd_simt(const FwdParams &p, bool bf16, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_simt(const BwdParams &p, bool bf16, cudaStream_t s, int *launches);

@@ -174,3 +174,48 @@ def test_epilogue_entry_points_reject_bad_arguments(L):
     assert dec(dk=64) == binding.GLA_ERR_UNSUPPORTED
     assert dec(eps=-1.0) == binding.GLA_ERR_INVALID_ARG
     assert dec(N=0) == binding.GLA_OK
+
+
+def test_conv_entry_points_reject_bad_arguments(L):
+    def fwd(**kw):
+        a = dict(x=FAKE, w=FAKE, b=None, wi=None, B=2, T=10, D=3072, dt=0, y=FAKE + 0x100, wo=FAKE)
+        a.update(kw)
+        return L.gla_conv1d_fwd(a["x"], a["w"], a["b"], a["wi"], a["B"], a["T"], a["D"], a["dt"], a["y"], a["wo"],
+                                None)
+    assert fwd(dt=7) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(B=-1) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(D=3076) == binding.GLA_ERR_UNSUPPORTED          # bf16 rows need D % 8 == 0
+    assert fwd(D=0) == binding.GLA_ERR_UNSUPPORTED
+    assert fwd(w=None) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(x=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(b=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(wi=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(y=FAKE, x=FAKE) == binding.GLA_ERR_INVALID_ARG    # y aliases x
+    assert fwd(B=0) == binding.GLA_OK
+    assert fwd(T=0, wo=None) == binding.GLA_OK                  # nothing to compute or copy
+
+    def var(**kw):
+        a = dict(x=FAKE, w=FAKE, b=None, cu=FAKE, slots=None, pool=FAKE, n_slots=8, nseq=4, T=100, D=3072, dt=0,
+                 y=FAKE + 0x100)
+        a.update(kw)
+        return L.gla_conv1d_varlen(a["x"], a["w"], a["b"], a["cu"], a["slots"], a["pool"], a["n_slots"], a["nseq"],
+                                   a["T"], a["D"], a["dt"], a["y"], None)
+    assert var(nseq=-1) == binding.GLA_ERR_INVALID_ARG
+    assert var(cu=None) == binding.GLA_ERR_INVALID_ARG
+    assert var(pool=None) == binding.GLA_ERR_INVALID_ARG
+    assert var(slots=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert var(n_slots=3) == binding.GLA_ERR_INVALID_ARG
+    assert var(dt=1, D=3074) == binding.GLA_ERR_UNSUPPORTED     # fp32 rows need D % 4 == 0
+    assert var(y=None) == binding.GLA_ERR_INVALID_ARG
+    assert var(nseq=0) == binding.GLA_OK
+    assert var(T=0) == binding.GLA_OK                           # every sequence empty: windows unchanged
+
+    def step(**kw):
+        a = dict(x=FAKE, w=FAKE, b=None, win=FAKE, N=4, D=3072, dt=0, y=FAKE + 0x100)
+        a.update(kw)
+        return L.gla_conv1d_step(a["x"], a["w"], a["b"], a["win"], a["N"], a["D"], a["dt"], a["y"], None)
+    assert step(win=None) == binding.GLA_ERR_INVALID_ARG
+    assert step(win=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert step(N=-2) == binding.GLA_ERR_INVALID_ARG
+    assert step(D=12) == binding.GLA_ERR_UNSUPPORTED
+    assert step(N=0) == binding.GLA_OK
