@@ -602,8 +602,9 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
         "config": {"workload": f"mixer_epilogue_bf16_B{B}_H16_T{T}", "B": B, "T": T, "H": H,
                    "l2": f"inputs larger than L2 ({bytes2 / 1e6:.0f} MB per step), no flush"},
         "roofline": {"bound": "hbm", "achieved": ach2, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": ach2 / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": bytes2,
-                     "avg_launch_ms": avg_ms, "peak_source": peaks["source"]},
+                     "frac": ach2 / peaks["hbm_gbs"], "traffic": committed_traffic("mixer_epilogue")[0],
+                     "algorithmic_bytes_per_launch": bytes2, "avg_launch_ms": avg_ms,
+                     "peak_source": peaks["source"]},
         "gpu_launches": launches,
         "clocks": sampler.summary(*win) if sampler else None,
     }
@@ -649,8 +650,9 @@ def bench_conv(args, dist, device, stream, peaks, sampler):
                    "window": "fp32 [B,4,D] per layer, in place",
                    "l2": f"{L} distinct layer inputs per step ({L * B * T * D * 2 / 1e6:.0f} MB), larger than L2"},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": bytes_,
-                     "avg_launch_ms": avg_ms, "peak_source": peaks["source"]},
+                     "frac": ach / peaks["hbm_gbs"], "traffic": committed_traffic("conv_stream")[0],
+                     "algorithmic_bytes_per_launch": bytes_, "avg_launch_ms": avg_ms,
+                     "peak_source": peaks["source"]},
         "gpu_launches": launches,
         "clocks": sampler.summary(*win) if sampler else None,
     }
@@ -681,8 +683,9 @@ def bench_conv(args, dist, device, stream, peaks, sampler):
         "config": {"workload": f"conv1d_step_bf16_N{N}_D{D}_L{L2}", "N": N, "D": D, "layers": L2,
                    "l2": f"{L2} distinct {N * 4 * D * 4 / 1e6:.0f} MB windows per step, larger than L2"},
         "roofline": {"bound": "hbm", "achieved": ach2, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": ach2 / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": bytes2,
-                     "avg_launch_ms": avg_ms, "peak_source": peaks["source"]},
+                     "frac": ach2 / peaks["hbm_gbs"], "traffic": committed_traffic("conv_step")[0],
+                     "algorithmic_bytes_per_launch": bytes2, "avg_launch_ms": avg_ms,
+                     "peak_source": peaks["source"]},
         "gpu_launches": launches,
         "clocks": sampler.summary(*win) if sampler else None,
     }

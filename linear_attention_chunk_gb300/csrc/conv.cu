@@ -28,7 +28,8 @@
 // channels per thread, 24 consumer warps at D = 3072) for latency hiding,
 // rows up to 7.5 KB 16-byte vectors; wider rows take a plain kernel (a
 // thread per 16-byte vector and tile of 16 tokens, loads issued up front)
-// followed by a small window kernel.
+// followed by a small window kernel. The serving step is a thread per four
+// channels of one sequence.
 #include <type_traits>
 
 #include "common.cuh"
@@ -131,23 +132,34 @@ __device__ __forceinline__ typename VecT<VB>::type ld_vec(const T *p) {
     return __ldg(reinterpret_cast<const typename VecT<VB>::type *>(p));
 }
 
-// fp32 pairs in memory (windows, bias): one 8-byte access per pair.
+// fp32 pairs in memory (windows, bias): 16-byte accesses, 8-byte for an odd pair.
 template <int P>
 __device__ __forceinline__ void load_pairs(const float *p, f2 (&f)[P]) {
 #pragma unroll
-    for (int e = 0; e < P; ++e) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(p + 2 * e);
+    for (int e = 0; e + 1 < P; e += 2) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p + 2 * e);
         f[e] = f2_bits(u.x, u.y);
+        f[e + 1] = f2_bits(u.z, u.w);
+    }
+    if (P % 2) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p + 2 * (P - 1));
+        f[P - 1] = f2_bits(u.x, u.y);
     }
 }
 
 template <int P>
 __device__ __forceinline__ void store_pairs(float *p, const f2 (&f)[P]) {
 #pragma unroll
-    for (int e = 0; e < P; ++e) {
-        uint32_t a, b;
+    for (int e = 0; e + 1 < P; e += 2) {
+        uint32_t a, b, c, d;
         f2_split(f[e], a, b);
-        *reinterpret_cast<uint2 *>(p + 2 * e) = make_uint2(a, b);
+        f2_split(f[e + 1], c, d);
+        *reinterpret_cast<uint4 *>(p + 2 * e) = make_uint4(a, b, c, d);
+    }
+    if (P % 2) {
+        uint32_t a, b;
+        f2_split(f[P - 1], a, b);
+        *reinterpret_cast<uint2 *>(p + 2 * (P - 1)) = make_uint2(a, b);
     }
 }
 
@@ -553,10 +565,16 @@ __global__ void __launch_bounds__(kThreads) conv_window_kernel(const ConvParams 
 }
 
 // One token per sequence n: the window gives the three previous inputs; it
-// shifts by one row and takes the new input, in place.
+// shifts by one row and takes the new input, in place. A thread owns four
+// channels (two pairs: one 16-byte access per window row), which keeps the
+// registers low enough for 48 resident warps per SM: the step is a latency-
+// bound gather of 7 rows per sequence.
+template <typename T> constexpr int step_vb() { return std::is_same<T, float>::value ? 16 : 8; }
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) conv_step_kernel(const ConvParams p) {
-    constexpr int V = 16 / (int)sizeof(T), P = V / 2;
+    constexpr int VB = step_vb<T>(), V = VB / (int)sizeof(T), P = V / 2;
+    using Vec = typename VecT<VB>::type;
     const int ncb = (p.D / V + kThreads - 1) / kThreads;
     const int n = blockIdx.x / ncb;
     const int g = (int)(blockIdx.x % ncb) * kThreads + threadIdx.x;
@@ -567,11 +585,11 @@ __global__ void __launch_bounds__(kThreads) conv_step_kernel(const ConvParams p)
     f2 h[3][P], xv[P], out[P];
 #pragma unroll
     for (int j = 0; j < 3; ++j) load_pairs<P>(win + (size_t)(j + 1) * D, h[j]);
-    unpack_pairs<T, 16>(ld_vec<T, 16>(static_cast<const T *>(p.x) + (size_t)n * D + c0), xv);
+    unpack_pairs<T, VB>(ld_vec<T, VB>(static_cast<const T *>(p.x) + (size_t)n * D + c0), xv);
     Taps<T, P> tp;
     tp.load(p.w, p.b, c0);
     conv_point<T, P>(tp, h, xv, out);
-    *reinterpret_cast<uint4 *>(static_cast<T *>(p.y) + (size_t)n * D + c0) = pack_pairs<T, 16>(out);
+    *reinterpret_cast<Vec *>(static_cast<T *>(p.y) + (size_t)n * D + c0) = pack_pairs<T, VB>(out);
 #pragma unroll
     for (int j = 0; j < 3; ++j) store_pairs<P>(win + (size_t)j * D, h[j]);
     store_pairs<P>(win + (size_t)3 * D, xv);
@@ -633,7 +651,7 @@ cudaError_t conv_fwd_impl(const ConvParams &p, bool var, cudaStream_t st, int *l
 
 template <typename T>
 cudaError_t conv_step_impl(const ConvParams &p, cudaStream_t st, int *launches) {
-    constexpr int V = 16 / (int)sizeof(T);
+    constexpr int V = step_vb<T>() / (int)sizeof(T);
     const size_t blocks = (size_t)p.nseq * ((p.D / V + kThreads - 1) / kThreads);
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffull) return cudaErrorInvalidValue;

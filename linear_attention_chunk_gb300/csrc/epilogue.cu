@@ -8,7 +8,8 @@
 // per (token, head). A stream over o, q, k, v, g in and z out (1,920 bytes
 // per head-token at bf16, dk = 96, dv = 192): one warp per (token, head),
 // 16-byte loads for the bf16 96 x 192 shape (lanes striding over channels
-// otherwise); the two reductions are warp shuffles.
+// otherwise); the two reductions are warp shuffles. The fp32 validation
+// path keeps exact sigmoids; the bf16 path uses the fast forms.
 #include <type_traits>
 
 #include "common.cuh"
@@ -76,6 +77,14 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_kernel(EpiloguePar
 
 // bf16, dk = 96, dv = 192: one warp per row with 16-byte accesses; lane l < 24
 // owns channels 8l..8l+7 of o, v, g, z and lane l < 12 dims 8l..8l+7 of q, k.
+// At bf16 output precision the gate's SiLU takes the tanh form,
+// g sigmoid(g) = (g/2)(1 + tanh(g/2)): one special-function op per channel.
+__device__ __forceinline__ float tanh_fast(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(EpilogueParams p) {
     const size_t row = (size_t)blockIdx.x * kWarps + threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -93,7 +102,9 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(Epilog
     }
     float dot = 0.f;
     if (lane < 12 && p.aug) {
-        const float *a = p.aug + (size_t)h * 96 + 8 * lane;
+        const float4 *a4 = reinterpret_cast<const float4 *>(p.aug + (size_t)h * 96 + 8 * lane);
+        const float4 a0 = __ldg(a4), a1 = __ldg(a4 + 1);
+        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
         const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -102,7 +113,7 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(Epilog
             dot = fmaf(qf.y * a[2 * e + 1], kf.y, dot);
         }
     }
-    const float gate = sigmoidf_(warp_sum(dot));
+    const float gate = __fdividef(1.f, 1.f + __expf(-warp_sum(dot)));
     float u[8];
     float ss = 0.f;
     const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
@@ -113,17 +124,23 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(Epilog
         u[2 * e + 1] = fmaf(gate, vf.y, of.y);
         ss = fmaf(u[2 * e], u[2 * e], fmaf(u[2 * e + 1], u[2 * e + 1], ss));
     }
-    const float r = rsqrtf(warp_sum(ss) / 192.f + p.eps);
+    const float r = rsqrtf(warp_sum(ss) * (1.f / 192.f) + p.eps);
     if (lane < 24) {
-        const float *w = p.norm_w ? p.norm_w + (size_t)h * 192 + 8 * lane : nullptr;
+        float w[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+        if (p.norm_w) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(p.norm_w + (size_t)h * 192 + 8 * lane);
+            const float4 w0 = __ldg(w4), w1 = __ldg(w4 + 1);
+            w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
+            w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
+        }
         const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
         uint32_t zw[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 gf = unpack_bf16x2(gw[e]);
-            const float z0 = u[2 * e] * r * (w ? w[2 * e] : 1.f) * gf.x * sigmoidf_(gf.x);
-            const float z1 = u[2 * e + 1] * r * (w ? w[2 * e + 1] : 1.f) * gf.y * sigmoidf_(gf.y);
-            zw[e] = pack_bf16x2(z0, z1);
+            const float h0 = 0.5f * gf.x, h1 = 0.5f * gf.y;
+            const float s0 = fmaf(h0, tanh_fast(h0), h0), s1 = fmaf(h1, tanh_fast(h1), h1);   // SiLU(g)
+            zw[e] = pack_bf16x2(u[2 * e] * r * w[2 * e] * s0, u[2 * e + 1] * r * w[2 * e + 1] * s1);
         }
         __stcs(static_cast<uint4 *>(p.z) + row * 24 + lane, make_uint4(zw[0], zw[1], zw[2], zw[3]));
     }
