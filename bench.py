@@ -608,6 +608,45 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
         "gpu_launches": launches,
         "clocks": sampler.summary(*win) if sampler else None,
     }
+    del o, v, g, q, k, z
+
+    # The layer forward with the epilogue applied in place (gla_chunk_fwd_mixer:
+    # the forward writes o into z, the epilogue rewrites z).
+    c = gen.layer_fwd(seed=1, B=B, T=T)
+    q, k, v = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v))
+    ll = torch.from_numpy(c.log_lambda).to(device)
+    g = torch.randn((B, T, H, DV), generator=gen_t, device=device).to(torch.bfloat16)
+    z = torch.empty((B, T, H, DV), dtype=torch.bfloat16, device=device)
+    hT = torch.empty((B, H, DK, DV), dtype=torch.float32, device=device)
+    ws = torch.empty(max(gla.gla_chunk_fwd_workspace_size(B, T, H, DK, DV, CHUNK), 16), dtype=torch.uint8,
+                     device=device)
+
+    def step3():
+        gla.gla_chunk_fwd_mixer(q, k, v, g, ll, None, c.scale, CHUNK, aug, nw, 1e-6, z=z, hT=hT, workspace=ws,
+                                stream=stream)
+        return gla.gla_last_launch_count()
+
+    total, per, win, launches = time_steps(step3, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    # q, k, v, g in, z out and hT; plus the epilogue's own pass over o (written, then read as z's
+    # input), q, k and v again: what the two launches move
+    bytes3 = B * T * H * (2 * DK * 2 + 3 * DV * 2) + B * H * STATE_BYTES
+    bytes3_moved = bytes3 + B * T * H * (2 * DK * 2 + 2 * DV * 2 + DV * 2)
+    avg_ms = statistics.mean(per)
+    dec["fwd_mixer"] = {
+        "value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+        "ms_per_step": total / args.steps,
+        "config": {"workload": f"layer_fwd_mixer_bf16_B{B}_H16_T{T}_C{CHUNK}", "B": B, "T": T, "H": H,
+                   "epilogue": "in place over z after the forward (two launches)",
+                   "l2": f"inputs larger than L2 ({bytes3 / 1e6:.0f} MB per step), no flush"},
+        "roofline": {"bound": "hbm", "achieved": bytes3_moved / (avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": bytes3_moved / (avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": None, "algorithmic_bytes_per_launch": bytes3_moved / 2,
+                     "avg_launch_ms": avg_ms / 2, "peak_source": peaks["source"],
+                     "note": "two launches per step; bytes are those both launches move"},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
     return dec
 
 
@@ -916,7 +955,8 @@ def main(argv=None):
         "gpu_launches": head["gpu_launches"],
         "clocks": head["clocks"],
         "modes": {k: v for k, v in results.items() if k != head_key},
-        **{key: head[key] for key in ("standalone", "chunk64", "step", "ms_per_layer_step") if key in head},
+        **{key: head[key] for key in ("standalone", "fwd_mixer", "chunk64", "step", "ms_per_layer_step")
+           if key in head},
         "peaks": peaks,
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

@@ -227,6 +227,16 @@ gla_status gla_decode_step(const void *q, const void *k, const void *v,
  * gla_decode_step_mixer: gla_decode_step followed by the epilogue in the same
  *   kernel (o never reaches memory); g [N, H, dv] of `dtype`, z [N, H, dv].
  */
+/* gla_chunk_fwd_mixer: gla_chunk_fwd followed by the epilogue, z in place of
+ *   o: g [B,T,H,dv] bf16, z [B,T,H,dv] bf16, hT and the workspace as for
+ *   gla_chunk_fwd. GLA_BF16 only (dk = 96, dv = 192). Two launches with no
+ *   scratch memory: the forward writes o into z, and the epilogue rewrites
+ *   each row of z in place. z may not alias q, k, v or g.
+ */
+gla_status gla_chunk_fwd_mixer(const void *q, const void *k, const void *v, const void *g, const float *log_lambda,
+                               const float *h0, float scale, const float *aug, const float *norm_w, float eps, int B,
+                               int T, int H, int dk, int dv, int chunk, gla_dtype dtype, void *z, float *hT,
+                               void *workspace, size_t workspace_bytes, void *stream);
 gla_status gla_mixer_epilogue(const void *o, const void *q, const void *k, const void *v, const void *g,
                               const float *aug, const float *norm_w, float eps, int NT, int H, int dk, int dv,
                               gla_dtype dtype, void *z, void *stream);

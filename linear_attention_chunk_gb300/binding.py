@@ -8,8 +8,16 @@ if libgla.so is missing or a call fails, a GlaError is raised.
 
 Functions:
   gla_chunk_fwd(q, k, v, log_lambda, h0=None, scale=None, chunk=128, ...) -> (o, hT)
+  gla_chunk_fwd_noalloc(...)                                              -> (o, hT)
+  gla_chunk_fwd_varlen(q, k, v, log_lambda, cu_seqlens, state_pool, ...)  -> o  (pool updated)
+  gla_chunk_fwd_mixer(q, k, v, g, log_lambda, ...)                        -> (z, hT)
   gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, ...)          -> (dq, dk, dv, dh0)
   gla_decode_step(q, k, v, log_lambda, S, scale=None, ...)                -> o  (S updated in place)
+  gla_decode_step_mixer(q, k, v, log_lambda, S, g, ...)                   -> z  (S updated in place)
+  gla_mixer_epilogue(o, q, k, v, g, aug=None, norm_w=None, eps=1e-6)      -> z
+  gla_conv1d_fwd(x, w, b=None, win_in=None, ...)                          -> (y, win_out)
+  gla_conv1d_varlen(x, w, b, cu_seqlens, win_pool, slots=None)            -> y  (pool updated)
+  gla_conv1d_step(x, w, b, win)                                           -> y  (window updated)
   gla_check(stream=None), gla_status_string(code), gla_version()
   gla_chunk_fwd_workspace_size(...), gla_chunk_bwd_workspace_size(...)
 `lib()` returns the loaded ctypes library for callers that hold raw pointers.
@@ -29,7 +37,7 @@ GLA_BF16, GLA_FP32 = 0, 1
 
 # The public entry points declared in include/gla.h.
 ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen",
-                 "gla_chunk_bwd",
+                 "gla_chunk_fwd_mixer", "gla_chunk_bwd",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
                  "gla_conv1d_fwd", "gla_conv1d_varlen", "gla_conv1d_step", "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
@@ -68,6 +76,9 @@ def lib():
             L.gla_chunk_fwd_varlen.argtypes = [_vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                                                _i, _i, _vp, _vp]
             L.gla_chunk_fwd_varlen.restype = _i
+            L.gla_chunk_fwd_mixer.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f, _i, _i, _i, _i, _i, _i,
+                                              _i, _vp, _vp, _vp, _sz, _vp]
+            L.gla_chunk_fwd_mixer.restype = _i
             L.gla_chunk_fwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
             L.gla_chunk_fwd_workspace_size.restype = _sz
             L.gla_chunk_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
@@ -228,6 +239,31 @@ def gla_chunk_fwd_varlen(q, k, v, log_lambda, cu_seqlens, state_pool, slots=None
                                     dk, dv, int(chunk), _dtype_code(q), _ptr(o), _stream(stream))
     _raise_on(st, "gla_chunk_fwd_varlen")
     return o
+
+
+def gla_chunk_fwd_mixer(q, k, v, g, log_lambda, h0=None, scale=None, chunk=128, aug=None, norm_w=None, eps=1e-6,
+                        *, z=None, hT=None, want_hT=True, workspace=None, stream=None):
+    """The chunked forward followed by the mixer epilogue, z in place of o
+    (bf16): returns (z, hT), z [B,T,H,dv] = Head RMSNorm(o + sigmoid(q.(aug*k)) v)
+    * norm_w * SiLU(g)."""
+    torch = _torch()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if z is None:
+        z = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = gla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device) if n else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gla_chunk_fwd_mixer(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(log_lambda), _ptr(h0), float(scale),
+                                   _ptr(aug), _ptr(norm_w), float(eps), B, T, H, dk, dv, int(chunk), _dtype_code(q),
+                                   _ptr(z), _ptr(hT), _ptr(workspace), ws_bytes, _stream(stream))
+    _raise_on(st, "gla_chunk_fwd_mixer")
+    return z, hT
 
 
 def gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, scale=None, chunk=128, *,

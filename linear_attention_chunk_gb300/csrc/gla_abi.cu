@@ -190,6 +190,55 @@ gla_status gla_chunk_fwd(const void *q, const void *k, const void *v, const floa
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd launch");
 }
 
+gla_status gla_chunk_fwd_mixer(const void *q, const void *k, const void *v, const void *g, const float *log_lambda,
+                               const float *h0, float scale, const float *aug, const float *norm_w, float eps, int B,
+                               int T, int H, int dk, int dv, int chunk, gla_dtype dtype, void *z, float *hT,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_chunk_shape(B, T, H, dk, dv, chunk, dtype);
+    if (st != GLA_OK) return st;
+    if (dtype != GLA_BF16) return fail(GLA_ERR_UNSUPPORTED, "gla_chunk_fwd_mixer supports GLA_BF16 only");
+    if (!(eps >= 0.f)) return fail(GLA_ERR_INVALID_ARG, "eps must be >= 0");
+    OPTIONAL_PTR(h0, "h0");
+    OPTIONAL_PTR(hT, "hT");
+    OPTIONAL_PTR(aug, "aug");
+    OPTIONAL_PTR(norm_w, "norm_w");
+    OPTIONAL_PTR(workspace, "workspace");
+    if (B == 0 || H == 0) return GLA_OK;
+    if ((long double)B * T * H > 2147483647.0L * 8.0L) return fail(GLA_ERR_INVALID_ARG, "B*T*H too large");
+    REQUIRE_PTR(log_lambda, "log_lambda");
+    if (T > 0) {
+        REQUIRE_PTR(q, "q");
+        REQUIRE_PTR(k, "k");
+        REQUIRE_PTR(v, "v");
+        REQUIRE_PTR(g, "g");
+        REQUIRE_PTR(z, "z");
+        if (z == q || z == k || z == v || z == g) return fail(GLA_ERR_INVALID_ARG, "z may not alias an input");
+    }
+    unsigned int *status = nullptr;
+    if ((st = status_word(&status)) != GLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    cudaError_t e;
+    if (T == 0) {
+        e = launch_copy_state(h0, hT, (size_t)B * H * dk * dv, s, &launches);
+        t_launches = launches;
+        return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_mixer(T=0)");
+    }
+    // The forward writes o into z's buffer; the epilogue then rewrites each
+    // row in place (a warp reads all of a row's inputs before storing it).
+    FwdParams p{q, k, v, log_lambda, h0, scale, B, T, H, dk, dv, chunk, z, hT,
+                workspace, workspace ? workspace_bytes : 0, status};
+    e = launch_fwd_tc(p, s, &launches);
+    if (e == cudaSuccess) {
+        EpilogueParams ep{z, q, k, v, g, aug, norm_w, eps, B * T, H, dk, dv, z};
+        e = launch_mixer_epilogue(ep, true, s, &launches);
+    }
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_mixer launch");
+}
+
 size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype) {
     if (check_chunk_shape(B, T, H, dk, dv, chunk, dtype) != GLA_OK) return 0;
     if (dtype != GLA_BF16) return 0;

@@ -219,3 +219,22 @@ def test_conv_entry_points_reject_bad_arguments(L):
     assert step(N=-2) == binding.GLA_ERR_INVALID_ARG
     assert step(D=12) == binding.GLA_ERR_UNSUPPORTED
     assert step(N=0) == binding.GLA_OK
+
+
+def test_fused_forward_epilogue_rejects_bad_arguments(L):
+    def call(**kw):
+        a = dict(q=FAKE, k=FAKE + 0x100, v=FAKE + 0x200, g=FAKE + 0x300, ll=FAKE, h0=None, aug=None, w=None,
+                 eps=1e-6, B=2, T=256, H=16, dk=96, dv=192, C=128, dt=0, z=FAKE + 0x400, hT=None)
+        a.update(kw)
+        return L.gla_chunk_fwd_mixer(a["q"], a["k"], a["v"], a["g"], a["ll"], a["h0"], 0.1, a["aug"], a["w"],
+                                     a["eps"], a["B"], a["T"], a["H"], a["dk"], a["dv"], a["C"], a["dt"], a["z"],
+                                     a["hT"], None, 0, None)
+    assert call(dt=1) == binding.GLA_ERR_UNSUPPORTED          # bf16 only
+    assert call(dk=64) == binding.GLA_ERR_UNSUPPORTED
+    assert call(C=32) == binding.GLA_ERR_UNSUPPORTED
+    assert call(eps=-1.0) == binding.GLA_ERR_INVALID_ARG
+    assert call(g=None) == binding.GLA_ERR_INVALID_ARG
+    assert call(g=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert call(aug=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert call(z=FAKE + 0x300) == binding.GLA_ERR_INVALID_ARG   # z aliases g
+    assert call(B=0) == binding.GLA_OK
