@@ -224,32 +224,52 @@ def dev_tensor(x, dtype_str, device):
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device)
 
 
-def time_steps(step_fns, K, W, dist, stream):
-    """Run W warm-up steps, then K timed steps. Returns (total_ms, per-step ms
-    list, wall window, launches in timed region)."""
+def time_steps(step_fns, K, W, dist, stream, graph=None):
+    """Run W warm-up steps, then K timed steps between one pair of CUDA events
+    on `stream` (an event between every step would add a gap of its own).
+    With graph (the default, see --no-graph) one step's launches are captured
+    once into a CUDA graph after the warm-up and the timed steps replay it: the
+    same kernels on the same buffers, without per-launch host overhead.
+    Returns (total_ms, per-step ms list, wall window, launches in timed region)."""
     import torch
     from linear_attention_chunk_gb300 import gla_check
+    graph = GRAPH if graph is None else graph
     for _ in range(W):
         step_fns()
     gla_check()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    g = None
+    per_step = 0
+    if graph:
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            per_step = step_fns()
+        torch.cuda.synchronize()
+        gla_check()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
     dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
     launches = 0
     with torch.cuda.stream(stream):
+        start.record(stream)
         for i in range(K):
-            starts[i].record(stream)
-            launches += step_fns()
-            ends[i].record(stream)
+            if g is not None:
+                g.replay()
+                launches += per_step
+            else:
+                launches += step_fns()
+        end.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     dist.barrier()
     gla_check()
-    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total = starts[0].elapsed_time(ends[-1])
-    return total, per, (t0, t1), launches
+    total = start.elapsed_time(end)
+    return total, [total / K] * K, (t0, t1), launches
+
+
+GRAPH = True
 
 
 def bench_fwd(args, dist, device, stream, peaks, sampler):
@@ -297,38 +317,92 @@ def bench_fwd(args, dist, device, stream, peaks, sampler):
     return res
 
 
+def e2e_pipelined(args, dist, device, stream, host_in, host_out, compute):
+    """Steps through the public API with host buffers, pipelined across steps:
+    step i's inputs are copied host -> device on their own stream while step
+    i-1 computes, and step i's outputs are read back on a third stream while
+    step i+1 computes. Device inputs and outputs are double-buffered; every
+    step's copies and kernels lie inside the timed region, which runs from
+    the first copy in to the last copy out. compute(d_in, d_out, stream)
+    launches one step on `stream` and returns its launch count."""
+    import torch
+    from linear_attention_chunk_gb300 import gla_check
+    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    d_in = [[torch.empty_like(h, device=device) for h in host_in] for _ in range(2)]
+    d_out = [[torch.empty_like(h, device=device) for h in host_out] for _ in range(2)]
+    ev = lambda: torch.cuda.Event()
+
+    def run(n_steps, start=None, end=None):
+        comp_done, out_done = [None, None], [None, None]
+        launches = 0
+        if start is not None:
+            start.record(s_in)
+        for i in range(n_steps):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if comp_done[b] is not None:
+                    s_in.wait_event(comp_done[b])          # step i-2 is done reading these inputs
+                for d, h in zip(d_in[b], host_in):
+                    d.copy_(h, non_blocking=True)
+                in_ready = ev()
+                in_ready.record(s_in)
+            stream.wait_event(in_ready)
+            if out_done[b] is not None:
+                stream.wait_event(out_done[b])             # step i-2's outputs have been read back
+            with torch.cuda.stream(stream):
+                launches += compute(d_in[b], d_out[b], stream)
+                comp_done[b] = ev()
+                comp_done[b].record(stream)
+            s_out.wait_event(comp_done[b])
+            with torch.cuda.stream(s_out):
+                for h, d in zip(host_out, d_out[b]):
+                    h.copy_(d, non_blocking=True)
+                out_done[b] = ev()
+                out_done[b].record(s_out)
+        if end is not None:
+            end.record(s_out)
+        return launches
+
+    run(max(args.warmup, 2))
+    torch.cuda.synchronize()
+    gla_check()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    run(args.steps, start, end)
+    torch.cuda.synchronize()
+    dist.barrier()
+    gla_check()
+    total = dist.max(start.elapsed_time(end))
+    bi = sum(x.numel() * x.element_size() for x in host_in)
+    bo = sum(x.numel() * x.element_size() for x in host_out)
+    return total, bi, bo
+
+
+E2E_OVERLAP = ("inputs copied in on their own stream while the previous step computes, outputs "
+               "read back on a third stream while the next one computes (device buffers doubled)")
+
+
 def e2e_fwd(args, dist, device, stream, c, ll):
     """Same metric through the public API with host buffers: every step
     copies q, k, v from pinned host memory, runs the forward, and reads o and
-    hT back to pinned host memory."""
+    hT back to pinned host memory (pipelined across steps)."""
     import torch
     import linear_attention_chunk_gb300 as gla
     B, T = c.B, c.T
     pin = lambda x: torch.from_numpy(gen.bf16_bits(x).view(np.int16)).view(torch.bfloat16).pin_memory()
-    qh, kh, vh = pin(c.q), pin(c.k), pin(c.v)
-    oh = torch.empty((B, T, H, DV), dtype=torch.bfloat16).pin_memory()
-    hh = torch.empty((B, H, DK, DV), dtype=torch.float32).pin_memory()
-    qd, kd, vd = (torch.empty_like(x, device=device) for x in (qh, kh, vh))
-    od = torch.empty((B, T, H, DV), dtype=torch.bfloat16, device=device)
-    hd = torch.empty((B, H, DK, DV), dtype=torch.float32, device=device)
+    host_in = [pin(c.q), pin(c.k), pin(c.v)]
+    host_out = [torch.empty((B, T, H, DV), dtype=torch.bfloat16).pin_memory(),
+                torch.empty((B, H, DK, DV), dtype=torch.float32).pin_memory()]
 
-    def step():
-        with torch.cuda.stream(stream):
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-            gla.gla_chunk_fwd(qd, kd, vd, ll, None, c.scale, CHUNK, o=od, hT=hd, stream=stream)
-            n = gla.gla_last_launch_count()
-            oh.copy_(od, non_blocking=True)
-            hh.copy_(hd, non_blocking=True)
-        return n
+    def compute(d_in, d_out, st):
+        q, k, v = d_in
+        gla.gla_chunk_fwd(q, k, v, ll, None, c.scale, CHUNK, o=d_out[0], hT=d_out[1], stream=st)
+        return gla.gla_last_launch_count()
 
-    total, _, _, _ = time_steps(step, args.steps, args.warmup, dist, stream)
-    total = dist.max(total)
-    bi = sum(x.numel() * x.element_size() for x in (qh, kh, vh))
-    bo = oh.numel() * oh.element_size() + hh.numel() * hh.element_size()
+    total, bi, bo = e2e_pipelined(args, dist, device, stream, host_in, host_out, compute)
     return {"value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "overlap": E2E_OVERLAP}
 
 
 def bench_fwd_bwd(args, dist, device, stream, peaks, sampler):
@@ -733,33 +807,25 @@ def bench_conv(args, dist, device, stream, peaks, sampler):
 
 def e2e_decode(args, dist, device, stream, toks, states, ll, scale, N, L):
     """Decode through the public API with host token buffers: per step the 24
-    layers' q, k, v come from pinned host memory and the 24 outputs go back;
-    the recurrent states stay resident on the device (the serving page)."""
+    layers' q, k, v come from pinned host memory and the 24 outputs go back
+    (pipelined across steps); the recurrent states stay resident on the
+    device (the serving page)."""
     import torch
     import linear_attention_chunk_gb300 as gla
-    host_in = [tuple(x.cpu().pin_memory() for x in t) for t in toks]
-    dev_in = [tuple(torch.empty_like(x) for x in t) for t in toks]
+    host_in = [x.cpu().pin_memory() for t in toks for x in t]
     host_out = [torch.empty((N, H, DV), dtype=torch.bfloat16).pin_memory() for _ in range(L)]
-    dev_out = [torch.empty((N, H, DV), dtype=torch.bfloat16, device=device) for _ in range(L)]
 
-    def step():
+    def compute(d_in, d_out, st):
         n = 0
-        with torch.cuda.stream(stream):
-            for layer in range(L):
-                for d, h in zip(dev_in[layer], host_in[layer]):
-                    d.copy_(h, non_blocking=True)
-                q, k, v = dev_in[layer]
-                gla.gla_decode_step(q, k, v, ll, states[layer], scale, o=dev_out[layer], stream=stream)
-                n += gla.gla_last_launch_count()
-                host_out[layer].copy_(dev_out[layer], non_blocking=True)
+        for layer in range(L):
+            q, k, v = d_in[3 * layer:3 * layer + 3]
+            gla.gla_decode_step(q, k, v, ll, states[layer], scale, o=d_out[layer], stream=st)
+            n += gla.gla_last_launch_count()
         return n
 
-    total, _, _, _ = time_steps(step, args.steps, args.warmup, dist, stream)
-    total = dist.max(total)
-    bi = sum(x.numel() * x.element_size() for t in host_in for x in t)
-    bo = sum(x.numel() * x.element_size() for x in host_out)
+    total, bi, bo = e2e_pipelined(args, dist, device, stream, host_in, host_out, compute)
     return {"value": N * dist.world * args.steps / (total * 1e-3), "unit": "seq-steps/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "overlap": E2E_OVERLAP}
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -898,9 +964,13 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="override the decode layer count (profiling)")
     ap.add_argument("--long-T", dest="long_T", type=int, default=0, help="override T of the long workload (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every timed step eagerly instead of replaying a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 0)
+    global GRAPH
+    GRAPH = not args.no_graph
 
     dist = Dist()
     if args.impl == "reference":
@@ -958,6 +1028,10 @@ def main(argv=None):
         **{key: head[key] for key in ("standalone", "fwd_mixer", "chunk64", "step", "ms_per_layer_step")
            if key in head},
         "peaks": peaks,
+        "timing": {"events": "one CUDA event pair around the K timed steps, on the launch stream",
+                   "steps": "replay of one step captured as a CUDA graph" if GRAPH else "eager launches",
+                   "e2e": "eager launches through the API; every step's host copies inside the timed region, "
+                          "overlapped with the neighbouring steps' kernels"},
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         base, base_modes = cpu_baseline()
