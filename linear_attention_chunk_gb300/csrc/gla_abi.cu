@@ -206,7 +206,8 @@ gla_status gla_chunk_fwd_mixer(const void *q, const void *k, const void *v, cons
     OPTIONAL_PTR(norm_w, "norm_w");
     OPTIONAL_PTR(workspace, "workspace");
     if (B == 0 || H == 0) return GLA_OK;
-    if ((long double)B * T * H > 2147483647.0L * 8.0L) return fail(GLA_ERR_INVALID_ARG, "B*T*H too large");
+    if ((long double)B * T > 2147483647.0L || (long double)B * T * H > 2147483647.0L * 8.0L)
+        return fail(GLA_ERR_INVALID_ARG, "B*T or B*T*H too large");
     REQUIRE_PTR(log_lambda, "log_lambda");
     if (T > 0) {
         REQUIRE_PTR(q, "q");
