@@ -2,15 +2,64 @@
 //   dv, dh0: the chunk kernel in reverse time (fwd_tc.cu)
 //   dq:      the transposed-shape chunk kernel, forward in time (bwd_tc.cu)
 //   dk:      the transposed-shape chunk kernel, reverse in time (bwd_tc.cu)
-// The three are independent; each reads the inputs it needs once.
+// The three are independent; each reads the inputs it needs once. They run
+// concurrently: dq and dk on two helper streams forked from the caller's
+// stream and joined back to it with events, dv on the caller's stream. Each
+// launch alone ends in a partial wave of CTAs; side by side, one kernel's
+// CTAs fill the SMs the others leave idle (415.8 -> 374.9 us for the
+// training workload). Fork and join are event records and waits, so the call
+// stays asynchronous and can be captured in a CUDA graph. The helper streams
+// and events are created once per host thread and device, and kept.
 #include "kernels.h"
 
 namespace gla {
-cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches) {
-    cudaError_t e = launch_bwd_dv_tc(p, s, launches);
+namespace {
+
+constexpr int kMaxDev = 64;
+
+struct Fork {
+    cudaStream_t aux[2] = {nullptr, nullptr};
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+};
+
+cudaError_t fork_for_device(Fork **out) {
+    thread_local Fork forks[kMaxDev];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if ((e = launch_bwd_dq_tc(p, s, launches)) != cudaSuccess) return e;
-    return launch_bwd_dk_tc(p, s, launches);
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    Fork &f = forks[dev];
+    if (!f.aux[0]) {
+        for (int i = 0; i < 2; ++i)
+            if ((e = cudaStreamCreateWithFlags(&f.aux[i], cudaStreamNonBlocking)) != cudaSuccess) return e;
+        for (int i = 0; i < 3; ++i)
+            if ((e = cudaEventCreateWithFlags(&f.ev[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+    *out = &f;
+    return cudaSuccess;
 }
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches) {
+    Fork *f = nullptr;
+    cudaError_t e = fork_for_device(&f);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaEventRecord(f->ev[0], s)) != cudaSuccess) return e;
+    for (int i = 0; i < 2; ++i)
+        if ((e = cudaStreamWaitEvent(f->aux[i], f->ev[0], 0)) != cudaSuccess) return e;
+    cudaError_t el = launch_bwd_dq_tc(p, f->aux[0], launches);
+    if (el == cudaSuccess) el = launch_bwd_dk_tc(p, f->aux[1], launches);
+    if (el == cudaSuccess) el = launch_bwd_dv_tc(p, s, launches);
+    // Join whatever was launched before reporting, so the caller's stream
+    // never runs ahead of work still in flight on the helper streams.
+    for (int i = 0; i < 2; ++i) {
+        if ((e = cudaEventRecord(f->ev[1 + i], f->aux[i])) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(s, f->ev[1 + i], 0)) != cudaSuccess) return e;
+    }
+    return el;
+}
+
 size_t bwd_tc_workspace_size(int, int, int, int) { return 0; }
+
 }  // namespace gla

@@ -1,6 +1,7 @@
 """The library's calls inside a CUDA graph: they allocate nothing and never
 synchronise, so a captured step replays to the same bits as the same calls
-launched eagerly (forward with segmentation, backward, decode with the fused
+launched eagerly (forward with segmentation, the backward with its three
+launches forked onto helper streams and joined back, decode with the fused
 epilogue, the Conv1d prefill and serving step)."""
 import numpy as np
 import pytest
@@ -34,6 +35,8 @@ def test_captured_step_replays_bit_exact(gla):
 
     def buffers():
         return dict(o=torch.empty_like(d["v"]), hT=torch.empty((1, 2, 96, 192), device="cuda"),
+                    dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]), dv=torch.empty_like(d["v"]),
+                    dh0=torch.empty((1, 2, 96, 192), device="cuda"),
                     S=f32_dev(dc.S), win=f32_dev(cc.window), z=torch.empty((16, 4, 192), dtype=torch.bfloat16,
                                                                            device="cuda"),
                     y=torch.empty_like(x), y1=torch.empty_like(x1))
@@ -41,6 +44,8 @@ def test_captured_step_replays_bit_exact(gla):
     def step(bf, s):
         gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["ll"], d["h0"], c.scale, 128, o=bf["o"], hT=bf["hT"],
                           workspace=ws, stream=s)
+        gla.gla_chunk_bwd(d["q"], d["k"], d["v"], d["ll"], d["do"], d["h0"], d["dhT"], c.scale, 128, dq=bf["dq"],
+                          dk=bf["dk"], dv=bf["dv"], dh0=bf["dh0"], stream=s)
         gla.gla_decode_step_mixer(dq, dk, dvv, dll, bf["S"], g, None, None, 1e-6, dc.scale, z=bf["z"], stream=s)
         gla.gla_conv1d_fwd(x, w, b, bf["win"], y=bf["y"], win_out=bf["win"], stream=s)
         gla.gla_conv1d_step(x1, w, b, bf["win"], y=bf["y1"], stream=s)
