@@ -457,11 +457,13 @@ __global__ void __launch_bounds__(stream_max_vecs<VB>() + 32, 1) conv_stream_ker
 }
 
 // ---------------------------------------------------------- plain kernel
-// y for one tile of kTile tokens x one 16-byte channel vector per thread
-// (rows too wide for the streaming kernel's ring).
-template <typename T, bool kVar>
+// y for one tile of TILE tokens x one VB-byte channel vector per thread, all
+// the tile's row loads (and the three rows before it) issued up front. The
+// windows are then written by conv_window_kernel in a second launch.
+template <typename T, bool kVar, int VB, int TILE>
 __global__ void __launch_bounds__(kThreads) conv_fwd_kernel(const ConvParams p) {
-    constexpr int V = 16 / (int)sizeof(T), P = V / 2;
+    constexpr int V = VB / (int)sizeof(T), P = V / 2;
+    using Vec = typename VecT<VB>::type;
     const int groups = p.D / V;
     const int ncb = (groups + kThreads - 1) / kThreads;
     const long tile = blockIdx.x / ncb;
@@ -469,22 +471,25 @@ __global__ void __launch_bounds__(kThreads) conv_fwd_kernel(const ConvParams p) 
     if (g >= groups) return;
     const int c0 = g * V;
     const size_t D = (size_t)p.D;
-    const long t0 = tile * kTile;
-    const long t1 = min(t0 + kTile, (long)p.NT);
+    const long t0 = tile * TILE;
+    const long t1 = min(t0 + TILE, (long)p.NT);
     const T *x = static_cast<const T *>(p.x) + c0;
     T *y = static_cast<T *>(p.y) + c0;
 
-    uint4 xr[kTile];
+    Vec xr[TILE], xh[3];
 #pragma unroll
-    for (int i = 0; i < kTile; ++i)
-        if (t0 + i < t1) xr[i] = ld_vec<T, 16>(x + (size_t)(t0 + i) * D);
+    for (int j = 0; j < 3; ++j)
+        if (t0 - 3 + j >= 0) xh[j] = ld_vec<T, VB>(x + (size_t)(t0 - 3 + j) * D);
+#pragma unroll
+    for (int i = 0; i < TILE; ++i)
+        if (t0 + i < t1) xr[i] = ld_vec<T, VB>(x + (size_t)(t0 + i) * D);
     Taps<T, P> tp;
     tp.load(p.w, p.b, c0);
 
     f2 h[3][P] = {};
     long s = 0, e = -1;
 #pragma unroll
-    for (int i = 0; i < kTile; ++i) {
+    for (int i = 0; i < TILE; ++i) {
         const long t = t0 + i;
         if (t >= t1) break;
         if (t >= e) {
@@ -494,10 +499,15 @@ __global__ void __launch_bounds__(kThreads) conv_fwd_kernel(const ConvParams p) 
                 e = t + 1;
                 continue;
             }
-            load_history<T, 16>(x, D, t, s, wi, c0, h);
+            if (i == 0 && t0 - 3 >= s) {   // the tile's first token, its history inside the sequence
+#pragma unroll
+                for (int j = 0; j < 3; ++j) unpack_pairs<T, VB>(xh[j], h[j]);
+            } else {
+                load_history<T, VB>(x, D, t, s, wi, c0, h);
+            }
         }
         f2 xv[P], out[P];
-        unpack_pairs<T, 16>(xr[i], xv);
+        unpack_pairs<T, VB>(xr[i], xv);
         conv_point<T, P>(tp, h, xv, out);
 #pragma unroll
         for (int k = 0; k < P; ++k) {
@@ -505,7 +515,7 @@ __global__ void __launch_bounds__(kThreads) conv_fwd_kernel(const ConvParams p) 
             h[1][k] = h[2][k];
             h[2][k] = xv[k];
         }
-        *reinterpret_cast<uint4 *>(y + (size_t)t * D) = pack_pairs<T, 16>(out);
+        *reinterpret_cast<Vec *>(y + (size_t)t * D) = pack_pairs<T, VB>(out);
     }
 }
 
@@ -634,8 +644,8 @@ cudaError_t conv_fwd_impl(const ConvParams &p, bool var, cudaStream_t st, int *l
     if (p.NT > 0) {
         const size_t blocks = (size_t)((p.NT + kTile - 1) / kTile) * ncb;
         if (blocks > 0x7fffffffull) return cudaErrorInvalidValue;
-        if (var) conv_fwd_kernel<T, true><<<(unsigned)blocks, kThreads, 0, st>>>(p);
-        else conv_fwd_kernel<T, false><<<(unsigned)blocks, kThreads, 0, st>>>(p);
+        if (var) conv_fwd_kernel<T, true, 16, kTile><<<(unsigned)blocks, kThreads, 0, st>>>(p);
+        else conv_fwd_kernel<T, false, 16, kTile><<<(unsigned)blocks, kThreads, 0, st>>>(p);
         if (launches) ++*launches;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
