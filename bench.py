@@ -41,6 +41,12 @@ import time
 
 import numpy as np
 
+# More hardware work queues than CUDA's default of 8, set before any CUDA
+# context exists: the library's backward helper streams, the copy streams of
+# the end-to-end legs and the compute stream must not share a queue, or their
+# work serialises behind one another.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -327,7 +333,9 @@ def e2e_pipelined(args, dist, device, stream, host_in, host_out, compute):
     launches one step on `stream` and returns its launch count."""
     import torch
     from linear_attention_chunk_gb300 import gla_check
-    s_in, s_out = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+    if device not in _COPY_STREAMS:   # created once: a fresh pair per call could land on busy queues
+        _COPY_STREAMS[device] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    s_in, s_out = _COPY_STREAMS[device]
     d_in = [[torch.empty_like(h, device=device) for h in host_in] for _ in range(2)]
     d_out = [[torch.empty_like(h, device=device) for h in host_out] for _ in range(2)]
     ev = lambda: torch.cuda.Event()
@@ -379,6 +387,7 @@ def e2e_pipelined(args, dist, device, stream, host_in, host_out, compute):
     return total, bi, bo
 
 
+_COPY_STREAMS = {}
 E2E_OVERLAP = ("inputs copied in on their own stream while the previous step computes, outputs "
                "read back on a third stream while the next one computes (device buffers doubled)")
 

@@ -182,6 +182,11 @@ gla_status gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, con
  *   dq, dk_ [B,T,H,dk], dv_ [B,T,H,dv] (dtype, written),
  *   dh0 [B,H,dk,dv] fp32 or NULL (not wanted),
  *   workspace: at least gla_chunk_bwd_workspace_size() bytes (may be 0).
+ * The three backward launches run side by side: two on helper streams that
+ * the call forks from `stream` and joins back with events (created once per
+ * host thread and device). CUDA maps streams onto a limited number of
+ * hardware queues (8 by default); setting CUDA_DEVICE_MAX_CONNECTIONS to 32
+ * before the first CUDA call keeps them from sharing one.
  */
 gla_status gla_chunk_bwd(const void *q, const void *k, const void *v,
                          const float *log_lambda, const float *h0, float scale,
