@@ -290,6 +290,18 @@ gla_status gla_conv1d_varlen(const void *x, const float *w, const float *b, cons
 gla_status gla_conv1d_step(const void *x, const float *w, const float *b, float *win, int N, int D,
                            gla_dtype dtype, void *y, void *stream);
 
+/*
+ * gla_selftest_wait_timeout -- diagnostic of the device-side failure
+ * detection, with no fault and no hang: one kernel waits on two mbarriers
+ * that nothing completes. The first wait gives up after limit_us (1 to
+ * 1,000,000) and flags a timeout; the second, with the kernels' own 2 s
+ * limit, must leave as soon as it sees that flag. result: 3 ints in device
+ * memory (16-byte aligned): [0], [1] = 1 if the wait completed, 0 if it gave
+ * up; [2] = microseconds the second wait lasted. The next gla_check()
+ * reports GLA_ERR_TIMEOUT and clears the status word.
+ */
+gla_status gla_selftest_wait_timeout(unsigned int limit_us, int *result, void *stream);
+
 /* Synchronise `stream` and report: GLA_ERR_CUDA if the stream or an earlier
  * launch failed, GLA_ERR_TIMEOUT if a device-side wait gave up since the last
  * gla_check (the status word is cleared on read), else GLA_OK. */

@@ -31,6 +31,7 @@ from .binding import (  # noqa: F401
     gla_decode_step_mixer,
     gla_last_launch_count,
     gla_mixer_epilogue,
+    gla_selftest_wait_timeout,
     gla_status_string,
     gla_version,
     lib,

@@ -39,7 +39,7 @@ GLA_BF16, GLA_FP32 = 0, 1
 ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen",
                  "gla_chunk_fwd_mixer", "gla_chunk_bwd",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
-                 "gla_conv1d_fwd", "gla_conv1d_varlen", "gla_conv1d_step", "gla_check",
+                 "gla_conv1d_fwd", "gla_conv1d_varlen", "gla_conv1d_step", "gla_selftest_wait_timeout", "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
 
 
@@ -99,6 +99,8 @@ def lib():
             L.gla_conv1d_varlen.restype = _i
             L.gla_conv1d_step.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp]
             L.gla_conv1d_step.restype = _i
+            L.gla_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp, _vp]
+            L.gla_selftest_wait_timeout.restype = _i
             L.gla_check.argtypes = [_vp]
             L.gla_check.restype = _i
             L.gla_status_string.argtypes = [_i]
@@ -381,6 +383,17 @@ def gla_conv1d_step(x, w, b, win, *, y=None, stream=None):
     st = lib().gla_conv1d_step(_ptr(x), _ptr(w), _ptr(b), _ptr(win), N, D, _dtype_code(x), _ptr(y), _stream(stream))
     _raise_on(st, "gla_conv1d_step")
     return y
+
+
+def gla_selftest_wait_timeout(limit_us=20000, *, stream=None):
+    """Diagnostic: make the device-side bounded waits run out (no fault, no
+    hang). Returns the int32 CUDA tensor [completed0, completed1, us_waited1];
+    the next gla_check() raises GlaError(GLA_ERR_TIMEOUT)."""
+    torch = _torch()
+    result = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    st = lib().gla_selftest_wait_timeout(int(limit_us), _ptr(result), _stream(stream))
+    _raise_on(st, "gla_selftest_wait_timeout")
+    return result[:3]
 
 
 def gla_check(stream=None):

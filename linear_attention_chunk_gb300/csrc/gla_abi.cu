@@ -455,6 +455,21 @@ gla_status gla_conv1d_step(const void *x, const float *w, const float *b, float 
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_conv1d_step launch");
 }
 
+gla_status gla_selftest_wait_timeout(unsigned int limit_us, int *result, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    if (limit_us == 0 || limit_us > 1000000u) return fail(GLA_ERR_INVALID_ARG, "limit_us must be in 1..1000000");
+    REQUIRE_PTR(result, "result");
+    unsigned int *status = nullptr;
+    gla_status st = status_word(&status);
+    if (st != GLA_OK) return st;
+    int launches = 0;
+    const cudaError_t e = launch_selftest_wait(status, (uint64_t)limit_us * 1000u, result,
+                                               static_cast<cudaStream_t>(stream), &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_selftest_wait_timeout launch");
+}
+
 gla_status gla_check(void *stream) {
     t_err[0] = 0;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

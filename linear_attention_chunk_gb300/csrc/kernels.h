@@ -89,6 +89,9 @@ struct ConvParams {
     void *y;
     unsigned int *status;
 };
+// Diagnostic: make the bounded device waits run out (selftest.cu).
+cudaError_t launch_selftest_wait(unsigned int *status, uint64_t limit_ns, int *result, cudaStream_t s,
+                                 int *launches);
 cudaError_t launch_conv_fwd(const ConvParams &p, bool varlen, bool bf16, cudaStream_t s, int *launches);
 cudaError_t launch_conv_step(const ConvParams &p, bool bf16, cudaStream_t s, int *launches);
 

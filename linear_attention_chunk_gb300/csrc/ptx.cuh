@@ -82,22 +82,27 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitim
 
 // Wait for the completion of the mbarrier phase with the given parity.
 // Returns false (after flagging the CTA and the device status word) if the
-// phase does not complete within kWaitLimitNs, or if another role of the CTA
+// phase does not complete within limit_ns, or if another role of the CTA
 // already gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, const WaitCtl &ctl, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 127u) == 0) {
             if (*ctl.abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *ctl.abort = 1;
                 atomicOr(ctl.status, kDevTimeout);
                 return false;
             }
         }
     }
+}
+
+// The same with the kernels' limit, kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+    return mbar_wait_for(bar, parity, ctl, kWaitLimitNs);
 }
 
 // Waits for a phase for at most limit_ns whatever the abort flag says: lets a

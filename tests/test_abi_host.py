@@ -238,3 +238,10 @@ def test_fused_forward_epilogue_rejects_bad_arguments(L):
     assert call(aug=ODD) == binding.GLA_ERR_INVALID_ARG
     assert call(z=FAKE + 0x300) == binding.GLA_ERR_INVALID_ARG   # z aliases g
     assert call(B=0) == binding.GLA_OK
+
+
+def test_selftest_rejects_bad_arguments(L):
+    assert L.gla_selftest_wait_timeout(0, FAKE, None) == binding.GLA_ERR_INVALID_ARG
+    assert L.gla_selftest_wait_timeout(2000000, FAKE, None) == binding.GLA_ERR_INVALID_ARG
+    assert L.gla_selftest_wait_timeout(1000, None, None) == binding.GLA_ERR_INVALID_ARG
+    assert L.gla_selftest_wait_timeout(1000, ODD, None) == binding.GLA_ERR_INVALID_ARG
