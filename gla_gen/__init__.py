@@ -87,6 +87,22 @@ def decay_log_uniform(rng: np.random.Generator, H: int, lo: float = 0.9, hi: flo
     return np.exp(rng.uniform(math.log(lo), math.log(hi), size=H))
 
 
+def log_gates(rng: np.random.Generator, shape, kind: str = "gla") -> np.ndarray:
+    """Per-token log-decays g <= 0 as fp32 (natural log; the decay is exp(g)).
+    kind "gla": log(sigmoid(x)) / 16 with x ~ N(0, 1), the gate-logit
+    normaliser of gated linear attention (about -0.045 per token, a decay of
+    about e^-5.8 across a 128-token chunk); "wide": uniform in [-3, 0], strong
+    decays whose products underflow inside a chunk."""
+    if kind == "gla":
+        x = rng.standard_normal(shape)
+        g = -np.logaddexp(0.0, -x) / 16.0
+    elif kind == "wide":
+        g = -rng.uniform(0.0, 3.0, size=shape)
+    else:
+        raise ValueError(f"unknown gate kind {kind!r}")
+    return np.minimum(g, 0.0).astype(np.float32)
+
+
 def log_lambda_of(lam: np.ndarray) -> np.ndarray:
     """Natural log of the decay, as the fp32 value the library receives.
     lambda = 0 maps to -inf."""
@@ -147,9 +163,12 @@ def make_case(B: int, T: int, H: int, dk: int, dv: int, *, seed: int, dtype: str
               lam_range=(0.9, 0.9999), normalise_k: bool = False,
               h0_std: Optional[float] = None, with_grad: bool = False,
               dhT_std: Optional[float] = None, do_std: float = 1.0,
-              scale: Optional[float] = None, chunk: int = 128, name: str = "") -> Case:
+              scale: Optional[float] = None, chunk: int = 128, name: str = "",
+              gate: Optional[str] = None) -> Case:
     """Draw one case. `lam` fixes the per-head decay (array of H, or a scalar);
-    `lam_random` draws it log-uniformly in `lam_range` after the tensors."""
+    `lam_random` draws it log-uniformly in `lam_range` after the tensors.
+    `gate` (a log_gates kind) also draws per-token log-decays g [B, T, H]
+    last, into extra["g"]."""
     rng = np.random.default_rng(seed)
     q = _normal(rng, (B, T, H, dk))
     k = _normal(rng, (B, T, H, dk))
@@ -163,6 +182,7 @@ def make_case(B: int, T: int, H: int, dk: int, dv: int, *, seed: int, dtype: str
         lam_arr = decay_layer_schedule(H)
     else:
         lam_arr = np.broadcast_to(np.asarray(lam, dtype=np.float64), (H,)).copy()
+    g = log_gates(rng, (B, T, H), gate) if gate is not None else None
     if normalise_k:
         k = _l2_normalise_last(k)
     q, k, v = _store(q, dtype), _store(k, dtype), _store(v, dtype)
@@ -172,7 +192,7 @@ def make_case(B: int, T: int, H: int, dk: int, dv: int, *, seed: int, dtype: str
         scale = 1.0 / math.sqrt(dk)
     return Case(B=B, T=T, H=H, dk=dk, dv=dv, dtype=dtype, scale=float(np.float32(scale)),
                 log_lambda=log_lambda_of(lam_arr), q=q, k=k, v=v, h0=h0, do=do, dhT=dhT,
-                chunk=chunk, name=name)
+                chunk=chunk, name=name, extra={} if g is None else {"g": g})
 
 
 # ----------------------------------------------------------------------------

@@ -18,6 +18,9 @@ Functions (all layouts token-major, see gla_oracle.c):
   decode         -- one recurrent step per (sequence, head) (O4)
   mixer_epilogue -- self-augmentation, Head RMSNorm and the SiLU(g) gate (O7)
   conv1d         -- causal depthwise Conv1d (width 4) with SiLU and its window (O8)
+  fwd_gated      -- per-token (data-dependent) decay: recurrence, unrolled and
+                    chunked forms (O9)
+  decode_gated   -- one recurrent step with a per-token decay (O10)
 """
 from __future__ import annotations
 
@@ -70,9 +73,17 @@ def _load():
             lib.gla_oracle_mixer_epilogue.argtypes = [_D, _D, _D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L,
                                                       _L, _D, ctypes.c_int]
             lib.gla_oracle_conv1d.argtypes = [_D, _D, _D, _D, _L, _L, _L, _D, _D, ctypes.c_int]
+            gsig = [_D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L, _L, _L, _D, _D, ctypes.c_int]
+            lib.gla_oracle_fwd_gated.argtypes = gsig
+            lib.gla_oracle_fwd_gated_quadratic.argtypes = gsig
+            lib.gla_oracle_fwd_gated_chunked.argtypes = gsig[:11] + [_L] + gsig[11:]
+            lib.gla_oracle_decode_gated.argtypes = [_D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L, _L,
+                                                    _D, ctypes.c_int]
             for f in ("gla_oracle_fwd_recurrent", "gla_oracle_fwd_quadratic", "gla_oracle_fwd_chunked",
                       "gla_oracle_bwd", "gla_oracle_bwd_chunked", "gla_oracle_decode",
-                      "gla_oracle_threads", "gla_oracle_mixer_epilogue", "gla_oracle_conv1d"):
+                      "gla_oracle_threads", "gla_oracle_mixer_epilogue", "gla_oracle_conv1d",
+                      "gla_oracle_fwd_gated", "gla_oracle_fwd_gated_quadratic", "gla_oracle_fwd_gated_chunked",
+                      "gla_oracle_decode_gated"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -204,3 +215,41 @@ def conv1d(x, w, b=None, window=None, nthreads=0):
     _check(lib.gla_oracle_conv1d(_p(x), _p(w), _p(b), _p(win), B, T, D, _p(y), _p(win_out), int(nthreads)),
            "conv1d")
     return y, win_out
+
+
+def fwd_gated(q, k, v, g, h0=None, scale=1.0, form="recurrent", chunk=128, nthreads=0, want_o=True):
+    """O9: the forward with a per-token log-decay g [B, T, H] (natural log,
+    <= 0, -inf allowed). form = "recurrent" (the token recurrence),
+    "quadratic" (unrolled sums, tiny inputs only) or "chunked" (the chunk
+    equations at `chunk`). Returns (o [B,T,H,dv], hT [B,H,dk,dv])."""
+    lib = _load()
+    q, k, v, g, h0 = _f64(q), _f64(k), _f64(v), _f64(g), _f64(h0)
+    B, T, H, dk, dv = _dims(q, v)
+    if g.shape != (B, T, H):
+        raise ValueError(f"oracle fwd_gated: g has shape {g.shape}, expected {(B, T, H)}")
+    o = np.zeros((B, T, H, dv)) if (want_o or form == "quadratic") else None
+    hT = np.zeros((B, H, dk, dv))
+    args = [_p(q), _p(k), _p(v), _p(g), _p(h0), float(scale), B, T, H, dk, dv]
+    name = {"recurrent": "gla_oracle_fwd_gated", "quadratic": "gla_oracle_fwd_gated_quadratic",
+            "chunked": "gla_oracle_fwd_gated_chunked"}[form]
+    if form == "chunked":
+        args.append(int(chunk))
+    args += [_p(o), _p(hT), int(nthreads)]
+    _check(getattr(lib, name)(*args), name)
+    return o, hT
+
+
+def decode_gated(q, k, v, g, S, scale=1.0, nthreads=0):
+    """O10: one step S <- exp(g) S + k v^T, o = scale S^T q per (n, h), with a
+    per-sequence, per-head log-decay g [N, H]. Returns (o [N,H,dv], S_new)."""
+    lib = _load()
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(g)
+    S = np.array(S, dtype=np.float64, copy=True, order="C")
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if g.shape != (N, H):
+        raise ValueError(f"oracle decode_gated: g has shape {g.shape}, expected {(N, H)}")
+    o = np.zeros((N, H, dv))
+    _check(lib.gla_oracle_decode_gated(_p(q), _p(k), _p(v), _p(g), _p(S), float(scale), N, H, dk, dv, _p(o),
+                                       int(nthreads)), "decode_gated")
+    return o, S

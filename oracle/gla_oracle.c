@@ -617,3 +617,218 @@ int gla_oracle_conv1d(const double *x, const double *w, const double *b, const d
     run_units(B * D, nthreads, conv_unit, &a);
     return 0;
 }
+
+/* ------------------------------------------- O9: per-token (gated) decay */
+/* The "next" variant of the same mixer with a data-dependent decay: the
+ * pages run the mixer through flash-linear-attention's fused_chunk_simple_gla
+ * ("Challenge 1") and list "Gated Linear Attention Transformers with
+ * Hardware-Efficient Training" among their resources; in that form the
+ * per-head decay is a per-token scalar per head, alpha_t = exp(g_t) with a
+ * log-decay g_t <= 0 (g may be -inf: the state is then cleared):
+ *   S_t = exp(g_t) S_{t-1} + k_t v_t^T,   o_t = scale * S_t^T q_t.
+ * With g_t = log lambda_h for every t it is the fixed-decay recurrence.
+ * g is [B,T,H] (decode: [N,H]).                                            */
+typedef struct {
+    const double *q, *k, *v, *g, *h0;
+    double scale;
+    long B, T, H, dk, dv, chunk;
+    double *o, *hT;
+} gated_t;
+
+#define GQIDX(a, b, t, h, i) ((((b) * (a)->T + (t)) * (a)->H + (h)) * (a)->dk + (i))
+#define GVIDX(a, b, t, h, j) ((((b) * (a)->T + (t)) * (a)->H + (h)) * (a)->dv + (j))
+#define GGIDX(a, b, t, h) (((b) * (a)->T + (t)) * (a)->H + (h))
+#define GSIDX(a, b, h) (((b) * (a)->H + (h)) * (a)->dk * (a)->dv)
+
+/* exp of the summed log-decays of tokens u+1..t (an empty sum is 0, so the
+ * weight of a token on itself is 1 even after a -inf gate). */
+static double gated_weight(const gated_t *a, long b, long h, long u, long t) {
+    double s = 0.0;
+    for (long r = u + 1; r <= t; ++r) s += a->g[GGIDX(a, b, r, h)];
+    return exp(s);
+}
+
+/* O9: the token recurrence with per-token decay. */
+static void gated_recurrent_unit(void *ctx, long unit) {
+    const gated_t *a = (const gated_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv;
+    double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    if (a->h0) memcpy(S, a->h0 + GSIDX(a, b, h), sizeof(double) * (size_t)(dk * dv));
+    for (long t = 0; t < a->T; ++t) {
+        double alpha = exp(a->g[GGIDX(a, b, t, h)]);
+        const double *kt = a->k + GQIDX(a, b, t, h, 0);
+        const double *vt = a->v + GVIDX(a, b, t, h, 0);
+        const double *qt = a->q + GQIDX(a, b, t, h, 0);
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < dv; ++j)
+                S[i * dv + j] = alpha * S[i * dv + j] + kt[i] * vt[j];
+        if (a->o) {
+            double *ot = a->o + GVIDX(a, b, t, h, 0);
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += S[i * dv + j] * qt[i];
+                ot[j] = a->scale * acc;
+            }
+        }
+    }
+    if (a->hT) memcpy(a->hT + GSIDX(a, b, h), S, sizeof(double) * (size_t)(dk * dv));
+    free(S);
+}
+
+/* O9, unrolled (tiny inputs only): with the decay of tokens u+1..t
+ *   o_t = scale * ( d(-1,t) h0^T q_t + sum_{u<=t} d(u,t) (q_t.k_u) v_u ),
+ *   hT  = d(-1,T-1) h0 + sum_u d(u,T-1) k_u v_u^T,   d(u,t) = exp(sum g_{u+1..t}). */
+static void gated_quadratic_unit(void *ctx, long unit) {
+    const gated_t *a = (const gated_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv;
+    const double *H0 = a->h0 ? a->h0 + GSIDX(a, b, h) : NULL;
+    for (long t = 0; t < a->T; ++t) {
+        const double *qt = a->q + GQIDX(a, b, t, h, 0);
+        double *ot = a->o + GVIDX(a, b, t, h, 0);
+        for (long j = 0; j < dv; ++j) ot[j] = 0.0;
+        if (H0) {
+            double w = gated_weight(a, b, h, -1, t);
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += H0[i * dv + j] * qt[i];
+                ot[j] += w * acc;
+            }
+        }
+        for (long u = 0; u <= t; ++u) {
+            const double *ku = a->k + GQIDX(a, b, u, h, 0);
+            const double *vu = a->v + GVIDX(a, b, u, h, 0);
+            double qk = 0.0;
+            for (long i = 0; i < dk; ++i) qk += qt[i] * ku[i];
+            double w = gated_weight(a, b, h, u, t) * qk;
+            for (long j = 0; j < dv; ++j) ot[j] += w * vu[j];
+        }
+        for (long j = 0; j < dv; ++j) ot[j] *= a->scale;
+    }
+    if (a->hT) {
+        double *S = a->hT + GSIDX(a, b, h);
+        double w0 = gated_weight(a, b, h, -1, a->T - 1);
+        for (long i = 0; i < dk; ++i)
+            for (long j = 0; j < dv; ++j) S[i * dv + j] = H0 ? w0 * H0[i * dv + j] : 0.0;
+        for (long u = 0; u < a->T; ++u) {
+            const double *ku = a->k + GQIDX(a, b, u, h, 0);
+            const double *vu = a->v + GVIDX(a, b, u, h, 0);
+            double w = gated_weight(a, b, h, u, a->T - 1);
+            for (long i = 0; i < dk; ++i)
+                for (long j = 0; j < dv; ++j) S[i * dv + j] += w * ku[i] * vu[j];
+        }
+    }
+}
+
+/* O9 in chunks of C (0-based i, j inside a chunk of Cc tokens entering with
+ * S_prev; d(j,i) the decay of the chunk's tokens j+1..i, d(-1,i) that of
+ * tokens 0..i):
+ *   o_i   = scale * ( d(-1,i) S_prev^T q_i + sum_{j<=i} d(j,i) (q_i.k_j) v_j )
+ *   S_new = d(-1,Cc-1) S_prev + sum_j d(j,Cc-1) k_j v_j^T
+ * With a constant gate it is the fixed-decay chunked form.                  */
+static void gated_chunked_unit(void *ctx, long unit) {
+    const gated_t *a = (const gated_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv, C = a->chunk;
+    double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    double *Sn = (double *)calloc((size_t)(dk * dv), sizeof(double));
+    if (a->h0) memcpy(S, a->h0 + GSIDX(a, b, h), sizeof(double) * (size_t)(dk * dv));
+    for (long c0 = 0; c0 < a->T; c0 += C) {
+        long Cc = a->T - c0 < C ? a->T - c0 : C;
+        for (long i = 0; i < Cc && a->o; ++i) {
+            const double *qi = a->q + GQIDX(a, b, c0 + i, h, 0);
+            double *oi = a->o + GVIDX(a, b, c0 + i, h, 0);
+            double wi = gated_weight(a, b, h, c0 - 1, c0 + i);
+            for (long jv = 0; jv < dv; ++jv) {
+                double acc = 0.0;
+                for (long r = 0; r < dk; ++r) acc += S[r * dv + jv] * qi[r];
+                oi[jv] = wi * acc;
+            }
+            for (long j = 0; j <= i; ++j) {
+                const double *kj = a->k + GQIDX(a, b, c0 + j, h, 0);
+                const double *vj = a->v + GVIDX(a, b, c0 + j, h, 0);
+                double qk = 0.0;
+                for (long r = 0; r < dk; ++r) qk += qi[r] * kj[r];
+                double w = gated_weight(a, b, h, c0 + j, c0 + i) * qk;
+                for (long jv = 0; jv < dv; ++jv) oi[jv] += w * vj[jv];
+            }
+            for (long jv = 0; jv < dv; ++jv) oi[jv] *= a->scale;
+        }
+        double wC = gated_weight(a, b, h, c0 - 1, c0 + Cc - 1);
+        for (long r = 0; r < dk * dv; ++r) Sn[r] = wC * S[r];
+        for (long j = 0; j < Cc; ++j) {
+            const double *kj = a->k + GQIDX(a, b, c0 + j, h, 0);
+            const double *vj = a->v + GVIDX(a, b, c0 + j, h, 0);
+            double w = gated_weight(a, b, h, c0 + j, c0 + Cc - 1);
+            for (long r = 0; r < dk; ++r)
+                for (long jv = 0; jv < dv; ++jv) Sn[r * dv + jv] += w * kj[r] * vj[jv];
+        }
+        double *tmp = S; S = Sn; Sn = tmp;
+    }
+    if (a->hT) memcpy(a->hT + GSIDX(a, b, h), S, sizeof(double) * (size_t)(dk * dv));
+    free(S); free(Sn);
+}
+
+static int gated_run(unit_fn fn, const double *q, const double *k, const double *v, const double *g,
+                     const double *h0, double scale, long B, long T, long H, long dk, long dv, long chunk,
+                     double *o, double *hT, int nthreads) {
+    if (!q || !k || !v || !g || B < 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    gated_t a; memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.h0 = h0; a.scale = scale;
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv; a.chunk = chunk; a.o = o; a.hT = hT;
+    run_units(B * H, nthreads, fn, &a);
+    return 0;
+}
+
+int gla_oracle_fwd_gated(const double *q, const double *k, const double *v, const double *g,
+                         const double *h0, double scale, long B, long T, long H, long dk, long dv,
+                         double *o, double *hT, int nthreads) {
+    return gated_run(gated_recurrent_unit, q, k, v, g, h0, scale, B, T, H, dk, dv, 0, o, hT, nthreads);
+}
+
+int gla_oracle_fwd_gated_quadratic(const double *q, const double *k, const double *v, const double *g,
+                                   const double *h0, double scale, long B, long T, long H, long dk, long dv,
+                                   double *o, double *hT, int nthreads) {
+    if (!o) return 1;
+    return gated_run(gated_quadratic_unit, q, k, v, g, h0, scale, B, T, H, dk, dv, 0, o, hT, nthreads);
+}
+
+int gla_oracle_fwd_gated_chunked(const double *q, const double *k, const double *v, const double *g,
+                                 const double *h0, double scale, long B, long T, long H, long dk, long dv,
+                                 long chunk, double *o, double *hT, int nthreads) {
+    if (chunk <= 0) return 1;
+    return gated_run(gated_chunked_unit, q, k, v, g, h0, scale, B, T, H, dk, dv, chunk, o, hT, nthreads);
+}
+
+/* O10: one serving step with per-token decay, per (n, h):
+ *   S <- exp(g[n,h]) S + k v^T (in place),  o = scale * S^T q.             */
+typedef struct {
+    const double *q, *k, *v, *g;
+    double *S, *o;
+    double scale;
+    long N, H, dk, dv;
+} gdec_t;
+
+static void gated_decode_unit(void *ctx, long unit) {
+    const gdec_t *a = (const gdec_t *)ctx;
+    long dk = a->dk, dv = a->dv;
+    double alpha = exp(a->g[unit]);
+    const double *q = a->q + unit * dk, *k = a->k + unit * dk, *v = a->v + unit * dv;
+    double *S = a->S + unit * dk * dv, *o = a->o + unit * dv;
+    for (long i = 0; i < dk; ++i)
+        for (long j = 0; j < dv; ++j) S[i * dv + j] = alpha * S[i * dv + j] + k[i] * v[j];
+    for (long j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (long i = 0; i < dk; ++i) acc += S[i * dv + j] * q[i];
+        o[j] = a->scale * acc;
+    }
+}
+
+int gla_oracle_decode_gated(const double *q, const double *k, const double *v, const double *g,
+                            double *S, double scale, long N, long H, long dk, long dv, double *o,
+                            int nthreads) {
+    if (!q || !k || !v || !g || !S || !o || N < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
+    gdec_t a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.S = S; a.o = o; a.scale = scale;
+    a.N = N; a.H = H; a.dk = dk; a.dv = dv;
+    run_units(N * H, nthreads, gated_decode_unit, &a);
+    return 0;
+}

@@ -1,0 +1,151 @@
+"""Pins of the oracle's per-token (data-dependent) decay, O9 and O10.
+
+The gated recurrence S_t = exp(g_t) S_{t-1} + k_t v_t^T, o_t = scale S_t^T q_t
+is checked against facts outside its own code, chosen so that a plausible
+slip (the decay applied after adding k v^T, the gate of token t used at
+t+1, a cumulative decay that includes the token's own gate, a missing h0
+decay, a transposed state) fails at least one of them:
+
+  - a hand-worked fixture with a cleared state (tests/golden/gated_hand_worked.json);
+  - a constant gate g_t = log lambda_h reproduces the fixed-decay oracle,
+    itself pinned in test_oracle_pins.py;
+  - the unrolled sums against the recurrence, -inf gates included;
+  - the chunk equations at several chunk lengths against the recurrence;
+  - g = 0: causal linear attention as a masked matrix product;
+  - a -inf gate clears the state: the outputs from there on are those of a
+    fresh call over the rest of the sequence;
+  - split-call invariance;
+  - the final state in closed form from cumulative sums of g;
+  - one decode step equals the forward at T = 1.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import gla_gen as gen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    den = max(np.max(np.abs(b)), 1e-300)
+    return float(np.max(np.abs(a - b)) / den)
+
+
+def case(seed, B=2, T=29, H=3, dk=4, dv=5, h0=True, kind="wide"):
+    rng = np.random.default_rng(4000 + seed)
+    q = rng.standard_normal((B, T, H, dk))
+    k = rng.standard_normal((B, T, H, dk))
+    v = rng.standard_normal((B, T, H, dv))
+    H0 = rng.standard_normal((B, H, dk, dv)) * 0.5 if h0 else None
+    g = gen.log_gates(rng, (B, T, H), kind).astype(np.float64)
+    return q, k, v, g, H0
+
+
+def test_hand_worked_forward():
+    f = json.load(open(os.path.join(GOLDEN, "gated_hand_worked.json")))["forward"]
+    q = np.array(f["q"], float)[None, :, None, :]
+    k = np.array(f["k"], float)[None, :, None, :]
+    v = np.array(f["v"], float)[None, :, None, :]
+    with np.errstate(divide="ignore"):
+        g = np.log(np.array(f["alpha"], float))[None, :, None]
+    h0 = np.array(f["h0"], float)[None, None]
+    for form in ("recurrent", "quadratic", "chunked"):
+        o, hT = oracle.fwd_gated(q, k, v, g, h0, f["scale"], form=form, chunk=2)
+        assert np.array_equal(o[0, :, 0], np.array(f["o"], float)), form
+        assert np.array_equal(hT[0, 0], np.array(f["hT"], float)), form
+
+
+def test_hand_worked_decode():
+    f = json.load(open(os.path.join(GOLDEN, "gated_hand_worked.json")))["decode"]
+    q = np.array(f["q"], float)[None, None]
+    k = np.array(f["k"], float)[None, None]
+    v = np.array(f["v"], float)[None, None]
+    S = np.array(f["S"], float)[None, None]
+    g = np.log(np.array([[f["alpha"]]], float))
+    o, S_new = oracle.decode_gated(q, k, v, g, S, f["scale"])
+    assert np.array_equal(o[0, 0], np.array(f["o"], float))
+    assert np.array_equal(S_new[0, 0], np.array(f["S_new"], float))
+
+
+@pytest.mark.parametrize("form", ["recurrent", "quadratic"])
+def test_constant_gate_is_the_fixed_decay(form):
+    q, k, v, _, h0 = case(1)
+    lam = np.array([0.3, 0.9, 0.999])
+    ll = np.log(lam)
+    g = np.broadcast_to(ll, q.shape[:3]).copy()
+    o_ref, hT_ref = oracle.fwd_recurrent(q, k, v, ll, h0, 0.37)
+    o, hT = oracle.fwd_gated(q, k, v, g, h0, 0.37, form=form)
+    assert rel(o, o_ref) < 1e-12 and rel(hT, hT_ref) < 1e-12
+
+
+@pytest.mark.parametrize("kind", ["wide", "gla"])
+def test_unrolled_sums_match_recurrence(kind):
+    q, k, v, g, h0 = case(2, kind=kind)
+    g[0, 5, 1] = -np.inf
+    g[1, 0, 2] = -np.inf
+    o1, h1 = oracle.fwd_gated(q, k, v, g, h0, 0.5)
+    o2, h2 = oracle.fwd_gated(q, k, v, g, h0, 0.5, form="quadratic")
+    assert rel(o2, o1) < 1e-12 and rel(h2, h1) < 1e-12
+
+
+@pytest.mark.parametrize("C", [1, 3, 16, 64])
+def test_chunk_equations_match_recurrence(C):
+    q, k, v, g, h0 = case(3, T=70, kind="gla")
+    g[0, 40, 0] = -np.inf
+    o1, h1 = oracle.fwd_gated(q, k, v, g, h0, 0.3)
+    o2, h2 = oracle.fwd_gated(q, k, v, g, h0, 0.3, form="chunked", chunk=C)
+    assert rel(o2, o1) < 1e-12 and rel(h2, h1) < 1e-12
+
+
+def test_zero_gate_is_causal_linear_attention():
+    q, k, v, _, h0 = case(4)
+    g = np.zeros(q.shape[:3])
+    o, hT = oracle.fwd_gated(q, k, v, g, h0, 0.7)
+    T = q.shape[1]
+    mask = np.tril(np.ones((T, T)))
+    ref = 0.7 * (np.einsum("btha,bsha,ts,bshc->bthc", q, k, mask, v) + np.einsum("btha,bhac->bthc", q, h0))
+    assert rel(o, ref) < 1e-12
+    assert rel(hT, h0 + np.einsum("btha,bthc->bhac", k, v)) < 1e-12
+
+
+def test_minus_inf_gate_clears_the_state():
+    q, k, v, g, h0 = case(5, T=24)
+    r = 11
+    g[:, r, :] = -np.inf
+    o, hT = oracle.fwd_gated(q, k, v, g, h0, 0.4)
+    g_rest = g[:, r:].copy()
+    g_rest[:, 0, :] = 0.0            # no state enters, so its decay does not matter
+    o2, hT2 = oracle.fwd_gated(q[:, r:], k[:, r:], v[:, r:], g_rest, None, 0.4)
+    assert rel(o[:, r:], o2) < 1e-12 and rel(hT, hT2) < 1e-12
+
+
+def test_split_call_invariance():
+    q, k, v, g, h0 = case(6, T=40, kind="gla")
+    t1 = 17
+    o, hT = oracle.fwd_gated(q, k, v, g, h0, 0.25)
+    oa, ha = oracle.fwd_gated(q[:, :t1], k[:, :t1], v[:, :t1], g[:, :t1], h0, 0.25)
+    ob, hb = oracle.fwd_gated(q[:, t1:], k[:, t1:], v[:, t1:], g[:, t1:], ha, 0.25)
+    assert rel(np.concatenate([oa, ob], axis=1), o) < 1e-12 and rel(hb, hT) < 1e-12
+
+
+def test_final_state_closed_form():
+    q, k, v, g, h0 = case(7, T=33, kind="gla")
+    _, hT = oracle.fwd_gated(q, k, v, g, h0, 1.0)
+    G = np.cumsum(g, axis=1)                       # G[t] = g_0 + ... + g_t
+    GT = G[:, -1]                                  # [B, H]
+    w = np.exp(GT[:, None, :] - G)                 # decay of tokens u+1..T-1
+    ref = np.exp(GT)[:, :, None, None] * h0 + np.einsum("bth,btha,bthc->bhac", w, k, v)
+    assert rel(hT, ref) < 1e-12
+
+
+def test_decode_step_is_forward_at_T1():
+    q, k, v, g, h0 = case(8, T=1)
+    o, hT = oracle.fwd_gated(q, k, v, g, h0, 0.6)
+    B, _, H, dk = q.shape
+    od, S = oracle.decode_gated(q[:, 0], k[:, 0], v[:, 0], g[:, 0], h0, 0.6)
+    assert rel(od, o[:, 0]) < 1e-14 and rel(S, hT) < 1e-14
