@@ -199,6 +199,36 @@ size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int chu
                                     gla_dtype dtype);
 
 /*
+ * gla_chunk_fwd_gated -- the chunked forward with a per-token decay: the
+ * gated form of the same mixer, in which the fixed per-head decay becomes
+ * a decay per token and head (flash-linear-attention's chunk_simple_gla,
+ * whose fused kernel "Challenge 1" names, takes it as its gate input g;
+ * with g constant over tokens it is gla_chunk_fwd):
+ *     S_t = exp(g_t) S_{t-1} + k_t v_t^T,   o_t = scale * S_t^T q_t
+ *   g [B,T,H] fp32: natural-log decay of each token and head, <= 0. -inf
+ *   (or any value <= -80, whose exp is below fp32's normal range) clears
+ *   the state. Positive values are outside the contract: the chunk weights
+ *   rely on decays <= 1.
+ *   Everything else as gla_chunk_fwd (q, k, v, h0, o, hT, chunk, dtype),
+ *   without segmentation: one serial chain per (b, h), no workspace.
+ *   GLA_BF16 runs the tensor-core kernel; GLA_FP32 the validation kernel.
+ */
+gla_status gla_chunk_fwd_gated(const void *q, const void *k, const void *v,
+                               const float *g, const float *h0, float scale,
+                               int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype,
+                               void *o, float *hT, void *stream);
+
+/*
+ * gla_decode_step_gated -- one recurrent step with a per-token decay:
+ *     S <- exp(g[n,h]) S + k v^T (in place),   o = scale * S^T q
+ *   g [N,H] fp32, the log-decay of this step's token per sequence and head
+ *   (<= 0; -inf clears the state). Otherwise as gla_decode_step.
+ */
+gla_status gla_decode_step_gated(const void *q, const void *k, const void *v, const float *g,
+                                 float *S_inout, float scale, int N, int H, int dk, int dv,
+                                 gla_dtype dtype, void *o, void *stream);
+
+/*
  * gla_decode_step -- one recurrent step per (sequence n, head h), the
  * serving path ("Inference optimization on Trainium2": the state lives in a
  * fixed page per sequence):

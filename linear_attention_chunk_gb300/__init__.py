@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     gla_chunk_bwd,
     gla_chunk_bwd_workspace_size,
     gla_chunk_fwd,
+    gla_chunk_fwd_gated,
     gla_chunk_fwd_mixer,
     gla_chunk_fwd_noalloc,
     gla_chunk_fwd_varlen,
@@ -28,6 +29,7 @@ from .binding import (  # noqa: F401
     gla_conv1d_step,
     gla_conv1d_varlen,
     gla_decode_step,
+    gla_decode_step_gated,
     gla_decode_step_mixer,
     gla_last_launch_count,
     gla_mixer_epilogue,

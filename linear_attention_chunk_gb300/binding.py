@@ -11,9 +11,11 @@ Functions:
   gla_chunk_fwd_noalloc(...)                                              -> (o, hT)
   gla_chunk_fwd_varlen(q, k, v, log_lambda, cu_seqlens, state_pool, ...)  -> o  (pool updated)
   gla_chunk_fwd_mixer(q, k, v, g, log_lambda, ...)                        -> (z, hT)
+  gla_chunk_fwd_gated(q, k, v, g, h0=None, scale=None, chunk=128, ...)    -> (o, hT)  per-token decay
   gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, ...)          -> (dq, dk, dv, dh0)
   gla_decode_step(q, k, v, log_lambda, S, scale=None, ...)                -> o  (S updated in place)
   gla_decode_step_mixer(q, k, v, log_lambda, S, g, ...)                   -> z  (S updated in place)
+  gla_decode_step_gated(q, k, v, g, S, scale=None, ...)                   -> o  (S updated in place)
   gla_mixer_epilogue(o, q, k, v, g, aug=None, norm_w=None, eps=1e-6)      -> z
   gla_conv1d_fwd(x, w, b=None, win_in=None, ...)                          -> (y, win_out)
   gla_conv1d_varlen(x, w, b, cu_seqlens, win_pool, slots=None)            -> y  (pool updated)
@@ -37,7 +39,7 @@ GLA_BF16, GLA_FP32 = 0, 1
 
 # The public entry points declared in include/gla.h.
 ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen",
-                 "gla_chunk_fwd_mixer", "gla_chunk_bwd",
+                 "gla_chunk_fwd_mixer", "gla_chunk_fwd_gated", "gla_decode_step_gated", "gla_chunk_bwd",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
                  "gla_conv1d_fwd", "gla_conv1d_varlen", "gla_conv1d_step", "gla_selftest_wait_timeout", "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
@@ -79,6 +81,10 @@ def lib():
             L.gla_chunk_fwd_mixer.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f, _i, _i, _i, _i, _i, _i,
                                               _i, _vp, _vp, _vp, _sz, _vp]
             L.gla_chunk_fwd_mixer.restype = _i
+            L.gla_chunk_fwd_gated.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]
+            L.gla_chunk_fwd_gated.restype = _i
+            L.gla_decode_step_gated.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _vp, _vp]
+            L.gla_decode_step_gated.restype = _i
             L.gla_chunk_fwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
             L.gla_chunk_fwd_workspace_size.restype = _sz
             L.gla_chunk_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
@@ -243,6 +249,26 @@ def gla_chunk_fwd_varlen(q, k, v, log_lambda, cu_seqlens, state_pool, slots=None
     return o
 
 
+def gla_chunk_fwd_gated(q, k, v, g, h0=None, scale=None, chunk=128, *, o=None, hT=None, want_hT=True,
+                        stream=None):
+    """Chunked forward with a per-token decay: g [B,T,H] fp32 natural-log
+    decays (<= 0, -inf clears the state); q, k, v, h0 as gla_chunk_fwd.
+    Returns (o, hT)."""
+    torch = _torch()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if hT is None and want_hT:
+        hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    st = lib().gla_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(h0), float(scale), B, T, H, dk, dv,
+                                   int(chunk), _dtype_code(q), _ptr(o), _ptr(hT), _stream(stream))
+    _raise_on(st, "gla_chunk_fwd_gated")
+    return o, hT
+
+
 def gla_chunk_fwd_mixer(q, k, v, g, log_lambda, h0=None, scale=None, chunk=128, aug=None, norm_w=None, eps=1e-6,
                         *, z=None, hT=None, want_hT=True, workspace=None, stream=None):
     """The chunked forward followed by the mixer epilogue, z in place of o
@@ -308,6 +334,22 @@ def gla_decode_step(q, k, v, log_lambda, S, scale=None, *, o=None, stream=None):
     st = lib().gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(S), float(scale),
                                N, H, dk, dv, dt, _ptr(o), _stream(stream))
     _raise_on(st, "gla_decode_step")
+    return o
+
+
+def gla_decode_step_gated(q, k, v, g, S, scale=None, *, o=None, stream=None):
+    """One recurrent step with a per-token decay g [N,H] fp32 (natural log).
+    S [N,H,dk,dv] fp32 is updated in place. Returns o [N,H,dv]."""
+    torch = _torch()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    st = lib().gla_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S), float(scale), N, H, dk, dv,
+                                     _dtype_code(q), _ptr(o), _stream(stream))
+    _raise_on(st, "gla_decode_step_gated")
     return o
 
 

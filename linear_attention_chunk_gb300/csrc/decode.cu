@@ -7,6 +7,8 @@
 // paragraph:
 //     S <- lambda * S + k v^T     (fp32, in place)
 //     o  = scale * S^T q          (after the update)
+// lambda = exp(log_lambda[h]), or exp(log_decay[n, h]) for the per-token
+// (data-dependent) decay of the gated variant.
 //
 // The step is a pure stream over S: 73,728 B read and 73,728 B written per
 // (n, h) at dk = 96, dv = 192, against 0.5 FLOP per byte -- HBM bound on any
@@ -64,7 +66,7 @@ __global__ void __launch_bounds__(kThreads96) decode_96x192_kernel(DecodeParams 
     }
     const float v0 = Elem<T>::load(v), v1 = Elem<T>::load(v + 1), v2 = Elem<T>::load(v + 2),
                 v3 = Elem<T>::load(v + 3);
-    const float lam = expf(p.log_lambda[h]);
+    const float lam = expf(p.log_decay ? p.log_decay[unit] : p.log_lambda[h]);
     __syncthreads();
     if constexpr (kEpi) {
         if (tid < 32) {   // the self-augmentation gate sigmoid(q . (a * k)) of this (n, h)
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(128) decode_generic_kernel(DecodeParams p) {
     const T *v = static_cast<const T *>(p.v) + unit * dv;
     T *o = static_cast<T *>(p.o) + unit * dv;
     float *S = p.S + unit * (size_t)dk * dv;
-    const float lam = expf(p.log_lambda[h]);
+    const float lam = expf(p.log_decay ? p.log_decay[unit] : p.log_lambda[h]);
     __shared__ float red[4];
     float u[2] = {0.f, 0.f};
     for (int m = 0; m < 2; ++m) {

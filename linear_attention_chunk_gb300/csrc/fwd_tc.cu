@@ -91,6 +91,90 @@ constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, 3 x 
 constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+// Gated mode: each P sub-group's running sums of the chunk's log2-decays and
+// counts of state-clearing gates, [128] float + [128] int per sub-group.
+constexpr uint32_t kOffGate = kSmemUsed, kGateBytes = 2 * 128 * 8;
+constexpr uint32_t kSmemBytesGated = kSmemBytes + kGateBytes;
+static_assert(kSmemBytesGated <= 232448, "shared memory budget (gated)");
+// A log-decay at or below this clears the state: exp(-80) is below fp32's
+// normal range.
+constexpr float kResetLogDecay = -80.f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Running sums over the C tokens of a chunk, lane l holding tokens 4l..4l+3
+// of gate values x[0..3] (natural-log decays; 0 past the chunk's end): the
+// log2-decay of tokens 0..t without the clearing gates, and the number of
+// clearing gates among them. Written to gl[t], rc[t] for t < 128.
+__device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, float *gl, int *rc) {
+    float ls[4];
+    int lc[4];
+    float s = 0.f;
+    int n = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        if (x[r] > kResetLogDecay)
+            s += x[r] * kLog2e;
+        else
+            ++n;
+        ls[r] = s;
+        lc[r] = n;
+    }
+    float si = s;
+    int ni = n;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float ys = __shfl_up_sync(0xffffffffu, si, d);
+        const int yn = __shfl_up_sync(0xffffffffu, ni, d);
+        if (lane >= d) {
+            si += ys;
+            ni += yn;
+        }
+    }
+    const float es = si - s;   // exclusive: the lanes below
+    const int en = ni - n;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        gl[4 * lane + r] = es + ls[r];
+        rc[4 * lane + r] = en + lc[r];
+    }
+}
+
+// The decay over a whole chunk from its gate values (lane l: tokens
+// 4l..4l+3, 0 past the end), reduced across the warp: exp of the summed
+// log-decays, or 0 when one of them clears the state.
+__device__ __forceinline__ float gate_chunk_decay(const float (&x)[4]) {
+    float s = 0.f;
+    int n = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        if (x[r] > kResetLogDecay)
+            s += x[r] * kLog2e;
+        else
+            ++n;
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, d);
+        n += __shfl_xor_sync(0xffffffffu, n, d);
+    }
+    return n == 0 ? exp2f(s) : 0.f;
+}
+
+// Gated mode: one 32-column block of P for TMEM lane row i, columns
+// j0..j0+31, from the fp32 scores x (raw bits): P_ij = A_ij exp(G_i - G_j)
+// for j <= i when no clearing gate lies in between, else 0; written as 16
+// bf16 pairs at taddr. gi, ri: row i's running sum and clearing count.
+__device__ __forceinline__ void build_p_block_gated(uint32_t (&x)[32], int i, int j0, float gi, int ri,
+                                                    const float *gl, const int *rc, uint32_t taddr) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        const int j = j0 + e;
+        const float w0 = j <= i && rc[j] == ri ? exp2f(gi - gl[j]) : 0.f;
+        const float w1 = j + 1 <= i && rc[j + 1] == ri ? exp2f(gi - gl[j + 1]) : 0.f;
+        x[e >> 1] = pack_bf16x2(__uint_as_float(x[e]) * w0, __uint_as_float(x[e + 1]) * w1);
+    }
+    tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
+}
 
 constexpr uint32_t kTmemCols = 512, kColR = 0, kColS = 256, kColP = 352, kColQ = 416;
 
@@ -115,6 +199,9 @@ struct FwdTcArgs {
     const int *slots;
     int n_slots;
     __nv_bfloat16 *o;      // the output, for the masked store of a sequence's last partial chunk
+    // Gated mode: per-token log-decays [B, T, H] (natural log) replacing the
+    // per-head decay.
+    const float *g;
 };
 
 // kRev = false: the forward pass. kRev = true: the same chunked recurrence
@@ -123,7 +210,14 @@ struct FwdTcArgs {
 // with lambda^(col-row), the row weights swap (lambda^(Cc-1-j) on the
 // readout, lambda^(i+1) on the state update), chunks run last to first, and
 // the state is the state gradient divided by the scale.
-template <bool kRev, int kC, bool kVar>
+//
+// kGate: the per-token decay of the gated form, S_t = exp(g_t) S_{t-1} +
+// k_t v_t^T. The lambda powers become decays of token runs: lambda^(i-j) ->
+// exp(G_i - G_j), lambda^(i+1) -> exp(G_i), lambda^(Cc-1-j) -> exp(G_last -
+// G_j), lambda^Cc -> exp(G_last), G the running sum of the chunk's g. A gate
+// at or below kResetLogDecay clears the state: G skips it and a running
+// count of such gates beside G gives any run that holds one the weight 0.
+template <bool kRev, int kC, bool kVar, bool kGate = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -138,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seg = (blockIdx.x >> 1) / a.BH;
     const int bh = (blockIdx.x >> 1) % a.BH;
     constexpr int C = kC;   // chunk length, 64 or 128: token loops are unrolled
+    static_assert(!(kGate && (kRev || kVar)), "the gated mode is the batched forward only");
     const int h = bh % a.H;
     // b: batch index of the states; bt, tok0: token coordinates of the sequence
     int b = bh / a.H, bt = b, tok0 = 0, T = a.T, nck_seq = a.nck;
@@ -160,6 +255,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool last_seg = seg == a.nseg - 1;
     const float *h0 = a.h0 ? a.h0 + (size_t)seg * a.h0_seg_stride : nullptr;
     constexpr int ksteps_tok = C / 16;
+    // Gated mode: this lane's four gate values (tokens 4 lane .. 4 lane + 3)
+    // of chunk c of this CTA, 0 past the sequence's end or the last chunk.
+    auto load_gates = [&](int c, float (&x)[4]) {
+        const int t0 = (cbeg + c) * C, cc = c < nck ? min(C, T - t0) : 0;
+        const int lane4 = 4 * (int)(threadIdx.x & 31);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            x[r] = lane4 + r < cc ? a.g[((size_t)bt * a.T + tok0 + t0 + lane4 + r) * a.H + h] : 0.f;
+    };
 
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
     uint32_t *pp = reinterpret_cast<uint32_t *>(sm + kOffPair);
@@ -181,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_o);
     }
-    {
+    if constexpr (!kGate) {   // the gated mode has no per-head decay (log_lambda is NULL)
         const float l2 = log2_of_decay(a.log_lambda[h]);
         for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
         fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
@@ -366,15 +470,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_st_wait();
         }
+        // Gated mode: the sub-group's running sums; its first warp scans each
+        // chunk's gates, loaded one chunk ahead into registers.
+        float *Gl = reinterpret_cast<float *>(sm + kOffGate + sub * 1024);
+        int *Rc = reinterpret_cast<int *>(sm + kOffGate + sub * 1024 + 512);
+        float gpre[4];
+        if constexpr (kGate) {
+            if (gt < 32) load_gates(0, gpre);
+        }
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
             const int Cc = min(C, T - (kRev ? nck - 1 - c : cbeg + c) * C);
+            if constexpr (kGate) {
+                // Every thread of the sub-group is past chunk c-1's reads (the
+                // barrier before its P-ready signal); the named barrier in the
+                // wait below publishes these sums to the sub-group.
+                if (gt < 32) {
+                    gate_scan_store(gpre, (int)gt, Gl, Rc);
+                    load_gates(c + 1, gpre);
+                }
+            }
             if (!group_wait(bar(BAR_QK0 + s), (c >> 1) & 1, ctl, mydec, gt, named, kw)) break;
             tc_fence_after();
             if (sub == 0) {
                 // K~ = diag(w) K with w = lambda^(Cc-1-j) (zero past the end of the
                 // sequence), or lambda^(i+1) in reverse; signalled at once.
-                const float wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
+                float wk;
+                if constexpr (kGate)
+                    wk = row < (uint32_t)Cc && Rc[Cc - 1] == Rc[row] ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
+                else
+                    wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
                 scale_rows<3>(sm + (uint32_t)s * kStageBytes + kStageK, row, wk);
                 fence_proxy_async_smem();
                 named_sync(named, kGroupThreads);
@@ -388,7 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (sub == 1) {
                 // Q~ = diag(lambda^(i+1)) Q (diag(lambda^(Cc-1-j)) in reverse) into TMEM as the
                 // A operand of Q~ S_prev: lane = token row, column c = dk pair (2c, 2c+1).
-                const float wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+                float wq;
+                if constexpr (kGate)
+                    wq = Rc[row] == 0 ? exp2f(Gl[row]) : 0.f;
+                else
+                    wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
                 const uint32_t wq2 = pack_bf16x2(wq, wq);
                 const unsigned char *qt = sm + (uint32_t)s * kStageBytes + kStageQ;
 #pragma unroll
@@ -416,10 +545,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (has0) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b0, r0);
                 if (has1) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b1, r1);
                 tmem_ld_wait();
-                pack_scores(r0);
-                pack_scores(r1);
-                if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, tl + kColP + 16u * b0, pp, pr);
-                if (has1) build_p_block<kRev>(r1, (int)row - 32 * b1, tl + kColP + 16u * b1, pp, pr);
+                if constexpr (kGate) {
+                    const float gi = Gl[row];
+                    const int ri = Rc[row];
+                    if (has0) build_p_block_gated(r0, (int)row, 32 * b0, gi, ri, Gl, Rc, tl + kColP + 16u * b0);
+                    if (has1) build_p_block_gated(r1, (int)row, 32 * b1, gi, ri, Gl, Rc, tl + kColP + 16u * b1);
+                } else {
+                    pack_scores(r0);
+                    pack_scores(r1);
+                    if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, tl + kColP + 16u * b0, pp, pr);
+                    if (has1) build_p_block<kRev>(r1, (int)row - 32 * b1, tl + kColP + 16u * b1, pp, pr);
+                }
             }
             tmem_st_wait();
             fence_proxy_async_smem();
@@ -437,8 +573,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kw = 0;
         // Initial state: S_prev copy 0 = bf16(h0 slice), TMEM S = lambda^C0 * h0,
         // with C0 the length of the first chunk processed.
+        float eg[4];   // gated mode: the gates of the next chunk whose decay the E group needs
+        if constexpr (kGate) load_gates(0, eg);
         {
-            const float w0 = pw[kRev ? T - (nck - 1) * C : min(C, T - cbeg * C)];
+            float w0;
+            if constexpr (kGate) {
+                w0 = gate_chunk_decay(eg);
+                load_gates(1, eg);
+            } else {
+                w0 = pw[kRev ? T - (nck - 1) * C : min(C, T - cbeg * C)];
+            }
             if (quad < 3) {
                 const float *src =
                     h0 ? h0 + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half : nullptr;
@@ -472,9 +616,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!group_wait(bar(BAR_SFULL), c & 1, ctl, mydec, gt, kBarE, kw)) break;
             tc_fence_after();
             const bool last = (c == nck - 1);
+            float wgate = 1.f;   // gated mode: the decay of chunk c+1
+            if constexpr (kGate) {
+                if (!last) {
+                    wgate = gate_chunk_decay(eg);
+                    load_gates(c + 2, eg);
+                }
+            }
             if (quad < 3) {
                 // rescale by lambda^(length of the next chunk processed)
-                const float wn = last ? 1.f : (kRev ? pw[C] : pw[min(C, T - t0 - C)]);
+                const float wn = last ? 1.f : (kGate ? wgate : (kRev ? pw[C] : pw[min(C, T - t0 - C)]));
                 unsigned char *sb_next = sm + kOffSb + (uint32_t)(s ^ 1) * kSbBytes;
                 float *dst = (last && last_seg && a.hT)
                                  ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
@@ -576,14 +727,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // One launch of the chunk kernel: `qm`, `km` are [B,T,H,96] maps, `vm` and
 // `om` [B,T,H,192] maps (box height = chunk).
-template <bool kRev>
+template <bool kRev, bool kGate = false>
 cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
                                 const CUtensorMap &om, const FwdTcArgs &a, int B, cudaStream_t s, int *launches) {
-    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<kRev, 128, false> : gla_fwd_tc_kernel<kRev, 64, false>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<kRev, 128, false, kGate> : gla_fwd_tc_kernel<kRev, 64, false, kGate>;
+    const uint32_t smem = kGate ? kSmemBytesGated : kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(B * a.H * 2 * a.nseg);
-    kernel<<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, om, a);
+    kernel<<<grid, kThreads, smem, s>>>(qm, km, vm, om, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }
@@ -604,7 +756,10 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     if ((e = make_token_map(&mo, p.o, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     const int nck = (p.T + p.chunk - 1) / p.chunk;
     FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, nck, 1, nck, p.B * p.H, 0, p.status,
-                nullptr, nullptr, 0, nullptr};
+                nullptr, nullptr, 0, nullptr, p.g};
+    // The gated form runs one chain per (b, h): its segment states would need
+    // the gates too.
+    if (p.g) return launch_chunk_kernel<false, true>(mq, mk, mv, mo, a, p.B, s, launches);
     // Few (b, h) pairs and a long sequence: split each sequence into segments
     // that run in parallel, when the caller gave the workspace for it.
     const SegPlan plan = plan_segments(p.B, p.T, p.H, p.chunk);

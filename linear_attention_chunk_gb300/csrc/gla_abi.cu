@@ -104,7 +104,8 @@ gla_status check_conv_shape(int B, int T, int D, gla_dtype dtype) {
 // The decode step with or without the mixer epilogue (g == NULL: plain o).
 gla_status decode_common(const void *q, const void *k, const void *v, const float *log_lambda, float *S_inout,
                          float scale, const void *g, const float *aug, const float *norm_w, float eps, int N,
-                         int H, int dk, int dv, gla_dtype dtype, void *o, void *stream, const char *name) {
+                         int H, int dk, int dv, gla_dtype dtype, void *o, void *stream, const char *name,
+                         const float *log_decay = nullptr) {
     t_err[0] = 0;
     t_launches = 0;
     if (dtype != GLA_BF16 && dtype != GLA_FP32) return fail(GLA_ERR_INVALID_ARG, "dtype %d invalid", (int)dtype);
@@ -122,13 +123,17 @@ gla_status decode_common(const void *q, const void *k, const void *v, const floa
     REQUIRE_PTR(q, "q");
     REQUIRE_PTR(k, "k");
     REQUIRE_PTR(v, "v");
-    REQUIRE_PTR(log_lambda, "log_lambda");
+    if (log_decay) {
+        REQUIRE_PTR(log_decay, "g");
+    } else {
+        REQUIRE_PTR(log_lambda, "log_lambda");
+    }
     REQUIRE_PTR(S_inout, "S_inout");
     REQUIRE_PTR(o, name);
     unsigned int *status = nullptr;
     gla_status st = status_word(&status);
     if (st != GLA_OK) return st;
-    DecodeParams p{q, k, v, log_lambda, S_inout, scale, N, H, dk, dv, o, status, g, aug, norm_w, eps};
+    DecodeParams p{q, k, v, log_lambda, S_inout, scale, N, H, dk, dv, o, status, g, aug, norm_w, eps, log_decay};
     int launches = 0;
     cudaError_t e = launch_decode(p, dtype == GLA_BF16, static_cast<cudaStream_t>(stream), &launches);
     t_launches = launches;
@@ -188,6 +193,49 @@ gla_status gla_chunk_fwd(const void *q, const void *k, const void *v, const floa
         e = launch_fwd_simt(p, false, s, &launches);
     t_launches = launches;
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd launch");
+}
+
+gla_status gla_chunk_fwd_gated(const void *q, const void *k, const void *v, const float *g, const float *h0,
+                               float scale, int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype,
+                               void *o, float *hT, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_chunk_shape(B, T, H, dk, dv, chunk, dtype);
+    if (st != GLA_OK) return st;
+    OPTIONAL_PTR(h0, "h0");
+    OPTIONAL_PTR(hT, "hT");
+    if (B == 0 || H == 0) return GLA_OK;
+    if (T > 0) {
+        REQUIRE_PTR(q, "q");
+        REQUIRE_PTR(k, "k");
+        REQUIRE_PTR(v, "v");
+        REQUIRE_PTR(g, "g");
+        REQUIRE_PTR(o, "o");
+    }
+    unsigned int *status = nullptr;
+    if ((st = status_word(&status)) != GLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    cudaError_t e;
+    if (T == 0) {
+        e = launch_copy_state(h0, hT, (size_t)B * H * dk * dv, s, &launches);
+        t_launches = launches;
+        return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_gated(T=0)");
+    }
+    FwdParams p{q, k, v, nullptr, h0, scale, B, T, H, dk, dv, chunk, o, hT, nullptr, 0, status, g};
+    if (dtype == GLA_BF16)
+        e = launch_fwd_tc(p, s, &launches);
+    else
+        e = launch_fwd_simt(p, false, s, &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_gated launch");
+}
+
+gla_status gla_decode_step_gated(const void *q, const void *k, const void *v, const float *g, float *S_inout,
+                                 float scale, int N, int H, int dk, int dv, gla_dtype dtype, void *o, void *stream) {
+    if (N > 0 && H > 0 && !g) return fail(GLA_ERR_INVALID_ARG, "g is NULL");
+    return decode_common(q, k, v, nullptr, S_inout, scale, nullptr, nullptr, nullptr, 0.f, N, H, dk, dv, dtype, o,
+                         stream, "o", g);
 }
 
 gla_status gla_chunk_fwd_mixer(const void *q, const void *k, const void *v, const void *g, const float *log_lambda,

@@ -19,6 +19,9 @@ struct FwdParams {
     void *workspace;
     size_t workspace_bytes;
     unsigned int *status;  // device status word
+    // Per-token log-decay [B, T, H] (the gated forward), replacing log_lambda;
+    // NULL for the fixed per-head decay.
+    const float *g;
 };
 
 struct BwdParams {
@@ -60,6 +63,8 @@ struct DecodeParams {
     const void *g;
     const float *aug, *norm_w;
     float eps;
+    // Per-(sequence, head) log-decay [N, H] replacing log_lambda, or NULL.
+    const float *log_decay;
 };
 
 // The mixer epilogue over [NT, H, d] rows (epilogue.cu).

@@ -17,6 +17,15 @@
 //                   G   <- lambda^Cc G + scale*sum_i lambda^(i+1) q_i do_i^T,  dh0 = final G.
 // Each CTA owns one (b, h) and a slice of the state's columns (forward, dv
 // slice) or rows (dq and dk chains, dk slice); fp32 throughout.
+//
+// The forward also takes a per-token log-decay g [B,T,H] in place of the
+// per-head one (the gated form: S_t = exp(g_t) S_{t-1} + k_t v_t^T). Every
+// lambda power then becomes the decay of a run of tokens, exp of a sum of
+// g: lambda^(i-j) -> exp(G_i - G_j), lambda^(i+1) -> exp(G_i), with G the
+// running sum of g inside the chunk. A gate at or below kResetLogDecay
+// (-inf included) clears the state; G skips it and a count of such gates
+// runs beside G, so that a run holding one gets weight 0 and runs on either
+// side keep finite sums.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -25,6 +34,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kSlice = 32;   // state columns (or rows) per CTA
+// exp(-80) is below fp32's normal range: such a gate clears the state.
+constexpr float kResetLogDecay = -80.f;
 
 __device__ __forceinline__ size_t tok_off(int b, int t, int h, int T, int H, int d) {
     return (((size_t)b * T + t) * H + h) * (size_t)d;
@@ -54,26 +65,51 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdParams p) {
     float *P = S + dk * kSlice;          // [C][C]
     float *Vs = P + C * C;               // [C][kSlice]
     float *pw = Vs + C * kSlice;         // [C+1]
+    float *Gl = pw + C + 1;              // [C] gated: log2 of the decay of tokens 0..i of the chunk
+    int *Rc = reinterpret_cast<int *>(Gl + C);   // [C] gated: clearing gates among tokens 0..i
+    const bool gated = p.g != nullptr;
     const T *q = static_cast<const T *>(p.q);
     const T *k = static_cast<const T *>(p.k);
     const T *v = static_cast<const T *>(p.v);
     T *o = static_cast<T *>(p.o);
-    const float l2 = log2_of_decay(p.log_lambda[h]);
-    fill_powers(pw, C, l2);
+    if (!gated) fill_powers(pw, C, log2_of_decay(p.log_lambda[h]));
     const size_t sbase = ((size_t)b * H + h) * dk * dv;
     for (int idx = threadIdx.x; idx < dk * nc; idx += blockDim.x) {
         int a = idx / nc, c = idx % nc;
         S[a * kSlice + c] = p.h0 ? p.h0[sbase + (size_t)a * dv + c0 + c] : 0.f;
     }
     __syncthreads();
+    // Decay of the chunk's tokens j+1..i (-1 <= j <= i), lambda^(i-j) for the
+    // fixed per-head decay.
+    auto decay = [&](int j, int i) -> float {
+        if (!gated) return pw[i - j];
+        if (j < 0) return Rc[i] == 0 ? exp2f(Gl[i]) : 0.f;
+        return Rc[i] == Rc[j] ? exp2f(Gl[i] - Gl[j]) : 0.f;
+    };
     for (int t0 = 0; t0 < Tn; t0 += C) {
         const int Cc = min(C, Tn - t0);
+        if (gated) {
+            if (threadIdx.x == 0) {
+                float acc = 0.f;
+                int r = 0;
+                for (int i = 0; i < Cc; ++i) {
+                    const float gi = p.g[((size_t)b * Tn + t0 + i) * H + h];
+                    if (gi > kResetLogDecay)
+                        acc += (float)((double)gi * 1.4426950408889634073599246810019);
+                    else
+                        ++r;
+                    Gl[i] = acc;
+                    Rc[i] = r;
+                }
+            }
+            __syncthreads();
+        }
         for (int idx = threadIdx.x; idx < Cc * Cc; idx += blockDim.x) {
             int i = idx / Cc, j = idx % Cc;
             float val = 0.f;
             if (j <= i)
                 val = dot_rows(q + tok_off(b, t0 + i, h, Tn, H, dk), k + tok_off(b, t0 + j, h, Tn, H, dk), dk) *
-                      pw[i - j];
+                      decay(j, i);
             P[i * C + j] = val;
         }
         for (int idx = threadIdx.x; idx < Cc * nc; idx += blockDim.x) {
@@ -88,14 +124,14 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(FwdParams p) {
             for (int a = 0; a < dk; ++a) inter = fmaf(Elem<T>::load(qi + a), S[a * kSlice + c], inter);
             float intra = 0.f;
             for (int j = 0; j <= i; ++j) intra = fmaf(P[i * C + j], Vs[j * kSlice + c], intra);
-            Elem<T>::store(o + tok_off(b, t0 + i, h, Tn, H, dv) + c0 + c, p.scale * fmaf(pw[i + 1], inter, intra));
+            Elem<T>::store(o + tok_off(b, t0 + i, h, Tn, H, dv) + c0 + c, p.scale * fmaf(decay(-1, i), inter, intra));
         }
         __syncthreads();
         for (int idx = threadIdx.x; idx < dk * nc; idx += blockDim.x) {
             int a = idx / nc, c = idx % nc;
-            float acc = pw[Cc] * S[a * kSlice + c];
+            float acc = decay(-1, Cc - 1) * S[a * kSlice + c];
             for (int j = 0; j < Cc; ++j)
-                acc = fmaf(pw[Cc - 1 - j] * Elem<T>::load(k + tok_off(b, t0 + j, h, Tn, H, dk) + a),
+                acc = fmaf(decay(j, Cc - 1) * Elem<T>::load(k + tok_off(b, t0 + j, h, Tn, H, dk) + a),
                            Vs[j * kSlice + c], acc);
             S[a * kSlice + c] = acc;
         }
@@ -297,7 +333,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 template <typename T>
 cudaError_t fwd_simt_impl(const FwdParams &p, cudaStream_t s, int *launches) {
     const size_t smem = sizeof(float) * ((size_t)p.dk * kSlice + (size_t)p.chunk * p.chunk +
-                                         (size_t)p.chunk * kSlice + p.chunk + 1);
+                                         (size_t)p.chunk * kSlice + p.chunk + 1 + 2 * (size_t)p.chunk);
     cudaError_t e = set_smem(fwd_simt_kernel<T>, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(p.B * p.H), (unsigned)((p.dv + kSlice - 1) / kSlice));

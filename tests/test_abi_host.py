@@ -245,3 +245,31 @@ def test_selftest_rejects_bad_arguments(L):
     assert L.gla_selftest_wait_timeout(2000000, FAKE, None) == binding.GLA_ERR_INVALID_ARG
     assert L.gla_selftest_wait_timeout(1000, None, None) == binding.GLA_ERR_INVALID_ARG
     assert L.gla_selftest_wait_timeout(1000, ODD, None) == binding.GLA_ERR_INVALID_ARG
+
+
+def test_gated_entry_points_reject_bad_arguments(L):
+    def fwd(**kw):
+        a = dict(q=FAKE, k=FAKE + 0x100, v=FAKE + 0x200, g=FAKE + 0x300, h0=None, B=2, T=256, H=16, dk=96, dv=192,
+                 C=128, dt=0, o=FAKE + 0x400, hT=None)
+        a.update(kw)
+        return L.gla_chunk_fwd_gated(a["q"], a["k"], a["v"], a["g"], a["h0"], 0.1, a["B"], a["T"], a["H"], a["dk"],
+                                     a["dv"], a["C"], a["dt"], a["o"], a["hT"], None)
+    assert fwd(g=None) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(g=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(h0=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(dk=64) == binding.GLA_ERR_UNSUPPORTED
+    assert fwd(C=96) == binding.GLA_ERR_UNSUPPORTED
+    assert fwd(dt=1, dv=300) == binding.GLA_ERR_UNSUPPORTED
+    assert fwd(T=-1) == binding.GLA_ERR_INVALID_ARG
+    assert fwd(B=0) == binding.GLA_OK
+
+    def dec(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, S=FAKE, N=4, H=16, dk=96, dv=192, dt=0, o=FAKE)
+        a.update(kw)
+        return L.gla_decode_step_gated(a["q"], a["k"], a["v"], a["g"], a["S"], 0.1, a["N"], a["H"], a["dk"],
+                                       a["dv"], a["dt"], a["o"], None)
+    assert dec(g=None) == binding.GLA_ERR_INVALID_ARG
+    assert dec(g=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert dec(S=None) == binding.GLA_ERR_INVALID_ARG
+    assert dec(dk=64) == binding.GLA_ERR_UNSUPPORTED
+    assert dec(N=0) == binding.GLA_OK

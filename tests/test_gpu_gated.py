@@ -1,0 +1,145 @@
+"""GPU parity of the per-token (data-dependent) decay against the oracle's
+gated recurrence (O9, O10), through the C ABI: gla_chunk_fwd_gated on the
+tensor-core path (bf16) and the validation path (fp32), and
+gla_decode_step_gated.
+
+Cases span several chunks and a ragged tail, both chunk lengths, gates that
+clear the state (-inf) inside a chunk and on a chunk's first token, strong
+decays whose products underflow inside a chunk, a constant gate (which must
+agree with the fixed-decay forward), and the layer-forward shape sampled.
+Bars (max |gpu - ref| / max |ref| per output tensor): 2e-2 for bf16 inputs,
+1e-4 for the fp32 validation mode."""
+import numpy as np
+import pytest
+
+import gla_gen as gen
+import oracle
+from gpu_util import TOL, case_to_dev, f32_dev, relerr, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gla():
+    import linear_attention_chunk_gb300 as m
+    from linear_attention_chunk_gb300.build import build
+    build()
+    return m
+
+
+def run_gated(gla, c, g, chunk=None):
+    d = case_to_dev(c)
+    o, hT = gla.gla_chunk_fwd_gated(d["q"], d["k"], d["v"], f32_dev(g), d["h0"], c.scale, chunk or c.chunk)
+    gla.gla_check()
+    return to_host(o), to_host(hT)
+
+
+def check_gated(gla, c, g, chunk=None):
+    o, hT = run_gated(gla, c, g, chunk)
+    ro, rhT = oracle.fwd_gated(c.q, c.k, c.v, g, c.h0, c.scale)
+    eo, eh = relerr(o, ro), relerr(hT, rhT)
+    assert eo <= TOL[c.dtype], f"o rel err {eo:.3g}"
+    assert eh <= TOL[c.dtype], f"hT rel err {eh:.3g}"
+    return eo, eh
+
+
+# --------------------------------------------------------------- fp32 mode
+@pytest.mark.parametrize("dk,dv,T,C", [(5, 7, 150, 64), (96, 192, 300, 128), (3, 2, 1, 64)])
+def test_gated_fwd_fp32(gla, dk, dv, T, C):
+    c = gen.make_case(2, T, 3, dk, dv, seed=300 + T, dtype="fp32", h0_std=0.3, chunk=C, gate="gla")
+    g = c.extra["g"].copy()
+    if T > 100:
+        g[0, 70, 1] = -np.inf
+    check_gated(gla, c, g)
+
+
+def test_gated_fwd_fp32_wide_gates(gla):
+    c = gen.make_case(1, 260, 2, 8, 16, seed=311, dtype="fp32", h0_std=0.3, chunk=128, gate="wide")
+    check_gated(gla, c, c.extra["g"])
+
+
+# --------------------------------------------------------------- bf16 path
+@pytest.mark.parametrize("T,C", [(300, 128), (300, 64), (128, 128), (1, 128), (129, 64), (700, 128)])
+def test_gated_fwd_bf16_ragged(gla, T, C):
+    c = gen.make_case(2, T, 3, 96, 192, seed=320 + T + C, dtype="bf16", normalise_k=True, h0_std=0.1, chunk=C,
+                      gate="gla")
+    check_gated(gla, c, c.extra["g"])
+
+
+def test_gated_fwd_bf16_clearing_gates(gla):
+    c = gen.make_case(2, 520, 4, 96, 192, seed=331, dtype="bf16", normalise_k=True, h0_std=0.1, chunk=128,
+                      gate="gla")
+    g = c.extra["g"].copy()
+    g[0, 45, 0] = -np.inf          # inside a chunk
+    g[0, 128, 1] = -np.inf         # a chunk's first token: S_prev is cleared
+    g[1, 127, 2] = -np.inf         # a chunk's last token
+    g[1, 300:303, 3] = -np.inf     # a run of them
+    g[1, 519, 0] = -np.inf         # the last token: hT = k v^T
+    check_gated(gla, c, g)
+
+
+def test_gated_fwd_bf16_strong_decays(gla):
+    c = gen.make_case(1, 400, 4, 96, 192, seed=332, dtype="bf16", h0_std=0.1, chunk=64, gate="wide")
+    check_gated(gla, c, c.extra["g"])
+
+
+def test_constant_gate_matches_fixed_decay_forward(gla):
+    c = gen.make_case(2, 333, 16, 96, 192, seed=333, dtype="bf16", normalise_k=True, h0_std=0.1, chunk=128)
+    g = np.broadcast_to(c.log_lambda.astype(np.float32), (c.B, c.T, c.H)).copy()
+    og, hg = run_gated(gla, c, g)
+    d = case_to_dev(c)
+    o, hT = gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["ll"], d["h0"], c.scale, 128)
+    gla.gla_check()
+    ro, rhT = oracle.fwd_recurrent(c.q, c.k, c.v, c.log_lambda, c.h0, c.scale)
+    assert relerr(og, ro) <= TOL["bf16"] and relerr(hg, rhT) <= TOL["bf16"]
+    # two kernels (decay tables against per-element exponentials) of one result
+    assert relerr(og, to_host(o)) <= TOL["bf16"] and relerr(hg, to_host(hT)) <= TOL["bf16"]
+
+
+def test_gated_layer_forward_sampled(gla):
+    """The layer-forward shape (8 x 2048 x 16) with GLA-style gates; the
+    oracle checks two batch rows, all heads."""
+    c = gen.make_case(8, 2048, 16, 96, 192, seed=334, dtype="bf16", normalise_k=True, chunk=128, gate="gla")
+    g = c.extra["g"]
+    o, hT = run_gated(gla, c, g)
+    for b in (0, 7):
+        ro, rhT = oracle.fwd_gated(c.q[b:b + 1], c.k[b:b + 1], c.v[b:b + 1], g[b:b + 1], None, c.scale)
+        assert relerr(o[b:b + 1], ro) <= TOL["bf16"], b
+        assert relerr(hT[b:b + 1], rhT) <= TOL["bf16"], b
+
+
+def test_gated_prefill_then_decode(gla):
+    """hT of a gated prefill feeds gated decode steps; the result equals one
+    longer gated prefill."""
+    import torch
+    c = gen.make_case(3, 261, 16, 96, 192, seed=335, dtype="bf16", normalise_k=True, chunk=128, gate="gla")
+    g = c.extra["g"]
+    d = case_to_dev(c)
+    t1 = 257
+    _, S = gla.gla_chunk_fwd_gated(d["q"][:, :t1].contiguous(), d["k"][:, :t1].contiguous(),
+                                   d["v"][:, :t1].contiguous(), f32_dev(g[:, :t1]), None, c.scale, 128)
+    outs = []
+    for t in range(t1, c.T):
+        outs.append(gla.gla_decode_step_gated(d["q"][:, t].contiguous(), d["k"][:, t].contiguous(),
+                                              d["v"][:, t].contiguous(), f32_dev(g[:, t]), S, c.scale))
+    gla.gla_check()
+    ro, rhT = oracle.fwd_gated(c.q, c.k, c.v, g, None, c.scale)
+    got = np.stack([to_host(x) for x in outs], axis=1)
+    assert relerr(got, ro[:, t1:]) <= TOL["bf16"]
+    assert relerr(to_host(S), rhT) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------------ decode
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_gated_decode(gla, dtype):
+    dc = gen.make_decode_case(37, 16, 96, 192, seed=340, dtype=dtype)
+    rng = np.random.default_rng(341)
+    g = gen.log_gates(rng, (37, 16), "wide")
+    g[3, 5] = -np.inf
+    S = f32_dev(dc.S)
+    o = gla.gla_decode_step_gated(to_dev(dc.q, dtype), to_dev(dc.k, dtype), to_dev(dc.v, dtype), f32_dev(g), S,
+                                  dc.scale)
+    gla.gla_check()
+    ro, rS = oracle.decode_gated(dc.q, dc.k, dc.v, g, dc.S, dc.scale)
+    assert relerr(to_host(o), ro) <= TOL[dtype]
+    assert relerr(to_host(S), rS) <= 1e-5   # the state itself stays fp32
