@@ -2,7 +2,7 @@
 """Benchmark of libgla, the Simple GLA mixer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gla|reference]
-                    [--mode all|fwd|fwd_bwd|decode|long|varlen|mixer|conv] [--batch B] [--no-e2e]
+                    [--mode all|fwd|fwd_bwd|decode|long|varlen|mixer|conv|gated] [--batch B] [--no-e2e]
                     [--no-cpu-baseline]
 
 Prints ONE JSON line (rank 0). The headline `value` is the chunked forward
@@ -12,9 +12,10 @@ measurement for the training forward+backward workload (B=16, tokens/s),
 the serving decode workload (1,280 sequences x 16 heads x 24 distinct layer
 states per step, seq-steps/s), the long-context prefill (T=65,536, chunk 128
 and 64) and the variable-length serving prefill into the decode state pool
-(64 prompts of 64..4,096 tokens), and the mixer epilogue (fused into the
-decode step, and standalone over the layer-forward output), each with its
-own roofline.
+(64 prompts of 64..4,096 tokens), the mixer epilogue (fused into the
+decode step, and standalone over the layer-forward output), the causal
+Conv1d, and the forward with a per-token (data-dependent) decay on the
+layer-forward shape, each with its own roofline.
 
 Timing: W untimed warm-up steps, then exactly K steps between two
 barrier + synchronize pairs, on the device with CUDA events recorded on the
@@ -320,6 +321,58 @@ def bench_fwd(args, dist, device, stream, peaks, sampler):
     if not args.no_e2e:
         res["e2e"] = e2e_fwd(args, dist, device, stream, c, ll)
     del q, k, v, o, hT
+    return res
+
+
+def gated_case(B=8, T=2048):
+    """The layer-forward shape with per-token log-decays of gated linear
+    attention (log sigmoid(x)/16, x ~ N(0, 1)) in place of the per-head one."""
+    c = gen.make_case(B, T, H, DK, DV, seed=1, normalise_k=True, chunk=CHUNK, gate="gla",
+                      name=f"gated_fwd_bf16_B{B}_H16_T{T}")
+    return c
+
+
+def bench_gated(args, dist, device, stream, peaks, sampler):
+    """The chunked forward with a per-token (data-dependent) decay,
+    gla_chunk_fwd_gated, on the layer-forward shape."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    B = args.batch or 8
+    T = 2048
+    c = gated_case(B, T)
+    q, k, v = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v))
+    g = torch.from_numpy(c.extra["g"]).to(device)
+    o = torch.empty((B, T, H, DV), dtype=torch.bfloat16, device=device)
+    hT = torch.empty((B, H, DK, DV), dtype=torch.float32, device=device)
+
+    def step():
+        gla.gla_chunk_fwd_gated(q, k, v, g, None, c.scale, CHUNK, o=o, hT=hT, stream=stream)
+        return gla.gla_last_launch_count()
+
+    total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    bytes_, fl_full, fl_causal = fwd_work(B, T, False, True)
+    bytes_ += B * T * H * 4                     # g, fp32 per token and head
+    avg_ms = statistics.mean(per)
+    ach_gbs = bytes_ / (avg_ms * 1e-3) / 1e9
+    ach_tf = fl_full / (avg_ms * 1e-3) / 1e12
+    res = {
+        "value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+        "ms_per_step": total / args.steps,
+        "config": {"workload": c.name, "B": B, "T": T, "H": H, "dk": DK, "dv": DV, "chunk": CHUNK,
+                   "gates": "log sigmoid(x)/16, x ~ N(0,1), per token and head", "h0": "none", "hT": "written",
+                   "l2": f"inputs larger than L2 ({bytes_ / 1e6:.0f} MB per step), no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_, "avg_launch_ms": avg_ms,
+                     "peak_source": peaks["source"]},
+        "tensor": {"achieved": ach_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                   "frac": ach_tf / peaks["bf16_tflops"], "flops_per_launch": fl_full,
+                   "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    del q, k, v, g, o, hT
     return res
 
 
@@ -855,6 +908,21 @@ def oracle_fwd_sample(units, seed=1):
     return dt, head_tokens / H, nthreads, f"{B}x{hs} (b,h) chains of T=2048 (of 8x16)"
 
 
+def oracle_gated_sample(units):
+    """The oracle's gated recurrence over `units` (b, h) chains of the gated
+    layer-forward workload (T=2048)."""
+    import oracle
+    B = max(1, math.ceil(units / H))
+    c = gated_case(B, 2048)
+    hs = min(units, H)
+    sl = lambda x: x[:, :, :hs]
+    nthreads = oracle.threads(0)
+    t0 = time.perf_counter()
+    oracle.fwd_gated(sl(c.q), sl(c.k), sl(c.v), c.extra["g"][:, :, :hs], None, c.scale, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, B * hs * 2048 / H, nthreads, f"{B}x{hs} (b,h) chains of T=2048 with per-token gates (of 8x16)"
+
+
 def oracle_bwd_sample(units, seed=2):
     import oracle
     B = max(1, math.ceil(units / H))
@@ -903,6 +971,9 @@ def cpu_baseline():
     dt, toks, nt, sample = oracle_conv_sample(8)
     modes["conv"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
                      "sample": sample, "seconds": dt}
+    dt, toks, nt, sample = oracle_gated_sample(32)
+    modes["gated"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                      "sample": sample, "seconds": dt}
     return base, modes
 
 
@@ -967,7 +1038,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gla", "reference"), default="gla")
-    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long", "varlen", "mixer", "conv"),
+    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long", "varlen", "mixer", "conv",
+                                       "gated"),
                     default="all")
     ap.add_argument("--batch", type=int, default=0, help="override B of the fwd / fwd_bwd workloads (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the decode layer count (profiling)")
@@ -1017,6 +1089,8 @@ def main(argv=None):
             results["mixer"] = bench_mixer(args, dist, device, stream, peaks, sampler)
         if args.mode in ("all", "conv"):
             results["conv"] = bench_conv(args, dist, device, stream, peaks, sampler)
+        if args.mode in ("all", "gated"):
+            results["gated"] = bench_gated(args, dist, device, stream, peaks, sampler)
     finally:
         sampler.stop()
 

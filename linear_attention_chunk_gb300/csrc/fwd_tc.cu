@@ -92,8 +92,10 @@ constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 // Gated mode: each P sub-group's running sums of the chunk's log2-decays and
-// counts of state-clearing gates, [128] float + [128] int per sub-group.
-constexpr uint32_t kOffGate = kSmemUsed, kGateBytes = 2 * 128 * 8;
+// positions of the last state-clearing gate, [128] float + [128] int per
+// sub-group.
+constexpr uint32_t kGateSub = 128 * 8;
+constexpr uint32_t kOffGate = kSmemUsed, kGateBytes = 2 * kGateSub;
 constexpr uint32_t kSmemBytesGated = kSmemBytes + kGateBytes;
 static_assert(kSmemBytesGated <= 232448, "shared memory budget (gated)");
 // A log-decay at or below this clears the state: exp(-80) is below fp32's
@@ -101,41 +103,51 @@ static_assert(kSmemBytesGated <= 232448, "shared memory budget (gated)");
 constexpr float kResetLogDecay = -80.f;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// 2^x for x <= 0 by the hardware approximation (relative error about 2^-22;
+// results below fp32's normal range flush to 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Running sums over the C tokens of a chunk, lane l holding tokens 4l..4l+3
 // of gate values x[0..3] (natural-log decays; 0 past the chunk's end): the
-// log2-decay of tokens 0..t without the clearing gates, and the number of
-// clearing gates among them. Written to gl[t], rc[t] for t < 128.
-__device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, float *gl, int *rc) {
+// log2-decay of tokens 0..t without the clearing gates, gl[t], and the
+// position of the last clearing gate among them, zc[t] (-1 if none), for
+// t < 128. The decay of tokens j+1..i is then 2^(gl[i] - gl[j]) when
+// zc[i] <= j, and 0 otherwise.
+__device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, float *gl, int *zc) {
     float ls[4];
-    int lc[4];
+    int lz[4];
     float s = 0.f;
-    int n = 0;
+    int z = -1;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         if (x[r] > kResetLogDecay)
             s += x[r] * kLog2e;
         else
-            ++n;
+            z = 4 * lane + r;
         ls[r] = s;
-        lc[r] = n;
+        lz[r] = z;
     }
     float si = s;
-    int ni = n;
+    int zi = z;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const float ys = __shfl_up_sync(0xffffffffu, si, d);
-        const int yn = __shfl_up_sync(0xffffffffu, ni, d);
+        const int yz = __shfl_up_sync(0xffffffffu, zi, d);
         if (lane >= d) {
             si += ys;
-            ni += yn;
+            zi = max(zi, yz);
         }
     }
     const float es = si - s;   // exclusive: the lanes below
-    const int en = ni - n;
+    const int ez = __shfl_up_sync(0xffffffffu, zi, 1);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         gl[4 * lane + r] = es + ls[r];
-        rc[4 * lane + r] = en + lc[r];
+        zc[4 * lane + r] = lz[r] >= 0 ? lz[r] : (lane > 0 ? ez : -1);
     }
 }
 
@@ -160,17 +172,21 @@ __device__ __forceinline__ float gate_chunk_decay(const float (&x)[4]) {
     return n == 0 ? exp2f(s) : 0.f;
 }
 
+
 // Gated mode: one 32-column block of P for TMEM lane row i, columns
-// j0..j0+31, from the fp32 scores x (raw bits): P_ij = A_ij exp(G_i - G_j)
-// for j <= i when no clearing gate lies in between, else 0; written as 16
-// bf16 pairs at taddr. gi, ri: row i's running sum and clearing count.
-__device__ __forceinline__ void build_p_block_gated(uint32_t (&x)[32], int i, int j0, float gi, int ri,
-                                                    const float *gl, const int *rc, uint32_t taddr) {
+// j0..j0+31, from the fp32 scores x (raw bits): P_ij = A_ij 2^(gi - gl[j])
+// for zi <= j <= i (no clearing gate among tokens j+1..i), else 0; written
+// as 16 bf16 pairs at taddr. gi = gl[i], zi = zc[i]. One hardware
+// exponential per element: a factored form, 2^(gi - gl[b]) 2^(gl[b] - gl[j])
+// with b the block's last column, measured slower.
+__device__ __forceinline__ void build_p_block_gated(uint32_t (&x)[32], int i, int j0, float gi, int zi,
+                                                    const float *gl, uint32_t taddr) {
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
         const int j = j0 + e;
-        const float w0 = j <= i && rc[j] == ri ? exp2f(gi - gl[j]) : 0.f;
-        const float w1 = j + 1 <= i && rc[j + 1] == ri ? exp2f(gi - gl[j + 1]) : 0.f;
+        const float2 gj = *reinterpret_cast<const float2 *>(gl + j);
+        const float w0 = j <= i && j >= zi ? ex2_approx(gi - gj.x) : 0.f;
+        const float w1 = j + 1 <= i && j + 1 >= zi ? ex2_approx(gi - gj.y) : 0.f;
         x[e >> 1] = pack_bf16x2(__uint_as_float(x[e]) * w0, __uint_as_float(x[e + 1]) * w1);
     }
     tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
@@ -215,8 +231,9 @@ struct FwdTcArgs {
 // k_t v_t^T. The lambda powers become decays of token runs: lambda^(i-j) ->
 // exp(G_i - G_j), lambda^(i+1) -> exp(G_i), lambda^(Cc-1-j) -> exp(G_last -
 // G_j), lambda^Cc -> exp(G_last), G the running sum of the chunk's g. A gate
-// at or below kResetLogDecay clears the state: G skips it and a running
-// count of such gates beside G gives any run that holds one the weight 0.
+// at or below kResetLogDecay clears the state: G skips it, and the position
+// of the last such gate, kept beside G, gives any run that holds one the
+// weight 0.
 template <bool kRev, int kC, bool kVar, bool kGate = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -257,12 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int ksteps_tok = C / 16;
     // Gated mode: this lane's four gate values (tokens 4 lane .. 4 lane + 3)
     // of chunk c of this CTA, 0 past the sequence's end or the last chunk.
+    // Callers load one chunk ahead of use.
     auto load_gates = [&](int c, float (&x)[4]) {
-        const int t0 = (cbeg + c) * C, cc = c < nck ? min(C, T - t0) : 0;
         const int lane4 = 4 * (int)(threadIdx.x & 31);
+        const float *gh = a.g + ((size_t)bt * a.T + tok0) * a.H + h;
+        const int t0 = (cbeg + c) * C, cc = c < nck ? min(C, T - t0) : 0;
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-            x[r] = lane4 + r < cc ? a.g[((size_t)bt * a.T + tok0 + t0 + lane4 + r) * a.H + h] : 0.f;
+        for (int r = 0; r < 4; ++r) x[r] = lane4 + r < cc ? gh[(size_t)(t0 + lane4 + r) * a.H] : 0.f;
     };
 
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
@@ -472,8 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Gated mode: the sub-group's running sums; its first warp scans each
         // chunk's gates, loaded one chunk ahead into registers.
-        float *Gl = reinterpret_cast<float *>(sm + kOffGate + sub * 1024);
-        int *Rc = reinterpret_cast<int *>(sm + kOffGate + sub * 1024 + 512);
+        float *Gl = reinterpret_cast<float *>(sm + kOffGate + sub * kGateSub);
+        int *Zc = reinterpret_cast<int *>(sm + kOffGate + sub * kGateSub + 512);
         float gpre[4];
         if constexpr (kGate) {
             if (gt < 32) load_gates(0, gpre);
@@ -486,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // barrier before its P-ready signal); the named barrier in the
                 // wait below publishes these sums to the sub-group.
                 if (gt < 32) {
-                    gate_scan_store(gpre, (int)gt, Gl, Rc);
+                    gate_scan_store(gpre, (int)gt, Gl, Zc);
                     load_gates(c + 1, gpre);
                 }
             }
@@ -497,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // sequence), or lambda^(i+1) in reverse; signalled at once.
                 float wk;
                 if constexpr (kGate)
-                    wk = row < (uint32_t)Cc && Rc[Cc - 1] == Rc[row] ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
+                    wk = row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
                 else
                     wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
                 scale_rows<3>(sm + (uint32_t)s * kStageBytes + kStageK, row, wk);
@@ -515,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // A operand of Q~ S_prev: lane = token row, column c = dk pair (2c, 2c+1).
                 float wq;
                 if constexpr (kGate)
-                    wq = Rc[row] == 0 ? exp2f(Gl[row]) : 0.f;
+                    wq = Zc[row] < 0 ? exp2f(Gl[row]) : 0.f;
                 else
                     wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
                 const uint32_t wq2 = pack_bf16x2(wq, wq);
@@ -547,9 +565,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 if constexpr (kGate) {
                     const float gi = Gl[row];
-                    const int ri = Rc[row];
-                    if (has0) build_p_block_gated(r0, (int)row, 32 * b0, gi, ri, Gl, Rc, tl + kColP + 16u * b0);
-                    if (has1) build_p_block_gated(r1, (int)row, 32 * b1, gi, ri, Gl, Rc, tl + kColP + 16u * b1);
+                    const int zi = Zc[row];
+                    if (has0) build_p_block_gated(r0, (int)row, 32 * b0, gi, zi, Gl, tl + kColP + 16u * b0);
+                    if (has1) build_p_block_gated(r1, (int)row, 32 * b1, gi, zi, Gl, tl + kColP + 16u * b1);
                 } else {
                     pack_scores(r0);
                     pack_scores(r1);
