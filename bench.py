@@ -955,14 +955,14 @@ def oracle_decode_sample(layers=1, N=640):
 
 
 def cpu_baseline():
-    dt, toks, nt, sample = oracle_fwd_sample(64)
+    dt, toks, nt, sample = oracle_fwd_sample(128)
     base = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle", "sample": sample,
             "seconds": dt}
     modes = {}
-    dt, toks, nt, sample = oracle_bwd_sample(32)
+    dt, toks, nt, sample = oracle_bwd_sample(128)
     modes["fwd_bwd"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
                         "sample": sample, "seconds": dt}
-    dt, ss, nt, sample = oracle_decode_sample(1)
+    dt, ss, nt, sample = oracle_decode_sample(2, 1280)
     modes["decode"] = {"value": ss / dt, "unit": "seq-steps/s", "cores": nt, "kind": "oracle",
                        "sample": sample, "seconds": dt}
     dt, toks, nt, sample = oracle_varlen_sample(8)
@@ -971,7 +971,7 @@ def cpu_baseline():
     dt, toks, nt, sample = oracle_conv_sample(8)
     modes["conv"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
                      "sample": sample, "seconds": dt}
-    dt, toks, nt, sample = oracle_gated_sample(32)
+    dt, toks, nt, sample = oracle_gated_sample(128)
     modes["gated"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
                       "sample": sample, "seconds": dt}
     return base, modes
