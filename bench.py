@@ -354,6 +354,7 @@ def bench_gated(args, dist, device, stream, peaks, sampler):
     bytes_, fl_full, fl_causal = fwd_work(B, T, False, True)
     bytes_ += B * T * H * 4                     # g, fp32 per token and head
     avg_ms = statistics.mean(per)
+    traffic, _ = committed_traffic("gla_fwd_gated")   # per B=8 launch
     ach_gbs = bytes_ / (avg_ms * 1e-3) / 1e9
     ach_tf = fl_full / (avg_ms * 1e-3) / 1e12
     res = {
@@ -363,7 +364,8 @@ def bench_gated(args, dist, device, stream, peaks, sampler):
                    "gates": "log sigmoid(x)/16, x ~ N(0,1), per token and head", "h0": "none", "hT": "written",
                    "l2": f"inputs larger than L2 ({bytes_ / 1e6:.0f} MB per step), no flush"},
         "roofline": {"bound": "hbm", "achieved": ach_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": ach_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": ach_gbs / peaks["hbm_gbs"],
+                     "traffic": traffic * B / 8 if traffic is not None else None,
                      "algorithmic_bytes_per_launch": bytes_, "avg_launch_ms": avg_ms,
                      "peak_source": peaks["source"]},
         "tensor": {"achieved": ach_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
