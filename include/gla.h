@@ -173,6 +173,19 @@ gla_status gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, con
                                 gla_dtype dtype, void *o, void *stream);
 
 /*
+ * gla_chunk_fwd_varlen_gated -- gla_chunk_fwd_varlen with a per-token decay
+ * (the gated form of gla_chunk_fwd_gated): g [total_T, H] fp32, the
+ * natural-log decay of each packed token and head, in place of log_lambda.
+ * Everything else, including the device-side checks of cu_seqlens and
+ * slots, as gla_chunk_fwd_varlen; the serving steps that follow are
+ * gla_decode_step_gated on the same pool.
+ */
+gla_status gla_chunk_fwd_varlen_gated(const void *q, const void *k, const void *v, const float *g,
+                                      float scale, const int *cu_seqlens, const int *slots, float *state_pool,
+                                      int n_slots, int nseq, int total_T, int H, int dk, int dv, int chunk,
+                                      gla_dtype dtype, void *o, void *stream);
+
+/*
  * gla_chunk_bwd -- gradients of L = sum_t <do_t, o_t> + <dhT, hT> through
  * the chunked forward ("Challenge 3": through every serial state update).
  * lambda is fixed (not learned), so there is no gradient for log_lambda.

@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     gla_chunk_fwd_mixer,
     gla_chunk_fwd_noalloc,
     gla_chunk_fwd_varlen,
+    gla_chunk_fwd_varlen_gated,
     gla_chunk_fwd_workspace_size,
     gla_conv1d_fwd,
     gla_conv1d_step,

@@ -10,6 +10,7 @@ Functions:
   gla_chunk_fwd(q, k, v, log_lambda, h0=None, scale=None, chunk=128, ...) -> (o, hT)
   gla_chunk_fwd_noalloc(...)                                              -> (o, hT)
   gla_chunk_fwd_varlen(q, k, v, log_lambda, cu_seqlens, state_pool, ...)  -> o  (pool updated)
+  gla_chunk_fwd_varlen_gated(q, k, v, g, cu_seqlens, state_pool, ...)     -> o  (pool updated) per-token decay
   gla_chunk_fwd_mixer(q, k, v, g, log_lambda, ...)                        -> (z, hT)
   gla_chunk_fwd_gated(q, k, v, g, h0=None, scale=None, chunk=128, ...)    -> (o, hT)  per-token decay
   gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, ...)          -> (dq, dk, dv, dh0)
@@ -38,7 +39,7 @@ GLA_OK, GLA_ERR_INVALID_ARG, GLA_ERR_UNSUPPORTED, GLA_ERR_CUDA, GLA_ERR_TIMEOUT,
 GLA_BF16, GLA_FP32 = 0, 1
 
 # The public entry points declared in include/gla.h.
-ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen",
+ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_gated",
                  "gla_chunk_fwd_mixer", "gla_chunk_fwd_gated", "gla_decode_step_gated", "gla_chunk_bwd",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
                  "gla_conv1d_fwd", "gla_conv1d_varlen", "gla_conv1d_step", "gla_selftest_wait_timeout", "gla_check",
@@ -81,6 +82,9 @@ def lib():
             L.gla_chunk_fwd_mixer.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f, _i, _i, _i, _i, _i, _i,
                                               _i, _vp, _vp, _vp, _sz, _vp]
             L.gla_chunk_fwd_mixer.restype = _i
+            L.gla_chunk_fwd_varlen_gated.argtypes = [_vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                                     _i, _i, _i, _vp, _vp]
+            L.gla_chunk_fwd_varlen_gated.restype = _i
             L.gla_chunk_fwd_gated.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]
             L.gla_chunk_fwd_gated.restype = _i
             L.gla_decode_step_gated.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _vp, _vp]
@@ -267,6 +271,26 @@ def gla_chunk_fwd_gated(q, k, v, g, h0=None, scale=None, chunk=128, *, o=None, h
                                    int(chunk), _dtype_code(q), _ptr(o), _ptr(hT), _stream(stream))
     _raise_on(st, "gla_chunk_fwd_gated")
     return o, hT
+
+
+def gla_chunk_fwd_varlen_gated(q, k, v, g, cu_seqlens, state_pool, slots=None, scale=None, chunk=128, *,
+                               o=None, stream=None):
+    """Variable-length forward with a per-token decay: g [total_T,H] fp32
+    natural-log decays, packed like q; otherwise as gla_chunk_fwd_varlen.
+    Returns o [total_T,H,dv]."""
+    torch = _torch()
+    total_T, H, dk = q.shape
+    dv = v.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    if o is None:
+        o = torch.empty((total_T, H, dv), dtype=q.dtype, device=q.device)
+    nseq = cu_seqlens.numel() - 1
+    st = lib().gla_chunk_fwd_varlen_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale), _ptr(cu_seqlens),
+                                          _ptr(slots), _ptr(state_pool), int(state_pool.shape[0]), nseq, total_T, H,
+                                          dk, dv, int(chunk), _dtype_code(q), _ptr(o), _stream(stream))
+    _raise_on(st, "gla_chunk_fwd_varlen_gated")
+    return o
 
 
 def gla_chunk_fwd_mixer(q, k, v, g, log_lambda, h0=None, scale=None, chunk=128, aug=None, norm_w=None, eps=1e-6,

@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seg = (blockIdx.x >> 1) / a.BH;
     const int bh = (blockIdx.x >> 1) % a.BH;
     constexpr int C = kC;   // chunk length, 64 or 128: token loops are unrolled
-    static_assert(!(kGate && (kRev || kVar)), "the gated mode is the batched forward only");
+    static_assert(!(kGate && kRev), "the gated mode is a forward");
     const int h = bh % a.H;
     // b: batch index of the states; bt, tok0: token coordinates of the sequence
     int b = bh / a.H, bt = b, tok0 = 0, T = a.T, nck_seq = a.nck;
@@ -803,12 +803,15 @@ cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *lau
     if ((e = make_token_map(&mv, p.v, 1, p.total_T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mo, p.o, 1, p.total_T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     FwdTcArgs a{p.log_lambda, p.pool, p.pool, p.scale, 1.f, 1.f, p.total_T, p.H, p.chunk, 0, 1, 0, p.nseq * p.H, 0,
-                p.status, p.cu_seqlens, p.slots, p.n_slots, static_cast<__nv_bfloat16 *>(p.o)};
-    auto kernel = p.chunk == 128 ? gla_fwd_tc_kernel<false, 128, true> : gla_fwd_tc_kernel<false, 64, true>;
-    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) !=
-        cudaSuccess)
+                p.status, p.cu_seqlens, p.slots, p.n_slots, static_cast<__nv_bfloat16 *>(p.o), p.g};
+    // gated: per-token log-decays [total_T, H] packed like q
+    auto kernel = p.g ? (p.chunk == 128 ? gla_fwd_tc_kernel<false, 128, true, true>
+                                        : gla_fwd_tc_kernel<false, 64, true, true>)
+                      : (p.chunk == 128 ? gla_fwd_tc_kernel<false, 128, true> : gla_fwd_tc_kernel<false, 64, true>);
+    const uint32_t smem = p.g ? kSmemBytesGated : kSmemBytes;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
-    kernel<<<(unsigned)(p.nseq * p.H * 2), kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, a);
+    kernel<<<(unsigned)(p.nseq * p.H * 2), kThreads, smem, s>>>(mq, mk, mv, mo, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

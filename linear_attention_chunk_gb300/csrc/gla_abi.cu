@@ -342,20 +342,25 @@ gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const floa
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_bwd launch");
 }
 
-gla_status gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *log_lambda, float scale,
+static gla_status varlen_common(const void *q, const void *k, const void *v, const float *log_lambda, const float *g,
+                                float scale,
                                 const int *cu_seqlens, const int *slots, float *state_pool, int n_slots, int nseq,
                                 int total_T, int H, int dk, int dv, int chunk, gla_dtype dtype, void *o,
-                                void *stream) {
+                                void *stream, const char *name) {
     t_err[0] = 0;
     t_launches = 0;
     gla_status st = check_chunk_shape(1, total_T, H, dk, dv, chunk, dtype);
     if (st != GLA_OK) return st;
-    if (dtype != GLA_BF16) return fail(GLA_ERR_UNSUPPORTED, "gla_chunk_fwd_varlen supports GLA_BF16 only");
+    if (dtype != GLA_BF16) return fail(GLA_ERR_UNSUPPORTED, "%s supports GLA_BF16 only", name);
     if (nseq < 0 || n_slots < 0) return fail(GLA_ERR_INVALID_ARG, "negative nseq=%d or n_slots=%d", nseq, n_slots);
     if ((long double)nseq * H * 2 > 2147483647.0L) return fail(GLA_ERR_INVALID_ARG, "nseq*H too large");
     OPTIONAL_PTR(slots, "slots");
     if (nseq == 0 || H == 0) return GLA_OK;
-    REQUIRE_PTR(log_lambda, "log_lambda");
+    if (g) {
+        REQUIRE_PTR(g, "g");
+    } else {
+        REQUIRE_PTR(log_lambda, "log_lambda");
+    }
     REQUIRE_PTR(cu_seqlens, "cu_seqlens");
     REQUIRE_PTR(state_pool, "state_pool");
     if (!slots && n_slots < nseq)
@@ -370,11 +375,28 @@ gla_status gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, con
     if ((st = status_word(&status)) != GLA_OK) return st;
     if (total_T == 0) return GLA_OK;   // every sequence is empty: no state changes
     VarlenParams p{q, k, v, log_lambda, scale, cu_seqlens, slots, state_pool, n_slots, nseq, total_T, H, dk, dv,
-                   chunk, o, status};
+                   chunk, o, status, g};
     int launches = 0;
     const cudaError_t e = launch_fwd_varlen_tc(p, static_cast<cudaStream_t>(stream), &launches);
     t_launches = launches;
-    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_varlen launch");
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, name);
+}
+
+gla_status gla_chunk_fwd_varlen(const void *q, const void *k, const void *v, const float *log_lambda, float scale,
+                                const int *cu_seqlens, const int *slots, float *state_pool, int n_slots, int nseq,
+                                int total_T, int H, int dk, int dv, int chunk, gla_dtype dtype, void *o,
+                                void *stream) {
+    return varlen_common(q, k, v, log_lambda, nullptr, scale, cu_seqlens, slots, state_pool, n_slots, nseq, total_T, H,
+                         dk, dv, chunk, dtype, o, stream, "gla_chunk_fwd_varlen");
+}
+
+gla_status gla_chunk_fwd_varlen_gated(const void *q, const void *k, const void *v, const float *g, float scale,
+                                      const int *cu_seqlens, const int *slots, float *state_pool, int n_slots,
+                                      int nseq, int total_T, int H, int dk, int dv, int chunk, gla_dtype dtype,
+                                      void *o, void *stream) {
+    if (nseq > 0 && H > 0 && total_T > 0 && !g) return fail(GLA_ERR_INVALID_ARG, "g is NULL");
+    return varlen_common(q, k, v, nullptr, g, scale, cu_seqlens, slots, state_pool, n_slots, nseq, total_T, H, dk,
+                         dv, chunk, dtype, o, stream, "gla_chunk_fwd_varlen_gated");
 }
 
 size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype) {

@@ -49,6 +49,7 @@ struct VarlenParams {
     int n_slots, nseq, total_T, H, dk, dv, chunk;
     void *o;                    // packed [total_T, H, dv]
     unsigned int *status;
+    const float *g;             // gated: per-token log-decays [total_T, H], or NULL
 };
 
 struct DecodeParams {

@@ -1,7 +1,8 @@
 """GPU parity of the per-token (data-dependent) decay against the oracle's
 gated recurrence (O9, O10), through the C ABI: gla_chunk_fwd_gated on the
 tensor-core path (bf16) and the validation path (fp32), and
-gla_decode_step_gated.
+gla_decode_step_gated, and the packed variable-length prefill
+gla_chunk_fwd_varlen_gated.
 
 Cases span several chunks and a ragged tail, both chunk lengths, gates that
 clear the state (-inf) inside a chunk and on a chunk's first token, strong
@@ -143,3 +144,30 @@ def test_gated_decode(gla, dtype):
     ro, rS = oracle.decode_gated(dc.q, dc.k, dc.v, g, dc.S, dc.scale)
     assert relerr(to_host(o), ro) <= TOL[dtype]
     assert relerr(to_host(S), rS) <= 1e-5   # the state itself stays fp32
+
+
+# ------------------------------------------------------- variable-length prefill
+@pytest.mark.parametrize("C", [128, 64])
+def test_gated_varlen_matches_oracle_per_sequence(gla, C):
+    """Packed prompts of mixed lengths with per-token gates, each from and
+    into its slot of a state pool; an empty prompt leaves its slot as it is."""
+    import torch
+    lengths = [0, 1, 63, 65, 128, 129, 300, 700]
+    c = gen.make_varlen_case(lengths, 4, seed=600 + C, n_slots=11)
+    rng = np.random.default_rng(601 + C)
+    g = gen.log_gates(rng, (c.q.shape[0], 4), "gla")
+    g[5, 2] = -np.inf                     # clears the state of sequence 2's head 2 inside its prompt
+    d = dict(q=to_dev(c.q, "bf16"), k=to_dev(c.k, "bf16"), v=to_dev(c.v, "bf16"),
+             cu=torch.from_numpy(c.cu_seqlens).cuda(), slots=torch.from_numpy(c.slots).cuda(), pool=f32_dev(c.pool))
+    o = gla.gla_chunk_fwd_varlen_gated(d["q"], d["k"], d["v"], f32_dev(g), d["cu"], d["pool"], d["slots"], c.scale, C)
+    gla.gla_check()
+    oh, pool = to_host(o), to_host(d["pool"])
+    for n in range(len(lengths)):
+        a, b = int(c.cu_seqlens[n]), int(c.cu_seqlens[n + 1])
+        if b == a:
+            assert np.array_equal(pool[c.slots[n]], c.pool[c.slots[n]].astype(np.float32).astype(np.float64))
+            continue
+        h0 = c.pool[c.slots[n]][None].astype(np.float32)
+        ro, rh = oracle.fwd_gated(c.q[None, a:b], c.k[None, a:b], c.v[None, a:b], g[None, a:b], h0, c.scale)
+        assert relerr(oh[a:b], ro[0]) <= TOL["bf16"], f"o of sequence {n} (length {b - a})"
+        assert relerr(pool[c.slots[n]], rh[0]) <= TOL["bf16"], f"state of sequence {n}"
