@@ -21,6 +21,7 @@ Functions (all layouts token-major, see gla_oracle.c):
   fwd_gated      -- per-token (data-dependent) decay: recurrence, unrolled and
                     chunked forms (O9)
   decode_gated   -- one recurrent step with a per-token decay (O10)
+  bwd_gated      -- gradients of the per-token decay form, the gate's included (O11)
 """
 from __future__ import annotations
 
@@ -79,11 +80,13 @@ def _load():
             lib.gla_oracle_fwd_gated_chunked.argtypes = gsig[:11] + [_L] + gsig[11:]
             lib.gla_oracle_decode_gated.argtypes = [_D, _D, _D, _D, _D, ctypes.c_double, _L, _L, _L, _L,
                                                     _D, ctypes.c_int]
+            lib.gla_oracle_bwd_gated.argtypes = [_D, _D, _D, _D, _D, ctypes.c_double, _D, _D, _L, _L, _L, _L, _L,
+                                                 _D, _D, _D, _D, _D, ctypes.c_int]
             for f in ("gla_oracle_fwd_recurrent", "gla_oracle_fwd_quadratic", "gla_oracle_fwd_chunked",
                       "gla_oracle_bwd", "gla_oracle_bwd_chunked", "gla_oracle_decode",
                       "gla_oracle_threads", "gla_oracle_mixer_epilogue", "gla_oracle_conv1d",
                       "gla_oracle_fwd_gated", "gla_oracle_fwd_gated_quadratic", "gla_oracle_fwd_gated_chunked",
-                      "gla_oracle_decode_gated"):
+                      "gla_oracle_decode_gated", "gla_oracle_bwd_gated"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -253,3 +256,18 @@ def decode_gated(q, k, v, g, S, scale=1.0, nthreads=0):
     _check(lib.gla_oracle_decode_gated(_p(q), _p(k), _p(v), _p(g), _p(S), float(scale), N, H, dk, dv, _p(o),
                                        int(nthreads)), "decode_gated")
     return o, S
+
+
+def bwd_gated(q, k, v, g, h0, scale, do, dhT=None, nthreads=0):
+    """O11: gradients of L = sum <do, o> + <dhT, hT> for the per-token decay
+    exp(g), g [B,T,H]. Returns (dq, dk, dv, dh0, dg)."""
+    lib = _load()
+    q, k, v, g, h0, do, dhT = map(_f64, (q, k, v, g, h0, do, dhT))
+    B, T, H, dk, dv = _dims(q, v)
+    dq, dk_, dv_ = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dh0 = np.zeros((B, H, dk, dv))
+    dg = np.zeros((B, T, H))
+    _check(lib.gla_oracle_bwd_gated(_p(q), _p(k), _p(v), _p(g), _p(h0), float(scale), _p(do), _p(dhT),
+                                    B, T, H, dk, dv, _p(dq), _p(dk_), _p(dv_), _p(dh0), _p(dg), int(nthreads)),
+           "bwd_gated")
+    return dq, dk_, dv_, dh0, dg

@@ -832,3 +832,111 @@ int gla_oracle_decode_gated(const double *q, const double *k, const double *v, c
     run_units(N * H, nthreads, gated_decode_unit, &a);
     return 0;
 }
+
+/* --------------------------------------------- O11: gated backward */
+/* Gradients of L = sum_t <do_t, o_t> + <dhT, hT> for the per-token decay
+ * alpha_t = exp(g_t): with G_t = dL/dS_t (all paths),
+ *   G_{T-1} = dhT + scale q_{T-1} do_{T-1}^T,
+ *   G_{t-1} = alpha_t G_t + scale q_{t-1} do_{t-1}^T,
+ *   dq_t = scale S_t do_t,  dk_t = G_t v_t,  dv_t = G_t^T k_t,
+ *   dh0  = alpha_0 G_0,
+ *   dg_t = alpha_t <G_t, S_{t-1}>      (dL/dalpha_t times dalpha_t/dg_t; S_{-1} = h0).
+ * S_{t-1} is recomputed going backwards from states saved every
+ * GATED_CKPT tokens in the forward pass (no division by alpha). g [B,T,H]. */
+#define GATED_CKPT 64
+
+typedef struct {
+    const double *q, *k, *v, *g, *h0, *do_, *dhT;
+    double scale;
+    long B, T, H, dk, dv;
+    double *dq, *dk_out, *dv_out, *dh0, *dg;
+} gbwd_t;
+
+#define GB_QIDX(a, b, t, h, i) ((((b) * (a)->T + (t)) * (a)->H + (h)) * (a)->dk + (i))
+#define GB_VIDX(a, b, t, h, j) ((((b) * (a)->T + (t)) * (a)->H + (h)) * (a)->dv + (j))
+#define GB_GIDX(a, b, t, h) (((b) * (a)->T + (t)) * (a)->H + (h))
+#define GB_SIDX(a, b, h) (((b) * (a)->H + (h)) * (a)->dk * (a)->dv)
+
+/* one forward step S <- alpha_t S + k_t v_t^T */
+static void gbwd_step(const gbwd_t *a, long b, long h, long t, double *S) {
+    long dk = a->dk, dv = a->dv;
+    double alpha = exp(a->g[GB_GIDX(a, b, t, h)]);
+    const double *kt = a->k + GB_QIDX(a, b, t, h, 0), *vt = a->v + GB_VIDX(a, b, t, h, 0);
+    for (long i = 0; i < dk; ++i)
+        for (long j = 0; j < dv; ++j) S[i * dv + j] = alpha * S[i * dv + j] + kt[i] * vt[j];
+}
+
+static void gated_bwd_unit(void *ctx, long unit) {
+    const gbwd_t *a = (const gbwd_t *)ctx;
+    long b = unit / a->H, h = unit % a->H, dk = a->dk, dv = a->dv, T = a->T, n = dk * dv;
+    long ncp = T / GATED_CKPT + 1;
+    double *cp = (double *)calloc((size_t)(ncp * n), sizeof(double));   /* S_{c*CKPT - 1} */
+    double *S = (double *)calloc((size_t)n, sizeof(double));
+    double *blk = (double *)calloc((size_t)(GATED_CKPT * n), sizeof(double));
+    double *G = (double *)calloc((size_t)n, sizeof(double));
+    if (a->h0) memcpy(S, a->h0 + GB_SIDX(a, b, h), sizeof(double) * (size_t)n);
+    /* forward: dq_t and the checkpoints */
+    for (long t = 0; t < T; ++t) {
+        if (t % GATED_CKPT == 0) memcpy(cp + (t / GATED_CKPT) * n, S, sizeof(double) * (size_t)n);
+        gbwd_step(a, b, h, t, S);
+        const double *dot = a->do_ + GB_VIDX(a, b, t, h, 0);
+        double *dqt = a->dq + GB_QIDX(a, b, t, h, 0);
+        for (long i = 0; i < dk; ++i) {
+            double acc = 0.0;
+            for (long j = 0; j < dv; ++j) acc += S[i * dv + j] * dot[j];
+            dqt[i] = a->scale * acc;
+        }
+    }
+    /* reverse: G_t, dk, dv, dg, one checkpoint block at a time */
+    if (a->dhT) memcpy(G, a->dhT + GB_SIDX(a, b, h), sizeof(double) * (size_t)n);
+    long t = T - 1;
+    for (long c = (T - 1) / GATED_CKPT; c >= 0 && T > 0; --c) {
+        long t0 = c * GATED_CKPT, t1 = t0 + GATED_CKPT < T ? t0 + GATED_CKPT : T;
+        /* blk[r] = S_{t0 + r - 1}, r = 0 .. t1 - t0 - 1 */
+        memcpy(S, cp + c * n, sizeof(double) * (size_t)n);
+        for (long r = 0; r < t1 - t0; ++r) {
+            memcpy(blk + r * n, S, sizeof(double) * (size_t)n);
+            gbwd_step(a, b, h, t0 + r, S);
+        }
+        for (; t >= t0; --t) {
+            const double *qt = a->q + GB_QIDX(a, b, t, h, 0), *dot = a->do_ + GB_VIDX(a, b, t, h, 0);
+            const double *kt = a->k + GB_QIDX(a, b, t, h, 0), *vt = a->v + GB_VIDX(a, b, t, h, 0);
+            for (long i = 0; i < dk; ++i)
+                for (long j = 0; j < dv; ++j) G[i * dv + j] += a->scale * qt[i] * dot[j];
+            double *dkt = a->dk_out + GB_QIDX(a, b, t, h, 0), *dvt = a->dv_out + GB_VIDX(a, b, t, h, 0);
+            for (long i = 0; i < dk; ++i) {
+                double acc = 0.0;
+                for (long j = 0; j < dv; ++j) acc += G[i * dv + j] * vt[j];
+                dkt[i] = acc;
+            }
+            for (long j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (long i = 0; i < dk; ++i) acc += G[i * dv + j] * kt[i];
+                dvt[j] = acc;
+            }
+            double alpha = exp(a->g[GB_GIDX(a, b, t, h)]);
+            const double *Sp = blk + (t - t0) * n;
+            double ip = 0.0;
+            for (long r = 0; r < n; ++r) ip += G[r] * Sp[r];
+            a->dg[GB_GIDX(a, b, t, h)] = alpha * ip;
+            for (long r = 0; r < n; ++r) G[r] *= alpha;   /* now dL/dS_{t-1} minus its own readout */
+        }
+    }
+    if (a->dh0) memcpy(a->dh0 + GB_SIDX(a, b, h), G, sizeof(double) * (size_t)n);
+    free(cp); free(S); free(blk); free(G);
+}
+
+int gla_oracle_bwd_gated(const double *q, const double *k, const double *v, const double *g,
+                         const double *h0, double scale, const double *do_, const double *dhT,
+                         long B, long T, long H, long dk, long dv,
+                         double *dq, double *dk_out, double *dv_out, double *dh0, double *dg, int nthreads) {
+    if (!q || !k || !v || !g || !do_ || !dq || !dk_out || !dv_out || !dg || B < 0 || T < 0 || H <= 0 ||
+        dk <= 0 || dv <= 0)
+        return 1;
+    gbwd_t a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.h0 = h0; a.do_ = do_; a.dhT = dhT; a.scale = scale;
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv;
+    a.dq = dq; a.dk_out = dk_out; a.dv_out = dv_out; a.dh0 = dh0; a.dg = dg;
+    run_units(B * H, nthreads, gated_bwd_unit, &a);
+    return 0;
+}

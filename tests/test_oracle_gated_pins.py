@@ -1,4 +1,5 @@
-"""Pins of the oracle's per-token (data-dependent) decay, O9 and O10.
+"""Pins of the oracle's per-token (data-dependent) decay, O9, O10 and its
+backward O11.
 
 The gated recurrence S_t = exp(g_t) S_{t-1} + k_t v_t^T, o_t = scale S_t^T q_t
 is checked against facts outside its own code, chosen so that a plausible
@@ -16,7 +17,12 @@ decay, a transposed state) fails at least one of them:
     fresh call over the rest of the sequence;
   - split-call invariance;
   - the final state in closed form from cumulative sums of g;
-  - one decode step equals the forward at T = 1.
+  - one decode step equals the forward at T = 1;
+  - O11: central differences of L = sum <do, o> + <dhT, hT> for every
+    gradient including the gate's (a sign slip in dg, the gate of t used at
+    t+1, a dh0 without its decay fail these); a constant gate reproduces the
+    fixed-decay backward, and its dg summed over tokens the gradient of
+    log lambda; a -inf gate has dg = 0 and cuts the gradient paths across it.
 """
 import json
 import os
@@ -149,3 +155,75 @@ def test_decode_step_is_forward_at_T1():
     B, _, H, dk = q.shape
     od, S = oracle.decode_gated(q[:, 0], k[:, 0], v[:, 0], g[:, 0], h0, 0.6)
     assert rel(od, o[:, 0]) < 1e-14 and rel(S, hT) < 1e-14
+
+
+# ------------------------------------------------------------- O11: backward
+def gated_loss(q, k, v, g, h0, scale, do, dhT):
+    o, hT = oracle.fwd_gated(q, k, v, g, h0, scale)
+    return float(np.sum(do * o) + np.sum(dhT * hT))
+
+
+@pytest.mark.parametrize("T", [7, 70])
+def test_gated_backward_finite_differences(T):
+    """Every gradient, the gate's included, against central differences of
+    L = sum <do, o> + <dhT, hT> (T = 70 crosses the oracle's checkpoints)."""
+    q, k, v, g, h0 = case(20 + T, B=1, T=T, H=2, dk=3, dv=4, kind="wide")
+    rng = np.random.default_rng(21 + T)
+    do = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape) * 0.5
+    grads = oracle.bwd_gated(q, k, v, g, h0, 0.6, do, dhT)
+    args = dict(q=q, k=k, v=v, g=g, h0=h0)
+    eps = 1e-6
+    for name, grad in zip(("q", "k", "v", "h0", "g"), grads):
+        x = args[name]
+        idx = [tuple(rng.integers(0, n) for n in x.shape) for _ in range(6)]
+        for ix in idx:
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += eps
+            xm[ix] -= eps
+            ap, am = dict(args, **{name: xp}), dict(args, **{name: xm})
+            fd = (gated_loss(ap["q"], ap["k"], ap["v"], ap["g"], ap["h0"], 0.6, do, dhT) -
+                  gated_loss(am["q"], am["k"], am["v"], am["g"], am["h0"], 0.6, do, dhT)) / (2 * eps)
+            assert abs(fd - grad[ix]) <= 1e-6 * max(1.0, abs(fd)), (name, ix, fd, grad[ix])
+
+
+def test_gated_backward_constant_gate_is_the_fixed_backward():
+    """A constant gate reproduces the fixed-decay gradients; the gate's
+    gradient summed over tokens is the gradient of log lambda (checked by
+    central differences of the fixed-decay loss)."""
+    q, k, v, _, h0 = case(22, B=1, T=40, H=3, dk=4, dv=5)
+    rng = np.random.default_rng(23)
+    do = rng.standard_normal(v.shape)
+    dhT = rng.standard_normal(h0.shape) * 0.3
+    ll = np.log(np.array([0.4, 0.8, 0.97]))
+    g = np.broadcast_to(ll, q.shape[:3]).copy()
+    dq, dk, dv, dh0, dg = oracle.bwd_gated(q, k, v, g, h0, 0.5, do, dhT)
+    rq, rk, rv, rh0 = oracle.bwd(q, k, v, ll, h0, 0.5, do, dhT)
+    for a, b in ((dq, rq), (dk, rk), (dv, rv), (dh0, rh0)):
+        assert rel(a, b) < 1e-12
+    eps = 1e-6
+
+    def loss(ll_):
+        o, hT = oracle.fwd_recurrent(q, k, v, ll_, h0, 0.5)
+        return float(np.sum(do * o) + np.sum(dhT * hT))
+    for h in range(3):
+        e = np.zeros(3)
+        e[h] = eps
+        fd = (loss(ll + e) - loss(ll - e)) / (2 * eps)
+        assert abs(dg[0, :, h].sum() - fd) <= 1e-6 * max(1.0, abs(fd))
+
+
+def test_gated_backward_clearing_gate():
+    """A -inf gate at r: its own gradient is 0, and nothing after r reaches
+    the tokens before it except through k_r v_r^T (so dq of tokens < r and
+    dh0 equal those of the loss restricted to outputs < r)."""
+    q, k, v, g, h0 = case(24, B=1, T=30, H=2, dk=3, dv=4, kind="gla")
+    r = 13
+    g[:, r, :] = -np.inf
+    rng = np.random.default_rng(25)
+    do = rng.standard_normal(v.shape)
+    dq, dk, dv, dh0, dg = oracle.bwd_gated(q, k, v, g, h0, 0.5, do, None)
+    assert np.all(dg[:, r, :] == 0.0)
+    dq2, dk2, dv2, dh02, dg2 = oracle.bwd_gated(q[:, :r], k[:, :r], v[:, :r], g[:, :r], h0, 0.5, do[:, :r], None)
+    assert rel(dq[:, :r], dq2) < 1e-12 and rel(dh0, dh02) < 1e-12
+    assert rel(dk[:, :r], dk2) < 1e-12 and rel(dv[:, :r], dv2) < 1e-12 and rel(dg[:, :r], dg2) < 1e-12
