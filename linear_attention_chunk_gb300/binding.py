@@ -175,6 +175,19 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _f32(t, shape, name):
+    """Pointer of an fp32 argument (decays, states), after checking its dtype
+    and shape: the C ABI reads these buffers as float without knowing them."""
+    if t is None:
+        return None
+    torch = _torch()
+    if t.dtype != torch.float32:
+        raise GlaError(GLA_ERR_INVALID_ARG, "argument", f"{name} must be float32, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise GlaError(GLA_ERR_INVALID_ARG, "argument", f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return _ptr(t)
+
+
 def _stream(stream):
     torch = _torch()
     if stream is None:
@@ -209,7 +222,8 @@ def gla_chunk_fwd(q, k, v, log_lambda, h0=None, scale=None, chunk=128, *, o=None
     if workspace is None and ws_need > 0:
         workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib().gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(h0), float(scale),
+    st = lib().gla_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _f32(log_lambda, (H,), "log_lambda"),
+                             _f32(h0, (B, H, dk, dv), "h0"), float(scale),
                              B, T, H, dk, dv, int(chunk), dt, _ptr(o), _ptr(hT),
                              _ptr(workspace), ws_bytes, _stream(stream))
     _raise_on(st, "gla_chunk_fwd")
@@ -267,7 +281,8 @@ def gla_chunk_fwd_gated(q, k, v, g, h0=None, scale=None, chunk=128, *, o=None, h
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if hT is None and want_hT:
         hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
-    st = lib().gla_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(h0), float(scale), B, T, H, dk, dv,
+    st = lib().gla_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _f32(g, (B, T, H), "g"), _f32(h0, (B, H, dk, dv), "h0"),
+                                   float(scale), B, T, H, dk, dv,
                                    int(chunk), _dtype_code(q), _ptr(o), _ptr(hT), _stream(stream))
     _raise_on(st, "gla_chunk_fwd_gated")
     return o, hT
@@ -286,7 +301,8 @@ def gla_chunk_fwd_varlen_gated(q, k, v, g, cu_seqlens, state_pool, slots=None, s
     if o is None:
         o = torch.empty((total_T, H, dv), dtype=q.dtype, device=q.device)
     nseq = cu_seqlens.numel() - 1
-    st = lib().gla_chunk_fwd_varlen_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), float(scale), _ptr(cu_seqlens),
+    st = lib().gla_chunk_fwd_varlen_gated(_ptr(q), _ptr(k), _ptr(v), _f32(g, (total_T, H), "g"), float(scale),
+                                          _ptr(cu_seqlens),
                                           _ptr(slots), _ptr(state_pool), int(state_pool.shape[0]), nseq, total_T, H,
                                           dk, dv, int(chunk), _dtype_code(q), _ptr(o), _stream(stream))
     _raise_on(st, "gla_chunk_fwd_varlen_gated")
@@ -355,7 +371,8 @@ def gla_decode_step(q, k, v, log_lambda, S, scale=None, *, o=None, stream=None):
         scale = 1.0 / math.sqrt(dk)
     if o is None:
         o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
-    st = lib().gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_lambda), _ptr(S), float(scale),
+    st = lib().gla_decode_step(_ptr(q), _ptr(k), _ptr(v), _f32(log_lambda, (H,), "log_lambda"),
+                               _f32(S, (N, H, dk, dv), "S"), float(scale),
                                N, H, dk, dv, dt, _ptr(o), _stream(stream))
     _raise_on(st, "gla_decode_step")
     return o
@@ -371,7 +388,8 @@ def gla_decode_step_gated(q, k, v, g, S, scale=None, *, o=None, stream=None):
         scale = 1.0 / math.sqrt(dk)
     if o is None:
         o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
-    st = lib().gla_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(S), float(scale), N, H, dk, dv,
+    st = lib().gla_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _f32(g, (N, H), "g"), _f32(S, (N, H, dk, dv), "S"),
+                                     float(scale), N, H, dk, dv,
                                      _dtype_code(q), _ptr(o), _stream(stream))
     _raise_on(st, "gla_decode_step_gated")
     return o
