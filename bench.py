@@ -375,6 +375,54 @@ def bench_gated(args, dist, device, stream, peaks, sampler):
         "clocks": sampler.summary(*win) if sampler else None,
     }
     del q, k, v, g, o, hT
+    res["long"] = bench_gated_long(args, dist, device, stream, peaks, sampler)
+    return res
+
+
+def bench_gated_long(args, dist, device, stream, peaks, sampler):
+    """The long-context prefill shape (B=1, H=16, T=65,536, chunk 128, h0 ~
+    N(0, 0.1)) with per-token gates: split into segments whose decays are the
+    exp of their summed gates. The single-chain time (workspace too small to
+    split) is reported beside it."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    T = args.long_T or 65536
+    c = gen.make_case(1, T, H, DK, DV, seed=4, normalise_k=False, h0_std=0.1, chunk=CHUNK, gate="gla",
+                      name=f"gated_long_prefill_bf16_B1_H16_T{T}")
+    q, k, v = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v))
+    g = torch.from_numpy(c.extra["g"]).to(device)
+    h0 = torch.from_numpy(c.h0).to(device)
+    o = torch.empty((1, T, H, DV), dtype=torch.bfloat16, device=device)
+    hT = torch.empty((1, H, DK, DV), dtype=torch.float32, device=device)
+    out = {}
+    for split in (True, False):
+        n = gla.gla_chunk_fwd_gated_workspace_size(1, T, H, DK, DV, CHUNK) if split else 0
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+        def step():
+            gla.gla_chunk_fwd_gated(q, k, v, g, h0, c.scale, CHUNK, o=o, hT=hT, workspace=ws, stream=stream)
+            return gla.gla_last_launch_count()
+
+        total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+        total = dist.max(total)
+        bytes_ = fwd_work(1, T, True, True)[0] + T * H * 4
+        avg_ms = statistics.mean(per)
+        ach = bytes_ / (avg_ms * 1e-3) / 1e9
+        out[split] = {
+            "value": T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+            "ms_per_step": total / args.steps,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_call": bytes_,
+                         "avg_call_ms": avg_ms, "launches_per_call": launches // max(args.steps, 1),
+                         "peak_source": peaks["source"]},
+            "gpu_launches": launches,
+            "clocks": sampler.summary(*win) if sampler else None,
+        }
+    res = dict(out[True])
+    res["config"] = {"workload": c.name, "B": 1, "T": T, "H": H, "chunk": CHUNK, "h0": "N(0,0.1)",
+                     "gates": "log sigmoid(x)/16, x ~ N(0,1), per token and head"}
+    res["single_chain"] = out[False]
+    del q, k, v, g, o, hT, h0
     return res
 
 
@@ -1110,7 +1158,7 @@ def main(argv=None):
         "gpu_launches": head["gpu_launches"],
         "clocks": head["clocks"],
         "modes": {k: v for k, v in results.items() if k != head_key},
-        **{key: head[key] for key in ("standalone", "fwd_mixer", "chunk64", "step", "ms_per_layer_step")
+        **{key: head[key] for key in ("standalone", "fwd_mixer", "chunk64", "step", "ms_per_layer_step", "long")
            if key in head},
         "peaks": peaks,
         "timing": {"events": "one CUDA event pair around the K timed steps, on the launch stream",

@@ -222,14 +222,22 @@ size_t gla_chunk_bwd_workspace_size(int B, int T, int H, int dk, int dv, int chu
  *   (or any value <= -80, whose exp is below fp32's normal range) clears
  *   the state. Positive values are outside the contract: the chunk weights
  *   rely on decays <= 1.
- *   Everything else as gla_chunk_fwd (q, k, v, h0, o, hT, chunk, dtype),
- *   without segmentation: one serial chain per (b, h), no workspace.
- *   GLA_BF16 runs the tensor-core kernel; GLA_FP32 the validation kernel.
+ *   Everything else as gla_chunk_fwd (q, k, v, h0, o, hT, chunk, dtype,
+ *   workspace): with at least gla_chunk_fwd_gated_workspace_size() bytes a
+ *   long sequence is split into segments that run in parallel, each
+ *   segment's decay the exp of its summed g. GLA_BF16 runs the tensor-core
+ *   kernel; GLA_FP32 the validation kernel (one chain per (b, h)).
  */
 gla_status gla_chunk_fwd_gated(const void *q, const void *k, const void *v,
                                const float *g, const float *h0, float scale,
                                int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype,
-                               void *o, float *hT, void *stream);
+                               void *o, float *hT,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace that let gla_chunk_fwd_gated split long sequences into
+ * segments (the segment states and decays; 0 when no split pays). */
+size_t gla_chunk_fwd_gated_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
+                                          gla_dtype dtype);
 
 /*
  * gla_decode_step_gated -- one recurrent step with a per-token decay:

@@ -21,6 +21,7 @@ from .binding import (  # noqa: F401
     gla_chunk_bwd_workspace_size,
     gla_chunk_fwd,
     gla_chunk_fwd_gated,
+    gla_chunk_fwd_gated_workspace_size,
     gla_chunk_fwd_mixer,
     gla_chunk_fwd_noalloc,
     gla_chunk_fwd_varlen,

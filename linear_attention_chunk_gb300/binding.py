@@ -40,7 +40,7 @@ GLA_BF16, GLA_FP32 = 0, 1
 
 # The public entry points declared in include/gla.h.
 ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_gated",
-                 "gla_chunk_fwd_mixer", "gla_chunk_fwd_gated", "gla_decode_step_gated", "gla_chunk_bwd",
+                 "gla_chunk_fwd_mixer", "gla_chunk_fwd_gated", "gla_chunk_fwd_gated_workspace_size", "gla_decode_step_gated", "gla_chunk_bwd",
                  "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
                  "gla_conv1d_fwd", "gla_conv1d_varlen", "gla_conv1d_step", "gla_selftest_wait_timeout", "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
@@ -85,8 +85,11 @@ def lib():
             L.gla_chunk_fwd_varlen_gated.argtypes = [_vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                                                      _i, _i, _i, _vp, _vp]
             L.gla_chunk_fwd_varlen_gated.restype = _i
-            L.gla_chunk_fwd_gated.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp]
+            L.gla_chunk_fwd_gated.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _i, _i, _vp, _vp,
+                                              _vp, _sz, _vp]
             L.gla_chunk_fwd_gated.restype = _i
+            L.gla_chunk_fwd_gated_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+            L.gla_chunk_fwd_gated_workspace_size.restype = _sz
             L.gla_decode_step_gated.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _vp, _vp]
             L.gla_decode_step_gated.restype = _i
             L.gla_chunk_fwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
@@ -267,8 +270,12 @@ def gla_chunk_fwd_varlen(q, k, v, log_lambda, cu_seqlens, state_pool, slots=None
     return o
 
 
+def gla_chunk_fwd_gated_workspace_size(B, T, H, dk, dv, chunk=128, dtype=GLA_BF16) -> int:
+    return int(lib().gla_chunk_fwd_gated_workspace_size(B, T, H, dk, dv, chunk, dtype))
+
+
 def gla_chunk_fwd_gated(q, k, v, g, h0=None, scale=None, chunk=128, *, o=None, hT=None, want_hT=True,
-                        stream=None):
+                        workspace=None, stream=None):
     """Chunked forward with a per-token decay: g [B,T,H] fp32 natural-log
     decays (<= 0, -inf clears the state); q, k, v, h0 as gla_chunk_fwd.
     Returns (o, hT)."""
@@ -281,9 +288,14 @@ def gla_chunk_fwd_gated(q, k, v, g, h0=None, scale=None, chunk=128, *, o=None, h
         o = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
     if hT is None and want_hT:
         hT = torch.empty((B, H, dk, dv), dtype=torch.float32, device=q.device)
+    dt = _dtype_code(q)
+    ws_need = gla_chunk_fwd_gated_workspace_size(B, T, H, dk, dv, chunk, dt)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib().gla_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _f32(g, (B, T, H), "g"), _f32(h0, (B, H, dk, dv), "h0"),
                                    float(scale), B, T, H, dk, dv,
-                                   int(chunk), _dtype_code(q), _ptr(o), _ptr(hT), _stream(stream))
+                                   int(chunk), dt, _ptr(o), _ptr(hT), _ptr(workspace), ws_bytes, _stream(stream))
     _raise_on(st, "gla_chunk_fwd_gated")
     return o, hT
 

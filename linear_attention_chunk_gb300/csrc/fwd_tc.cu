@@ -760,8 +760,8 @@ cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, co
 
 }  // namespace
 
-size_t fwd_tc_workspace_size(int B, int T, int H, int chunk) {
-    return seg_workspace_bytes(B, H, plan_segments(B, T, H, chunk));
+size_t fwd_tc_workspace_size(int B, int T, int H, int chunk, bool gated) {
+    return seg_workspace_bytes(B, H, plan_segments(B, T, H, chunk), gated);
 }
 
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
@@ -775,13 +775,11 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     const int nck = (p.T + p.chunk - 1) / p.chunk;
     FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, nck, 1, nck, p.B * p.H, 0, p.status,
                 nullptr, nullptr, 0, nullptr, p.g};
-    // The gated form runs one chain per (b, h): its segment states would need
-    // the gates too.
-    if (p.g) return launch_chunk_kernel<false, true>(mq, mk, mv, mo, a, p.B, s, launches);
     // Few (b, h) pairs and a long sequence: split each sequence into segments
     // that run in parallel, when the caller gave the workspace for it.
+    const bool gated = p.g != nullptr;
     const SegPlan plan = plan_segments(p.B, p.T, p.H, p.chunk);
-    if (plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan)) {
+    if (plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan, gated)) {
         float *S_in = nullptr;
         if ((e = launch_seg_prologue(p, plan, &S_in, s, launches)) != cudaSuccess) return e;
         a.h0 = S_in;
@@ -789,7 +787,8 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
         a.seg_chunks = plan.seg_chunks;
         a.h0_seg_stride = (size_t)p.B * p.H * kDk * kDv;
     }
-    return launch_chunk_kernel<false>(mq, mk, mv, mo, a, p.B, s, launches);
+    return gated ? launch_chunk_kernel<false, true>(mq, mk, mv, mo, a, p.B, s, launches)
+                 : launch_chunk_kernel<false>(mq, mk, mv, mo, a, p.B, s, launches);
 }
 
 // Variable-length forward: one CTA per (sequence, head, dv half) over the

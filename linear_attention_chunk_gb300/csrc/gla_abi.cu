@@ -197,13 +197,14 @@ gla_status gla_chunk_fwd(const void *q, const void *k, const void *v, const floa
 
 gla_status gla_chunk_fwd_gated(const void *q, const void *k, const void *v, const float *g, const float *h0,
                                float scale, int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype,
-                               void *o, float *hT, void *stream) {
+                               void *o, float *hT, void *workspace, size_t workspace_bytes, void *stream) {
     t_err[0] = 0;
     t_launches = 0;
     gla_status st = check_chunk_shape(B, T, H, dk, dv, chunk, dtype);
     if (st != GLA_OK) return st;
     OPTIONAL_PTR(h0, "h0");
     OPTIONAL_PTR(hT, "hT");
+    OPTIONAL_PTR(workspace, "workspace");
     if (B == 0 || H == 0) return GLA_OK;
     if (T > 0) {
         REQUIRE_PTR(q, "q");
@@ -222,13 +223,20 @@ gla_status gla_chunk_fwd_gated(const void *q, const void *k, const void *v, cons
         t_launches = launches;
         return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_gated(T=0)");
     }
-    FwdParams p{q, k, v, nullptr, h0, scale, B, T, H, dk, dv, chunk, o, hT, nullptr, 0, status, g};
+    FwdParams p{q, k, v, nullptr, h0, scale, B, T, H, dk, dv, chunk, o, hT,
+                workspace, workspace ? workspace_bytes : 0, status, g};
     if (dtype == GLA_BF16)
         e = launch_fwd_tc(p, s, &launches);
     else
         e = launch_fwd_simt(p, false, s, &launches);
     t_launches = launches;
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_gated launch");
+}
+
+size_t gla_chunk_fwd_gated_workspace_size(int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype) {
+    if (check_chunk_shape(B, T, H, dk, dv, chunk, dtype) != GLA_OK) return 0;
+    if (dtype != GLA_BF16) return 0;
+    return fwd_tc_workspace_size(B, T, H, chunk, true);
 }
 
 gla_status gla_decode_step_gated(const void *q, const void *k, const void *v, const float *g, float *S_inout,

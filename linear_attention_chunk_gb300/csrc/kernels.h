@@ -121,7 +121,7 @@ cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // dq and dk: the transposed-shape chunk kernel (192-wide scores, 96-wide outputs).
 cudaError_t launch_bwd_dq_tc(const BwdParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_dk_tc(const BwdParams &p, cudaStream_t s, int *launches);
-size_t fwd_tc_workspace_size(int B, int T, int H, int chunk);
+size_t fwd_tc_workspace_size(int B, int T, int H, int chunk, bool gated = false);
 
 // Sequence segmentation of the forward (seg_tc.cu): a plan, its workspace,
 // and the two launches that produce each segment's initial state.
@@ -130,7 +130,7 @@ struct SegPlan {
     int seg_chunks;  // chunks per segment (the last may be shorter)
 };
 SegPlan plan_segments(int B, int T, int H, int chunk);
-size_t seg_workspace_bytes(int B, int H, const SegPlan &p);
+size_t seg_workspace_bytes(int B, int H, const SegPlan &p, bool gated = false);
 cudaError_t launch_seg_prologue(const FwdParams &p, const SegPlan &plan, float **S_in, cudaStream_t s,
                                 int *launches);
 size_t bwd_tc_workspace_size(int B, int T, int H, int chunk);

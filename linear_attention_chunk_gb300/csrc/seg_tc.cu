@@ -15,6 +15,12 @@
 // This reads k and v of all but the last segment twice (up to 1,728 instead
 // of 1,152 bytes per head-token) in exchange for B*H*2*G CTAs instead of B*H*2.
 // Workspace: dS and S_in, each [G][B][H][96][192] fp32.
+//
+// With a per-token decay (the gated form, g [B,T,H]) the segment's decay
+// lambda^L becomes D(g) = exp(sum of the segment's g), 0 when one of its
+// gates clears the state, and the row weight of K the decay of the tokens
+// after it in the segment. The state pass also writes D(g) ([G][B][H] fp32,
+// after S_in in the workspace) for the scan.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -40,7 +46,9 @@ enum { BAR_FULL0 = 0, BAR_EMPTY0 = kStages, BAR_KREADY0 = 2 * kStages, BAR_SFULL
        kNumBars };
 constexpr uint32_t kOffBar = kStages * kStageBytes;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffMisc + 32 + 1024;
+// gated: the chunk's running log2-decays [128], then 4 + 4 reduction slots
+constexpr uint32_t kOffGate = kOffMisc + 32;
+constexpr uint32_t kSmemBytes = kOffGate + 128 * 4 + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemCols = 256;                 // the 192-column state
 constexpr uint32_t kBarK = 1;
@@ -50,7 +58,15 @@ struct SegArgs {
     float *dS;             // [G][B][H][96][192]
     int H, C, seg_chunks, BH;
     unsigned int *status;
+    const float *g;        // gated: per-token log-decays [B, T, H], else NULL
+    int T;
+    float *dseg;           // gated: the segments' decays D [G][B][H]
 };
+
+// A log-decay at or below this clears the state (exp(-80) is below fp32's
+// normal range).
+constexpr float kResetLogDecay = -80.f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 // dS of segment g < G-1 of sequence (b, h): its end state from a zero start,
 //   dS = sum_i lambda^((n-1-i) C) sum_j lambda^(C-1-j) k_ij v_ij^T
@@ -61,6 +77,11 @@ struct SegArgs {
 // between chunks: a streaming K~^T V reduction (M = 96 padded to 128,
 // N = 192), one CTA per (segment, b, h).
 // Warps: 0 TMA, 1 TMEM + MMA, 2-5 row weights on K and the final dS store.
+// kGate: the row weight of token j is the decay of the segment's tokens after
+// j, 2^(A_end - A_j) with A the running sum of log2-decays from the segment's
+// start (0 when a clearing gate lies after j), and the segment's decay D is
+// written out for the scan.
+template <bool kGate>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_seg_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const SegArgs a) {
@@ -155,20 +176,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row = quad * 32 + (uint32_t)lane;
         const uint32_t gt = (uint32_t)threadIdx.x - 64;
         const uint32_t tl = tmem + ((quad * 32) << 16);
-        const float l2 = log2_of_decay(a.log_lambda[h]);
+        const float l2 = kGate ? 0.f : log2_of_decay(a.log_lambda[h]);
         uint32_t kw = 0;
         bool ok = true;
+        // Gated: the segment's total log2-decay and its last clearing position,
+        // then a running sum carried from chunk to chunk.
+        float *gl = reinterpret_cast<float *>(sm + kOffGate);
+        float *red = gl + 128;
+        int *redz = reinterpret_cast<int *>(red + 4);
+        const float *gh = kGate ? a.g + ((size_t)b * a.T + (size_t)cbeg * C) * a.H + h : nullptr;
+        float a_end = 0.f, a_before = 0.f;
+        int z_end = -1;
+        if constexpr (kGate) {
+            float part = 0.f;
+            int zp = -1;
+            for (int t = (int)gt; t < n * C; t += kGroupThreads) {
+                const float x = gh[(size_t)t * a.H];
+                if (x > kResetLogDecay)
+                    part += x * kLog2e;
+                else
+                    zp = t;
+            }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                part += __shfl_xor_sync(0xffffffffu, part, d);
+                zp = max(zp, __shfl_xor_sync(0xffffffffu, zp, d));
+            }
+            if (lane == 0) {
+                red[quad] = part;
+                redz[quad] = zp;
+            }
+            named_sync(kBarK, kGroupThreads);
+            a_end = red[0] + red[1] + red[2] + red[3];
+            z_end = max(max(redz[0], redz[1]), max(redz[2], redz[3]));
+            if (gt == 0) a.dseg[(size_t)seg * a.BH + bh] = z_end < 0 ? exp2f(a_end) : 0.f;
+        }
         for (int c = 0; c < n; ++c) {
             const int s = c % kStages;
             if (!group_wait(bar(BAR_FULL0 + s), (c / kStages) & 1, ctl, dec, gt, kBarK, kw)) {
                 ok = false;
                 break;
             }
-            // rows past the chunk (C = 64) are never read by the MMA; keep them finite
-            const float wk = row < (uint32_t)C ? decay_pow(l2, (n - 1 - c) * C + C - 1 - (int)row) : 0.f;
+            float wk;
+            if constexpr (kGate) {
+                // the chunk's running sums: one warp scans its 128 gates
+                if (gt < 32) {
+                    float x[4], ls[4], sacc = 0.f;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int t = 4 * (int)gt + r;
+                        x[r] = t < C ? gh[(size_t)(c * C + t) * a.H] : 0.f;
+                        if (x[r] > kResetLogDecay) sacc += x[r] * kLog2e;
+                        ls[r] = sacc;
+                    }
+                    float si = sacc;
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, si, d);
+                        if ((int)gt >= d) si += y;
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) gl[4 * gt + r] = si - sacc + ls[r];
+                }
+                named_sync(kBarK, kGroupThreads);
+                const int pos = c * C + (int)row;   // position in the segment
+                wk = row < (uint32_t)C && z_end <= pos ? exp2f(a_end - (a_before + gl[row])) : 0.f;
+                a_before += gl[C - 1];
+            } else {
+                // rows past the chunk (C = 64) are never read by the MMA; keep them finite
+                wk = row < (uint32_t)C ? decay_pow(l2, (n - 1 - c) * C + C - 1 - (int)row) : 0.f;
+            }
             scale_rows<3>(sm + (uint32_t)s * kStageBytes + kStageK, row, wk);
             fence_proxy_async_smem();
-            named_sync(kBarK, kGroupThreads);
+            named_sync(kBarK, kGroupThreads);   // also: every thread is done with gl
             if (gt == 0) mbar_arrive(bar(BAR_KREADY0 + s));
         }
         if (ok && group_wait(bar(BAR_SFULL), 0, ctl, dec, gt, kBarK, kw)) {
@@ -201,24 +281,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// S_in(0) = h0 (or 0); S_in(g) = lambda^L S_in(g-1) + dS(g-1), L = seg_chunks * C.
+// S_in(0) = h0 (or 0); S_in(g) = lambda^L S_in(g-1) + dS(g-1), L = seg_chunks * C
+// (gated: D(g-1) in place of lambda^L).
 // One CTA per (b, h, slice of 1024 state entries); each thread carries one
 // float4 through the G segments.
 constexpr int kScanSlice = 1024;
 static_assert(kStates % kScanSlice == 0 && kScanSlice == 4 * 256, "scan slices");
 __global__ void __launch_bounds__(256) gla_seg_scan_kernel(const float *log_lambda, const float *h0,
                                                            const float *dS, float *S_in, int G, int H, int BH,
-                                                           int seg_tokens) {
+                                                           int seg_tokens, const float *dseg) {
     const int bh = blockIdx.x / (kStates / kScanSlice), slice = blockIdx.x % (kStates / kScanSlice);
     const int h = bh % H;
-    const float wL = decay_pow(log2_of_decay(log_lambda[h]), seg_tokens);
+    const float wL = dseg ? 0.f : decay_pow(log2_of_decay(log_lambda[h]), seg_tokens);
     const size_t off = (size_t)bh * kStates + (size_t)slice * kScanSlice + 4 * threadIdx.x;
     float4 s = h0 ? *reinterpret_cast<const float4 *>(h0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int g = 0; g < G; ++g) {
         *reinterpret_cast<float4 *>(S_in + (size_t)g * BH * kStates + off) = s;
         if (g + 1 < G) {
             const float4 x = *reinterpret_cast<const float4 *>(dS + (size_t)g * BH * kStates + off);
-            s = make_float4(fmaf(wL, s.x, x.x), fmaf(wL, s.y, x.y), fmaf(wL, s.z, x.z), fmaf(wL, s.w, x.w));
+            const float w = dseg ? dseg[(size_t)g * BH + bh] : wL;
+            s = make_float4(fmaf(w, s.x, x.x), fmaf(w, s.y, x.y), fmaf(w, s.z, x.z), fmaf(w, s.w, x.w));
         }
     }
 }
@@ -250,9 +332,10 @@ SegPlan plan_segments(int B, int T, int H, int chunk) {
     return p;
 }
 
-size_t seg_workspace_bytes(int B, int H, const SegPlan &p) {
+size_t seg_workspace_bytes(int B, int H, const SegPlan &p, bool gated) {
     if (p.nseg <= 1) return 0;
-    return 2 * (size_t)p.nseg * B * H * kStates * sizeof(float);
+    return 2 * (size_t)p.nseg * B * H * kStates * sizeof(float) +
+           (gated ? (((size_t)p.nseg * B * H * sizeof(float) + 255) & ~(size_t)255) : 0);
 }
 
 cudaError_t launch_seg_prologue(const FwdParams &p, const SegPlan &plan, float **S_in, cudaStream_t s,
@@ -263,15 +346,17 @@ cudaError_t launch_seg_prologue(const FwdParams &p, const SegPlan &plan, float *
     cudaError_t e;
     if ((e = make_token_map(&mk, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gla_seg_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto kernel = p.g ? gla_seg_state_kernel<true> : gla_seg_state_kernel<false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    SegArgs a{p.log_lambda, dS, p.H, p.chunk, plan.seg_chunks, p.B * p.H, p.status};
+    float *dseg = p.g ? *S_in + (size_t)plan.nseg * p.B * p.H * kStates : nullptr;
+    SegArgs a{p.log_lambda, dS, p.H, p.chunk, plan.seg_chunks, p.B * p.H, p.status, p.g, p.T, dseg};
     // The last segment's own contribution is never needed: G-1 segments per sequence.
-    gla_seg_state_kernel<<<(unsigned)(p.B * p.H * (plan.nseg - 1)), kThreads, kSmemBytes, s>>>(mk, mv, a);
+    kernel<<<(unsigned)(p.B * p.H * (plan.nseg - 1)), kThreads, kSmemBytes, s>>>(mk, mv, a);
     if (launches) ++*launches;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     gla_seg_scan_kernel<<<(unsigned)(p.B * p.H * (kStates / kScanSlice)), 256, 0, s>>>(
-        p.log_lambda, p.h0, dS, *S_in, plan.nseg, p.H, p.B * p.H, plan.seg_chunks * p.chunk);
+        p.log_lambda, p.h0, dS, *S_in, plan.nseg, p.H, p.B * p.H, plan.seg_chunks * p.chunk, dseg);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

@@ -253,7 +253,7 @@ def test_gated_entry_points_reject_bad_arguments(L):
                  C=128, dt=0, o=FAKE + 0x400, hT=None)
         a.update(kw)
         return L.gla_chunk_fwd_gated(a["q"], a["k"], a["v"], a["g"], a["h0"], 0.1, a["B"], a["T"], a["H"], a["dk"],
-                                     a["dv"], a["C"], a["dt"], a["o"], a["hT"], None)
+                                     a["dv"], a["C"], a["dt"], a["o"], a["hT"], a.get("ws"), 0, None)
     assert fwd(g=None) == binding.GLA_ERR_INVALID_ARG
     assert fwd(g=ODD) == binding.GLA_ERR_INVALID_ARG
     assert fwd(h0=ODD) == binding.GLA_ERR_INVALID_ARG
@@ -262,6 +262,10 @@ def test_gated_entry_points_reject_bad_arguments(L):
     assert fwd(dt=1, dv=300) == binding.GLA_ERR_UNSUPPORTED
     assert fwd(T=-1) == binding.GLA_ERR_INVALID_ARG
     assert fwd(B=0) == binding.GLA_OK
+    assert fwd(ws=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert binding.gla_chunk_fwd_gated_workspace_size(1, 65536, 16, 96, 192, 128) > \
+        binding.gla_chunk_fwd_workspace_size(1, 65536, 16, 96, 192, 128) > 0
+    assert binding.gla_chunk_fwd_gated_workspace_size(8, 2048, 16, 96, 192, 128) == 0
 
     def dec(**kw):
         a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, S=FAKE, N=4, H=16, dk=96, dv=192, dt=0, o=FAKE)

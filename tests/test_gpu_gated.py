@@ -171,3 +171,28 @@ def test_gated_varlen_matches_oracle_per_sequence(gla, C):
         ro, rh = oracle.fwd_gated(c.q[None, a:b], c.k[None, a:b], c.v[None, a:b], g[None, a:b], h0, c.scale)
         assert relerr(oh[a:b], ro[0]) <= TOL["bf16"], f"o of sequence {n} (length {b - a})"
         assert relerr(pool[c.slots[n]], rh[0]) <= TOL["bf16"], f"state of sequence {n}"
+
+
+# ---------------------------------------------------- long sequences, segmented
+@pytest.mark.parametrize("T,C", [(5120, 128), (5000, 128), (2600, 64)])
+def test_gated_segmented_matches_oracle_and_single_chain(gla, T, C):
+    """Few (b, h) and a long sequence: the forward splits it into segments
+    whose decays are the exp of their summed gates. Clearing gates sit inside
+    a segment and on a segment's first token. The result matches the oracle
+    and the single-chain run (workspace too small to split)."""
+    import torch
+    c = gen.make_case(1, T, 2, 96, 192, seed=350 + T + C, dtype="bf16", normalise_k=True, h0_std=0.1, chunk=C,
+                      gate="gla")
+    assert gla.gla_chunk_fwd_gated_workspace_size(1, T, 2, 96, 192, C) > 0
+    g = c.extra["g"].copy()
+    g[0, 1500, 0] = -np.inf
+    g[0, 8 * C, 1] = -np.inf          # the first token of the second segment when segments are 8 chunks long
+    g[0, 9 * C, 0] = -np.inf          # ... and when they are 9 chunks long
+    og, hg = run_gated(gla, c, g)
+    ro, rhT = oracle.fwd_gated(c.q, c.k, c.v, g, c.h0, c.scale)
+    assert relerr(og, ro) <= TOL["bf16"] and relerr(hg, rhT) <= TOL["bf16"]
+    d = case_to_dev(c)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    o1, h1 = gla.gla_chunk_fwd_gated(d["q"], d["k"], d["v"], f32_dev(g), d["h0"], c.scale, C, workspace=small)
+    gla.gla_check()
+    assert relerr(og, to_host(o1)) <= TOL["bf16"] and relerr(hg, to_host(h1)) <= TOL["bf16"]
