@@ -196,3 +196,79 @@ def test_gated_segmented_matches_oracle_and_single_chain(gla, T, C):
     o1, h1 = gla.gla_chunk_fwd_gated(d["q"], d["k"], d["v"], f32_dev(g), d["h0"], c.scale, C, workspace=small)
     gla.gla_check()
     assert relerr(og, to_host(o1)) <= TOL["bf16"] and relerr(hg, to_host(h1)) <= TOL["bf16"]
+
+
+def test_gated_calls_capture_and_replay_bit_exact(gla):
+    """The gated forward (split into segments), the gated packed prefill and
+    the gated serving step inside a CUDA graph replay to the bits of the same
+    calls launched eagerly."""
+    import torch
+    c = gen.make_case(1, 4096, 2, 96, 192, seed=360, normalise_k=True, h0_std=0.1, chunk=128, gate="gla")
+    d = case_to_dev(c)
+    g = f32_dev(c.extra["g"])
+    ws = torch.empty(max(gla.gla_chunk_fwd_gated_workspace_size(1, 4096, 2, 96, 192, 128), 16), dtype=torch.uint8,
+                     device="cuda")
+    vc = gen.make_varlen_case([70, 300, 5], 2, seed=361, n_slots=4)
+    vd = dict(q=to_dev(vc.q, "bf16"), k=to_dev(vc.k, "bf16"), v=to_dev(vc.v, "bf16"),
+              cu=torch.from_numpy(vc.cu_seqlens).cuda(), slots=torch.from_numpy(vc.slots).cuda())
+    vg = f32_dev(gen.log_gates(np.random.default_rng(362), (vc.q.shape[0], 2), "gla"))
+    dc = gen.make_decode_case(8, 2, 96, 192, seed=363)
+    dg = f32_dev(gen.log_gates(np.random.default_rng(364), (8, 2), "wide"))
+    dq_, dk_, dv_ = to_dev(dc.q, "bf16"), to_dev(dc.k, "bf16"), to_dev(dc.v, "bf16")
+
+    def buffers():
+        return dict(o=torch.empty_like(d["v"]), hT=torch.empty((1, 2, 96, 192), device="cuda"),
+                    vo=torch.empty_like(vd["v"]), pool=f32_dev(vc.pool), S=f32_dev(dc.S),
+                    od=torch.empty((8, 2, 192), dtype=torch.bfloat16, device="cuda"))
+
+    def step(bf, s):
+        gla.gla_chunk_fwd_gated(d["q"], d["k"], d["v"], g, d["h0"], c.scale, 128, o=bf["o"], hT=bf["hT"],
+                                workspace=ws, stream=s)
+        gla.gla_chunk_fwd_varlen_gated(vd["q"], vd["k"], vd["v"], vg, vd["cu"], bf["pool"], vd["slots"], vc.scale,
+                                       128, o=bf["vo"], stream=s)
+        gla.gla_decode_step_gated(dq_, dk_, dv_, dg, bf["S"], dc.scale, o=bf["od"], stream=s)
+
+    s = torch.cuda.Stream()
+    eager = buffers()
+    with torch.cuda.stream(s):
+        step(eager, s)
+    torch.cuda.synchronize()
+    gla.gla_check()
+    with torch.cuda.stream(s):
+        step(buffers(), s)            # warm-up outside the capture
+    torch.cuda.synchronize()
+    graphed = buffers()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(graphed, s)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        graph.replay()
+    torch.cuda.synchronize()
+    gla.gla_check()
+    for name in eager:
+        assert torch.equal(eager[name], graphed[name]), name
+
+
+def test_gated_varlen_bad_device_offsets_are_reported(gla):
+    """A decreasing packed offset is skipped on the device and reported by
+    gla_check, as in the fixed-decay prefill; the other sequences complete."""
+    import torch
+    vc = gen.make_varlen_case([100, 50, 80], 2, seed=365, n_slots=3)
+    vc.slots[:] = np.arange(3, dtype=np.int32)
+    g = gen.log_gates(np.random.default_rng(366), (vc.q.shape[0], 2), "gla")
+    bad = vc.cu_seqlens.copy()
+    bad[2] = bad[1] - 1
+    pool = f32_dev(vc.pool)
+    gla.gla_chunk_fwd_varlen_gated(to_dev(vc.q, "bf16"), to_dev(vc.k, "bf16"), to_dev(vc.v, "bf16"), f32_dev(g),
+                                   torch.from_numpy(bad).cuda(), pool, None, vc.scale, 128)
+    with pytest.raises(gla.GlaError) as ei:
+        gla.gla_check()
+    assert ei.value.status == gla.GLA_ERR_INVALID_ARG
+    ph = to_host(pool)
+    assert np.array_equal(ph[1], vc.pool[1].astype(np.float32).astype(np.float64))
+    a, b = int(bad[0]), int(bad[1])
+    _, rh = oracle.fwd_gated(vc.q[None, a:b], vc.k[None, a:b], vc.v[None, a:b], g[None, a:b],
+                             vc.pool[0][None].astype(np.float32), vc.scale)
+    assert relerr(ph[0], rh[0]) <= TOL["bf16"]
+    gla.gla_check()
