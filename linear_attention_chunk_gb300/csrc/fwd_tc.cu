@@ -83,7 +83,7 @@ constexpr uint32_t kOffOut = kOffSb + 2 * kSbBytes;  // output staging, 3 blocks
 constexpr uint32_t kOffPw = kOffOut + 3 * kBlk;      // lambda^n, n = 0..128 (+pad)
 enum { BAR_FULL0, BAR_FULL1, BAR_FULLV0, BAR_FULLV1, BAR_EMPTY0, BAR_EMPTY1, BAR_QK0, BAR_QK1, BAR_KREADY0, BAR_KREADY1,
        BAR_PREADY0, BAR_PREADY1, BAR_SBREADY, BAR_SFULL, BAR_OFULL0, BAR_OFULL1, BAR_OEMPTY0, BAR_OEMPTY1,
-       BAR_KFREE0, BAR_KFREE1, BAR_DONE, kNumBars };
+       BAR_KFREE0, BAR_KFREE1, BAR_DONE, BAR_GDEC0, BAR_GDEC1, kNumBars };
 constexpr uint32_t kOffPair = kOffPw + 132 * 4;     // pp, pr: packed decay pairs
 constexpr uint32_t kOffBar = kOffPair + 2 * 164 * 4;
 static_assert(kPairLen <= 164, "pair table stride");
@@ -95,7 +95,9 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 // positions of the last state-clearing gate, [128] float + [128] int per
 // sub-group.
 constexpr uint32_t kGateSub = 128 * 8;
-constexpr uint32_t kOffGate = kSmemUsed, kGateBytes = 2 * kGateSub;
+// ... then two floats: the decay of chunk c in slot c % 2, published by P
+// sub-group 0 (BAR_GDEC) for the E group's rescale of the state.
+constexpr uint32_t kOffGate = kSmemUsed, kGateBytes = 2 * kGateSub + 16;
 constexpr uint32_t kSmemBytesGated = kSmemBytes + kGateBytes;
 static_assert(kSmemBytesGated <= 232448, "shared memory budget (gated)");
 // A log-decay at or below this clears the state: exp(-80) is below fp32's
@@ -150,28 +152,6 @@ __device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, f
         zc[4 * lane + r] = lz[r] >= 0 ? lz[r] : (lane > 0 ? ez : -1);
     }
 }
-
-// The decay over a whole chunk from its gate values (lane l: tokens
-// 4l..4l+3, 0 past the end), reduced across the warp: exp of the summed
-// log-decays, or 0 when one of them clears the state.
-__device__ __forceinline__ float gate_chunk_decay(const float (&x)[4]) {
-    float s = 0.f;
-    int n = 0;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        if (x[r] > kResetLogDecay)
-            s += x[r] * kLog2e;
-        else
-            ++n;
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, d);
-        n += __shfl_xor_sync(0xffffffffu, n, d);
-    }
-    return n == 0 ? exp2f(s) : 0.f;
-}
-
 
 // Gated mode: one 32-column block of P for TMEM lane row i, columns
 // j0..j0+31, from the fp32 scores x (raw bits): P_ij = A_ij 2^(gi - gl[j])
@@ -506,6 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (gt < 32) {
                     gate_scan_store(gpre, (int)gt, Gl, Zc);
                     load_gates(c + 1, gpre);
+                    if (sub == 0) {
+                        // the chunk's decay for the E group's rescale of the state
+                        __syncwarp();
+                        if (gt == 0) {
+                            float *slot = reinterpret_cast<float *>(sm + kOffGate + 2 * kGateSub) + s;
+                            *slot = Zc[Cc - 1] < 0 ? exp2f(Gl[Cc - 1]) : 0.f;
+                            mbar_arrive(bar(BAR_GDEC0 + s));
+                        }
+                    }
                 }
             }
             if (!group_wait(bar(BAR_QK0 + s), (c >> 1) & 1, ctl, mydec, gt, named, kw)) break;
@@ -591,13 +580,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kw = 0;
         // Initial state: S_prev copy 0 = bf16(h0 slice), TMEM S = lambda^C0 * h0,
         // with C0 the length of the first chunk processed.
-        float eg[4];   // gated mode: the gates of the next chunk whose decay the E group needs
-        if constexpr (kGate) load_gates(0, eg);
+        // gated mode: chunk decays published by P sub-group 0, slot c % 2
+        const volatile float *dslot = reinterpret_cast<const volatile float *>(sm + kOffGate + 2 * kGateSub);
         {
-            float w0;
+            float w0 = 1.f;
             if constexpr (kGate) {
-                w0 = gate_chunk_decay(eg);
-                load_gates(1, eg);
+                if (group_wait(bar(BAR_GDEC0), 0, ctl, mydec, gt, kBarE, kw)) w0 = dslot[0];
             } else {
                 w0 = pw[kRev ? T - (nck - 1) * C : min(C, T - cbeg * C)];
             }
@@ -637,8 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float wgate = 1.f;   // gated mode: the decay of chunk c+1
             if constexpr (kGate) {
                 if (!last) {
-                    wgate = gate_chunk_decay(eg);
-                    load_gates(c + 2, eg);
+                    const int cn = c + 1;
+                    if (!group_wait(bar(BAR_GDEC0 + (cn & 1)), (cn >> 1) & 1, ctl, mydec, gt, kBarE, kw)) break;
+                    wgate = dslot[cn & 1];
                 }
             }
             if (quad < 3) {
