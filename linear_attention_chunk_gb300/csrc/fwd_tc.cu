@@ -91,13 +91,14 @@ constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, 3 x 
 constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-// Gated mode: each P sub-group's running sums of the chunk's log2-decays and
-// positions of the last state-clearing gate, [128] float + [128] int per
-// sub-group.
-constexpr uint32_t kGateSub = 128 * 8;
+// Gated mode: each P sub-group's running sums of the chunk's log2-decays,
+// positions of the last state-clearing gate and per-token decay factors,
+// [128] float + [128] int + [128] float per sub-group.
+constexpr uint32_t kGateSub = 128 * 12;
 // ... then two floats: the decay of chunk c in slot c % 2, published by P
 // sub-group 0 (BAR_GDEC) for the E group's rescale of the state.
-constexpr uint32_t kOffGate = kSmemUsed, kGateBytes = 2 * kGateSub + 16;
+constexpr uint32_t kOffGate = (kSmemUsed + 15) & ~15u, kGateBytes = 2 * kGateSub + 32;
+static_assert(kOffGate % 16 == 0, "the decay factors are read as float4");
 constexpr uint32_t kSmemBytesGated = kSmemBytes + kGateBytes;
 static_assert(kSmemBytesGated <= 232448, "shared memory budget (gated)");
 // A log-decay at or below this clears the state: exp(-80) is below fp32's
@@ -118,8 +119,9 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // log2-decay of tokens 0..t without the clearing gates, gl[t], and the
 // position of the last clearing gate among them, zc[t] (-1 if none), for
 // t < 128. The decay of tokens j+1..i is then 2^(gl[i] - gl[j]) when
-// zc[i] <= j, and 0 otherwise.
-__device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, float *gl, int *zc) {
+// zc[i] <= j, and 0 otherwise. Also each token's own decay factor, af[t] =
+// exp(x) (0 for a clearing gate).
+__device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, float *gl, int *zc, float *af) {
     float ls[4];
     int lz[4];
     float s = 0.f;
@@ -151,24 +153,38 @@ __device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, f
         gl[4 * lane + r] = es + ls[r];
         zc[4 * lane + r] = lz[r] >= 0 ? lz[r] : (lane > 0 ? ez : -1);
     }
+    float a[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r] = x[r] > kResetLogDecay ? ex2_approx(x[r] * kLog2e) : 0.f;
+    *reinterpret_cast<float4 *>(af + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
 }
 
 // Gated mode: one 32-column block of P for TMEM lane row i, columns
-// j0..j0+31, from the fp32 scores x (raw bits): P_ij = A_ij 2^(gi - gl[j])
-// for zi <= j <= i (no clearing gate among tokens j+1..i), else 0; written
-// as 16 bf16 pairs at taddr. gi = gl[i], zi = zc[i]. One hardware
-// exponential per element: a factored form, 2^(gi - gl[b]) 2^(gl[b] - gl[j])
-// with b the block's last column, measured slower.
-__device__ __forceinline__ void build_p_block_gated(uint32_t (&x)[32], int i, int j0, float gi, int zi,
-                                                    const float *gl, uint32_t taddr) {
+// j0..j0+31, from the fp32 scores x (raw bits): P_ij = A_ij d_ij with d_ij
+// the decay of tokens j+1..i, written as 16 bf16 pairs at taddr. The weights
+// are walked from the block's right end leftwards, d_i,j-1 = d_ij af[j]: a
+// clearing gate's factor 0 zeroes every column left of it. Off the diagonal
+// the walk starts from d0 = d_i,j0+31 (one exponential per row, dl = 32); in
+// the diagonal block (d0 = 0, dl = i - j0) it starts at the row's own column
+// with 1, and the columns right of it stay 0. One copy of this code serves
+// every block: the kernel's roles share the instruction cache.
+__device__ __forceinline__ void build_p_block_gated(uint32_t (&x)[32], int dl, int j0, float d0, const float *af,
+                                                    uint32_t taddr) {
+    float d = d0;
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-        const int j = j0 + e;
-        const float2 gj = *reinterpret_cast<const float2 *>(gl + j);
-        const float w0 = j <= i && j >= zi ? ex2_approx(gi - gj.x) : 0.f;
-        const float w1 = j + 1 <= i && j + 1 >= zi ? ex2_approx(gi - gj.y) : 0.f;
-        x[e >> 1] = pack_bf16x2(__uint_as_float(x[e]) * w0, __uint_as_float(x[e + 1]) * w1);
+    for (int m = 7; m >= 0; --m) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(af + j0 + 4 * m);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int r = 3; r >= 0; --r) {
+            const int e = 4 * m + r;
+            d = e == dl ? 1.f : d;
+            x[e] = __float_as_uint(__uint_as_float(x[e]) * d);
+            d *= av[r];
+        }
     }
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) x[e >> 1] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
     tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
 }
 
@@ -472,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // chunk's gates, loaded one chunk ahead into registers.
         float *Gl = reinterpret_cast<float *>(sm + kOffGate + sub * kGateSub);
         int *Zc = reinterpret_cast<int *>(sm + kOffGate + sub * kGateSub + 512);
+        float *Af = reinterpret_cast<float *>(sm + kOffGate + sub * kGateSub + 1024);
         float gpre[4];
         if constexpr (kGate) {
             if (gt < 32) load_gates(0, gpre);
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // barrier before its P-ready signal); the named barrier in the
                 // wait below publishes these sums to the sub-group.
                 if (gt < 32) {
-                    gate_scan_store(gpre, (int)gt, Gl, Zc);
+                    gate_scan_store(gpre, (int)gt, Gl, Zc, Af);
                     load_gates(c + 1, gpre);
                     if (sub == 0) {
                         // the chunk's decay for the E group's rescale of the state
@@ -548,16 +565,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b0 = (int)sub, b1 = (int)sub + 2;
                 const bool has0 = b0 < nblk && (kRev ? b0 >= diag : b0 <= diag);
                 const bool has1 = b1 < nblk && (kRev ? b1 >= diag : b1 <= diag);
-                uint32_t r0[32], r1[32];
-                if (has0) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b0, r0);
-                if (has1) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b1, r1);
-                tmem_ld_wait();
                 if constexpr (kGate) {
+                    // one block at a time through a single copy of the builder
                     const float gi = Gl[row];
                     const int zi = Zc[row];
-                    if (has0) build_p_block_gated(r0, (int)row, 32 * b0, gi, zi, Gl, tl + kColP + 16u * b0);
-                    if (has1) build_p_block_gated(r1, (int)row, 32 * b1, gi, zi, Gl, tl + kColP + 16u * b1);
+#pragma unroll 1
+                    for (int blk = b0; blk <= b1; blk += 2) {
+                        if (blk == b0 ? !has0 : !has1) continue;
+                        uint32_t x[32];
+                        tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, x);
+                        const int jr = 32 * blk + 31;   // the block's last column
+                        const bool dg = blk == diag;
+                        const float d0 = dg || zi > jr ? 0.f : ex2_approx(gi - Gl[jr]);
+                        tmem_ld_wait();
+                        build_p_block_gated(x, dg ? lane : 32, 32 * blk, d0, Af, tl + kColP + 16u * blk);
+                    }
                 } else {
+                    uint32_t r0[32], r1[32];
+                    if (has0) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b0, r0);
+                    if (has1) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b1, r1);
+                    tmem_ld_wait();
                     pack_scores(r0);
                     pack_scores(r1);
                     if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, tl + kColP + 16u * b0, pp, pr);
