@@ -581,14 +581,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         build_p_block_gated(x, dg ? lane : 32, 32 * blk, d0, Af, tl + kColP + 16u * blk);
                     }
                 } else {
-                    uint32_t r0[32], r1[32];
-                    if (has0) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b0, r0);
-                    if (has1) tmem_ld_32cols(tl + kColR + 128u * s + 32u * b1, r1);
-                    tmem_ld_wait();
-                    pack_scores(r0);
-                    pack_scores(r1);
-                    if (has0) build_p_block<kRev>(r0, (int)row - 32 * b0, tl + kColP + 16u * b0, pp, pr);
-                    if (has1) build_p_block<kRev>(r1, (int)row - 32 * b1, tl + kColP + 16u * b1, pp, pr);
+#pragma unroll 1
+                    for (int blk = b0; blk <= b1; blk += 2) {
+                        if (blk == b0 ? !has0 : !has1) continue;
+                        uint32_t x[32];
+                        tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, x);
+                        tmem_ld_wait();
+                        pack_scores(x);
+                        build_p_block<kRev>(x, (int)row - 32 * blk, tl + kColP + 16u * blk, pp, pr);
+                    }
                 }
             }
             tmem_st_wait();
@@ -664,7 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *dst = (last && last_seg && a.hT)
                                  ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
                                  : nullptr;
-                // Three 32-column blocks; the next block's TMEM load overlaps this one's work.
+                // Three 32-column blocks through one copy of the code (the roles share
+                // the instruction cache).
                 auto handle = [&](uint32_t (&r)[32], int blk) {
                     if (last) {
                         if (dst) {
@@ -681,16 +683,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st_32cols(tl + kColS + blk * 32, r);
                     }
                 };
-                uint32_t ra[32], rb[32];
-                tmem_ld_32cols(tl + kColS, ra);
-                tmem_ld_wait();
-                tmem_ld_32cols(tl + kColS + 32, rb);
-                handle(ra, 0);
-                tmem_ld_wait();
-                tmem_ld_32cols(tl + kColS + 64, ra);
-                handle(rb, 1);
-                tmem_ld_wait();
-                handle(ra, 2);
+#pragma unroll 1
+                for (int blk = 0; blk < 3; ++blk) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(tl + kColS + 32u * blk, r);
+                    tmem_ld_wait();
+                    handle(r, blk);
+                }
                 tmem_st_wait();
             }
             fence_proxy_async_smem();
@@ -726,16 +725,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pack_bf16x2(__uint_as_float(r[e + 6]) * a.scale, __uint_as_float(r[e + 7]) * a.scale));
                     }
                 };
-                uint32_t ra[32], rb[32];
-                tmem_ld_32cols(src, ra);
-                tmem_ld_wait();
-                tmem_ld_32cols(src + 32, rb);
-                handle(ra, 0);
-                tmem_ld_wait();
-                tmem_ld_32cols(src + 64, ra);
-                handle(rb, 1);
-                tmem_ld_wait();
-                handle(ra, 2);
+#pragma unroll 1
+                for (int blk = 0; blk < 3; ++blk) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(src + 32u * blk, r);
+                    tmem_ld_wait();
+                    handle(r, blk);
+                }
             }
             tc_fence_before();
             fence_proxy_async_smem();
