@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // Blocks in increasing order: P block bk lands in columns [16bk, 16bk+16),
             // inside score block bk/2, which this warp has already read (or never needs).
+#pragma unroll 1
             for (int bk = 0; bk < nblk; ++bk) {
                 const bool keep = kRev ? (bk >= diag) : (bk <= diag);
                 if (keep) {
@@ -327,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float w0 = pw[kRev ? T - (nck - 1) * C : min(C, T)];
             if (quad < 3) {
                 const float *src = a.s0 ? a.s0 + (((size_t)b * a.H + h) * kDk + row) * kDv : nullptr;
+#pragma unroll 1
                 for (int blk = 0; blk < 6; ++blk) {
                     uint32_t r[32];
 #pragma unroll
@@ -359,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (!last && quad < 3) {
                 const float wn = kRev ? pw[C] : pw[min(C, T - t0 - C)];
+#pragma unroll 1
                 for (int blk = 0; blk < 6; ++blk) {
                     uint32_t r[32];
                     tmem_ld_32cols(tl + kColS + blk * 32, r);
@@ -381,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(kBarE, kGroupThreads);
             {
                 const float wr = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+#pragma unroll 1
                 for (int blk = 0; blk < 3; ++blk) {
                     uint32_t r2[32], r1[32];
                     tmem_ld_32cols(tl + kColO2 + blk * 32, r2);
