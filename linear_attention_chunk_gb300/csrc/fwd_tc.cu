@@ -683,12 +683,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_st_32cols(tl + kColS + blk * 32, r);
                     }
                 };
-#pragma unroll 1
-                for (int blk = 0; blk < 3; ++blk) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(tl + kColS + 32u * blk, r);
+                if constexpr (C < 128) {
+                    // short chunks: the hand-off is a larger share of the chunk's
+                    // period, so the next block's TMEM load overlaps this one's work
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32cols(tl + kColS, ra);
                     tmem_ld_wait();
-                    handle(r, blk);
+                    tmem_ld_32cols(tl + kColS + 32, rb);
+                    handle(ra, 0);
+                    tmem_ld_wait();
+                    tmem_ld_32cols(tl + kColS + 64, ra);
+                    handle(rb, 1);
+                    tmem_ld_wait();
+                    handle(ra, 2);
+                } else {
+#pragma unroll 1
+                    for (int blk = 0; blk < 3; ++blk) {
+                        uint32_t r[32];
+                        tmem_ld_32cols(tl + kColS + 32u * blk, r);
+                        tmem_ld_wait();
+                        handle(r, blk);
+                    }
                 }
                 tmem_st_wait();
             }
@@ -725,12 +740,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 pack_bf16x2(__uint_as_float(r[e + 6]) * a.scale, __uint_as_float(r[e + 7]) * a.scale));
                     }
                 };
-#pragma unroll 1
-                for (int blk = 0; blk < 3; ++blk) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(src + 32u * blk, r);
+                if constexpr (C < 128) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld_32cols(src, ra);
                     tmem_ld_wait();
-                    handle(r, blk);
+                    tmem_ld_32cols(src + 32, rb);
+                    handle(ra, 0);
+                    tmem_ld_wait();
+                    tmem_ld_32cols(src + 64, ra);
+                    handle(rb, 1);
+                    tmem_ld_wait();
+                    handle(ra, 2);
+                } else {
+#pragma unroll 1
+                    for (int blk = 0; blk < 3; ++blk) {
+                        uint32_t r[32];
+                        tmem_ld_32cols(src + 32u * blk, r);
+                        tmem_ld_wait();
+                        handle(r, blk);
+                    }
                 }
             }
             tc_fence_before();

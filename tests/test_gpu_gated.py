@@ -79,6 +79,27 @@ def test_gated_fwd_bf16_clearing_gates(gla):
     check_gated(gla, c, g)
 
 
+@pytest.mark.parametrize("C", [128, 64])
+def test_gated_fwd_bf16_clears_on_block_edges(gla, C):
+    """The tensor-core kernel builds P in 32-column blocks, walking each row's
+    weights leftwards from the block's last column: clearing gates on either
+    side of a block edge, two in one block, on a chunk's last and the next
+    chunk's first token, and gates at and just above the kernel's clearing
+    threshold (a log-decay of -80, whose exp is below 1e-34)."""
+    c = gen.make_case(1, 552, 6, 96, 192, seed=334 + C, dtype="bf16", normalise_k=True, h0_std=0.1, chunk=C,
+                      gate="gla")
+    g = c.extra["g"].copy()
+    g[0, 31, 0] = -np.inf                  # a block's last column
+    g[0, 32, 1] = -np.inf                  # the next block's first column
+    g[0, 191:193, 2] = -np.inf             # both sides of an edge
+    g[0, 352, 3] = -80.0                   # at the threshold
+    g[0, 356, 3] = -79.0                   # just above it: a strong decay
+    g[0, 389, 4] = -np.inf                 # two clears in one block
+    g[0, 404, 4] = -np.inf
+    g[0, 511:513, 5] = -np.inf             # a chunk's last and the next one's first token
+    check_gated(gla, c, g)
+
+
 def test_gated_fwd_bf16_strong_decays(gla):
     c = gen.make_case(1, 400, 4, 96, 192, seed=332, dtype="bf16", h0_std=0.1, chunk=64, gate="wide")
     check_gated(gla, c, c.extra["g"])
