@@ -33,6 +33,15 @@
 //               chunk's Q~ S, S <- lambda^C' S in TMEM, hT at the end) and the
 //               output epilogue (O * scale -> bf16 -> smem -> TMA store)
 //
+// Gated mode (kGate, a per-token log-decay g in place of log lambda): every
+// power of lambda becomes the decay of a run of tokens. The first warp of
+// each P sub-group loads its chunk's gates one chunk ahead and scans them
+// into running log2-sums, last-clear positions and per-token factors exp(g);
+// P's weights are walked along the factors block by block, and sub-group 0
+// publishes the chunk's total decay for the E group's rescale of the state.
+// The hot per-block loops run one copy of their code: the roles share the
+// instruction cache, and the gated kernel was bound by instruction fetch.
+//
 // TMEM (512 columns): R0, R1 = [0,128), [128,256) hold A = Q K^T of chunk c
 // in R[c%2], then that chunk's O (first 96 columns); S = [256,352) fp32;
 // P = [352,416) bf16 pairs (A operand of P V); Q~ = [416,464) bf16 pairs (A
@@ -559,14 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // P = bf16((Q K^T) .* D) for this sub-group's blocks on the kept side of the
-            // diagonal (at most two per warp; both TMEM loads are issued before one wait).
+            // diagonal (at most two per warp), one block at a time through one copy of the code.
             // Tokens past the end of a ragged chunk have zero q and k, so A is zero there.
             {
                 const int b0 = (int)sub, b1 = (int)sub + 2;
                 const bool has0 = b0 < nblk && (kRev ? b0 >= diag : b0 <= diag);
                 const bool has1 = b1 < nblk && (kRev ? b1 >= diag : b1 <= diag);
                 if constexpr (kGate) {
-                    // one block at a time through a single copy of the builder
                     const float gi = Gl[row];
                     const int zi = Zc[row];
 #pragma unroll 1
@@ -665,8 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *dst = (last && last_seg && a.hT)
                                  ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
                                  : nullptr;
-                // Three 32-column blocks through one copy of the code (the roles share
-                // the instruction cache).
+                // Three 32-column blocks through one copy of the code at C = 128 (the
+                // roles share the instruction cache).
                 auto handle = [&](uint32_t (&r)[32], int blk) {
                     if (last) {
                         if (dst) {
