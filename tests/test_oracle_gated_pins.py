@@ -17,7 +17,9 @@ decay, a transposed state) fails at least one of them:
     fresh call over the rest of the sequence;
   - split-call invariance;
   - the final state in closed form from cumulative sums of g;
-  - one decode step equals the forward at T = 1;
+  - one decode step equals the forward at T = 1, and a prefill followed by
+    decode steps equals one longer prefill;
+  - linearity in (v, h0) jointly;
   - O11: central differences of L = sum <do, o> + <dhT, hT> for every
     gradient including the gate's (a sign slip in dg, the gate of t used at
     t+1, a dh0 without its decay fail these); a constant gate reproduces the
@@ -155,6 +157,39 @@ def test_decode_step_is_forward_at_T1():
     B, _, H, dk = q.shape
     od, S = oracle.decode_gated(q[:, 0], k[:, 0], v[:, 0], g[:, 0], h0, 0.6)
     assert rel(od, o[:, 0]) < 1e-14 and rel(S, hT) < 1e-14
+
+
+def test_linear_in_v_and_h0():
+    """For fixed q, k and g the outputs and the final state are linear in
+    (v, h0) jointly: a term that does not scale with them (a bias, a gate
+    applied to k v^T twice, a squared state) breaks this."""
+    q, k, v, g, h0 = case(9, T=37, kind="gla")
+    rng = np.random.default_rng(4109)
+    v2 = rng.standard_normal(v.shape)
+    h2 = rng.standard_normal(h0.shape)
+    a, b = 0.7, -1.3
+    o1, s1 = oracle.fwd_gated(q, k, v, g, h0, 0.5)
+    o2, s2 = oracle.fwd_gated(q, k, v2, g, h2, 0.5)
+    o3, s3 = oracle.fwd_gated(q, k, a * v + b * v2, g, a * h0 + b * h2, 0.5)
+    assert rel(o3, a * o1 + b * o2) < 1e-12 and rel(s3, a * s1 + b * s2) < 1e-12
+
+
+def test_prefill_then_decode_equals_longer_prefill():
+    """A prefill over T tokens followed by decode steps over the next ones
+    gives the outputs and state of one prefill over all of them, clearing
+    gates in both parts included."""
+    q, k, v, g, h0 = case(10, T=24, kind="gla")
+    g = g.copy()
+    g[0, 5, 1] = -np.inf
+    g[1, 21, 2] = -np.inf                            # inside the decoded tail
+    t1 = 18
+    o, hT = oracle.fwd_gated(q, k, v, g, h0, 0.3)
+    op, S = oracle.fwd_gated(q[:, :t1], k[:, :t1], v[:, :t1], g[:, :t1], h0, 0.3)
+    outs = [op]
+    for t in range(t1, q.shape[1]):
+        ot, S = oracle.decode_gated(q[:, t], k[:, t], v[:, t], g[:, t], S, 0.3)
+        outs.append(ot[:, None])
+    assert rel(np.concatenate(outs, axis=1), o) < 1e-12 and rel(S, hT) < 1e-12
 
 
 # ------------------------------------------------------------- O11: backward
