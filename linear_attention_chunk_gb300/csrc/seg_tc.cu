@@ -38,10 +38,14 @@ using namespace tc;
 constexpr int kDk = 96, kDv = 192;
 constexpr int kStates = kDk * kDv;                  // floats per (b, h) state
 constexpr int kThreads = 192;
-constexpr int kStages = 2;
-constexpr uint32_t kStageK = 0;                     // 4 blocks (the 4th stays zero: dk pad to 128)
-constexpr uint32_t kStageV = 4 * kBlk;              // 6 blocks: all 192 dv columns
-constexpr uint32_t kStageBytes = 10 * kBlk;         // 80 KB
+constexpr int kStages = 3;
+// K's three dk blocks, then V's six. The state MMA runs at M = 128 over dk =
+// 96: its fourth M block reads V's first block in place of a zero pad. Those
+// products land only in TMEM lanes 96..127, which nothing reads, and without
+// the pad three stages fit.
+constexpr uint32_t kStageK = 0;                     // 3 blocks
+constexpr uint32_t kStageV = 3 * kBlk;              // 6 blocks: all 192 dv columns
+constexpr uint32_t kStageBytes = 9 * kBlk;          // 72 KB
 enum { BAR_FULL0 = 0, BAR_EMPTY0 = kStages, BAR_KREADY0 = 2 * kStages, BAR_SFULL = 3 * kStages, BAR_DONE,
        kNumBars };
 constexpr uint32_t kOffBar = kStages * kStageBytes;
@@ -74,8 +78,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // the sequence's end, and its dS is never needed). The decay of the later
 // chunks is folded into the row weight of K, lambda^((n-1-i) C + C-1-j), so
 // the state accumulates in TMEM over the whole segment with no rescale
-// between chunks: a streaming K~^T V reduction (M = 96 padded to 128,
-// N = 192), one CTA per (segment, b, h).
+// between chunks: a streaming K~^T V reduction (M = 96 run as 128, N = 192)
+// through a three-stage ring, one CTA per (segment, b, h).
 // Warps: 0 TMA, 1 TMEM + MMA, 2-5 row weights on K and the final dS store.
 // kGate: the row weight of token j is the decay of the segment's tokens after
 // j, 2^(A_end - A_j) with A the running sum of log2-decays from the segment's
@@ -111,11 +115,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
-    for (uint32_t i = threadIdx.x; i < kStages * (kBlk / 16); i += kThreads) {
-        const uint32_t s = i / (kBlk / 16), o = (i % (kBlk / 16)) * 16;
-        *reinterpret_cast<uint4 *>(sm + s * kStageBytes + kStageK + 3 * kBlk + o) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
