@@ -119,13 +119,21 @@ def fwd_work(B, T, with_h0, with_hT, C=CHUNK):
 
 
 def bwd_work(B, T, with_h0, with_dhT, with_dh0, C=CHUNK):
+    """Algorithmic bytes and tensor FLOPs of one gla_chunk_bwd call.
+    Bytes: q, k, v, do read once and dq, dk, dv written once (1,920 B per
+    head-token at bf16) plus the states. FLOPs, full tiles, per head-token:
+    the two scores dO V^T (2 C dv, shared by dq and dk) and Q K^T (2 C dk),
+    the three intra products dP K, dP^T Q (2 C dk each) and P^T dO (2 C dv),
+    and five state-sized products (dO S^T, V G^T, K G, the recomputed K^T V
+    and the gradient update Q^T dO; 2 dk dv each): 356,352 at C = 128. The
+    launches issue more (each of the dq and dk kernels forms dO V^T, and both
+    dv-half CTAs of a head form Q K^T): `issued` counts those."""
     ht = B * H * T
-    bytes_ = ht * (4 * DK * 2 + 3 * DV * 2 + DV * 2) + \
+    bytes_ = ht * (4 * DK * 2 + 3 * DV * 2) + \
         B * H * STATE_BYTES * (int(with_h0) + int(with_dhT) + int(with_dh0))
-    # dq chain: dO V^T (C*DV), dP K (C*DK), dO S^T (DK*DV), state K^T V (DK*DV)  [x2 per MAC]
-    # dk/dv chain: QK^T, dO V^T, dP^T Q, P^T dO, V G^T, K G, Q^T dO
-    macs = (C * DV + C * DK + 2 * DK * DV) + (C * DK + C * DV + C * DK + C * DV + 3 * DK * DV)
-    return bytes_, 2 * ht * macs
+    flops = ht * (2 * 2 * C * DV + 3 * 2 * C * DK + 5 * 2 * DK * DV)
+    issued = flops + ht * (2 * C * DV + 2 * C * DK)
+    return bytes_, flops, issued
 
 
 def decode_work(N):
@@ -279,6 +287,16 @@ def time_steps(step_fns, K, W, dist, stream, graph=None):
 GRAPH = True
 
 
+def headline_config(world, B=8, T=2048):
+    """The config of the headline line (the layer forward); the reference arm
+    reports the same dict."""
+    bytes_ = fwd_work(B, T, False, True)[0]
+    return {"workload": f"layer_fwd_bf16_B{B}_H16_T{T}", "B": B, "T": T, "H": H, "dk": DK, "dv": DV,
+            "chunk": CHUNK, "h0": "none", "hT": "written",
+            "l2": f"inputs larger than L2 ({bytes_ / 1e6:.0f} MB per step), no flush",
+            "parallelism": f"replicas x{world} (independent batches)"}
+
+
 def bench_fwd(args, dist, device, stream, peaks, sampler):
     import torch
     import linear_attention_chunk_gb300 as gla
@@ -306,8 +324,7 @@ def bench_fwd(args, dist, device, stream, peaks, sampler):
     traffic, traffic_wl = committed_traffic("gla_fwd_tc")
     res = {
         "value": tokens * args.steps / (total * 1e-3), "unit": "tokens/s", "ms_per_step": total / args.steps,
-        "config": {"workload": c.name, "B": B, "T": T, "H": H, "dk": DK, "dv": DV, "chunk": CHUNK,
-                   "h0": "none", "hT": "written", "l2": f"inputs larger than L2 ({bytes_ / 1e6:.0f} MB per step), no flush"},
+        "config": headline_config(dist.world, B, T),
         "roofline": {"bound": "hbm", "achieved": ach_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ach_gbs / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": bytes_, "avg_launch_ms": avg_ms,
@@ -495,6 +512,17 @@ E2E_OVERLAP = ("inputs copied in on their own stream while the previous step com
                "read back on a third stream while the next one computes (device buffers doubled)")
 
 
+def copy_ceiling(args, dist, device, stream, host_in, host_out, units_per_step, unit, e2e_value):
+    """The host-link bound of an e2e leg: the same harness and the same pinned
+    host buffers (one copy per tensor, in and out every step), with no kernel
+    in between. Returns the metric this allows and e2e's fraction of it."""
+    total, bi, bo = e2e_pipelined(args, dist, device, stream, host_in, host_out, lambda d_in, d_out, st: 0)
+    ceil = units_per_step * dist.world * args.steps / (total * 1e-3)
+    return {"value": ceil, "unit": unit, "frac": e2e_value / ceil, "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": total / args.steps,
+            "what": "the same pipelined copies with no kernel: pinned host -> device in, device -> pinned host out"}
+
+
 def e2e_fwd(args, dist, device, stream, c, ll):
     """Same metric through the public API with host buffers: every step
     copies q, k, v from pinned host memory, runs the forward, and reads o and
@@ -513,11 +541,15 @@ def e2e_fwd(args, dist, device, stream, c, ll):
         return gla.gla_last_launch_count()
 
     total, bi, bo = e2e_pipelined(args, dist, device, stream, host_in, host_out, compute)
-    return {"value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "overlap": E2E_OVERLAP}
+    value = B * T * dist.world * args.steps / (total * 1e-3)
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "overlap": E2E_OVERLAP,
+            "copy_ceiling": copy_ceiling(args, dist, device, stream, host_in, host_out, B * T, "tokens/s", value)}
 
 
 def bench_fwd_bwd(args, dist, device, stream, peaks, sampler):
+    """Training forward + backward (B=16, h0 ~ N(0, 0.02), dh0 written), and
+    the backward alone on the same buffers (its own CUDA-event time)."""
     import torch
     import linear_attention_chunk_gb300 as gla
     B, T = args.batch or 16, 2048
@@ -531,32 +563,61 @@ def bench_fwd_bwd(args, dist, device, stream, peaks, sampler):
     dh0 = torch.empty_like(h0)
     wsf = torch.empty(max(gla.gla_chunk_fwd_workspace_size(B, T, H, DK, DV, CHUNK), 16), dtype=torch.uint8, device=device)
     wsb = torch.empty(max(gla.gla_chunk_bwd_workspace_size(B, T, H, DK, DV, CHUNK), 16), dtype=torch.uint8, device=device)
-    t_f, t_b = [], []
+
+    def bwd():
+        gla.gla_chunk_bwd(q, k, v, ll, do, h0, None, c.scale, CHUNK, dq=dq, dk=dk, dv=dv, dh0=dh0,
+                          workspace=wsb, stream=stream)
+        return gla.gla_last_launch_count()
 
     def step():
         gla.gla_chunk_fwd(q, k, v, ll, h0, c.scale, CHUNK, o=o, hT=hT, workspace=wsf, stream=stream)
-        n = gla.gla_last_launch_count()
-        gla.gla_chunk_bwd(q, k, v, ll, do, h0, None, c.scale, CHUNK, dq=dq, dk=dk, dv=dv, dh0=dh0,
-                          workspace=wsb, stream=stream)
-        return n + gla.gla_last_launch_count()
+        return gla.gla_last_launch_count() + bwd()
 
     total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
     total = dist.max(total)
     fb, ff, _ = fwd_work(B, T, True, True)
-    bb, bf = bwd_work(B, T, True, False, True)
+    bb, bf, b_issued = bwd_work(B, T, True, False, True)
     avg_ms = statistics.mean(per)
     ach = (fb + bb) / (avg_ms * 1e-3) / 1e9
     ach_tf = (ff + bf) / (avg_ms * 1e-3) / 1e12
+    l2 = f"inputs larger than L2 ({(fb + bb) / 1e6:.0f} MB per step), no flush"
     res = {
         "value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
         "ms_per_step": total / args.steps,
         "config": {"workload": c.name, "B": B, "T": T, "H": H, "chunk": CHUNK, "h0": "N(0,0.02)", "dhT": "none",
-                   "l2": f"inputs larger than L2 ({(fb + bb) / 1e6:.0f} MB per step), no flush"},
+                   "l2": l2},
         "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ach / peaks["hbm_gbs"], "traffic": None,
-                     "algorithmic_bytes_per_step": fb + bb, "avg_step_ms": avg_ms, "peak_source": peaks["source"]},
+                     "algorithmic_bytes_per_step": fb + bb, "avg_step_ms": avg_ms, "peak_source": peaks["source"],
+                     "bytes_per_head_token": "fwd 1,152 + bwd 1,920, plus states"},
         "tensor": {"achieved": ach_tf, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                   "frac": ach_tf / peaks["bf16_tflops_sustained"], "flops_per_step": ff + bf},
+                   "frac": ach_tf / peaks["bf16_tflops_sustained"], "flops_per_step": ff + bf,
+                   "flops_per_head_token": "fwd 147,456 + bwd 356,352 (full tiles)",
+                   "issued_flops_per_step": ff + b_issued, "peak_source": peaks["source"]},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+
+    total, per, win, launches = time_steps(bwd, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    avg_ms = statistics.mean(per)
+    ach = bb / (avg_ms * 1e-3) / 1e9
+    ach_tf = bf / (avg_ms * 1e-3) / 1e12
+    traffic, _ = committed_traffic("gla_chunk_bwd")   # dq + dk + dv launches of one B=16 call
+    res["bwd"] = {
+        "value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+        "ms_per_step": total / args.steps,
+        "config": {"workload": f"train_bwd_bf16_B{B}_H16_T{T}", "B": B, "T": T, "H": H, "chunk": CHUNK,
+                   "h0": "N(0,0.02)", "dhT": "none", "dh0": "written",
+                   "l2": f"inputs larger than L2 ({bb / 1e6:.0f} MB per call), no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": traffic * B / 16 if traffic is not None else None,
+                     "algorithmic_bytes_per_call": bb, "avg_call_ms": avg_ms,
+                     "launches_per_call": launches // max(args.steps, 1), "peak_source": peaks["source"],
+                     "note": "one call = the dq, dk and dv launches side by side on forked streams"},
+        "tensor": {"achieved": ach_tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                   "frac": ach_tf / peaks["bf16_tflops"], "flops_per_call": bf, "issued_flops_per_call": b_issued,
+                   "peak_source": peaks["source"]},
         "gpu_launches": launches,
         "clocks": sampler.summary(*win) if sampler else None,
     }
@@ -814,8 +875,9 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
 
     total, per, win, launches = time_steps(step3, args.steps, args.warmup, dist, stream)
     total = dist.max(total)
-    # q, k, v, g in, z out and hT; plus the epilogue's own pass over o (written, then read as z's
-    # input), q, k and v again: what the two launches move
+    # Algorithmic bytes of the call: q, k, v, g in, z out and hT. The two launches also move
+    # the epilogue's own pass (o written as z, then read back with q, k and v again): reported
+    # beside it, not counted as work.
     bytes3 = B * T * H * (2 * DK * 2 + 3 * DV * 2) + B * H * STATE_BYTES
     bytes3_moved = bytes3 + B * T * H * (2 * DK * 2 + 2 * DV * 2 + DV * 2)
     avg_ms = statistics.mean(per)
@@ -825,11 +887,11 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
         "config": {"workload": f"layer_fwd_mixer_bf16_B{B}_H16_T{T}_C{CHUNK}", "B": B, "T": T, "H": H,
                    "epilogue": "in place over z after the forward (two launches)",
                    "l2": f"inputs larger than L2 ({bytes3 / 1e6:.0f} MB per step), no flush"},
-        "roofline": {"bound": "hbm", "achieved": bytes3_moved / (avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": bytes3_moved / (avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                     "traffic": None, "algorithmic_bytes_per_launch": bytes3_moved / 2,
-                     "avg_launch_ms": avg_ms / 2, "peak_source": peaks["source"],
-                     "note": "two launches per step; bytes are those both launches move"},
+        "roofline": {"bound": "hbm", "achieved": bytes3 / (avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": bytes3 / (avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": None, "algorithmic_bytes_per_call": bytes3, "avg_call_ms": avg_ms,
+                     "bytes_moved_by_both_launches": bytes3_moved, "peak_source": peaks["source"],
+                     "note": "one call = the forward, then the epilogue in place over z"},
         "gpu_launches": launches,
         "clocks": sampler.summary(*win) if sampler else None,
     }
@@ -936,8 +998,10 @@ def e2e_decode(args, dist, device, stream, toks, states, ll, scale, N, L):
         return n
 
     total, bi, bo = e2e_pipelined(args, dist, device, stream, host_in, host_out, compute)
-    return {"value": N * dist.world * args.steps / (total * 1e-3), "unit": "seq-steps/s",
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "overlap": E2E_OVERLAP}
+    value = N * dist.world * args.steps / (total * 1e-3)
+    return {"value": value, "unit": "seq-steps/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "overlap": E2E_OVERLAP,
+            "copy_ceiling": copy_ceiling(args, dist, device, stream, host_in, host_out, N, "seq-steps/s", value)}
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -1070,10 +1134,9 @@ def run_reference(args, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "layer_fwd_bf16_B8_H16_T2048_C128", "B": 8, "T": 2048, "H": H, "dk": DK,
-                   "dv": DV, "chunk": CHUNK, "parallelism": "host threads over (b, h)"},
+        "config": headline_config(dist.world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nt, "kind": "oracle",
-                         "sample": f"per step: {sample}"},
+                         "sample": f"per step: {sample}; tokens/s counts the sampled chains' tokens"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -1082,13 +1145,35 @@ def run_reference(args, dist):
 
 
 # ----------------------------------------------------------------- main
+def summary_line(key, res):
+    """One human-readable line per mode (stderr), nested rows included."""
+    def one(name, r):
+        rf = r.get("roofline") or {}
+        tn = r.get("tensor") or {}
+        parts = [f"{name}: {r['value']:.4g} {r['unit']}", f"{r['ms_per_step']:.4f} ms/step"]
+        if rf:
+            parts.append(f"HBM {rf['achieved']:.0f} GB/s = {rf['frac']:.3f} of {rf['peak']:.0f}")
+        if tn:
+            parts.append(f"tensor {tn['achieved']:.0f} TFLOP/s = {tn['frac']:.3f} of {tn['peak']:.0f}")
+        if r.get("e2e"):
+            parts.append(f"e2e {r['e2e']['value']:.4g} {r['e2e']['unit']}")
+        return "[bench] " + ", ".join(parts)
+    lines = [one(key, res)]
+    for sub in ("standalone", "fwd_mixer", "chunk64", "step", "long", "single_chain"):
+        if isinstance(res.get(sub), dict) and "value" in res[sub]:
+            lines.append(one(f"{key}.{sub}", res[sub]))
+            if isinstance(res[sub].get("single_chain"), dict):
+                lines.append(one(f"{key}.{sub}.single_chain", res[sub]["single_chain"]))
+    return "\n".join(lines)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("gla", "reference"), default="gla")
-    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "decode", "long", "varlen", "mixer", "conv",
+    ap.add_argument("--mode", choices=("all", "fwd", "fwd_bwd", "bwd", "decode", "long", "varlen", "mixer", "conv",
                                        "gated"),
                     default="all")
     ap.add_argument("--batch", type=int, default=0, help="override B of the fwd / fwd_bwd workloads (profiling)")
@@ -1127,8 +1212,11 @@ def main(argv=None):
     try:
         if args.mode in ("all", "fwd"):
             results["fwd"] = bench_fwd(args, dist, device, stream, peaks, sampler)
-        if args.mode in ("all", "fwd_bwd"):
-            results["fwd_bwd"] = bench_fwd_bwd(args, dist, device, stream, peaks, sampler)
+        if args.mode in ("all", "fwd_bwd", "bwd"):
+            fb = bench_fwd_bwd(args, dist, device, stream, peaks, sampler)
+            results["bwd"] = fb.pop("bwd")
+            if args.mode != "bwd":
+                results["fwd_bwd"] = fb
         if args.mode in ("all", "decode"):
             results["decode"] = bench_decode(args, dist, device, stream, peaks, sampler)
         if args.mode in ("all", "long"):
@@ -1173,6 +1261,8 @@ def main(argv=None):
             if k in line["modes"]:
                 line["modes"][k]["cpu_baseline"] = v
     if dist.rank == 0:
+        for key, res in results.items():
+            log(summary_line(key, res))
         print(json.dumps(line), flush=True)
     dist.close()
     return 0

@@ -120,9 +120,12 @@ size_t gla_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int chu
  * exits. It never calls cudaMalloc, cudaFree or any allocating routine.
  *
  * Arguments, layouts and results are those of gla_chunk_fwd (without the
- * workspace). A shape whose segmentation would need more scratch than the
- * array holds is rejected with GLA_ERR_WORKSPACE (see gla_last_error); no
- * launch happens then.
+ * workspace). The segment plan needs at most 2 x SMs x dk x dv x 4 bytes
+ * (22.4 MB on the GB300's 152 SMs), so the array covers every shape on a GPU
+ * with up to 170 SMs. Should a plan ever need more, the call runs the
+ * unsegmented forward (one chain per (b, h), as gla_chunk_fwd does without a
+ * workspace): slower on few long sequences, the same result, still no
+ * allocation.
  *
  * - The first call on a device that needs scratch looks up the array's
  *   device address (cudaGetSymbolAddress). Make that first call before any

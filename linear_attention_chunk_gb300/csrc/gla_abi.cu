@@ -150,6 +150,11 @@ void set_error_detail(const char *fmt, ...) {
     va_end(ap);
 }
 
+void reset_call_state() {
+    t_err[0] = 0;
+    t_launches = 0;
+}
+
 }  // namespace gla
 
 using namespace gla;

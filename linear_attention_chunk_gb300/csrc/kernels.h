@@ -137,5 +137,7 @@ size_t bwd_tc_workspace_size(int B, int T, int H, int chunk);
 
 // Per-thread error detail, set by the launchers on failure.
 void set_error_detail(const char *fmt, ...);
+// Clears this thread's error detail and launch count (the start of a call).
+void reset_call_state();
 
 }  // namespace gla

@@ -22,8 +22,11 @@
 namespace {
 
 // Scratch of the segmented forward: per-segment local end states and
-// per-segment initial states, 2 x segments x B x H x 73,728 bytes. The
-// segment plan keeps this under 23 MB on GPUs with up to 160 SMs.
+// per-segment initial states, 2 x segments x B x H x dk x dv x 4 bytes. The
+// segment plan splits only when B x H x 2 CTAs leave the GPU under-filled,
+// and keeps segments x B x H at or below the SM count, so the scratch is at
+// most 2 x SMs x 73,728 bytes: 22.4 MB on the GB300's 152 SMs, and within
+// this 24 MiB array on any GPU with up to 170 SMs.
 constexpr size_t kNoallocScratchBytes = 24u << 20;   // 24 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -65,19 +68,17 @@ extern "C" gla_status gla_chunk_fwd_noalloc(const void *q, const void *k, const 
                                             const float *log_lambda, const float *h0, float scale, int B,
                                             int T, int H, int dk, int dv, int chunk, gla_dtype dtype, void *o,
                                             float *hT, void *stream) {
+    // No launch has happened yet: a failure below reports none.
+    gla::reset_call_state();
     const size_t need = gla_chunk_fwd_workspace_size(B, T, H, dk, dv, chunk, dtype);
-    if (need > kNoallocScratchBytes) {
-        gla::set_error_detail(
-            "gla_chunk_fwd_noalloc: this shape needs %zu bytes of scratch, more than the built-in %zu; "
-            "use gla_chunk_fwd with a caller-provided workspace",
-            need, kNoallocScratchBytes);
-        return GLA_ERR_WORKSPACE;
-    }
+    // A segment plan larger than the array (only possible on a GPU with more
+    // than 170 SMs) falls back to one chain per (b, h), which needs no
+    // scratch: slower, but the same result, and still no allocation.
     void *scratch = nullptr;
-    if (need > 0) {
+    if (need > 0 && need <= kNoallocScratchBytes) {
         const gla_status st = scratch_address(&scratch);
         if (st != GLA_OK) return st;
     }
     return gla_chunk_fwd(q, k, v, log_lambda, h0, scale, B, T, H, dk, dv, chunk, dtype, o, hT, scratch,
-                         need > 0 ? kNoallocScratchBytes : 0, stream);
+                         scratch ? kNoallocScratchBytes : 0, stream);
 }

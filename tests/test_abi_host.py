@@ -277,3 +277,23 @@ def test_gated_entry_points_reject_bad_arguments(L):
     assert dec(S=None) == binding.GLA_ERR_INVALID_ARG
     assert dec(dk=64) == binding.GLA_ERR_UNSUPPORTED
     assert dec(N=0) == binding.GLA_OK
+
+
+def test_noalloc_reports_no_launch_when_it_fails(L):
+    """A rejected gla_chunk_fwd_noalloc call launches nothing, and
+    gla_last_launch_count says so (it never carries an earlier call's count)."""
+    def noalloc(chunk=128, T=256, H=1):
+        return L.gla_chunk_fwd_noalloc(FAKE, FAKE, FAKE, FAKE, None, 0.1, 1, T, H, 96, 192, chunk, 0, FAKE, None,
+                                       None)
+    assert noalloc(chunk=100) == binding.GLA_ERR_UNSUPPORTED
+    assert L.gla_last_launch_count() == 0
+    assert "chunk 100" in L.gla_last_error().decode()
+    # A shape that is split into segments looks up the scratch array's device
+    # address first; without a device that lookup fails, before any launch.
+    # (Skipped where a GPU is visible: the fake pointers must never reach a kernel.)
+    from conftest import gpu_available
+    if not gpu_available():
+        assert binding.gla_chunk_fwd_workspace_size(1, 8192, 4, 96, 192, 128) > 0
+        assert noalloc(T=8192, H=4) == binding.GLA_ERR_CUDA
+        assert L.gla_last_launch_count() == 0
+        assert "noalloc" in L.gla_last_error().decode()

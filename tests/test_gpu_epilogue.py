@@ -170,3 +170,35 @@ def test_forward_epilogue_full_size_sampled_heads(gla):
                           "log_lambda": c.log_lambda[h:h + 1]})
         ref, _, kappa = fused_reference(one, sl(g), aug[h:h + 1], nw[h:h + 1], 1e-6)
         check_fused(zh[b:b + 1, :, h:h + 1], ref, kappa)
+
+
+def test_standalone_epilogue_on_the_oracle_output_kappa106(gla):
+    """Where the widened bar of the fused forward comes from. On the page-
+    schedule case with the kappa = 106 row, the standalone epilogue is fed the
+    oracle's own forward output o (double), so the forward kernel's error is
+    out of the picture:
+      - bf16 mode, o rounded to bf16: the GPU result equals the oracle's
+        epilogue of the same bf16 o within the plain bar (the kernel's own
+        error), yet is off from the exact z by about 2.8 % of max|z| on the
+        kappa = 106 row: rounding o to bf16 alone costs that much there;
+      - fp32 mode, o in fp32: the plain fp32 bar (1e-4) against the exact z,
+        on every row including kappa = 106."""
+    lam = gen.decay_page_schedule(16)
+    c, g, aug, nw = fused_case(1, 260, 16, 630, lam=lam)
+    ref, _, kappa = fused_reference(c, g, aug, nw, 1e-5)
+    assert kappa.max() > 100
+    o, _ = oracle.fwd_recurrent(c.q, c.k, c.v, c.log_lambda, None, c.scale)
+    ob = gen.bf16_round(o)
+    z = gla.gla_mixer_epilogue(to_dev(ob, "bf16"), to_dev(c.q, "bf16"), to_dev(c.k, "bf16"), to_dev(c.v, "bf16"),
+                               to_dev(g, "bf16"), f32_dev(aug), f32_dev(nw), 1e-5)
+    gla.gla_check()
+    zh = to_host(z)
+    assert relerr(zh, oracle.mixer_epilogue(ob, c.q, c.k, c.v, g, aug, nw, 1e-5)) <= TOL["bf16"]
+    row_err = np.abs(zh - ref).max(-1) / np.abs(ref).max()
+    assert row_err[kappa > 100].max() > TOL["bf16"]          # bf16 storage of o, amplified by kappa
+    assert row_err[kappa <= 4].max() <= TOL["bf16"]
+    check_fused(zh, ref, kappa)
+    z32 = gla.gla_mixer_epilogue(f32_dev(o), f32_dev(c.q), f32_dev(c.k), f32_dev(c.v), f32_dev(g), f32_dev(aug),
+                                 f32_dev(nw), 1e-5)
+    gla.gla_check()
+    assert relerr(to_host(z32), ref) <= TOL["fp32"]
