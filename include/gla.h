@@ -253,6 +253,34 @@ gla_status gla_decode_step_gated(const void *q, const void *k, const void *v, co
                                  gla_dtype dtype, void *o, void *stream);
 
 /*
+ * gla_chunk_bwd_gated -- gradients of L = sum_t <do_t, o_t> + <dhT, hT>
+ * through the gated form of gla_chunk_fwd_gated, the gates' own included:
+ *     G_t = dL/dS_t (through every later state update),
+ *     dq_t = scale S_t do_t,   dk_t = G_t v_t,   dv_t = G_t^T k_t,
+ *     dh0 = exp(g_0) G_0,      dg_t = exp(g_t) <G_t, S_{t-1}>   (S_{-1} = h0)
+ * ("Challenge 3": the backward passes through every serial state update of
+ * the chunked form of "Challenge 1"; the gate enters each update as its decay).
+ *   q, k, v, g, h0, scale, do, dhT, dq, dk_, dv_, dh0 as gla_chunk_bwd, with
+ *   g [B,T,H] fp32 (as gla_chunk_fwd_gated) in place of log_lambda;
+ *   dg [B,T,H] fp32 (written; 0 for a clearing gate).
+ *   workspace: at least gla_chunk_bwd_gated_workspace_size() bytes (required
+ *   when T > 0). It receives the state entering every chunk and the state
+ *   gradient leaving it, from which dg is formed chunk by chunk.
+ * GLA_BF16 runs four tensor-core launches (dq, dk, dv side by side on helper
+ * streams as in gla_chunk_bwd, then dg); GLA_FP32 the validation kernels.
+ */
+gla_status gla_chunk_bwd_gated(const void *q, const void *k, const void *v, const float *g,
+                               const float *h0, float scale, const void *do_, const float *dhT,
+                               int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype,
+                               void *dq, void *dk_, void *dv_, float *dh0, float *dg,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace gla_chunk_bwd_gated needs: two states per (b, h, chunk)
+ * (bf16: 2 x B x H x ceil(T / chunk) x 36,864 bytes; fp32: twice that). */
+size_t gla_chunk_bwd_gated_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
+                                          gla_dtype dtype);
+
+/*
  * gla_decode_step -- one recurrent step per (sequence n, head h), the
  * serving path ("Inference optimization on Trainium2": the state lives in a
  * fixed page per sequence):

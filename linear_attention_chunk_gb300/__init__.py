@@ -18,6 +18,8 @@ from .binding import (  # noqa: F401
     GlaError,
     gla_check,
     gla_chunk_bwd,
+    gla_chunk_bwd_gated,
+    gla_chunk_bwd_gated_workspace_size,
     gla_chunk_bwd_workspace_size,
     gla_chunk_fwd,
     gla_chunk_fwd_gated,

@@ -14,6 +14,7 @@ Functions:
   gla_chunk_fwd_mixer(q, k, v, g, log_lambda, ...)                        -> (z, hT)
   gla_chunk_fwd_gated(q, k, v, g, h0=None, scale=None, chunk=128, ...)    -> (o, hT)  per-token decay
   gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, ...)          -> (dq, dk, dv, dh0)
+  gla_chunk_bwd_gated(q, k, v, g, do, h0=None, dhT=None, ...)             -> (dq, dk, dv, dh0, dg)
   gla_decode_step(q, k, v, log_lambda, S, scale=None, ...)                -> o  (S updated in place)
   gla_decode_step_mixer(q, k, v, log_lambda, S, g, ...)                   -> z  (S updated in place)
   gla_decode_step_gated(q, k, v, g, S, scale=None, ...)                   -> o  (S updated in place)
@@ -41,7 +42,7 @@ GLA_BF16, GLA_FP32 = 0, 1
 # The public entry points declared in include/gla.h.
 ABI_FUNCTIONS = ("gla_chunk_fwd", "gla_chunk_fwd_workspace_size", "gla_chunk_fwd_noalloc", "gla_chunk_fwd_varlen", "gla_chunk_fwd_varlen_gated",
                  "gla_chunk_fwd_mixer", "gla_chunk_fwd_gated", "gla_chunk_fwd_gated_workspace_size", "gla_decode_step_gated", "gla_chunk_bwd",
-                 "gla_chunk_bwd_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
+                 "gla_chunk_bwd_workspace_size", "gla_chunk_bwd_gated", "gla_chunk_bwd_gated_workspace_size", "gla_decode_step", "gla_decode_step_mixer", "gla_mixer_epilogue",
                  "gla_conv1d_fwd", "gla_conv1d_varlen", "gla_conv1d_step", "gla_selftest_wait_timeout", "gla_check",
                  "gla_status_string", "gla_last_error", "gla_last_launch_count", "gla_version")
 
@@ -99,6 +100,11 @@ def lib():
             L.gla_chunk_bwd.restype = _i
             L.gla_chunk_bwd_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
             L.gla_chunk_bwd_workspace_size.restype = _sz
+            L.gla_chunk_bwd_gated.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                              _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+            L.gla_chunk_bwd_gated.restype = _i
+            L.gla_chunk_bwd_gated_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+            L.gla_chunk_bwd_gated_workspace_size.restype = _sz
             L.gla_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i, _vp, _vp]
             L.gla_decode_step.restype = _i
             L.gla_decode_step_mixer.argtypes = [_vp, _vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _f, _i, _i, _i, _i, _i,
@@ -370,6 +376,41 @@ def gla_chunk_bwd(q, k, v, log_lambda, do, h0=None, dhT=None, scale=None, chunk=
                              _stream(stream))
     _raise_on(st, "gla_chunk_bwd")
     return dq, dk, dv, dh0
+
+
+def gla_chunk_bwd_gated_workspace_size(B, T, H, dk, dv, chunk=128, dtype=GLA_BF16) -> int:
+    return int(lib().gla_chunk_bwd_gated_workspace_size(B, T, H, dk, dv, chunk, dtype))
+
+
+def gla_chunk_bwd_gated(q, k, v, g, do, h0=None, dhT=None, scale=None, chunk=128, *,
+                        dq=None, dk=None, dv=None, dh0=None, dg=None, want_dh0=True, workspace=None, stream=None):
+    """Chunked backward with a per-token decay: g [B,T,H] fp32 natural-log
+    decays as gla_chunk_fwd_gated; otherwise as gla_chunk_bwd. Returns
+    (dq, dk, dv, dh0, dg), dg [B,T,H] fp32."""
+    torch = _torch()
+    B, T, H, dk_ = q.shape
+    dv_ = v.shape[-1]
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk_)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dh0 is None and want_dh0:
+        dh0 = torch.empty((B, H, dk_, dv_), dtype=torch.float32, device=q.device)
+    if dg is None:
+        dg = torch.empty((B, T, H), dtype=torch.float32, device=q.device)
+    ws_need = gla_chunk_bwd_gated_workspace_size(B, T, H, dk_, dv_, chunk, dt)
+    if workspace is None and ws_need > 0:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gla_chunk_bwd_gated(_ptr(q), _ptr(k), _ptr(v), _f32(g, (B, T, H), "g"),
+                                   _f32(h0, (B, H, dk_, dv_), "h0"), float(scale), _ptr(do),
+                                   _f32(dhT, (B, H, dk_, dv_), "dhT"), B, T, H, dk_, dv_, int(chunk), dt,
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _f32(dh0, (B, H, dk_, dv_), "dh0"),
+                                   _f32(dg, (B, T, H), "dg"), _ptr(workspace), ws_bytes, _stream(stream))
+    _raise_on(st, "gla_chunk_bwd_gated")
+    return dq, dk, dv, dh0, dg
 
 
 def gla_decode_step(q, k, v, log_lambda, S, scale=None, *, o=None, stream=None):

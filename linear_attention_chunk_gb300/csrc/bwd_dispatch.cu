@@ -1,4 +1,5 @@
-// bwd_dispatch.cu -- bf16 backward dispatch: three tensor-core launches.
+// bwd_dispatch.cu -- bf16 backward dispatch: three tensor-core launches (four
+// with a per-token decay, whose gate gradient follows dq and dk).
 //   dv, dh0: the chunk kernel in reverse time (fwd_tc.cu)
 //   dq:      the transposed-shape chunk kernel, forward in time (bwd_tc.cu)
 //   dk:      the transposed-shape chunk kernel, reverse in time (bwd_tc.cu)
@@ -57,6 +58,30 @@ cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches) {
         if ((e = cudaEventRecord(f->ev[1 + i], f->aux[i])) != cudaSuccess) return e;
         if ((e = cudaStreamWaitEvent(s, f->ev[1 + i], 0)) != cudaSuccess) return e;
     }
+    return el;
+}
+
+// The gated backward: the same three launches in gated mode, dq and dk each
+// saving the state copy entering every chunk in its half of the workspace,
+// then the gate gradient from both sets of copies (after dq and dk, beside
+// dv, on the first helper stream).
+cudaError_t launch_bwd_gated_tc(const BwdParams &p, cudaStream_t s, int *launches) {
+    Fork *f = nullptr;
+    cudaError_t e = fork_for_device(&f);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaEventRecord(f->ev[0], s)) != cudaSuccess) return e;
+    for (int i = 0; i < 2; ++i)
+        if ((e = cudaStreamWaitEvent(f->aux[i], f->ev[0], 0)) != cudaSuccess) return e;
+    cudaError_t el = launch_bwd_dq_tc(p, f->aux[0], launches);
+    if (el == cudaSuccess) el = launch_bwd_dk_tc(p, f->aux[1], launches);
+    if (el == cudaSuccess) el = launch_bwd_dv_tc(p, s, launches);
+    if ((e = cudaEventRecord(f->ev[1], f->aux[1])) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(f->aux[0], f->ev[1], 0)) != cudaSuccess) return e;
+    if (el == cudaSuccess) el = launch_bwd_dg_tc(p, f->aux[0], launches);
+    // Join both helper streams before reporting (see launch_bwd_tc).
+    if ((e = cudaEventRecord(f->ev[2], f->aux[0])) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, f->ev[2], 0)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, f->ev[1], 0)) != cudaSuccess) return e;
     return el;
 }
 

@@ -35,6 +35,18 @@
 // intra MMA (and the copy). The MMA issuer is a non-blocking event loop.
 // Warps: 0 TMA, 1 TMEM + MMA, 2-5 make C~, 6-9 build P, 10-13 state hand-off
 // and output epilogue.
+//
+// Gated mode (kGate, the per-token decay S_t = exp(g_t) S_{t-1} + k_t v_t^T):
+// each lambda power becomes the decay of a run of tokens of the chunk,
+// lambda^(i-j) -> exp(G_i - G_j), lambda^(i+1) -> exp(G_i), lambda^(Cc-1-j)
+// -> exp(G_last - G_j), lambda^Cc -> exp(G_last), G the running sum of g. The
+// first warp of each group (C~, P, epilogue) loads its chunk's gates one
+// chunk ahead and scans them into the group's own shared-memory arrays, so
+// no group waits on another for them. P's weights are walked along the
+// per-token factors exp(g) (leftwards for dq, rightwards for dk). The
+// epilogue group also saves the bf16 copy of the state entering every chunk
+// (S_prev for dq, G / s for dk) to a workspace slot per (b, h, chunk), from
+// which the gate gradient is formed (dg_tc.cu).
 #include <cuda.h>
 
 #include "common.cuh"
@@ -70,6 +82,15 @@ constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+// Gated mode: the gate arrays of the C~ group, the P group and (double
+// buffered) the epilogue group: [128] float running log2-decays, [128] int
+// last clearing positions, [128] float factors exp(g) each.
+constexpr uint32_t kGateArr = 128 * 12;
+constexpr uint32_t kOffGate = (kSmemUsed + 15) & ~15u;
+constexpr uint32_t kSmemBytesGated = kSmemBytes + 4 * kGateArr + 16;
+static_assert(kSmemBytesGated <= 232448, "shared memory budget (gated)");
+// One saved state copy: 6 blocks of [96 rows][32 bf16], as held in shared memory.
+constexpr uint32_t kStateCopyBytes = 6 * kSbBlk;
 
 constexpr uint32_t kTmemCols = 512, kColX = 0, kColO2 = 128, kColO1 = 224, kColS = 320;
 
@@ -79,9 +100,13 @@ struct TrArgs {
     float scale, init_mul;
     int T, H, C, nck;
     unsigned int *status;
+    // Gated mode: per-token log-decays [B, T, H], and the state copies'
+    // workspace, kStateCopyBytes per (b, h, chunk) in natural chunk order.
+    const float *g;
+    unsigned char *saved;
 };
 
-template <bool kRev>
+template <bool kRev, bool kGate>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_bwd_tr_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_o,
@@ -103,6 +128,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl ctl{abort_flag, a.status};
     auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
     auto natural = [&](int c) { return kRev ? nck - 1 - c : c; };
+    // Gated mode: this lane's four gates (tokens 4 lane .. 4 lane + 3) of
+    // chunk c in processing order, 0 past the sequence's end or the last chunk.
+    auto load_gates = [&](int c, float (&x)[4]) {
+        const int t0 = natural(c) * C, cc = c < nck ? min(C, T - t0) : 0;
+        const float *gh = a.g + (size_t)b * T * a.H + h;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) x[r] = 4 * lane + r < cc ? gh[(size_t)(t0 + 4 * lane + r) * a.H] : 0.f;
+    };
+    // Gated mode: group `grp`'s gate arrays (0: C~, 1: P, 2 and 3: epilogue).
+    auto gate_arrays = [&](int grp, float *&gl, int *&zc, float *&af) {
+        unsigned char *g0 = sm + kOffGate + (uint32_t)grp * kGateArr;
+        gl = reinterpret_cast<float *>(g0);
+        zc = reinterpret_cast<int *>(g0 + 512);
+        af = reinterpret_cast<float *>(g0 + 1024);
+    };
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -114,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_c);
         prefetch_tmap(&tm_o);
     }
-    {
+    if constexpr (!kGate) {   // the gated mode has no per-head decay (log_lambda is NULL)
         const float l2 = log2_of_decay(a.log_lambda[h]);
         for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
         fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
@@ -270,12 +310,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row = quad * 32 + (uint32_t)lane;
         const uint32_t gt = (uint32_t)threadIdx.x - 64;
         uint32_t kw = 0;
+        float *Gl, *Af;
+        int *Zc;
+        gate_arrays(0, Gl, Zc, Af);
+        float gpre[4];
+        if (kGate && gt < 32) load_gates(0, gpre);
         for (int c = 0; c < nck; ++c) {
             const int Cc = min(C, T - natural(c) * C);
+            // gated: scan this chunk's gates (the group's barrier in the wait publishes them)
+            if (kGate && gt < 32) {
+                gate_scan_store(gpre, lane, Gl, Zc, Af);
+                load_gates(c + 1, gpre);
+            }
             if (!group_wait(bar(BAR_FULLC), (uint32_t)c & 1u, ctl, dec, gt, kBarScale, kw)) break;
             // C~ is a single buffer: the state MMA of chunk c-1 must have read it.
             if (c >= 1 && !group_wait(bar(BAR_SFULL), (uint32_t)(c - 1) & 1u, ctl, dec, gt, kBarScale, kw)) break;
-            const float w = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
+            float w;
+            if constexpr (kGate)   // dk: decay of tokens 0..i; dq: decay of tokens j+1..Cc-1
+                w = kRev ? (Zc[row] < 0 ? exp2f(Gl[row]) : 0.f)
+                         : (row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f);
+            else
+                w = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
             scale_rows_to<3>(sm + kOffC, sm + kOffCt, row, w);
             fence_proxy_async_smem();
             named_sync(kBarScale, kGroupThreads);
@@ -290,7 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nblk = C / 32;
         const int diag = (int)quad;
         uint32_t kw = 0;
+        float *Gl, *Af;
+        int *Zc;
+        gate_arrays(1, Gl, Zc, Af);
+        float gpre[4];
+        if (kGate && gt < 32) load_gates(0, gpre);
         for (int c = 0; c < nck; ++c) {
+            if (kGate && gt < 32) {
+                gate_scan_store(gpre, lane, Gl, Zc, Af);
+                load_gates(c + 1, gpre);
+            }
             if (!group_wait(bar(BAR_SCORE), c & 1, ctl, dec + 2, gt, kBarP, kw)) break;
             tc_fence_after();
             // Blocks in increasing order: P block bk lands in columns [16bk, 16bk+16),
@@ -301,9 +365,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (keep) {
                     uint32_t r[32];
                     tmem_ld_32cols(tl + kColX + 32u * bk, r);
-                    tmem_ld_wait();
-                    pack_scores(r);
-                    build_p_block<kRev>(r, (int)row - 32 * bk, tl + kColX + 16u * bk, pp, pr);
+                    if constexpr (kGate) {
+                        const bool dg = bk == diag;
+                        const float gi = Gl[row];
+                        if constexpr (kRev) {
+                            // row j, columns i >= j: walked rightwards from the block's first column
+                            const int il = 32 * bk;
+                            const float d0 = dg || Zc[il] > (int)row ? 0.f : ex2_approx(Gl[il] - gi);
+                            tmem_ld_wait();
+                            build_p_block_gated_rev(r, dg ? lane : -1, il, d0, Af, tl + kColX + 16u * bk);
+                        } else {
+                            // row i, columns j <= i: walked leftwards from the block's last column
+                            const int jr = 32 * bk + 31;
+                            const float d0 = dg || Zc[row] > jr ? 0.f : ex2_approx(gi - Gl[jr]);
+                            tmem_ld_wait();
+                            build_p_block_gated(r, dg ? lane : 32, 32 * bk, d0, Af, tl + kColX + 16u * bk);
+                        }
+                    } else {
+                        tmem_ld_wait();
+                        pack_scores(r);
+                        build_p_block<kRev>(r, (int)row - 32 * bk, tl + kColX + 16u * bk, pp, pr);
+                    }
                 } else {
                     uint32_t z[16];
 #pragma unroll
@@ -323,9 +405,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t gt = (uint32_t)threadIdx.x - 320;
         const uint32_t tl = tmem + ((quad * 32) << 16);
         uint32_t kw = 0;
+        // Gated mode: the group's gate arrays for chunks of even / odd processing
+        // index; chunk c+1 is scanned at the start of iteration c.
+        float *Gls[2], *Afs[2];
+        int *Zcs[2];
+        gate_arrays(2, Gls[0], Zcs[0], Afs[0]);
+        gate_arrays(3, Gls[1], Zcs[1], Afs[1]);
+        // decay of the whole chunk whose arrays sit in slot `sl`, Cc tokens long
+        auto chunk_decay = [&](int sl, int Cc) { return Zcs[sl][Cc - 1] < 0 ? exp2f(Gls[sl][Cc - 1]) : 0.f; };
+        // where the state copy entering chunk c (processing order) is saved
+        auto saved_slot = [&](int c) {
+            return a.saved + ((size_t)(b * a.H + h) * nck + natural(c)) * kStateCopyBytes;
+        };
+        float gpre[4];
+        if constexpr (kGate) {
+            if (gt < 32) {
+                load_gates(0, gpre);
+                gate_scan_store(gpre, lane, Gls[0], Zcs[0], Afs[0]);
+                load_gates(1, gpre);
+            }
+            named_sync(kBarE, kGroupThreads);
+        }
         // Initial state: copy = bf16(s0), TMEM S = lambda^C0 * s0 (C0: first chunk processed).
         {
-            const float w0 = pw[kRev ? T - (nck - 1) * C : min(C, T)];
+            const float w0 = kGate ? chunk_decay(0, min(C, T - natural(0) * C))
+                                   : pw[kRev ? T - (nck - 1) * C : min(C, T)];
             if (quad < 3) {
                 const float *src = a.s0 ? a.s0 + (((size_t)b * a.H + h) * kDk + row) * kDv : nullptr;
 #pragma unroll 1
@@ -351,16 +455,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             named_sync(kBarE, kGroupThreads);
             if (gt == 0) mbar_arrive(bar(BAR_SBREADY));
+            if (kGate && gt == 0) {
+                bulk_store(saved_slot(0), base + kOffSb, kStateCopyBytes);
+                tma_store_commit();
+            }
         }
         for (int c = 0; c < nck; ++c) {
             const int nc = natural(c);
             const int t0 = nc * C;
             const int Cc = min(C, T - t0);
             const bool last = (c == nck - 1);
+            if constexpr (kGate) {
+                if (gt < 32) {
+                    gate_scan_store(gpre, lane, Gls[(c + 1) & 1], Zcs[(c + 1) & 1], Afs[(c + 1) & 1]);
+                    load_gates(c + 2, gpre);
+                }
+                // the saved copy of the state must be read out before the hand-off rewrites it
+                if (gt == 0) tma_store_wait_read_all();
+            }
             if (!group_wait(bar(BAR_SFULL), c & 1, ctl, dec + 4, gt, kBarE, kw)) break;
             tc_fence_after();
             if (!last && quad < 3) {
-                const float wn = kRev ? pw[C] : pw[min(C, T - t0 - C)];
+                const float wn = kGate ? chunk_decay((c + 1) & 1, min(C, T - natural(c + 1) * C))
+                                       : (kRev ? pw[C] : pw[min(C, T - t0 - C)]);
 #pragma unroll 1
                 for (int blk = 0; blk < 6; ++blk) {
                     uint32_t r[32];
@@ -377,13 +494,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             named_sync(kBarE, kGroupThreads);
             if (gt == 0 && !last) mbar_arrive(bar(BAR_SBREADY));
+            if (kGate && gt == 0 && !last) {
+                bulk_store(saved_slot(c + 1), base + kOffSb, kStateCopyBytes);
+                tma_store_commit();
+            }
 
             if (!group_wait(bar(BAR_OFULL), c & 1, ctl, dec + 4, gt, kBarE, kw)) break;
             tc_fence_after();
             if (gt == 0) tma_store_wait_read_all();
             named_sync(kBarE, kGroupThreads);
             {
-                const float wr = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+                float wr;
+                if constexpr (kGate) {   // dk: decay of tokens j+1..Cc-1; dq: decay of tokens 0..i
+                    const float *Gl = Gls[c & 1];
+                    const int *Zc = Zcs[c & 1];
+                    wr = kRev ? (row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f)
+                              : (Zc[row] < 0 ? exp2f(Gl[row]) : 0.f);
+                } else {
+                    wr = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+                }
 #pragma unroll 1
                 for (int blk = 0; blk < 3; ++blk) {
                     uint32_t r2[32], r1[32];
@@ -415,35 +544,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <bool kRev>
+template <bool kRev, bool kGate>
 cudaError_t launch_tr(const void *A, const void *Bt, const void *Ct, void *out, const float *s0, float init_mul,
-                      const BwdParams &p, cudaStream_t s, int *launches) {
+                      const BwdParams &p, unsigned char *saved, cudaStream_t s, int *launches) {
     CUtensorMap ma, mb, mc, mo;
     cudaError_t e;
     if ((e = make_token_map(&ma, A, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mb, Bt, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mc, Ct, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mo, out, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gla_bwd_tr_kernel<kRev>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const uint32_t smem = kGate ? kSmemBytesGated : kSmemBytes;
+    e = cudaFuncSetAttribute(gla_bwd_tr_kernel<kRev, kGate>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    TrArgs a{p.log_lambda, s0, p.scale, init_mul, p.T, p.H, p.chunk, (p.T + p.chunk - 1) / p.chunk, p.status};
-    gla_bwd_tr_kernel<kRev><<<(unsigned)(p.B * p.H), kThreads, kSmemBytes, s>>>(ma, mb, mc, mo, a);
+    TrArgs a{p.log_lambda, s0, p.scale, init_mul, p.T, p.H, p.chunk, (p.T + p.chunk - 1) / p.chunk, p.status,
+             p.g, saved};
+    gla_bwd_tr_kernel<kRev, kGate><<<(unsigned)(p.B * p.H), kThreads, smem, s>>>(ma, mb, mc, mo, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-// dq: rows do, columns v, values k, state S from h0, forward in time.
+size_t bwd_gated_tc_workspace_size(int B, int T, int H, int chunk) {
+    const size_t nck = ((size_t)T + chunk - 1) / chunk;
+    return 2 * (size_t)B * H * nck * kStateCopyBytes;
+}
+
+// dq: rows do, columns v, values k, state S from h0, forward in time. Gated:
+// the state copy entering each chunk is saved in the first half of the workspace.
 cudaError_t launch_bwd_dq_tc(const BwdParams &p, cudaStream_t s, int *launches) {
     if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
-    return launch_tr<false>(p.do_, p.v, p.k, p.dq_out, p.h0, 1.f, p, s, launches);
+    if (p.g)
+        return launch_tr<false, true>(p.do_, p.v, p.k, p.dq_out, p.h0, 1.f, p,
+                                      static_cast<unsigned char *>(p.workspace), s, launches);
+    return launch_tr<false, false>(p.do_, p.v, p.k, p.dq_out, p.h0, 1.f, p, nullptr, s, launches);
 }
 
 // dk: rows v, columns do, values q, state G / s from dhT / s, reverse in time.
+// Gated: the state copy entering each chunk (G / s) is saved in the second half.
 cudaError_t launch_bwd_dk_tc(const BwdParams &p, cudaStream_t s, int *launches) {
     if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
-    return launch_tr<true>(p.v, p.do_, p.q, p.dk_out, p.dhT, 1.f / p.scale, p, s, launches);
+    if (p.g)
+        return launch_tr<true, true>(p.v, p.do_, p.q, p.dk_out, p.dhT, 1.f / p.scale, p,
+                                     static_cast<unsigned char *>(p.workspace) +
+                                         bwd_gated_tc_workspace_size(p.B, p.T, p.H, p.chunk) / 2,
+                                     s, launches);
+    return launch_tr<true, false>(p.v, p.do_, p.q, p.dk_out, p.dhT, 1.f / p.scale, p, nullptr, s, launches);
 }
 
 }  // namespace gla

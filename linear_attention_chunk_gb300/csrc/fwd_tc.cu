@@ -110,93 +110,6 @@ constexpr uint32_t kOffGate = (kSmemUsed + 15) & ~15u, kGateBytes = 2 * kGateSub
 static_assert(kOffGate % 16 == 0, "the decay factors are read as float4");
 constexpr uint32_t kSmemBytesGated = kSmemBytes + kGateBytes;
 static_assert(kSmemBytesGated <= 232448, "shared memory budget (gated)");
-// A log-decay at or below this clears the state: exp(-80) is below fp32's
-// normal range.
-constexpr float kResetLogDecay = -80.f;
-constexpr float kLog2e = 1.4426950408889634f;
-
-// 2^x for x <= 0 by the hardware approximation (relative error about 2^-22;
-// results below fp32's normal range flush to 0).
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Running sums over the C tokens of a chunk, lane l holding tokens 4l..4l+3
-// of gate values x[0..3] (natural-log decays; 0 past the chunk's end): the
-// log2-decay of tokens 0..t without the clearing gates, gl[t], and the
-// position of the last clearing gate among them, zc[t] (-1 if none), for
-// t < 128. The decay of tokens j+1..i is then 2^(gl[i] - gl[j]) when
-// zc[i] <= j, and 0 otherwise. Also each token's own decay factor, af[t] =
-// exp(x) (0 for a clearing gate).
-__device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, float *gl, int *zc, float *af) {
-    float ls[4];
-    int lz[4];
-    float s = 0.f;
-    int z = -1;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        if (x[r] > kResetLogDecay)
-            s += x[r] * kLog2e;
-        else
-            z = 4 * lane + r;
-        ls[r] = s;
-        lz[r] = z;
-    }
-    float si = s;
-    int zi = z;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const float ys = __shfl_up_sync(0xffffffffu, si, d);
-        const int yz = __shfl_up_sync(0xffffffffu, zi, d);
-        if (lane >= d) {
-            si += ys;
-            zi = max(zi, yz);
-        }
-    }
-    const float es = si - s;   // exclusive: the lanes below
-    const int ez = __shfl_up_sync(0xffffffffu, zi, 1);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        gl[4 * lane + r] = es + ls[r];
-        zc[4 * lane + r] = lz[r] >= 0 ? lz[r] : (lane > 0 ? ez : -1);
-    }
-    float a[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) a[r] = x[r] > kResetLogDecay ? ex2_approx(x[r] * kLog2e) : 0.f;
-    *reinterpret_cast<float4 *>(af + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
-}
-
-// Gated mode: one 32-column block of P for TMEM lane row i, columns
-// j0..j0+31, from the fp32 scores x (raw bits): P_ij = A_ij d_ij with d_ij
-// the decay of tokens j+1..i, written as 16 bf16 pairs at taddr. The weights
-// are walked from the block's right end leftwards, d_i,j-1 = d_ij af[j]: a
-// clearing gate's factor 0 zeroes every column left of it. Off the diagonal
-// the walk starts from d0 = d_i,j0+31 (one exponential per row, dl = 32); in
-// the diagonal block (d0 = 0, dl = i - j0) it starts at the row's own column
-// with 1, and the columns right of it stay 0. One copy of this code serves
-// every block: the kernel's roles share the instruction cache.
-__device__ __forceinline__ void build_p_block_gated(uint32_t (&x)[32], int dl, int j0, float d0, const float *af,
-                                                    uint32_t taddr) {
-    float d = d0;
-#pragma unroll
-    for (int m = 7; m >= 0; --m) {
-        const float4 a4 = *reinterpret_cast<const float4 *>(af + j0 + 4 * m);
-        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-        for (int r = 3; r >= 0; --r) {
-            const int e = 4 * m + r;
-            d = e == dl ? 1.f : d;
-            x[e] = __float_as_uint(__uint_as_float(x[e]) * d);
-            d *= av[r];
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 32; e += 2) x[e >> 1] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
-    tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
-}
-
 constexpr uint32_t kTmemCols = 512, kColR = 0, kColS = 256, kColP = 352, kColQ = 416;
 
 struct FwdTcArgs {
@@ -254,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seg = (blockIdx.x >> 1) / a.BH;
     const int bh = (blockIdx.x >> 1) % a.BH;
     constexpr int C = kC;   // chunk length, 64 or 128: token loops are unrolled
-    static_assert(!(kGate && kRev), "the gated mode is a forward");
     const int h = bh % a.H;
     // b: batch index of the states; bt, tok0: token coordinates of the sequence
     int b = bh / a.H, bt = b, tok0 = 0, T = a.T, nck_seq = a.nck;
@@ -283,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_gates = [&](int c, float (&x)[4]) {
         const int lane4 = 4 * (int)(threadIdx.x & 31);
         const float *gh = a.g + ((size_t)bt * a.T + tok0) * a.H + h;
-        const int t0 = (cbeg + c) * C, cc = c < nck ? min(C, T - t0) : 0;
+        const int t0 = (kRev ? nck - 1 - c : cbeg + c) * C, cc = c < nck ? min(C, T - t0) : 0;
 #pragma unroll
         for (int r = 0; r < 4; ++r) x[r] = lane4 + r < cc ? gh[(size_t)(t0 + lane4 + r) * a.H] : 0.f;
     };
@@ -529,7 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // K~ = diag(w) K with w = lambda^(Cc-1-j) (zero past the end of the
                 // sequence), or lambda^(i+1) in reverse; signalled at once.
                 float wk;
-                if constexpr (kGate)
+                if constexpr (kGate && kRev)   // the decay of the chunk's tokens 0..i
+                    wk = Zc[row] < 0 ? exp2f(Gl[row]) : 0.f;
+                else if constexpr (kGate)      // the decay of tokens j+1..Cc-1
                     wk = row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
                 else
                     wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
@@ -547,7 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Q~ = diag(lambda^(i+1)) Q (diag(lambda^(Cc-1-j)) in reverse) into TMEM as the
                 // A operand of Q~ S_prev: lane = token row, column c = dk pair (2c, 2c+1).
                 float wq;
-                if constexpr (kGate)
+                if constexpr (kGate && kRev)   // the decay of tokens j+1..Cc-1
+                    wq = row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
+                else if constexpr (kGate)      // the decay of the chunk's tokens 0..i
                     wq = Zc[row] < 0 ? exp2f(Gl[row]) : 0.f;
                 else
                     wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
@@ -582,11 +498,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (blk == b0 ? !has0 : !has1) continue;
                         uint32_t x[32];
                         tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, x);
-                        const int jr = 32 * blk + 31;   // the block's last column
                         const bool dg = blk == diag;
-                        const float d0 = dg || zi > jr ? 0.f : ex2_approx(gi - Gl[jr]);
-                        tmem_ld_wait();
-                        build_p_block_gated(x, dg ? lane : 32, 32 * blk, d0, Af, tl + kColP + 16u * blk);
+                        if constexpr (kRev) {
+                            // row j, columns i >= j: the walk starts at the block's first column
+                            const int il = 32 * blk;
+                            const float d0 = dg || Zc[il] > (int)row ? 0.f : ex2_approx(Gl[il] - gi);
+                            tmem_ld_wait();
+                            build_p_block_gated_rev(x, dg ? lane : -1, il, d0, Af, tl + kColP + 16u * blk);
+                        } else {
+                            const int jr = 32 * blk + 31;   // the block's last column
+                            const float d0 = dg || zi > jr ? 0.f : ex2_approx(gi - Gl[jr]);
+                            tmem_ld_wait();
+                            build_p_block_gated(x, dg ? lane : 32, 32 * blk, d0, Af, tl + kColP + 16u * blk);
+                        }
                     }
                 } else {
 #pragma unroll 1
@@ -876,8 +800,10 @@ cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches) 
     if ((e = make_token_map(&mout, p.dv_out, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     const int nck = (p.T + p.chunk - 1) / p.chunk;
     FwdTcArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, p.chunk, nck, 1, nck,
-                p.B * p.H, 0, p.status, nullptr, nullptr, 0, nullptr};
-    return launch_chunk_kernel<true>(mrow, mcol, mval, mout, a, p.B, s, launches);
+                p.B * p.H, 0, p.status, nullptr, nullptr, 0, nullptr, p.g};
+    // gated: the per-token decays replace the per-head one in reverse time too
+    return p.g ? launch_chunk_kernel<true, true>(mrow, mcol, mval, mout, a, p.B, s, launches)
+               : launch_chunk_kernel<true>(mrow, mcol, mval, mout, a, p.B, s, launches);
 }
 
 }  // namespace gla

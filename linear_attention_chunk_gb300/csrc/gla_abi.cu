@@ -355,6 +355,66 @@ gla_status gla_chunk_bwd(const void *q, const void *k, const void *v, const floa
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_bwd launch");
 }
 
+size_t gla_chunk_bwd_gated_workspace_size(int B, int T, int H, int dk, int dv, int chunk, gla_dtype dtype) {
+    if (check_chunk_shape(B, T, H, dk, dv, chunk, dtype) != GLA_OK) return 0;
+    if (dtype == GLA_BF16) return bwd_gated_tc_workspace_size(B, T, H, chunk);
+    const size_t nck = ((size_t)T + chunk - 1) / chunk;
+    return 2 * (size_t)B * H * nck * dk * dv * sizeof(float);
+}
+
+gla_status gla_chunk_bwd_gated(const void *q, const void *k, const void *v, const float *g, const float *h0,
+                               float scale, const void *do_, const float *dhT, int B, int T, int H, int dk, int dv,
+                               int chunk, gla_dtype dtype, void *dq, void *dk_, void *dv_, float *dh0, float *dg,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+    t_err[0] = 0;
+    t_launches = 0;
+    gla_status st = check_chunk_shape(B, T, H, dk, dv, chunk, dtype);
+    if (st != GLA_OK) return st;
+    OPTIONAL_PTR(h0, "h0");
+    OPTIONAL_PTR(dhT, "dhT");
+    OPTIONAL_PTR(dh0, "dh0");
+    OPTIONAL_PTR(workspace, "workspace");
+    if (B == 0 || H == 0) return GLA_OK;
+    if ((long double)B * H * ((T + (long double)chunk - 1) / chunk) > 2147483647.0L)
+        return fail(GLA_ERR_INVALID_ARG, "B*H*chunks too large");
+    if (dtype == GLA_FP32 && (T + chunk - 1) / chunk > 65535)
+        return fail(GLA_ERR_UNSUPPORTED, "GLA_FP32 gated backward needs at most 65535 chunks");
+    if (T > 0) {
+        REQUIRE_PTR(q, "q");
+        REQUIRE_PTR(k, "k");
+        REQUIRE_PTR(v, "v");
+        REQUIRE_PTR(g, "g");
+        REQUIRE_PTR(do_, "do");
+        REQUIRE_PTR(dq, "dq");
+        REQUIRE_PTR(dk_, "dk");
+        REQUIRE_PTR(dv_, "dv");
+        REQUIRE_PTR(dg, "dg");
+        const size_t need = gla_chunk_bwd_gated_workspace_size(B, T, H, dk, dv, chunk, dtype);
+        if (workspace == nullptr || workspace_bytes < need)
+            return fail(GLA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                        workspace ? workspace_bytes : (size_t)0);
+    }
+    unsigned int *status = nullptr;
+    if ((st = status_word(&status)) != GLA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    cudaError_t e;
+    if (T == 0) {
+        // No tokens: dh0 = dhT (the state passes through untouched); no gates.
+        e = launch_copy_state(dhT, dh0, (size_t)B * H * dk * dv, s, &launches);
+        t_launches = launches;
+        return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_bwd_gated(T=0)");
+    }
+    BwdParams p{q, k, v, nullptr, h0, scale, do_, dhT, B, T, H, dk, dv, chunk, dq, dk_, dv_, dh0,
+                workspace, workspace_bytes, status, g, dg};
+    if (dtype == GLA_BF16)
+        e = launch_bwd_gated_tc(p, s, &launches);
+    else
+        e = launch_bwd_simt(p, false, s, &launches);
+    t_launches = launches;
+    return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_bwd_gated launch");
+}
+
 static gla_status varlen_common(const void *q, const void *k, const void *v, const float *log_lambda, const float *g,
                                 float scale,
                                 const int *cu_seqlens, const int *slots, float *state_pool, int n_slots, int nseq,

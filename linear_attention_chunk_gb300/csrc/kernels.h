@@ -37,6 +37,10 @@ struct BwdParams {
     void *workspace;
     size_t workspace_bytes;
     unsigned int *status;
+    // Gated backward: per-token log-decays [B, T, H] replacing log_lambda, and
+    // the gate gradient dg [B, T, H] fp32 (written).
+    const float *g;
+    float *dg;
 };
 
 struct VarlenParams {
@@ -121,6 +125,14 @@ cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // dq and dk: the transposed-shape chunk kernel (192-wide scores, 96-wide outputs).
 cudaError_t launch_bwd_dq_tc(const BwdParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_dk_tc(const BwdParams &p, cudaStream_t s, int *launches);
+// The gated backward (p.g, p.dg set): dq, dk, dv, dh0 by the three chunk
+// kernels in gated mode, the dq and dk kernels saving the bf16 state copy of
+// every chunk in the workspace, then dg from those copies (dg_tc.cu).
+cudaError_t launch_bwd_gated_tc(const BwdParams &p, cudaStream_t s, int *launches);
+cudaError_t launch_bwd_dg_tc(const BwdParams &p, cudaStream_t s, int *launches);
+// Workspace of the gated backward: two bf16 96 x 192 state copies per
+// (b, h, chunk), in the layout the chunk kernels keep them in shared memory.
+size_t bwd_gated_tc_workspace_size(int B, int T, int H, int chunk);
 size_t fwd_tc_workspace_size(int B, int T, int H, int chunk, bool gated = false);
 
 // Sequence segmentation of the forward (seg_tc.cu): a plan, its workspace,

@@ -136,6 +136,20 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *m, uint32_t src,
         : "memory");
 }
 
+// 1-D bulk copies (no tensor map): both addresses 16-byte aligned, the size a
+// multiple of 16 bytes. The load completes `bytes` of transaction count on
+// the mbarrier; the store joins the thread's bulk group (commit, then wait).
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void *gsrc, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(sdst),
+                 "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *gdst, uint32_t ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+                 "r"(ssrc), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void tma_store_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

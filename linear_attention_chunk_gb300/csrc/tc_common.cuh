@@ -138,6 +138,127 @@ __device__ __forceinline__ void build_p_block(uint32_t (&x)[32], int n0, uint32_
     tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
 }
 
+// ------------------------------------------------------------ gated mode
+// The per-token decay of the gated form, S_t = exp(g_t) S_{t-1} + k_t v_t^T:
+// every power of a fixed decay becomes the decay of a run of tokens, exp of a
+// sum of g inside the chunk.
+// A log-decay at or below this clears the state: exp(-80) is below fp32's
+// normal range.
+constexpr float kResetLogDecay = -80.f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x for x <= 0 by the hardware approximation (relative error about 2^-22;
+// results below fp32's normal range flush to 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Running sums over the C tokens of a chunk, lane l holding tokens 4l..4l+3
+// of gate values x[0..3] (natural-log decays; 0 past the chunk's end): the
+// log2-decay of tokens 0..t without the clearing gates, gl[t], and the
+// position of the last clearing gate among them, zc[t] (-1 if none), for
+// t < 128. The decay of tokens j+1..i is then 2^(gl[i] - gl[j]) when
+// zc[i] <= j, and 0 otherwise. Also each token's own decay factor, af[t] =
+// exp(x) (0 for a clearing gate).
+__device__ __forceinline__ void gate_scan_store(const float (&x)[4], int lane, float *gl, int *zc, float *af) {
+    float ls[4];
+    int lz[4];
+    float s = 0.f;
+    int z = -1;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        if (x[r] > kResetLogDecay)
+            s += x[r] * kLog2e;
+        else
+            z = 4 * lane + r;
+        ls[r] = s;
+        lz[r] = z;
+    }
+    float si = s;
+    int zi = z;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float ys = __shfl_up_sync(0xffffffffu, si, d);
+        const int yz = __shfl_up_sync(0xffffffffu, zi, d);
+        if (lane >= d) {
+            si += ys;
+            zi = max(zi, yz);
+        }
+    }
+    const float es = si - s;   // exclusive: the lanes below
+    const int ez = __shfl_up_sync(0xffffffffu, zi, 1);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        gl[4 * lane + r] = es + ls[r];
+        zc[4 * lane + r] = lz[r] >= 0 ? lz[r] : (lane > 0 ? ez : -1);
+    }
+    float a[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a[r] = x[r] > kResetLogDecay ? ex2_approx(x[r] * kLog2e) : 0.f;
+    *reinterpret_cast<float4 *>(af + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
+}
+
+// Gated, forward direction: one 32-column block of P for TMEM lane row i,
+// columns j0..j0+31 (j <= i), from the fp32 scores x (raw bits): P_ij =
+// A_ij d_ij with d_ij the decay of tokens j+1..i, written as 16 bf16 pairs at
+// taddr. The weights
+// are walked from the block's right end leftwards, d_i,j-1 = d_ij af[j]: a
+// clearing gate's factor 0 zeroes every column left of it. Off the diagonal
+// the walk starts from d0 = d_i,j0+31 (one exponential per row, dl = 32); in
+// the diagonal block (d0 = 0, dl = i - j0) it starts at the row's own column
+// with 1, and the columns right of it stay 0. One copy of this code serves
+// every block: the kernel's roles share the instruction cache.
+__device__ __forceinline__ void build_p_block_gated(uint32_t (&x)[32], int dl, int j0, float d0, const float *af,
+                                                    uint32_t taddr) {
+    float d = d0;
+#pragma unroll
+    for (int m = 7; m >= 0; --m) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(af + j0 + 4 * m);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int r = 3; r >= 0; --r) {
+            const int e = 4 * m + r;
+            d = e == dl ? 1.f : d;
+            x[e] = __float_as_uint(__uint_as_float(x[e]) * d);
+            d *= av[r];
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) x[e >> 1] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+    tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
+}
+
+
+// Gated, reverse direction: one 32-column block for TMEM lane row j, columns
+// i0..i0+31 (i >= j), P_ji = X_ji d_ji with d_ji the decay of tokens j+1..i,
+// written as 16 bf16 pairs at taddr. The weights are walked from the block's
+// left end rightwards, d_j,i+1 = d_ji af[i+1]: a clearing gate's factor 0
+// zeroes every column right of it. Off the diagonal the walk starts from d0 =
+// d_j,i0 (one exponential per row, dl = -1); in the diagonal block (d0 = 0,
+// dl = j - i0) it starts at the row's own column with 1, and the columns left
+// of it stay 0.
+__device__ __forceinline__ void build_p_block_gated_rev(uint32_t (&x)[32], int dl, int i0, float d0,
+                                                        const float *af, uint32_t taddr) {
+    float d = d0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(af + i0 + 4 * m);
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int e = 4 * m + r;
+            if (e > 0) d *= av[r];
+            d = e == dl ? 1.f : d;
+            x[e] = __float_as_uint(__uint_as_float(x[e]) * d);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) x[e >> 1] = pack_bf16x2(__uint_as_float(x[e]), __uint_as_float(x[e + 1]));
+    tmem_st_16cols(taddr, *reinterpret_cast<uint32_t(*)[16]>(&x[0]));
+}
+
 // Calls f(ks) for the n = C / 16 token steps of a chunk (4 or 8), fully
 // unrolled: an MMA issued from a loop with a run-time trip count costs about
 // twice the issue time of one whose descriptors are formed from constants.

@@ -297,3 +297,31 @@ def test_noalloc_reports_no_launch_when_it_fails(L):
         assert noalloc(T=8192, H=4) == binding.GLA_ERR_CUDA
         assert L.gla_last_launch_count() == 0
         assert "noalloc" in L.gla_last_error().decode()
+
+
+def test_gated_backward_rejects_bad_arguments(L):
+    def bwd(**kw):
+        a = dict(q=FAKE, k=FAKE + 0x100, v=FAKE + 0x200, g=FAKE + 0x300, h0=None, do=FAKE + 0x400, dhT=None, B=2,
+                 T=256, H=16, dk=96, dv=192, C=128, dt=0, dq=FAKE + 0x500, dk_=FAKE + 0x600, dv_=FAKE + 0x700,
+                 dh0=None, dg=FAKE + 0x800, ws=FAKE + 0x900, wsb=1 << 40)
+        a.update(kw)
+        return L.gla_chunk_bwd_gated(a["q"], a["k"], a["v"], a["g"], a["h0"], 0.1, a["do"], a["dhT"], a["B"],
+                                     a["T"], a["H"], a["dk"], a["dv"], a["C"], a["dt"], a["dq"], a["dk_"],
+                                     a["dv_"], a["dh0"], a["dg"], a["ws"], a["wsb"], None)
+    assert bwd(g=None) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(g=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(dg=None) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(do=None) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(dhT=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(dh0=ODD) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(dk=64) == binding.GLA_ERR_UNSUPPORTED
+    assert bwd(C=32) == binding.GLA_ERR_UNSUPPORTED
+    assert bwd(T=-1) == binding.GLA_ERR_INVALID_ARG
+    assert bwd(B=0) == binding.GLA_OK
+    assert bwd(ws=None) == binding.GLA_ERR_WORKSPACE
+    need = binding.gla_chunk_bwd_gated_workspace_size(2, 256, 16, 96, 192, 128)
+    assert need == 2 * 2 * 16 * 2 * 96 * 192 * 2            # two bf16 states per (b, h, chunk)
+    assert bwd(wsb=need - 16) == binding.GLA_ERR_WORKSPACE
+    assert "workspace" in L.gla_last_error().decode()
+    assert binding.gla_chunk_bwd_gated_workspace_size(1, 300, 2, 8, 16, 64, binding.GLA_FP32) == 2 * 2 * 5 * 8 * 16 * 4
+    assert bwd(dt=1, dk=8, dv=16, C=64, T=64 * 65536, B=1, H=1) == binding.GLA_ERR_UNSUPPORTED   # 65,536 chunks
