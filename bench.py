@@ -393,6 +393,55 @@ def bench_gated(args, dist, device, stream, peaks, sampler):
     }
     del q, k, v, g, o, hT
     res["long"] = bench_gated_long(args, dist, device, stream, peaks, sampler)
+    res["bwd"] = bench_gated_bwd(args, dist, device, stream, peaks, sampler)
+    return res
+
+
+def bench_gated_bwd(args, dist, device, stream, peaks, sampler):
+    """The backward with a per-token decay, gla_chunk_bwd_gated (dq, dk, dv,
+    dh0 and the gate gradient dg), on the training shape (B=16, H=16,
+    T=2048, chunk 128, h0 ~ N(0, 0.02)) with gated linear attention's gates."""
+    import torch
+    import linear_attention_chunk_gb300 as gla
+    B, T = args.batch or 16, 2048
+    c = gen.make_case(B, T, H, DK, DV, seed=2, normalise_k=True, h0_std=0.02, with_grad=True, chunk=CHUNK,
+                      gate="gla", name=f"gated_bwd_bf16_B{B}_H16_T{T}")
+    q, k, v, do = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v, c.do))
+    g = torch.from_numpy(c.extra["g"]).to(device)
+    h0 = torch.from_numpy(c.h0).to(device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dh0 = torch.empty_like(h0)
+    dg = torch.empty_like(g)
+    ws = torch.empty(gla.gla_chunk_bwd_gated_workspace_size(B, T, H, DK, DV, CHUNK), dtype=torch.uint8,
+                     device=device)
+
+    def step():
+        gla.gla_chunk_bwd_gated(q, k, v, g, do, h0, None, c.scale, CHUNK, dq=dq, dk=dk, dv=dv, dh0=dh0, dg=dg,
+                                workspace=ws, stream=stream)
+        return gla.gla_last_launch_count()
+
+    total, per, win, launches = time_steps(step, args.steps, args.warmup, dist, stream)
+    total = dist.max(total)
+    bytes_ = bwd_work(B, T, True, False, True)[0] + B * T * H * 4 * 2     # + g in, dg out
+    avg_ms = statistics.mean(per)
+    ach = bytes_ / (avg_ms * 1e-3) / 1e9
+    traffic, _ = committed_traffic("gla_chunk_bwd_gated")
+    res = {
+        "value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
+        "ms_per_step": total / args.steps,
+        "config": {"workload": c.name, "B": B, "T": T, "H": H, "chunk": CHUNK, "h0": "N(0,0.02)", "dhT": "none",
+                   "gates": "log sigmoid(x)/16, x ~ N(0,1), per token and head", "outputs": "dq, dk, dv, dh0, dg",
+                   "l2": f"inputs larger than L2 ({bytes_ / 1e6:.0f} MB per call), no flush"},
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ach / peaks["hbm_gbs"], "traffic": traffic * B / 16 if traffic is not None else None,
+                     "algorithmic_bytes_per_call": bytes_, "avg_call_ms": avg_ms,
+                     "launches_per_call": launches // max(args.steps, 1), "peak_source": peaks["source"],
+                     "note": "q, k, v, do, g in; dq, dk, dv, dg out (1,928 B per head-token) + h0, dh0; the saved "
+                             "chunk states (2 x 288 B per head-token written and read) are not counted as work"},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(*win) if sampler else None,
+    }
+    del q, k, v, do, g, h0, dq, dk, dv, dh0, dg, ws
     return res
 
 
@@ -1037,6 +1086,23 @@ def oracle_gated_sample(units):
     return dt, B * hs * 2048 / H, nthreads, f"{B}x{hs} (b,h) chains of T=2048 with per-token gates (of 8x16)"
 
 
+def oracle_gated_bwd_sample(units):
+    """The oracle's gated backward (O11, the gate gradient included) over
+    `units` (b, h) chains of the gated training workload (T=2048)."""
+    import oracle
+    B = max(1, math.ceil(units / H))
+    hs = min(units, H)
+    c = gen.make_case(B, 2048, H, DK, DV, seed=2, normalise_k=True, h0_std=0.02, with_grad=True, chunk=CHUNK,
+                      gate="gla")
+    sl = lambda x: x[:, :, :hs]
+    nthreads = oracle.threads(0)
+    t0 = time.perf_counter()
+    oracle.bwd_gated(sl(c.q), sl(c.k), sl(c.v), sl(c.extra["g"]), c.h0[:, :hs], c.scale, sl(c.do), None,
+                     nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, B * hs * 2048 / H, nthreads, f"{B}x{hs} (b,h) chains of T=2048, gated backward (of 16x16)"
+
+
 def oracle_bwd_sample(units, seed=2):
     import oracle
     B = max(1, math.ceil(units / H))
@@ -1088,6 +1154,9 @@ def cpu_baseline():
     dt, toks, nt, sample = oracle_gated_sample(128)
     modes["gated"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
                       "sample": sample, "seconds": dt}
+    dt, toks, nt, sample = oracle_gated_bwd_sample(64)
+    modes["gated_bwd"] = {"value": toks / dt, "unit": "tokens/s", "cores": nt, "kind": "oracle",
+                          "sample": sample, "seconds": dt}
     return base, modes
 
 
@@ -1159,7 +1228,7 @@ def summary_line(key, res):
             parts.append(f"e2e {r['e2e']['value']:.4g} {r['e2e']['unit']}")
         return "[bench] " + ", ".join(parts)
     lines = [one(key, res)]
-    for sub in ("standalone", "fwd_mixer", "chunk64", "step", "long", "single_chain"):
+    for sub in ("standalone", "fwd_mixer", "chunk64", "step", "long", "single_chain", "bwd"):
         if isinstance(res.get(sub), dict) and "value" in res[sub]:
             lines.append(one(f"{key}.{sub}", res[sub]))
             if isinstance(res[sub].get("single_chain"), dict):
@@ -1260,6 +1329,8 @@ def main(argv=None):
         for k, v in base_modes.items():
             if k in line["modes"]:
                 line["modes"][k]["cpu_baseline"] = v
+        if "gated_bwd" in base_modes and "bwd" in line["modes"].get("gated", {}):
+            line["modes"]["gated"]["bwd"]["cpu_baseline"] = base_modes["gated_bwd"]
     if dist.rank == 0:
         for key, res in results.items():
             log(summary_line(key, res))
