@@ -751,7 +751,10 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     // that run in parallel, when the caller gave the workspace for it.
     const bool gated = p.g != nullptr;
     const SegPlan plan = plan_segments(p.B, p.T, p.H, p.chunk);
-    if (plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan, gated)) {
+    const bool segmented = plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan, gated);
+    // One chain per (b, h) with the per-head decay: one CTA holds the whole state.
+    if (!gated && !segmented) return launch_fwd_full_tc(p, nullptr, 1, nck, s, launches);
+    if (segmented) {
         float *S_in = nullptr;
         if ((e = launch_seg_prologue(p, plan, &S_in, s, launches)) != cudaSuccess) return e;
         a.h0 = S_in;
