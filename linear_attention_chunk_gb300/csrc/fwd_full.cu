@@ -27,17 +27,18 @@
 //     the V slot of its own stage once the state and output MMAs have read V.
 //   One P-group warp per TMEM lane quadrant owns its 32 token rows, so P
 //     can overwrite the score columns that warp has already read.
-// Warps (13, 416 threads):
-//   0           TMA producer
+// Warps (16, 512 threads; a warp reaches the TMEM lanes of quadrant warp % 4):
+//   15          TMA producer
 //   3           TMEM owner and MMA issuer (a non-blocking event loop)
-//   4-7         P group: its rows of Q to registers (Q's single buffer is then
-//               free for the next chunk, whose tile the producer has already
-//               prefetched into L2), K~ = diag(lambda^(Cc-1-j)) K in place
-//               (signalled at once), P = bf16(A .* D) by packed bf16x2
-//               multiplies with a table of decay pairs whose zeros mask the
-//               diagonal block, then Q~ into TMEM
+//   4-7         P group: its rows of Q to registers as soon as Q lands (Q's
+//               single buffer is then free once QK has read it; the producer
+//               has already prefetched the next tile into L2), K~ =
+//               diag(lambda^(Cc-1-j)) K in place (signalled at once), P =
+//               bf16(A .* D) by packed bf16x2 multiplies with a table of decay
+//               pairs whose zeros mask the diagonal block, then Q~ into TMEM
 //   8-11        E group: output epilogue (O * scale -> bf16 -> V slot -> TMA store)
-//   12, 1, 2    H group (TMEM quadrants 0-2, the state's 96 rows): the state
+//   12-14, 0-2  H group (quadrants 0-2, the state's 96 rows; the first three
+//               warps take column blocks 0-2, the last three 3-5): the state
 //               hand-off (bf16 copy of S for the next chunk's Q~ S, S <-
 //               lambda^C' S) and hT
 // Per chunk c the MMA issuer runs, in order, as soon as their inputs are ready:
@@ -60,9 +61,9 @@ using namespace ptx;
 using namespace tc;
 
 constexpr int kDk = 96, kDv = 192;
-constexpr int kThreads = 416;
+constexpr int kThreads = 512;
 constexpr uint32_t kBarP = 1, kBarE = 2, kBarH = 3;   // named barriers of the three groups
-constexpr uint32_t kHThreads = 96;
+constexpr uint32_t kHThreads = 192;
 
 constexpr uint32_t kOffQ = 0;                        // Q: 3 blocks
 constexpr uint32_t kOffStage = 3 * kBlk;             // stage s: K (3 blocks), then V (6 blocks)
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
+    if (warp == 15) {
         // ------------------------------------------------------- TMA producer
         // K(c) into stage c % 2 once ST(c-2) has completed; Q(c) once QK(c-1)
         // has completed and Q~(c-1) is in TMEM; V(c) into stage c % 2 once the
@@ -318,10 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t kw = 0;
         for (int c = 0; c < nck; ++c) {
             const int Cc = clen(c);
-            if (!gwait(bar(BAR_QKDONE), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
-            tc_fence_after();
-            // Q has one buffer: this thread's row of it goes to registers and the
-            // tile is released at once (QK(c), its other reader, has completed).
+            // Q has one buffer: as soon as it lands, this thread's row of it goes to
+            // registers, and the tile is free once QK(c), its other reader, is done.
+            if (!gwait(bar(BAR_FULLQ), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
             uint4 qrow[12];
 #pragma unroll
             for (int j = 0; j < 3; ++j)
@@ -330,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     qrow[4 * j + cc] = ld_shared_v4(base + kOffQ + j * kBlk + sw64_offset(row, (uint32_t)cc));
             named_sync(kBarP, 128);
             if (gt == 0) mbar_arrive(bar(BAR_QFREE));
+            if (!gwait(bar(BAR_QKDONE), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
+            tc_fence_after();
             // K~ = diag(lambda^(Cc-1-j)) K in place (zero past the end), signalled at once.
             scale_rows<3>(sm + (stage(c) - base) + kStK, row, row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
             fence_proxy_async_smem();
@@ -390,12 +392,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // Stage in V(c)'s slot: ST(c) and OUT(c), its readers, have completed.
             const uint32_t stg = stage(c) + kStV;
+            // Six 32-column blocks, the next block's TMEM load in flight while
+            // this one is converted and staged.
+            {
+                uint32_t ra[32], rb[32];
+                tmem_ld_32cols(tl + kColO, ra);
 #pragma unroll 1
-            for (int blk = 0; blk < 6; ++blk) {
-                uint32_t r[32];
-                tmem_ld_32cols(tl + kColO + 32u * blk, r);
-                tmem_ld_wait();
-                write_row_sw64_bits(sm + (stg - base) + blk * kBlk, row, r, a.scale);
+                for (int bp = 0; bp < 3; ++bp) {
+                    const int blk = 2 * bp;
+                    tmem_ld_wait();
+                    tmem_ld_32cols(tl + kColO + 32u * (blk + 1), rb);
+                    write_row_sw64_bits(sm + (stg - base) + blk * kBlk, row, ra, a.scale);
+                    tmem_ld_wait();
+                    if (bp < 2) tmem_ld_32cols(tl + kColO + 32u * (blk + 2), ra);
+                    write_row_sw64_bits(sm + (stg - base) + (blk + 1) * kBlk, row, rb, a.scale);
+                }
             }
             tc_fence_before();
             fence_proxy_async_smem();
@@ -412,18 +423,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (gt == 0) tma_store_wait_all();
     } else {
-        // --------------------------------- H group (warps 12, 1, 2: rows 0..95)
+        // ------------------- H group (warps 12-14 and 0-2: rows 0..95, two column halves)
         const uint32_t quad = (uint32_t)(warp & 3);               // 0, 1, 2
         const uint32_t row = quad * 32 + (uint32_t)lane;          // state row (dk index)
-        const uint32_t gt = row;                                  // 0..95
+        const int half = warp >= 12 ? 0 : 1;                      // column blocks 3 half .. 3 half + 2
+        const uint32_t gt = (uint32_t)half * 96u + row;           // 0..191
         const uint32_t tl = tmem + ((quad * 32) << 16);
+        const int blk0 = 3 * half;
         uint32_t kw = 0;
         // Initial state: copy = bf16(h0), TMEM S = lambda^C0 h0 (C0: the first chunk's length).
         {
             const float w0 = pw[clen(0)];
             const float *src = h0 ? h0 + (((size_t)b * a.H + h) * kDk + row) * kDv : nullptr;
 #pragma unroll 1
-            for (int blk = 0; blk < 6; ++blk) {
+            for (int blk = blk0; blk < blk0 + 3; ++blk) {
                 float x[32];
                 uint32_t r[32];
 #pragma unroll
@@ -446,26 +459,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(kBarH, kHThreads);
             if (gt == 0) mbar_arrive(bar(BAR_SBREADY));
         }
+        bool hT_staged = false;
         for (int c = 0; c < nck; ++c) {
             const bool last = c == nck - 1;
+            const bool write_hT = last && last_seg && a.hT;
             if (!gwait(bar(BAR_SFULL), (uint32_t)c & 1u, ctl, dec + 4, gt, kBarH, kHThreads, kw)) break;
             // the copy is single: OUT(c) must have read it before it changes
             if (!gwait(bar(BAR_OFULL), (uint32_t)c & 1u, ctl, dec + 4, gt, kBarH, kHThreads, kw)) break;
+            // hT goes out as one 73,728-byte bulk store, staged row-major in the other
+            // stage's K and V slots (72 KB, contiguous), free once the output of chunk
+            // c-1, staged in that V slot, has been read out (K's last reader, ST(c-1),
+            // is long complete).
+            if (write_hT && c >= 1 &&
+                !gwait(bar(BAR_VFREE0 + ((c - 1) & 1)), (uint32_t)((c - 1) >> 1) & 1u, ctl, dec + 4, gt, kBarH,
+                       kHThreads, kw))
+                break;
             tc_fence_after();
             const float wn = last ? 1.f : pw[clen(c + 1)];
-            float *dst = (last && last_seg && a.hT) ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv : nullptr;
-#pragma unroll 1
-            for (int blk = 0; blk < 6; ++blk) {
-                uint32_t r[32];
-                tmem_ld_32cols(tl + kColS + 32u * blk, r);
-                tmem_ld_wait();
+            // the staging row of hT (fp32, 768 bytes): the stage not holding chunk c
+            unsigned char *hrow = write_hT ? sm + (stage(c + 1) - base) + row * (kDv * 4) : nullptr;
+            // Three 32-column blocks, the next block's TMEM load in flight while
+            // this one is copied and rescaled.
+            auto handle = [&](uint32_t (&r)[32], int blk) {
                 if (last) {
-                    if (dst) {
+                    if (hrow) {
+                        // (once per sequence: the bank conflicts of rows 768 bytes apart are
+                        // cheaper than the per-thread global stores they replace)
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4 *>(dst + blk * 32 + e) =
-                                make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
-                                            __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+                            st_shared_v4(smem_u32(hrow + (blk * 32 + e) * 4), r[e], r[e + 1], r[e + 2], r[e + 3]);
                     }
                 } else {
                     write_row_sw64_bits(sm + kOffSb + blk * kSbBlk, row, r, 1.f);
@@ -473,13 +495,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * wn);
                     tmem_st_32cols(tl + kColS + 32u * blk, r);
                 }
+            };
+            {
+                uint32_t ra[32], rb[32];
+                tmem_ld_32cols(tl + kColS + 32u * blk0, ra);
+                tmem_ld_wait();
+                tmem_ld_32cols(tl + kColS + 32u * (blk0 + 1), rb);
+                handle(ra, blk0);
+                tmem_ld_wait();
+                tmem_ld_32cols(tl + kColS + 32u * (blk0 + 2), ra);
+                handle(rb, blk0 + 1);
+                tmem_ld_wait();
+                handle(ra, blk0 + 2);
             }
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             named_sync(kBarH, kHThreads);
             if (gt == 0 && !last) mbar_arrive(bar(BAR_SBREADY));
+            if (gt == 0 && write_hT) {
+                bulk_store(a.hT + ((size_t)b * a.H + h) * kDk * kDv, stage(c + 1), kDk * kDv * 4);
+                tma_store_commit();
+                hT_staged = true;
+            }
         }
+        if (hT_staged) tma_store_wait_all();
     }
 
     tc_fence_before();
