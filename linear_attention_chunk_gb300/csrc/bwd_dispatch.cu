@@ -51,7 +51,7 @@ cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches) {
         if ((e = cudaStreamWaitEvent(f->aux[i], f->ev[0], 0)) != cudaSuccess) return e;
     cudaError_t el = launch_bwd_dq_tc(p, f->aux[0], launches);
     if (el == cudaSuccess) el = launch_bwd_dk_tc(p, f->aux[1], launches);
-    if (el == cudaSuccess) el = launch_bwd_dv_tc(p, s, launches);
+    if (el == cudaSuccess) el = launch_bwd_dv_full_tc(p, s, launches);
     // Join whatever was launched before reporting, so the caller's stream
     // never runs ahead of work still in flight on the helper streams.
     for (int i = 0; i < 2; ++i) {

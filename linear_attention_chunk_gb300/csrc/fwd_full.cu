@@ -88,9 +88,9 @@ constexpr uint32_t kTmemCols = 512, kColAP = 0, kColQt = 64, kColO = 128, kColS 
 
 struct FullArgs {
     const float *log_lambda;
-    const float *h0;       // initial state [B,H,96,192], or NULL
-    float *hT;             // final state, or NULL
-    float scale;
+    const float *h0;       // initial state [B,H,96,192] (times init_mul), or NULL
+    float *hT;             // final state (times final_mul), or NULL
+    float scale, init_mul, final_mul;
     int T, H, nck;
     // Sequence segmentation: the grid covers nseg segments of seg_chunks
     // chunks; segment g starts from h0 + g * h0_seg_stride and only the last
@@ -110,7 +110,13 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, const WaitC
     return decision[(k++) & 1] == 0;
 }
 
-template <int kC>
+// kRev = false: the forward pass. kRev = true: the same chunked recurrence
+// run backwards in time, which is how the backward pass obtains dv and dh0:
+// rows are k tokens, columns q tokens, values dO, the mask keeps col >= row
+// with lambda^(col-row), the row weights swap (lambda^(Cc-1-j) on the
+// readout, lambda^(i+1) on the state update), chunks run last to first, and
+// the state is the state gradient divided by the scale.
+template <bool kRev, int kC>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_fwd_full_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -128,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nck = min(a.seg_chunks, a.nck - cbeg);     // chunks of this CTA
     const bool last_seg = seg == a.nseg - 1;
     const float *h0 = a.h0 ? a.h0 + (size_t)seg * a.h0_seg_stride : nullptr;
-    auto tok0 = [&](int c) { return (cbeg + c) * C; };
+    auto tok0 = [&](int c) { return (kRev ? nck - 1 - c : cbeg + c) * C; };
     auto clen = [&](int c) { return min(C, T - tok0(c)); };
 
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // load, which waits for this one to be consumed, is served from L2.
                 if (c + 1 < nck)
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) tma_prefetch_4d(&tm_q, 32 * j, h, t0 + C, b);
+                    for (int j = 0; j < 3; ++j) tma_prefetch_4d(&tm_q, 32 * j, h, tok0(c + 1), b);
             }
             __syncwarp();
             nq = c + 1;
@@ -332,23 +338,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (gt == 0) mbar_arrive(bar(BAR_QFREE));
             if (!gwait(bar(BAR_QKDONE), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
             tc_fence_after();
-            // K~ = diag(lambda^(Cc-1-j)) K in place (zero past the end), signalled at once.
-            scale_rows<3>(sm + (stage(c) - base) + kStK, row, row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
+            // K~ = diag(lambda^(Cc-1-j)) K in place (zero past the end), or lambda^(i+1)
+            // in reverse; signalled at once.
+            scale_rows<3>(sm + (stage(c) - base) + kStK, row,
+                          kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f));
             fence_proxy_async_smem();
             named_sync(kBarP, 128);
             if (gt == 0) mbar_arrive(bar(BAR_KREADY));
             // P = bf16((Q K^T) .* D) in place over A. Blocks in increasing order:
             // P block bk lands in columns [16 bk, 16 bk + 16), inside score block
             // bk / 2, which this warp has already read (or never needs). Blocks on
-            // the masked side of the diagonal are written as zeros.
+            // the masked side of the diagonal (above it forward, below it in
+            // reverse) are written as zeros.
 #pragma unroll 1
             for (int bk = 0; bk < nblk; ++bk) {
-                if (bk <= (int)quad) {
+                if (kRev ? bk >= (int)quad : bk <= (int)quad) {
                     uint32_t x[32];
                     tmem_ld_32cols(tl + kColAP + 32u * bk, x);
                     tmem_ld_wait();
                     pack_scores(x);
-                    build_p_block<false>(x, (int)row - 32 * bk, tl + kColAP + 16u * bk, pp, pr);
+                    build_p_block<kRev>(x, (int)row - 32 * bk, tl + kColAP + 16u * bk, pp, pr);
                 } else {
                     uint32_t z[16];
 #pragma unroll
@@ -360,7 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Q~ S_prev: lane = token row, column = dk pair, from the row kept in
             // registers. This warp's score columns there (C = 128) were read above.
             {
-                const uint32_t wq2 = pack_bf16x2(pw[row + 1], pw[row + 1]);
+                // lambda^(i+1); lambda^(Cc-1-j) in reverse (zero past the end)
+                const float wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+                const uint32_t wq2 = pack_bf16x2(wq, wq);
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {
                     uint32_t pk[16];
@@ -443,10 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 32; e += 4) {
                     const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + blk * 32 + e)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x[e] = v4.x;
-                    x[e + 1] = v4.y;
-                    x[e + 2] = v4.z;
-                    x[e + 3] = v4.w;
+                    x[e] = v4.x * a.init_mul;
+                    x[e + 1] = v4.y * a.init_mul;
+                    x[e + 2] = v4.z * a.init_mul;
+                    x[e + 3] = v4.w * a.init_mul;
                 }
                 write_row_sw64(sm + kOffSb + blk * kSbBlk, row, x);
 #pragma unroll
@@ -485,6 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (hrow) {
                         // (once per sequence: the bank conflicts of rows 768 bytes apart are
                         // cheaper than the per-thread global stores they replace)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a.final_mul);
 #pragma unroll
                         for (int e = 0; e < 32; e += 4)
                             st_shared_v4(smem_u32(hrow + (blk * 32 + e) * 4), r[e], r[e + 1], r[e + 2], r[e + 3]);
@@ -540,12 +553,35 @@ cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int se
     if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mo, p.o, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     const int nck = (p.T + p.chunk - 1) / p.chunk;
-    FullArgs a{p.log_lambda, S_in ? S_in : p.h0, p.hT, p.scale, p.T, p.H, nck, nseg, nseg > 1 ? seg_chunks : nck,
-               p.B * p.H, nseg > 1 ? (size_t)p.B * p.H * kDk * kDv : 0, p.status};
-    auto kernel = p.chunk == 128 ? gla_fwd_full_kernel<128> : gla_fwd_full_kernel<64>;
+    FullArgs a{p.log_lambda, S_in ? S_in : p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, nck, nseg,
+               nseg > 1 ? seg_chunks : nck, p.B * p.H, nseg > 1 ? (size_t)p.B * p.H * kDk * kDv : 0, p.status};
+    auto kernel = p.chunk == 128 ? gla_fwd_full_kernel<false, 128> : gla_fwd_full_kernel<false, 64>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     kernel<<<(unsigned)(p.B * p.H * nseg), kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, a);
+    if (launches) ++*launches;
+    return cudaGetLastError();
+}
+
+// dv and dh0 of the backward pass with one CTA per (b, h): the chunk
+// recurrence in reverse time with rows = k, columns = q, values = dO; state =
+// (state gradient) / scale, seeded by dhT / scale and written out times the
+// scale as dh0.
+cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launches) {
+    if (p.dk != kDk || p.dv != kDv || p.g) return cudaErrorInvalidValue;
+    CUtensorMap mrow, mcol, mval, mout;
+    cudaError_t e;
+    if ((e = make_token_map(&mrow, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mcol, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mval, p.do_, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mout, p.dv_out, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    const int nck = (p.T + p.chunk - 1) / p.chunk;
+    FullArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, nck, 1, nck, p.B * p.H, 0,
+               p.status};
+    auto kernel = p.chunk == 128 ? gla_fwd_full_kernel<true, 128> : gla_fwd_full_kernel<true, 64>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kernel<<<(unsigned)(p.B * p.H), kThreads, kSmemBytes, s>>>(mrow, mcol, mval, mout, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

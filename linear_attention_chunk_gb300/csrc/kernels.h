@@ -121,6 +121,7 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
 // S_in (or NULL: p.h0) holds each segment's initial state when nseg > 1.
 cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int seg_chunks, cudaStream_t s,
                                int *launches);
+cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // Variable-length forward with the states in a pool (bf16, dk = 96, dv = 192).
 cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
