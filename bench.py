@@ -321,7 +321,7 @@ def bench_fwd(args, dist, device, stream, peaks, sampler):
     avg_ms = statistics.mean(per)
     ach_gbs = bytes_ / (avg_ms * 1e-3) / 1e9
     ach_tf = fl_full / (avg_ms * 1e-3) / 1e12
-    traffic, traffic_wl = committed_traffic("gla_fwd_tc")
+    traffic, traffic_wl = committed_traffic("gla_fwd_full")
     res = {
         "value": tokens * args.steps / (total * 1e-3), "unit": "tokens/s", "ms_per_step": total / args.steps,
         "config": headline_config(dist.world, B, T),
