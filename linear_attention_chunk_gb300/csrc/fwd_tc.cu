@@ -752,8 +752,13 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     const bool gated = p.g != nullptr;
     const SegPlan plan = plan_segments(p.B, p.T, p.H, p.chunk);
     const bool segmented = plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan, gated);
-    // One chain per (b, h) with the per-head decay: one CTA holds the whole state.
-    if (!gated && !segmented) return launch_fwd_full_tc(p, nullptr, 1, nck, s, launches);
+    // The per-head decay: one CTA holds the whole state of a (b, h) chain or segment.
+    if (!gated) {
+        if (!segmented) return launch_fwd_full_tc(p, nullptr, 1, nck, s, launches);
+        float *S_in = nullptr;
+        if ((e = launch_seg_prologue(p, plan, &S_in, s, launches)) != cudaSuccess) return e;
+        return launch_fwd_full_tc(p, S_in, plan.nseg, plan.seg_chunks, s, launches);
+    }
     if (segmented) {
         float *S_in = nullptr;
         if ((e = launch_seg_prologue(p, plan, &S_in, s, launches)) != cudaSuccess) return e;
@@ -762,8 +767,7 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
         a.seg_chunks = plan.seg_chunks;
         a.h0_seg_stride = (size_t)p.B * p.H * kDk * kDv;
     }
-    return gated ? launch_chunk_kernel<false, true>(mq, mk, mv, mo, a, p.B, s, launches)
-                 : launch_chunk_kernel<false>(mq, mk, mv, mo, a, p.B, s, launches);
+    return launch_chunk_kernel<false, true>(mq, mk, mv, mo, a, p.B, s, launches);
 }
 
 // Variable-length forward: one CTA per (sequence, head, dv half) over the
@@ -790,11 +794,12 @@ cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *lau
     return cudaGetLastError();
 }
 
-// dv and dh0 of the backward pass: the chunk recurrence in reverse time with
-// rows = k, columns = q, values = dO; state = (state gradient) / scale,
-// seeded by dhT / scale.
+// dv and dh0 of the backward pass of the per-token decay: the chunk
+// recurrence in reverse time with rows = k, columns = q, values = dO; state =
+// (state gradient) / scale, seeded by dhT / scale. (The per-head decay's dv
+// runs on the one-CTA-per-head kernel, fwd_full.cu.)
 cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches) {
-    if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
+    if (p.dk != kDk || p.dv != kDv || !p.g) return cudaErrorInvalidValue;
     CUtensorMap mrow, mcol, mval, mout;
     cudaError_t e;
     if ((e = make_token_map(&mrow, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
@@ -804,9 +809,7 @@ cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches) 
     const int nck = (p.T + p.chunk - 1) / p.chunk;
     FwdTcArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, p.chunk, nck, 1, nck,
                 p.B * p.H, 0, p.status, nullptr, nullptr, 0, nullptr, p.g};
-    // gated: the per-token decays replace the per-head one in reverse time too
-    return p.g ? launch_chunk_kernel<true, true>(mrow, mcol, mval, mout, a, p.B, s, launches)
-               : launch_chunk_kernel<true>(mrow, mcol, mval, mout, a, p.B, s, launches);
+    return launch_chunk_kernel<true, true>(mrow, mcol, mval, mout, a, p.B, s, launches);
 }
 
 }  // namespace gla

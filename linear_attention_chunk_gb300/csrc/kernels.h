@@ -115,7 +115,9 @@ cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s, int 
 // hT = h0 (or 0) for an empty sequence.
 cudaError_t launch_copy_state(const float *src, float *dst, size_t n, cudaStream_t s, int *launches);
 
-// tcgen05 / TMA tensor-core kernels (bf16, dk = 96, dv = 192).
+// tcgen05 / TMA tensor-core kernels (bf16, dk = 96, dv = 192). The forward:
+// the per-head decay on the one-CTA-per-(b, h) kernel (segmented when the
+// plan and the workspace allow), the per-token decay on the dv-half kernel.
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
 // The forward with one CTA per (b, h) holding the whole state (fwd_full.cu);
 // S_in (or NULL: p.h0) holds each segment's initial state when nseg > 1.
@@ -125,7 +127,8 @@ cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launc
 // Variable-length forward with the states in a pool (bf16, dk = 96, dv = 192).
 cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
-// dv and dh0 of the backward pass: the chunk kernel run in reverse time.
+// dv and dh0 of the per-token decay's backward: the dv-half chunk kernel run
+// in reverse time (p.g required).
 cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // dq and dk: the transposed-shape chunk kernel (192-wide scores, 96-wide outputs).
 cudaError_t launch_bwd_dq_tc(const BwdParams &p, cudaStream_t s, int *launches);
