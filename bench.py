@@ -126,13 +126,13 @@ def bwd_work(B, T, with_h0, with_dhT, with_dh0, C=CHUNK):
     the three intra products dP K, dP^T Q (2 C dk each) and P^T dO (2 C dv),
     and five state-sized products (dO S^T, V G^T, K G, the recomputed K^T V
     and the gradient update Q^T dO; 2 dk dv each): 356,352 at C = 128. The
-    launches issue more (each of the dq and dk kernels forms dO V^T, and both
-    dv-half CTAs of a head form Q K^T): `issued` counts those."""
+    launches issue more (each of the dq and dk kernels forms dO V^T):
+    `issued` counts that."""
     ht = B * H * T
     bytes_ = ht * (4 * DK * 2 + 3 * DV * 2) + \
         B * H * STATE_BYTES * (int(with_h0) + int(with_dhT) + int(with_dh0))
     flops = ht * (2 * 2 * C * DV + 3 * 2 * C * DK + 5 * 2 * DK * DV)
-    issued = flops + ht * (2 * C * DV + 2 * C * DK)
+    issued = flops + ht * 2 * C * DV
     return bytes_, flops, issued
 
 

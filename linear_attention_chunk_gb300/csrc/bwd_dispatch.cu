@@ -1,16 +1,21 @@
-// bwd_dispatch.cu -- bf16 backward dispatch: three tensor-core launches (four
-// with a per-token decay, whose gate gradient follows dq and dk).
-//   dv, dh0: the chunk kernel in reverse time (fwd_tc.cu)
-//   dq:      the transposed-shape chunk kernel, forward in time (bwd_tc.cu)
-//   dk:      the transposed-shape chunk kernel, reverse in time (bwd_tc.cu)
-// The three are independent; each reads the inputs it needs once. They run
-// concurrently: dq and dk on two helper streams forked from the caller's
-// stream and joined back to it with events, dv on the caller's stream. Each
-// launch alone ends in a partial wave of CTAs; side by side, one kernel's
-// CTAs fill the SMs the others leave idle (415.8 -> 374.9 us for the
-// training workload). Fork and join are event records and waits, so the call
-// stays asynchronous and can be captured in a CUDA graph. The helper streams
-// and events are created once per host thread and device, and kept.
+// bwd_dispatch.cu -- bf16 backward dispatch.
+// The per-head decay: two tensor-core launches.
+//   dk, dv, dh0: one launch pairing, for each (b, h), the transposed-shape
+//                chunk kernel in reverse time (dk) with the one-CTA-per-head
+//                chunk kernel in reverse time (dv, dh0) on neighbouring CTAs,
+//                so that q and do leave DRAM once for both (bwd_tc.cu)
+//   dq:          the transposed-shape chunk kernel, forward in time (bwd_tc.cu)
+// The per-token decay: dq, dk (bwd_tc.cu) and dv, dh0 (the dv-half chunk
+// kernel in reverse time, fwd_tc.cu) as three launches, then the gate
+// gradient after dq and dk (dg_tc.cu).
+// The launches are independent and run concurrently, on the caller's stream
+// and on helper streams forked from it and joined back to it with events:
+// each launch alone ends in a partial wave of CTAs; side by side, one
+// kernel's CTAs fill the SMs the others leave idle (415.8 -> 374.9 us for the
+// training workload when the backward was three launches). Fork and join are
+// event records and waits, so the call stays asynchronous and can be
+// captured in a CUDA graph. The helper streams and events are created once
+// per host thread and device, and kept.
 #include "kernels.h"
 
 namespace gla {
@@ -47,17 +52,13 @@ cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches) {
     cudaError_t e = fork_for_device(&f);
     if (e != cudaSuccess) return e;
     if ((e = cudaEventRecord(f->ev[0], s)) != cudaSuccess) return e;
-    for (int i = 0; i < 2; ++i)
-        if ((e = cudaStreamWaitEvent(f->aux[i], f->ev[0], 0)) != cudaSuccess) return e;
-    cudaError_t el = launch_bwd_dq_tc(p, f->aux[0], launches);
-    if (el == cudaSuccess) el = launch_bwd_dk_tc(p, f->aux[1], launches);
-    if (el == cudaSuccess) el = launch_bwd_dv_full_tc(p, s, launches);
+    if ((e = cudaStreamWaitEvent(f->aux[0], f->ev[0], 0)) != cudaSuccess) return e;
+    cudaError_t el = launch_bwd_kv_tc(p, s, launches);
+    if (el == cudaSuccess) el = launch_bwd_dq_tc(p, f->aux[0], launches);
     // Join whatever was launched before reporting, so the caller's stream
-    // never runs ahead of work still in flight on the helper streams.
-    for (int i = 0; i < 2; ++i) {
-        if ((e = cudaEventRecord(f->ev[1 + i], f->aux[i])) != cudaSuccess) return e;
-        if ((e = cudaStreamWaitEvent(s, f->ev[1 + i], 0)) != cudaSuccess) return e;
-    }
+    // never runs ahead of work still in flight on the helper stream.
+    if ((e = cudaEventRecord(f->ev[1], f->aux[0])) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(s, f->ev[1], 0)) != cudaSuccess) return e;
     return el;
 }
 

@@ -50,6 +50,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "fwd_full.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tc_common.cuh"
@@ -106,16 +107,17 @@ struct TrArgs {
     unsigned char *saved;
 };
 
+// The kernel body for the chain (b, h) = (unit / H, unit % H), run by warps
+// 0-13; a launch of more threads (the paired dk / dv launch below) leaves the
+// rest without a role.
 template <bool kRev, bool kGate>
-__global__ void __launch_bounds__(kThreads, 1)
-    gla_bwd_tr_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                      const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_o,
-                      const TrArgs a) {
+__device__ __forceinline__ void tr_body(const CUtensorMap &tm_a, const CUtensorMap &tm_b, const CUtensorMap &tm_c,
+                                        const CUtensorMap &tm_o, const TrArgs &a, int unit) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = smem_u32(sm);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+    const int b = unit / a.H, h = unit % a.H;
     const int C = a.C, T = a.T, nck = a.nck;
     const int ksteps_tok = C / 16;
 
@@ -154,20 +156,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tm_c);
         prefetch_tmap(&tm_o);
     }
-    if constexpr (!kGate) {   // the gated mode has no per-head decay (log_lambda is NULL)
-        const float l2 = log2_of_decay(a.log_lambda[h]);
-        for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
-        fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
-    }
-    // Zero what TMA never writes: the M-padding block of C~, and for C = 64 the
-    // rows 64..127 of every tile block (C~ rows there are made from zero C rows).
-    for (uint32_t i = threadIdx.x; i < kBlk / 16; i += kThreads)
-        *reinterpret_cast<uint4 *>(sm + kOffCt + 3 * kBlk + i * 16) = make_uint4(0, 0, 0, 0);
-    if (C < 128) {
-        const uint32_t lo = (uint32_t)C * 64, per_blk = (kBlk - lo) / 16;
-        for (uint32_t i = threadIdx.x; i < 15 * per_blk; i += kThreads) {
-            const uint32_t blk = i / per_blk, o = lo + (i % per_blk) * 16;
-            *reinterpret_cast<uint4 *>(sm + blk * kBlk + o) = make_uint4(0, 0, 0, 0);   // A, B, C blocks
+    if (threadIdx.x < kThreads) {
+        if constexpr (!kGate) {   // the gated mode has no per-head decay (log_lambda is NULL)
+            const float l2 = log2_of_decay(a.log_lambda[h]);
+            for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
+            fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
+        }
+        // Zero what TMA never writes: the M-padding block of C~, and for C = 64 the
+        // rows 64..127 of every tile block (C~ rows there are made from zero C rows).
+        for (uint32_t i = threadIdx.x; i < kBlk / 16; i += kThreads)
+            *reinterpret_cast<uint4 *>(sm + kOffCt + 3 * kBlk + i * 16) = make_uint4(0, 0, 0, 0);
+        if (C < 128) {
+            const uint32_t lo = (uint32_t)C * 64, per_blk = (kBlk - lo) / 16;
+            for (uint32_t i = threadIdx.x; i < 15 * per_blk; i += kThreads) {
+                const uint32_t blk = i / per_blk, o = lo + (i % per_blk) * 16;
+                *reinterpret_cast<uint4 *>(sm + blk * kBlk + o) = make_uint4(0, 0, 0, 0);   // A, B, C blocks
+            }
         }
     }
     fence_proxy_async_smem();
@@ -398,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_sync(kBarP, kGroupThreads);
             if (gt == 0) mbar_arrive(bar(BAR_PREADY));
         }
-    } else {
+    } else if (warp < 14) {
         // ------------------------------- warps 10-13: state hand-off, output
         const uint32_t quad = (uint32_t)(warp & 3);
         const uint32_t row = quad * 32 + (uint32_t)lane;
@@ -545,6 +549,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool kRev, bool kGate>
+__global__ void __launch_bounds__(kThreads, 1)
+    gla_bwd_tr_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_o,
+                      const TrArgs a) {
+    tr_body<kRev, kGate>(tm_a, tm_b, tm_c, tm_o, a, (int)blockIdx.x);
+}
+
+// dk and dv of the per-head decay in one launch. Each (b, h) has a dk CTA
+// (this file's kernel in reverse time: rows v, columns do, values q) and a dv
+// CTA (the one-CTA-per-head kernel of fwd_full.cuh in reverse time: rows k,
+// columns q, values do). Both walk the chunks last to first. The CTAs come in
+// groups of four, [dk u, dk u+1, dv u, dv u+1] for u = 2 g: CTAs that start
+// together read each q and do tile close in time, so the second read is served
+// from L2 and q and do leave DRAM once for both gradients. (With [dk u, dv u]
+// side by side the launch measured 19 % slower: neighbouring SMs then run
+// different code.) An odd B H ends in one group of two, [dk, dv].
+constexpr int kPairThreads = 512;
+static_assert(kPairThreads >= kThreads && kPairThreads == fullhead::kThreads, "paired launch width");
+constexpr uint32_t kPairSmem = kSmemBytes > fullhead::kSmemBytes ? kSmemBytes : fullhead::kSmemBytes;
+
+template <int kC>
+__global__ void __launch_bounds__(kPairThreads, 1)
+    gla_bwd_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_dk,
+                      const __grid_constant__ CUtensorMap tm_row, const __grid_constant__ CUtensorMap tm_col,
+                      const __grid_constant__ CUtensorMap tm_val, const __grid_constant__ CUtensorMap tm_dv,
+                      const TrArgs ta, const fullhead::FullArgs fa) {
+    const int BH = (int)(gridDim.x >> 1), g = (int)(blockIdx.x >> 2), r = (int)(blockIdx.x & 3);
+    const bool full_group = 2 * g + 1 < BH;
+    const int unit = full_group ? 2 * g + (r & 1) : 2 * g;
+    const bool dv = full_group ? (r >> 1) != 0 : (r & 1) != 0;
+    if (dv)
+        fullhead::full_body<true, kC>(tm_row, tm_col, tm_val, tm_dv, fa, unit);
+    else
+        tr_body<true, false>(tm_a, tm_b, tm_c, tm_dk, ta, unit);
+}
+
+template <bool kRev, bool kGate>
 cudaError_t launch_tr(const void *A, const void *Bt, const void *Ct, void *out, const float *s0, float init_mul,
                       const BwdParams &p, unsigned char *saved, cudaStream_t s, int *launches) {
     CUtensorMap ma, mb, mc, mo;
@@ -590,6 +632,33 @@ cudaError_t launch_bwd_dk_tc(const BwdParams &p, cudaStream_t s, int *launches) 
                                          bwd_gated_tc_workspace_size(p.B, p.T, p.H, p.chunk) / 2,
                                      s, launches);
     return launch_tr<true, false>(p.v, p.do_, p.q, p.dk_out, p.dhT, 1.f / p.scale, p, nullptr, s, launches);
+}
+
+// dk, dv and dh0 of the per-head decay: one launch of 2 B H CTAs (see
+// gla_bwd_kv_kernel). dk: state G / s from dhT / s; dv: the same state,
+// written out times s as dh0.
+cudaError_t launch_bwd_kv_tc(const BwdParams &p, cudaStream_t s, int *launches) {
+    if (p.dk != kDk || p.dv != kDv || p.g) return cudaErrorInvalidValue;
+    CUtensorMap ma, mb, mc, mdk, mrow, mcol, mval, mdv;
+    cudaError_t e;
+    if ((e = make_token_map(&ma, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mb, p.do_, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mc, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mdk, p.dk_out, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mrow, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mcol, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mval, p.do_, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mdv, p.dv_out, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    const int nck = (p.T + p.chunk - 1) / p.chunk;
+    const TrArgs ta{p.log_lambda, p.dhT, p.scale, 1.f / p.scale, p.T, p.H, p.chunk, nck, p.status, nullptr, nullptr};
+    const fullhead::FullArgs fa{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, nck, 1, nck,
+                                p.B * p.H, 0, p.status};
+    auto kernel = p.chunk == 128 ? gla_bwd_kv_kernel<128> : gla_bwd_kv_kernel<64>;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem)) != cudaSuccess)
+        return e;
+    kernel<<<(unsigned)(2 * p.B * p.H), kPairThreads, kPairSmem, s>>>(ma, mb, mc, mdk, mrow, mcol, mval, mdv, ta, fa);
+    if (launches) ++*launches;
+    return cudaGetLastError();
 }
 
 }  // namespace gla

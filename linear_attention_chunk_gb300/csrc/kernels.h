@@ -123,7 +123,6 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
 // S_in (or NULL: p.h0) holds each segment's initial state when nseg > 1.
 cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int seg_chunks, cudaStream_t s,
                                int *launches);
-cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // Variable-length forward with the states in a pool (bf16, dk = 96, dv = 192).
 cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
@@ -133,6 +132,9 @@ cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // dq and dk: the transposed-shape chunk kernel (192-wide scores, 96-wide outputs).
 cudaError_t launch_bwd_dq_tc(const BwdParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_dk_tc(const BwdParams &p, cudaStream_t s, int *launches);
+// dk, dv and dh0 of the per-head decay in one launch: the dk and the dv chain
+// of each (b, h) on neighbouring CTAs, so q and do are read from DRAM once.
+cudaError_t launch_bwd_kv_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // The gated backward (p.g, p.dg set): dq, dk, dv, dh0 by the three chunk
 // kernels in gated mode, the dq and dk kernels saving the bf16 state copy of
 // every chunk in the workspace, then dg from those copies (dg_tc.cu).

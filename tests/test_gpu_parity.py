@@ -165,6 +165,15 @@ def test_bwd_bf16(gla, T, C):
     check_bwd(gla, c)
 
 
+@pytest.mark.parametrize("B,H", [(1, 1), (1, 3), (3, 5)])
+def test_bwd_bf16_odd_head_count(gla, B, H):
+    """dk and dv run in one launch whose CTAs come in groups of four (two
+    (b, h) chains each); an odd number of chains ends in a group of two."""
+    c = gen.make_case(B, 200, H, 96, 192, seed=73 + B * H, dtype="bf16", normalise_k=True, h0_std=0.05,
+                      with_grad=True, dhT_std=0.05, lam_random=True, chunk=128)
+    check_bwd(gla, c)
+
+
 def test_bwd_bf16_page_schedule(gla):
     lam = gen.decay_page_schedule(16)
     lam[2] = 0.0
