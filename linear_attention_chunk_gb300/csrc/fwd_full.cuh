@@ -129,6 +129,10 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     const uint32_t base = smem_u32(sm);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int C = kC;   // chunk length, 64 or 128
+    // Token rows of the score, P, Q~ and output tiles: M = C. An M = 64 tile
+    // holds row i in TMEM lane 32 (i / 16) + i % 16 (lanes 0-15 of each
+    // quadrant), as accumulator and as the A operand read from TMEM.
+    constexpr int kM = C;
     constexpr int ksteps_tok = C / 16;
     const int seg = blk / a.BH, bh = blk % a.BH;
     const int b = bh / a.H, h = bh % a.H;
@@ -164,13 +168,6 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         const float l2 = log2_of_decay(a.log_lambda[h]);
         for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
         fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
-    }
-    if constexpr (C < 128) {
-        // Q's rows C..127 feed the unused rows of A (M = 128): keep them zero.
-        const uint32_t lo = (uint32_t)C * 64, per_blk = (kBlk - lo) / 16;
-        for (uint32_t i = threadIdx.x; i < 3 * per_blk; i += kThreads)
-            st_shared_v4(base + kOffQ + (i / per_blk) * kBlk + lo + (i % per_blk) * 16, 0, 0, 0, 0);
-        fence_proxy_async_smem();
     }
     if (warp == 3) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -235,9 +232,9 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     } else if (warp == 3) {
         // ----------------------------------------------- MMA issuer (event loop)
         if (lane == 0) {
-            const uint32_t idA = idesc_bf16(128, C, false, false);    // Q K^T: both K-major
+            const uint32_t idA = idesc_bf16(kM, C, false, false);     // Q K^T: both K-major
             const uint32_t idS = idesc_bf16(128, kDv, true, true);    // K~^T V: both MN-major
-            const uint32_t idO = idesc_bf16(128, kDv, false, true);   // Q~ S, P V: A in TMEM, B MN-major
+            const uint32_t idO = idesc_bf16(kM, kDv, false, true);    // Q~ S, P V: A in TMEM, B MN-major
             int qk = 0, stt = 0, out = 0;   // next chunk of each event kind
             uint64_t t_idle = globaltimer_ns();
             uint32_t spins = 0;
@@ -321,7 +318,11 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     } else if (warp >= 4 && warp < 8) {
         // ------------------------------------------------- P group (4..7)
         const uint32_t quad = (uint32_t)(warp & 3);
-        const uint32_t row = quad * 32 + (uint32_t)lane;          // TMEM lane = token row
+        const uint32_t row = quad * 32 + (uint32_t)lane;          // K row scaled by this thread
+        // the token row in this thread's TMEM lane (M = 64: lanes 16-31 hold none and
+        // repeat the row of lane - 16, into TMEM lanes no MMA reads)
+        const uint32_t trow = kM == 128 ? row : quad * 16 + ((uint32_t)lane & 15u);
+        const int dblk = (int)trow / 32;                          // the diagonal P block
         const uint32_t gt = (uint32_t)threadIdx.x - 128;         // 0..127
         const uint32_t tl = tmem + ((quad * 32) << 16);
         constexpr int nblk = C / 32;
@@ -336,7 +337,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             for (int j = 0; j < 3; ++j)
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    qrow[4 * j + cc] = ld_shared_v4(base + kOffQ + j * kBlk + sw64_offset(row, (uint32_t)cc));
+                    qrow[4 * j + cc] = ld_shared_v4(base + kOffQ + j * kBlk + sw64_offset(trow, (uint32_t)cc));
             named_sync(kBarP, 128);
             if (gt == 0) mbar_arrive(bar(BAR_QFREE));
             if (!gwait(bar(BAR_QKDONE), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
@@ -355,12 +356,12 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             // reverse) are written as zeros.
 #pragma unroll 1
             for (int bk = 0; bk < nblk; ++bk) {
-                if (kRev ? bk >= (int)quad : bk <= (int)quad) {
+                if (kRev ? bk >= dblk : bk <= dblk) {
                     uint32_t x[32];
                     tmem_ld_32cols(tl + kColAP + 32u * bk, x);
                     tmem_ld_wait();
                     pack_scores(x);
-                    build_p_block<kRev>(x, (int)row - 32 * bk, tl + kColAP + 16u * bk, pp, pr);
+                    build_p_block<kRev>(x, (int)trow - 32 * bk, tl + kColAP + 16u * bk, pp, pr);
                 } else {
                     uint32_t z[16];
 #pragma unroll
@@ -373,7 +374,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             // registers. This warp's score columns there (C = 128) were read above.
             {
                 // lambda^(i+1); lambda^(Cc-1-j) in reverse (zero past the end)
-                const float wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+                const float wq = kRev ? (trow < (uint32_t)Cc ? pw[Cc - 1 - (int)trow] : 0.f) : pw[trow + 1];
                 const uint32_t wq2 = pack_bf16x2(wq, wq);
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {
@@ -397,7 +398,9 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     } else if (warp >= 8 && warp < 12) {
         // ------------------------------------------------- E group (8..11)
         const uint32_t quad = (uint32_t)(warp & 3);
-        const uint32_t row = quad * 32 + (uint32_t)lane;
+        // the output row in this thread's TMEM lane (M = 64: lanes 0-15 of the quadrant)
+        const uint32_t row = kM == 128 ? quad * 32 + (uint32_t)lane : quad * 16 + (uint32_t)lane;
+        const bool has_row = kM == 128 || lane < 16;
         const uint32_t gt = (uint32_t)threadIdx.x - 256;         // 0..127
         const uint32_t tl = tmem + ((quad * 32) << 16);
         uint32_t kw = 0;
@@ -416,10 +419,10 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                     const int blk = 2 * bp;
                     tmem_ld_wait();
                     tmem_ld_32cols(tl + kColO + 32u * (blk + 1), rb);
-                    write_row_sw64_bits(sm + (stg - base) + blk * kBlk, row, ra, a.scale);
+                    if (has_row) write_row_sw64_bits(sm + (stg - base) + blk * kBlk, row, ra, a.scale);
                     tmem_ld_wait();
                     if (bp < 2) tmem_ld_32cols(tl + kColO + 32u * (blk + 2), ra);
-                    write_row_sw64_bits(sm + (stg - base) + (blk + 1) * kBlk, row, rb, a.scale);
+                    if (has_row) write_row_sw64_bits(sm + (stg - base) + (blk + 1) * kBlk, row, rb, a.scale);
                 }
             }
             tc_fence_before();
