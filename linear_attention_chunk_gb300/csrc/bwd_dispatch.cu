@@ -5,8 +5,8 @@
 //                chunk kernel in reverse time (dv, dh0) on neighbouring CTAs,
 //                so that q and do leave DRAM once for both (bwd_tc.cu)
 //   dq:          the transposed-shape chunk kernel, forward in time (bwd_tc.cu)
-// The per-token decay: dq, dk (bwd_tc.cu) and dv, dh0 (the dv-half chunk
-// kernel in reverse time, fwd_tc.cu) as three launches, then the gate
+// The per-token decay: dq, dk (bwd_tc.cu) and dv, dh0 (the one-CTA-per-head
+// chunk kernel in reverse time, fwd_full.cu) as three launches, then the gate
 // gradient after dq and dk (dg_tc.cu).
 // The launches are independent and run concurrently, on the caller's stream
 // and on helper streams forked from it and joined back to it with events:
@@ -75,7 +75,7 @@ cudaError_t launch_bwd_gated_tc(const BwdParams &p, cudaStream_t s, int *launche
         if ((e = cudaStreamWaitEvent(f->aux[i], f->ev[0], 0)) != cudaSuccess) return e;
     cudaError_t el = launch_bwd_dq_tc(p, f->aux[0], launches);
     if (el == cudaSuccess) el = launch_bwd_dk_tc(p, f->aux[1], launches);
-    if (el == cudaSuccess) el = launch_bwd_dv_tc(p, s, launches);
+    if (el == cudaSuccess) el = launch_bwd_dv_full_tc(p, s, launches);
     if ((e = cudaEventRecord(f->ev[1], f->aux[1])) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(f->aux[0], f->ev[1], 0)) != cudaSuccess) return e;
     if (el == cudaSuccess) el = launch_bwd_dg_tc(p, f->aux[0], launches);

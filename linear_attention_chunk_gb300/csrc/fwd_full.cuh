@@ -83,7 +83,13 @@ enum { BAR_FULLQ, BAR_FULLK0, BAR_FULLK1, BAR_FULLV0, BAR_FULLV1, BAR_QFREE, BAR
 constexpr uint32_t kOffBar = kOffPair + 2 * 164 * 4;
 static_assert(kPairLen <= 164, "pair table stride");
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag, 3 x 2 decision slots
-constexpr uint32_t kSmemUsed = kOffMisc + 32;
+// Per-token decay: the H group's two chunk-decay slots, and the P group's gate
+// arrays for the chunk in hand ([128] running log2-decays, [128] last clearing
+// positions, [128] per-token factors exp(g)).
+constexpr uint32_t kOffHDec = kOffMisc + 32;
+constexpr uint32_t kOffGate = kOffHDec + 16;
+constexpr uint32_t kGateArr = 128 * 12;
+constexpr uint32_t kSmemUsed = kOffGate + kGateArr;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;       // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffSb % 1024 == 0, "tile alignment");
@@ -102,6 +108,7 @@ struct FullArgs {
     int nseg, seg_chunks, BH;
     size_t h0_seg_stride;
     unsigned int *status;
+    const float *g;        // per-token log-decays [B, T, H] (the gated form), or NULL
 };
 
 // One elected thread of an n-thread group waits; the verdict is published
@@ -114,14 +121,44 @@ __device__ __forceinline__ bool gwait(uint32_t bar, uint32_t parity, const WaitC
     return decision[(k++) & 1] == 0;
 }
 
+// Gated mode: the decay of a whole chunk from one warp's gates (four per lane,
+// 0 past the chunk's end): 0 if any gate clears the state, else 2^(the sum of
+// the log2-decays).
+__device__ __forceinline__ float chunk_decay_warp(const float (&x)[4]) {
+    float s = 0.f;
+    int clr = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        if (x[r] > kResetLogDecay)
+            s += x[r] * kLog2e;
+        else
+            clr = 1;
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, d);
+        clr |= __shfl_xor_sync(0xffffffffu, clr, d);
+    }
+    return clr ? 0.f : exp2f(s);
+}
+
 // kRev = false: the forward pass. kRev = true: the same chunked recurrence
 // run backwards in time, which is how the backward pass obtains dv and dh0:
 // rows are k tokens, columns q tokens, values dO, the mask keeps col >= row
 // with lambda^(col-row), the row weights swap (lambda^(Cc-1-j) on the
 // readout, lambda^(i+1) on the state update), chunks run last to first, and
 // the state is the state gradient divided by the scale.
+// kGate: the per-token decay of the gated form, S_t = exp(g_t) S_{t-1} +
+// k_t v_t^T, in place of lambda: every power of lambda becomes the decay of a
+// run of the chunk's tokens, lambda^(i-j) -> exp(G_i - G_j), lambda^(i+1) ->
+// exp(G_i), lambda^(Cc-1-j) -> exp(G_last - G_j), lambda^Cc -> exp(G_last),
+// with G the running sum of g over the chunk; a gate at or below the clearing
+// threshold zeroes every decay across it. The P group's first warp scans each
+// chunk's gates into shared arrays (loaded one chunk ahead), and P's weights
+// are walked along the factors exp(g); the H group's first warp reduces each
+// chunk's gates to its total decay for the state's rescale, one chunk ahead.
 // `blk` is the CTA's unit: segment blk / BH of chain (b, h) = blk % BH.
-template <bool kRev, int kC>
+template <bool kRev, int kC, bool kGate = false>
 __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                           const CUtensorMap &tm_o, const FullArgs &a, int blk) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -143,6 +180,14 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     const float *h0 = a.h0 ? a.h0 + (size_t)seg * a.h0_seg_stride : nullptr;
     auto tok0 = [&](int c) { return (kRev ? nck - 1 - c : cbeg + c) * C; };
     auto clen = [&](int c) { return min(C, T - tok0(c)); };
+    // Gated mode: this lane's four gates (tokens 4 lane .. 4 lane + 3) of chunk
+    // c in processing order, 0 past the sequence's end or the CTA's last chunk.
+    auto load_gates = [&](int c, float (&x)[4]) {
+        const int t0 = c < nck ? tok0(c) : 0, cc = c < nck ? clen(c) : 0;
+        const float *gh = a.g + ((size_t)b * T + t0) * a.H + h;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) x[r] = 4 * lane + r < cc ? gh[(size_t)(4 * lane + r) * a.H] : 0.f;
+    };
 
     float *pw = reinterpret_cast<float *>(sm + kOffPw);
     uint32_t *pp = reinterpret_cast<uint32_t *>(sm + kOffPair);
@@ -164,7 +209,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_o);
     }
-    {
+    if constexpr (!kGate) {   // the gated form has no per-head decay (log_lambda is NULL)
         const float l2 = log2_of_decay(a.log_lambda[h]);
         for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
         fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
@@ -327,8 +372,21 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         const uint32_t tl = tmem + ((quad * 32) << 16);
         constexpr int nblk = C / 32;
         uint32_t kw = 0;
+        // gated: the group's gate arrays, scanned by its first warp one chunk at a time
+        float *Gl = reinterpret_cast<float *>(sm + kOffGate);
+        int *Zc = reinterpret_cast<int *>(sm + kOffGate + 512);
+        float *Af = reinterpret_cast<float *>(sm + kOffGate + 1024);
+        float gpre[4];
+        if (kGate && gt < 32) load_gates(0, gpre);
         for (int c = 0; c < nck; ++c) {
             const int Cc = clen(c);
+            if (kGate && gt < 32) {
+                // every thread of the group is past chunk c-1's reads of the arrays (the
+                // barrier before its P-ready signal); the barrier in the wait below
+                // publishes the new ones
+                gate_scan_store(gpre, lane, Gl, Zc, Af);
+                load_gates(c + 1, gpre);
+            }
             // Q has one buffer: as soon as it lands, this thread's row of it goes to
             // registers, and the tile is free once QK(c), its other reader, is done.
             if (!gwait(bar(BAR_FULLQ), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
@@ -344,8 +402,16 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             tc_fence_after();
             // K~ = diag(lambda^(Cc-1-j)) K in place (zero past the end), or lambda^(i+1)
             // in reverse; signalled at once.
-            scale_rows<3>(sm + (stage(c) - base) + kStK, row,
-                          kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f));
+            {
+                float wk;
+                if constexpr (kGate && kRev)   // the decay of the chunk's tokens 0..i
+                    wk = Zc[row] < 0 ? exp2f(Gl[row]) : 0.f;
+                else if constexpr (kGate)      // the decay of tokens j+1..Cc-1
+                    wk = row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
+                else
+                    wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
+                scale_rows<3>(sm + (stage(c) - base) + kStK, row, wk);
+            }
             fence_proxy_async_smem();
             named_sync(kBarP, 128);
             if (gt == 0) mbar_arrive(bar(BAR_KREADY));
@@ -359,9 +425,28 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                 if (kRev ? bk >= dblk : bk <= dblk) {
                     uint32_t x[32];
                     tmem_ld_32cols(tl + kColAP + 32u * bk, x);
-                    tmem_ld_wait();
-                    pack_scores(x);
-                    build_p_block<kRev>(x, (int)trow - 32 * bk, tl + kColAP + 16u * bk, pp, pr);
+                    if constexpr (kGate) {
+                        const bool dg = bk == dblk;
+                        const float gi = Gl[trow];
+                        if constexpr (kRev) {
+                            // row j, columns i >= j: walked rightwards from the block's first column
+                            const int il = 32 * bk;
+                            const float d0 = dg || Zc[il] > (int)trow ? 0.f : ex2_approx(Gl[il] - gi);
+                            tmem_ld_wait();
+                            build_p_block_gated_rev(x, dg ? (int)trow - il : -1, il, d0, Af, tl + kColAP + 16u * bk);
+                        } else {
+                            // row i, columns j <= i: walked leftwards from the block's last column
+                            const int jr = 32 * bk + 31;
+                            const float d0 = dg || Zc[trow] > jr ? 0.f : ex2_approx(gi - Gl[jr]);
+                            tmem_ld_wait();
+                            build_p_block_gated(x, dg ? (int)trow - 32 * bk : 32, 32 * bk, d0, Af,
+                                                tl + kColAP + 16u * bk);
+                        }
+                    } else {
+                        tmem_ld_wait();
+                        pack_scores(x);
+                        build_p_block<kRev>(x, (int)trow - 32 * bk, tl + kColAP + 16u * bk, pp, pr);
+                    }
                 } else {
                     uint32_t z[16];
 #pragma unroll
@@ -374,7 +459,13 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             // registers. This warp's score columns there (C = 128) were read above.
             {
                 // lambda^(i+1); lambda^(Cc-1-j) in reverse (zero past the end)
-                const float wq = kRev ? (trow < (uint32_t)Cc ? pw[Cc - 1 - (int)trow] : 0.f) : pw[trow + 1];
+                float wq;
+                if constexpr (kGate && kRev)   // the decay of tokens j+1..Cc-1
+                    wq = trow < (uint32_t)Cc && Zc[Cc - 1] <= (int)trow ? exp2f(Gl[Cc - 1] - Gl[trow]) : 0.f;
+                else if constexpr (kGate)      // the decay of the chunk's tokens 0..i
+                    wq = Zc[trow] < 0 ? exp2f(Gl[trow]) : 0.f;
+                else
+                    wq = kRev ? (trow < (uint32_t)Cc ? pw[Cc - 1 - (int)trow] : 0.f) : pw[trow + 1];
                 const uint32_t wq2 = pack_bf16x2(wq, wq);
 #pragma unroll
                 for (int j = 0; j < 3; ++j) {
@@ -448,9 +539,19 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         const uint32_t tl = tmem + ((quad * 32) << 16);
         const int blk0 = 3 * half;
         uint32_t kw = 0;
+        // gated: chunk decays, reduced by the group's first warp one chunk ahead
+        volatile float *hdec = reinterpret_cast<volatile float *>(sm + kOffHDec);
+        float hpre[4];
+        if (kGate && gt < 32) {
+            load_gates(0, hpre);
+            const float d = chunk_decay_warp(hpre);
+            if (lane == 0) hdec[0] = d;
+            load_gates(1, hpre);
+        }
+        if constexpr (kGate) named_sync(kBarH, kHThreads);
         // Initial state: copy = bf16(h0), TMEM S = lambda^C0 h0 (C0: the first chunk's length).
         {
-            const float w0 = pw[clen(0)];
+            const float w0 = kGate ? hdec[0] : pw[clen(0)];
             const float *src = h0 ? h0 + (((size_t)b * a.H + h) * kDk + row) * kDv : nullptr;
 #pragma unroll 1
             for (int blk = blk0; blk < blk0 + 3; ++blk) {
@@ -480,6 +581,12 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         for (int c = 0; c < nck; ++c) {
             const bool last = c == nck - 1;
             const bool write_hT = last && last_seg && a.hT;
+            if (kGate && gt < 32) {
+                // the decay of chunk c+1 (published by the barrier in the wait below)
+                const float d = chunk_decay_warp(hpre);
+                if (lane == 0) hdec[(c + 1) & 1] = d;
+                load_gates(c + 2, hpre);
+            }
             if (!gwait(bar(BAR_SFULL), (uint32_t)c & 1u, ctl, dec + 4, gt, kBarH, kHThreads, kw)) break;
             // the copy is single: OUT(c) must have read it before it changes
             if (!gwait(bar(BAR_OFULL), (uint32_t)c & 1u, ctl, dec + 4, gt, kBarH, kHThreads, kw)) break;
@@ -492,7 +599,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                        kHThreads, kw))
                 break;
             tc_fence_after();
-            const float wn = last ? 1.f : pw[clen(c + 1)];
+            const float wn = last ? 1.f : (kGate ? hdec[(c + 1) & 1] : pw[clen(c + 1)]);
             // the staging row of hT (fp32, 768 bytes): the stage not holding chunk c
             unsigned char *hrow = write_hT ? sm + (stage(c + 1) - base) + row * (kDv * 4) : nullptr;
             // Three 32-column blocks, the next block's TMEM load in flight while

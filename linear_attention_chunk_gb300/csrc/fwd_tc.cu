@@ -715,19 +715,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// One launch of the chunk kernel: `qm`, `km` are [B,T,H,96] maps, `vm` and
-// `om` [B,T,H,192] maps (box height = chunk).
-template <bool kRev, bool kGate = false>
+// One launch of the dv-half chunk kernel: `qm`, `km` are [B,T,H,96] maps,
+// `vm` and `om` [B,T,H,192] maps (box height = chunk).
+template <bool kGate>
 cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
                                 const CUtensorMap &om, const FwdTcArgs &a, int B, cudaStream_t s, int *launches) {
-    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<kRev, 128, false, kGate> : gla_fwd_tc_kernel<kRev, 64, false, kGate>;
+    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<false, 128, false, kGate> : gla_fwd_tc_kernel<false, 64, false, kGate>;
     const uint32_t smem = kGate ? kSmemBytesGated : kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(B * a.H * 2 * a.nseg);
-    kernel<<<grid, kThreads, smem, s>>>(qm, km, vm, om, a);
+    kernel<<<(unsigned)(B * a.H * 2), kThreads, smem, s>>>(qm, km, vm, om, a);
     if (launches) ++*launches;
     return cudaGetLastError();
+}
+
+// The forward with two CTAs per (b, h) chain, one per half of the value
+// columns: for few chains, whose chunk period the halved state shortens.
+cudaError_t launch_fwd_half_tc(const FwdParams &p, cudaStream_t s, int *launches) {
+    CUtensorMap mq, mk, mv, mo;
+    cudaError_t e;
+    if ((e = make_token_map(&mq, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mk, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mo, p.o, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    const int nck = (p.T + p.chunk - 1) / p.chunk;
+    const FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, nck, 1, nck, p.B * p.H, 0,
+                      p.status, nullptr, nullptr, 0, nullptr, p.g};
+    return p.g ? launch_chunk_kernel<true>(mq, mk, mv, mo, a, p.B, s, launches)
+               : launch_chunk_kernel<false>(mq, mk, mv, mo, a, p.B, s, launches);
 }
 
 }  // namespace
@@ -738,36 +753,21 @@ size_t fwd_tc_workspace_size(int B, int T, int H, int chunk, bool gated) {
 
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv, mo;
-    cudaError_t e;
-    if ((e = make_token_map(&mq, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
-    if ((e = make_token_map(&mk, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
-    if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
-    if ((e = make_token_map(&mo, p.o, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
-    const int nck = (p.T + p.chunk - 1) / p.chunk;
-    FwdTcArgs a{p.log_lambda, p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, p.chunk, nck, 1, nck, p.B * p.H, 0, p.status,
-                nullptr, nullptr, 0, nullptr, p.g};
-    // Few (b, h) pairs and a long sequence: split each sequence into segments
-    // that run in parallel, when the caller gave the workspace for it.
-    const bool gated = p.g != nullptr;
+    // One CTA holds the whole state of a (b, h) chain. Few chains and a long
+    // sequence: split each sequence into segments that run in parallel, when
+    // the caller gave the workspace for it. Few chains otherwise (two CTAs per
+    // chain still within one wave): two CTAs per chain, each half the state.
     const SegPlan plan = plan_segments(p.B, p.T, p.H, p.chunk);
-    const bool segmented = plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan, gated);
-    // The per-head decay: one CTA holds the whole state of a (b, h) chain or segment.
-    if (!gated) {
-        if (!segmented) return launch_fwd_full_tc(p, nullptr, 1, nck, s, launches);
-        float *S_in = nullptr;
-        if ((e = launch_seg_prologue(p, plan, &S_in, s, launches)) != cudaSuccess) return e;
-        return launch_fwd_full_tc(p, S_in, plan.nseg, plan.seg_chunks, s, launches);
+    const bool segmented =
+        plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan, p.g != nullptr);
+    if (!segmented) {
+        if (2L * p.B * p.H <= device_sm_count()) return launch_fwd_half_tc(p, s, launches);
+        return launch_fwd_full_tc(p, nullptr, 1, 0, s, launches);
     }
-    if (segmented) {
-        float *S_in = nullptr;
-        if ((e = launch_seg_prologue(p, plan, &S_in, s, launches)) != cudaSuccess) return e;
-        a.h0 = S_in;
-        a.nseg = plan.nseg;
-        a.seg_chunks = plan.seg_chunks;
-        a.h0_seg_stride = (size_t)p.B * p.H * kDk * kDv;
-    }
-    return launch_chunk_kernel<false, true>(mq, mk, mv, mo, a, p.B, s, launches);
+    float *S_in = nullptr;
+    cudaError_t e = launch_seg_prologue(p, plan, &S_in, s, launches);
+    if (e != cudaSuccess) return e;
+    return launch_fwd_full_tc(p, S_in, plan.nseg, plan.seg_chunks, s, launches);
 }
 
 // Variable-length forward: one CTA per (sequence, head, dv half) over the
@@ -792,24 +792,6 @@ cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *lau
     kernel<<<(unsigned)(p.nseq * p.H * 2), kThreads, smem, s>>>(mq, mk, mv, mo, a);
     if (launches) ++*launches;
     return cudaGetLastError();
-}
-
-// dv and dh0 of the backward pass of the per-token decay: the chunk
-// recurrence in reverse time with rows = k, columns = q, values = dO; state =
-// (state gradient) / scale, seeded by dhT / scale. (The per-head decay's dv
-// runs on the one-CTA-per-head kernel, fwd_full.cu.)
-cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches) {
-    if (p.dk != kDk || p.dv != kDv || !p.g) return cudaErrorInvalidValue;
-    CUtensorMap mrow, mcol, mval, mout;
-    cudaError_t e;
-    if ((e = make_token_map(&mrow, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
-    if ((e = make_token_map(&mcol, p.q, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
-    if ((e = make_token_map(&mval, p.do_, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
-    if ((e = make_token_map(&mout, p.dv_out, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
-    const int nck = (p.T + p.chunk - 1) / p.chunk;
-    FwdTcArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, p.chunk, nck, 1, nck,
-                p.B * p.H, 0, p.status, nullptr, nullptr, 0, nullptr, p.g};
-    return launch_chunk_kernel<true, true>(mrow, mcol, mval, mout, a, p.B, s, launches);
 }
 
 }  // namespace gla

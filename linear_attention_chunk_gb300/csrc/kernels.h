@@ -115,20 +115,21 @@ cudaError_t launch_decode(const DecodeParams &p, bool bf16, cudaStream_t s, int 
 // hT = h0 (or 0) for an empty sequence.
 cudaError_t launch_copy_state(const float *src, float *dst, size_t n, cudaStream_t s, int *launches);
 
-// tcgen05 / TMA tensor-core kernels (bf16, dk = 96, dv = 192). The forward:
-// the per-head decay on the one-CTA-per-(b, h) kernel (segmented when the
-// plan and the workspace allow), the per-token decay on the dv-half kernel.
+// tcgen05 / TMA tensor-core kernels (bf16, dk = 96, dv = 192). The forward
+// runs on the one-CTA-per-(b, h) kernel, segmented when the plan and the
+// workspace allow, and on the dv-half kernel (two CTAs per chain) when few
+// chains run unsegmented; the variable-length prefill on the dv-half kernel.
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
 // The forward with one CTA per (b, h) holding the whole state (fwd_full.cu);
 // S_in (or NULL: p.h0) holds each segment's initial state when nseg > 1.
 cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int seg_chunks, cudaStream_t s,
                                int *launches);
+// dv and dh0 of the per-token decay's backward on the one-CTA-per-(b, h)
+// kernel in reverse time (p.g required).
+cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // Variable-length forward with the states in a pool (bf16, dk = 96, dv = 192).
 cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
-// dv and dh0 of the per-token decay's backward: the dv-half chunk kernel run
-// in reverse time (p.g required).
-cudaError_t launch_bwd_dv_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // dq and dk: the transposed-shape chunk kernel (192-wide scores, 96-wide outputs).
 cudaError_t launch_bwd_dq_tc(const BwdParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_dk_tc(const BwdParams &p, cudaStream_t s, int *launches);
@@ -152,6 +153,8 @@ struct SegPlan {
     int seg_chunks;  // chunks per segment (the last may be shorter)
 };
 SegPlan plan_segments(int B, int T, int H, int chunk);
+// The current device's SM count (152 if it cannot be read).
+int device_sm_count();
 size_t seg_workspace_bytes(int B, int H, const SegPlan &p, bool gated = false);
 cudaError_t launch_seg_prologue(const FwdParams &p, const SegPlan &plan, float **S_in, cudaStream_t s,
                                 int *launches);

@@ -309,12 +309,14 @@ int sm_count() {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
         cudaGetLastError();
-        return 148;
+        return 152;
     }
     return n;
 }
 
 }  // namespace
+
+int device_sm_count() { return sm_count(); }
 
 SegPlan plan_segments(int B, int T, int H, int chunk) {
     SegPlan p{1, 0};

@@ -80,13 +80,15 @@ def test_gated_fwd_bf16_clearing_gates(gla):
 
 
 @pytest.mark.parametrize("C", [128, 64])
-def test_gated_fwd_bf16_clears_on_block_edges(gla, C):
-    """The tensor-core kernel builds P in 32-column blocks, walking each row's
+@pytest.mark.parametrize("H", [6, 80])
+def test_gated_fwd_bf16_clears_on_block_edges(gla, C, H):
+    """The tensor-core kernels build P in 32-column blocks, walking each row's
     weights leftwards from the block's last column: clearing gates on either
     side of a block edge, two in one block, on a chunk's last and the next
     chunk's first token, and gates at and just above the kernel's clearing
-    threshold (a log-decay of -80, whose exp is below 1e-34)."""
-    c = gen.make_case(1, 552, 6, 96, 192, seed=334 + C, dtype="bf16", normalise_k=True, h0_std=0.1, chunk=C,
+    threshold (a log-decay of -80, whose exp is below 1e-34). 6 chains run two
+    CTAs each (half the state each), 80 chains one CTA each (the whole state)."""
+    c = gen.make_case(1, 552, H, 96, 192, seed=334 + C + H, dtype="bf16", normalise_k=True, h0_std=0.1, chunk=C,
                       gate="gla")
     g = c.extra["g"].copy()
     g[0, 31, 0] = -np.inf                  # a block's last column

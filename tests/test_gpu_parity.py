@@ -111,6 +111,20 @@ def test_fwd_bf16_ragged(gla, T, C):
     check_fwd(gla, c)
 
 
+@pytest.mark.parametrize("T,C", [(300, 128), (260, 64), (1, 128), (129, 64)])
+def test_fwd_bf16_one_cta_per_chain(gla, T, C):
+    """More chains than half the SMs run one CTA per (b, h), which holds the
+    whole state; fewer chains run two CTAs each (the cases above). Ragged T,
+    both chunk lengths, the page schedule with lambda = 0 and lambda = 1 among
+    the 80 heads, h0 and hT."""
+    lam = np.tile(gen.decay_page_schedule(16), 5)
+    lam[3] = 0.0
+    lam[21] = 1.0
+    c = gen.make_case(1, T, 80, 96, 192, seed=57 + T + C, dtype="bf16", lam=lam, normalise_k=True, h0_std=0.1,
+                      chunk=C)
+    check_fwd(gla, c)
+
+
 def test_fwd_bf16_page_schedule_and_lambda_zero(gla):
     lam = gen.decay_page_schedule(16)
     lam[3] = 0.0                      # lambda = 0: o_t = scale (q_t.k_t) v_t
