@@ -261,6 +261,13 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                 mbar_arrive_expect_tx(bar(BAR_FULLV0 + s), tx6);
 #pragma unroll
                 for (int j = 0; j < 6; ++j) tma_load_4d(st + kStV + j * kBlk, &tm_v, bar(BAR_FULLV0 + s), 32 * j, h, t0, b);
+                // V(c+1)'s slot frees only once the output of chunk c-1 has been stored from
+                // it; bring that tile into L2 now, so that its load is served from L2 (the
+                // per-head decay's forward: measured 62.5 -> 60.6 us on the layer shape; the
+                // reverse and gated modes measured 0.5-1.5 % slower with it).
+                if (!kRev && !kGate && c + 1 < nck)
+#pragma unroll
+                    for (int j = 0; j < 6; ++j) tma_prefetch_4d(&tm_v, 32 * j, h, tok0(c + 1), b);
             }
             __syncwarp();
             nv = c + 1;
