@@ -329,7 +329,9 @@ SegPlan plan_segments(int B, int T, int H, int chunk) {
     G = min(G, nck / 8);
     if (G < 2) return p;
     p.seg_chunks = (nck + G - 1) / G;
+    if (chunk == 64) p.seg_chunks += p.seg_chunks & 1;   // the state pass then runs 128-token tiles
     p.nseg = (nck + p.seg_chunks - 1) / p.seg_chunks;
+    if (p.nseg < 2) p.seg_chunks = nck;
     return p;
 }
 
@@ -343,15 +345,20 @@ cudaError_t launch_seg_prologue(const FwdParams &p, const SegPlan &plan, float *
                                 int *launches) {
     float *dS = static_cast<float *>(p.workspace);
     *S_in = dS + (size_t)plan.nseg * p.B * p.H * kStates;
+    // A segment's state does not depend on the chunk length (each token's weight
+    // is the decay of the segment's tokens after it): with 64-token chunks the
+    // pass runs over 128-token tiles when a segment holds an even number of chunks.
+    const bool wide = p.chunk == 64 && plan.seg_chunks % 2 == 0;
+    const int tile = wide ? 128 : p.chunk, tiles = wide ? plan.seg_chunks / 2 : plan.seg_chunks;
     CUtensorMap mk, mv;
     cudaError_t e;
-    if ((e = make_token_map(&mk, p.k, p.B, p.T, p.H, kDk, p.chunk)) != cudaSuccess) return e;
-    if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mk, p.k, p.B, p.T, p.H, kDk, tile)) != cudaSuccess) return e;
+    if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, tile)) != cudaSuccess) return e;
     auto kernel = p.g ? gla_seg_state_kernel<true> : gla_seg_state_kernel<false>;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     float *dseg = p.g ? *S_in + (size_t)plan.nseg * p.B * p.H * kStates : nullptr;
-    SegArgs a{p.log_lambda, dS, p.H, p.chunk, plan.seg_chunks, p.B * p.H, p.status, p.g, p.T, dseg};
+    SegArgs a{p.log_lambda, dS, p.H, tile, tiles, p.B * p.H, p.status, p.g, p.T, dseg};
     // The last segment's own contribution is never needed: G-1 segments per sequence.
     kernel<<<(unsigned)(p.B * p.H * (plan.nseg - 1)), kThreads, kSmemBytes, s>>>(mk, mv, a);
     if (launches) ++*launches;
