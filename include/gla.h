@@ -198,9 +198,10 @@ gla_status gla_chunk_fwd_varlen_gated(const void *q, const void *k, const void *
  *   dq, dk_ [B,T,H,dk], dv_ [B,T,H,dv] (dtype, written),
  *   dh0 [B,H,dk,dv] fp32 or NULL (not wanted),
  *   workspace: at least gla_chunk_bwd_workspace_size() bytes (may be 0).
- * The three backward launches run side by side: two on helper streams that
- * the call forks from `stream` and joins back with events (created once per
- * host thread and device). CUDA maps streams onto a limited number of
+ * GLA_BF16 runs two tensor-core launches side by side: dk and dv (with dh0)
+ * in one launch on `stream`, dq on a helper stream that the call forks from
+ * `stream` and joins back with events (created once per host thread and
+ * device); GLA_FP32 the validation kernels. CUDA maps streams onto a limited number of
  * hardware queues (8 by default); setting CUDA_DEVICE_MAX_CONNECTIONS to 32
  * before the first CUDA call keeps them from sharing one.
  */
@@ -266,8 +267,9 @@ gla_status gla_decode_step_gated(const void *q, const void *k, const void *v, co
  *   workspace: at least gla_chunk_bwd_gated_workspace_size() bytes (required
  *   when T > 0). It receives the state entering every chunk and the state
  *   gradient leaving it, from which dg is formed chunk by chunk.
- * GLA_BF16 runs four tensor-core launches (dq, dk, dv side by side on helper
- * streams as in gla_chunk_bwd, then dg); GLA_FP32 the validation kernels.
+ * GLA_BF16 runs four tensor-core launches (dq, dk, dv side by side, dq and
+ * dk on helper streams forked from `stream` and joined back as in
+ * gla_chunk_bwd, then dg); GLA_FP32 the validation kernels.
  */
 gla_status gla_chunk_bwd_gated(const void *q, const void *k, const void *v, const float *g,
                                const float *h0, float scale, const void *do_, const float *dhT,
