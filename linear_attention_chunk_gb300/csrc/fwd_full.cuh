@@ -109,6 +109,13 @@ struct FullArgs {
     size_t h0_seg_stride;
     unsigned int *status;
     const float *g;        // per-token log-decays [B, T, H] (the gated form), or NULL
+    // Variable-length mode (kVar): BH = nseq * H; sequence n holds tokens
+    // cu_seqlens[n] .. cu_seqlens[n+1] of the packed [1, T, H, d] tensors and
+    // its state in pool slot slots[n] (or n) of h0 == hT; a partial last chunk
+    // is stored row by row to o (its tile would overlap the next sequence).
+    const int *cu_seqlens, *slots;
+    int n_slots;
+    __nv_bfloat16 *o;
 };
 
 // One elected thread of an n-thread group waits; the verdict is published
@@ -158,7 +165,7 @@ __device__ __forceinline__ float chunk_decay_warp(const float (&x)[4]) {
 // are walked along the factors exp(g); the H group's first warp reduces each
 // chunk's gates to its total decay for the state's rescale, one chunk ahead.
 // `blk` is the CTA's unit: segment blk / BH of chain (b, h) = blk % BH.
-template <bool kRev, int kC, bool kGate = false>
+template <bool kRev, int kC, bool kGate = false, bool kVar = false>
 __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                           const CUtensorMap &tm_o, const FullArgs &a, int blk) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -171,11 +178,28 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     // quadrant), as accumulator and as the A operand read from TMEM.
     constexpr int kM = C;
     constexpr int ksteps_tok = C / 16;
+    static_assert(!kVar || !kRev, "variable-length mode is a forward");
     const int seg = blk / a.BH, bh = blk % a.BH;
-    const int b = bh / a.H, h = bh % a.H;
-    const int T = a.T;
+    const int h = bh % a.H;
+    // b: the state's index; bt, tokb: the batch and first-token coordinates of
+    // the sequence in the token tensors; T: its length
+    int b = bh / a.H, bt = b, tokb = 0, T = a.T, nck_seq = a.nck;
+    if constexpr (kVar) {
+        const int n = b, beg = a.cu_seqlens[n], end = a.cu_seqlens[n + 1];
+        const int slot = a.slots ? a.slots[n] : n;
+        if (beg < 0 || end < beg || end > a.T || slot < 0 || slot >= a.n_slots) {
+            if (threadIdx.x == 0) atomicOr(a.status, kDevBadState);
+            return;
+        }
+        if (end == beg) return;   // empty sequence: its state stays as it is
+        b = slot;
+        bt = 0;
+        tokb = beg;
+        T = end - beg;
+        nck_seq = (T + kC - 1) / kC;
+    }
     const int cbeg = seg * a.seg_chunks;                 // first chunk of this segment
-    const int nck = min(a.seg_chunks, a.nck - cbeg);     // chunks of this CTA
+    const int nck = kVar ? nck_seq : min(a.seg_chunks, nck_seq - cbeg);   // chunks of this CTA
     const bool last_seg = seg == a.nseg - 1;
     const float *h0 = a.h0 ? a.h0 + (size_t)seg * a.h0_seg_stride : nullptr;
     auto tok0 = [&](int c) { return (kRev ? nck - 1 - c : cbeg + c) * C; };
@@ -184,7 +208,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     // c in processing order, 0 past the sequence's end or the CTA's last chunk.
     auto load_gates = [&](int c, float (&x)[4]) {
         const int t0 = c < nck ? tok0(c) : 0, cc = c < nck ? clen(c) : 0;
-        const float *gh = a.g + ((size_t)b * T + t0) * a.H + h;
+        const float *gh = a.g + ((size_t)bt * a.T + tokb + t0) * a.H + h;
 #pragma unroll
         for (int r = 0; r < 4; ++r) x[r] = 4 * lane + r < cc ? gh[(size_t)(4 * lane + r) * a.H] : 0.f;
     };
@@ -239,7 +263,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(BAR_FULLK0 + s), tx3);
 #pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStK + j * kBlk, &tm_k, bar(BAR_FULLK0 + s), 32 * j, h, t0, b);
+                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStK + j * kBlk, &tm_k, bar(BAR_FULLK0 + s), 32 * j, h, tokb + t0, bt);
             }
             __syncwarp();
             nk = c + 1;
@@ -247,12 +271,12 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(BAR_FULLQ), tx3);
 #pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffQ + j * kBlk, &tm_q, bar(BAR_FULLQ), 32 * j, h, t0, b);
+                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffQ + j * kBlk, &tm_q, bar(BAR_FULLQ), 32 * j, h, tokb + t0, bt);
                 // Q has one buffer: bring the next chunk's tile into L2 now, so that its
                 // load, which waits for this one to be consumed, is served from L2.
                 if (c + 1 < nck)
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) tma_prefetch_4d(&tm_q, 32 * j, h, tok0(c + 1), b);
+                    for (int j = 0; j < 3; ++j) tma_prefetch_4d(&tm_q, 32 * j, h, tokb + tok0(c + 1), bt);
             }
             __syncwarp();
             nq = c + 1;
@@ -260,14 +284,14 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(BAR_FULLV0 + s), tx6);
 #pragma unroll
-                for (int j = 0; j < 6; ++j) tma_load_4d(st + kStV + j * kBlk, &tm_v, bar(BAR_FULLV0 + s), 32 * j, h, t0, b);
+                for (int j = 0; j < 6; ++j) tma_load_4d(st + kStV + j * kBlk, &tm_v, bar(BAR_FULLV0 + s), 32 * j, h, tokb + t0, bt);
                 // V(c+1)'s slot frees only once the output of chunk c-1 has been stored from
                 // it; bring that tile into L2 now, so that its load is served from L2 (the
                 // per-head decay's forward: measured 62.5 -> 60.6 us on the layer shape; the
                 // reverse and gated modes measured 0.5-1.5 % slower with it).
                 if (!kRev && !kGate && c + 1 < nck)
 #pragma unroll
-                    for (int j = 0; j < 6; ++j) tma_prefetch_4d(&tm_v, 32 * j, h, tok0(c + 1), b);
+                    for (int j = 0; j < 6; ++j) tma_prefetch_4d(&tm_v, 32 * j, h, tokb + tok0(c + 1), bt);
             }
             __syncwarp();
             nv = c + 1;
@@ -507,6 +531,24 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             tc_fence_after();
             // Stage in V(c)'s slot: ST(c) and OUT(c), its readers, have completed.
             const uint32_t stg = stage(c) + kStV;
+            const int t0 = tok0(c);
+            // a packed sequence's partial last chunk: rows straight to o
+            const bool rowwise = kVar && clen(c) < C;
+            __nv_bfloat16 *orow = kVar ? a.o + ((size_t)(tokb + t0 + (int)row) * a.H + h) * kDv : nullptr;
+            const bool row_out = has_row && (int)row < clen(c);
+            auto put = [&](const uint32_t (&r)[32], int blk) {
+                if (!rowwise) {
+                    if (has_row) write_row_sw64_bits(sm + (stg - base) + blk * kBlk, row, r, a.scale);
+                } else if (row_out) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8)
+                        *reinterpret_cast<uint4 *>(orow + 32 * blk + e) = make_uint4(
+                            pack_bf16x2(__uint_as_float(r[e]) * a.scale, __uint_as_float(r[e + 1]) * a.scale),
+                            pack_bf16x2(__uint_as_float(r[e + 2]) * a.scale, __uint_as_float(r[e + 3]) * a.scale),
+                            pack_bf16x2(__uint_as_float(r[e + 4]) * a.scale, __uint_as_float(r[e + 5]) * a.scale),
+                            pack_bf16x2(__uint_as_float(r[e + 6]) * a.scale, __uint_as_float(r[e + 7]) * a.scale));
+                }
+            };
             // Six 32-column blocks, the next block's TMEM load in flight while
             // this one is converted and staged.
             {
@@ -517,10 +559,10 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                     const int blk = 2 * bp;
                     tmem_ld_wait();
                     tmem_ld_32cols(tl + kColO + 32u * (blk + 1), rb);
-                    if (has_row) write_row_sw64_bits(sm + (stg - base) + blk * kBlk, row, ra, a.scale);
+                    put(ra, blk);
                     tmem_ld_wait();
                     if (bp < 2) tmem_ld_32cols(tl + kColO + 32u * (blk + 2), ra);
-                    if (has_row) write_row_sw64_bits(sm + (stg - base) + (blk + 1) * kBlk, row, rb, a.scale);
+                    put(rb, blk + 1);
                 }
             }
             tc_fence_before();
@@ -528,11 +570,12 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             named_sync(kBarE, 128);
             if (gt == 0) {
                 mbar_arrive(bar(BAR_OEMPTY));
-                const int t0 = tok0(c);
+                if (!rowwise) {
 #pragma unroll
-                for (int blk = 0; blk < 6; ++blk) tma_store_4d(&tm_o, stg + blk * kBlk, 32 * blk, h, t0, b);
-                tma_store_commit();
-                tma_store_wait_read_all();
+                    for (int blk = 0; blk < 6; ++blk) tma_store_4d(&tm_o, stg + blk * kBlk, 32 * blk, h, tokb + t0, bt);
+                    tma_store_commit();
+                    tma_store_wait_read_all();
+                }
                 mbar_arrive(bar(BAR_VFREE0 + (c & 1)));
             }
         }

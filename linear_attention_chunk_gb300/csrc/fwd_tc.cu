@@ -770,10 +770,13 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     return launch_fwd_full_tc(p, S_in, plan.nseg, plan.seg_chunks, s, launches);
 }
 
-// Variable-length forward: one CTA per (sequence, head, dv half) over the
-// packed [1, total_T, H, d] tensors; states in the pool.
+// Variable-length forward over the packed [1, total_T, H, d] tensors; states
+// in the pool.
 cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *launches) {
     if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
+    // More chains than half the SMs: one CTA per (sequence, head) holds the
+    // whole state; fewer: two per chain, each half the state.
+    if (2L * p.nseq * p.H > device_sm_count()) return launch_fwd_varlen_full_tc(p, s, launches);
     CUtensorMap mq, mk, mv, mo;
     cudaError_t e;
     if ((e = make_token_map(&mq, p.q, 1, p.total_T, p.H, kDk, p.chunk)) != cudaSuccess) return e;

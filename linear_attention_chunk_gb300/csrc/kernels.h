@@ -118,7 +118,8 @@ cudaError_t launch_copy_state(const float *src, float *dst, size_t n, cudaStream
 // tcgen05 / TMA tensor-core kernels (bf16, dk = 96, dv = 192). The forward
 // runs on the one-CTA-per-(b, h) kernel, segmented when the plan and the
 // workspace allow, and on the dv-half kernel (two CTAs per chain) when few
-// chains run unsegmented; the variable-length prefill on the dv-half kernel.
+// chains run unsegmented; the variable-length prefill likewise by its
+// number of (sequence, head) chains.
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
 // The forward with one CTA per (b, h) holding the whole state (fwd_full.cu);
 // S_in (or NULL: p.h0) holds each segment's initial state when nseg > 1.
@@ -129,6 +130,8 @@ cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int se
 cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // Variable-length forward with the states in a pool (bf16, dk = 96, dv = 192).
 cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *launches);
+// The same on the one-CTA-per-(sequence, head) kernel (fwd_full.cu).
+cudaError_t launch_fwd_varlen_full_tc(const VarlenParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // dq and dk: the transposed-shape chunk kernel (192-wide scores, 96-wide outputs).
 cudaError_t launch_bwd_dq_tc(const BwdParams &p, cudaStream_t s, int *launches);

@@ -37,9 +37,12 @@ def oracle_seq(c, n, pool_before):
 
 
 @pytest.mark.parametrize("C", [128, 64])
-def test_varlen_matches_oracle_per_sequence(gla, C):
+@pytest.mark.parametrize("H", [4, 8])
+def test_varlen_matches_oracle_per_sequence(gla, C, H):
+    """40 (sequence, head) chains run two CTAs each (half the state each), 80
+    chains one CTA each (the whole state)."""
     lengths = [0, 1, 63, 64, 65, 128, 129, 200, 333, 1000]
-    c = gen.make_varlen_case(lengths, 4, seed=500 + C, n_slots=14)
+    c = gen.make_varlen_case(lengths, H, seed=500 + C + H, n_slots=14)
     d = dev_case(c)
     o = gla.gla_chunk_fwd_varlen(d["q"], d["k"], d["v"], d["ll"], d["cu"], d["pool"], d["slots"], c.scale, C)
     gla.gla_check()
@@ -58,12 +61,14 @@ def test_varlen_matches_oracle_per_sequence(gla, C):
         assert np.array_equal(pool[s], c.pool[s].astype(np.float32).astype(np.float64)), f"slot {s} changed"
 
 
-def test_varlen_equals_batched_forward(gla):
+@pytest.mark.parametrize("H", [8, 32])
+def test_varlen_equals_batched_forward(gla, H):
     """Equal lengths, slot n = sequence n: the packed call and the batched call
     compute the same chunks from the same states, so they agree bit for bit,
-    including the masked last partial chunk."""
+    including the masked last partial chunk (24 chains: two CTAs per chain in
+    both calls; 96: one CTA per chain in both)."""
     import torch
-    nseq, T, H = 3, 300, 8
+    nseq, T = 3, 300
     c = gen.make_varlen_case([T] * nseq, H, seed=510, n_slots=nseq)
     c.slots[:] = np.arange(nseq, dtype=np.int32)
     d = dev_case(c)
