@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // different code.) An odd B H ends in one group of two, [dk, dv].
 constexpr int kPairThreads = 512;
 static_assert(kPairThreads >= kThreads && kPairThreads == fullhead::kThreads, "paired launch width");
-constexpr uint32_t kPairSmem = kSmemBytes > fullhead::kSmemBytes ? kSmemBytes : fullhead::kSmemBytes;
+constexpr uint32_t kPairSmem = kSmemBytes > fullhead::kSmemBytesMax ? kSmemBytes : fullhead::kSmemBytesMax;
 
 template <int kC>
 __global__ void __launch_bounds__(kPairThreads, 1)

@@ -35,9 +35,10 @@ cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int se
     auto kernel = p.g ? (p.chunk == 128 ? gla_fwd_full_kernel<false, 128, true> : gla_fwd_full_kernel<false, 64, true>)
                       : (p.chunk == 128 ? gla_fwd_full_kernel<false, 128, false>
                                         : gla_fwd_full_kernel<false, 64, false>);
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const uint32_t smem = p.chunk == 128 ? Layout<128>::kSmemBytes : Layout<64>::kSmemBytes;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<(unsigned)(p.B * p.H * nseg), kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, a);
+    kernel<<<(unsigned)(p.B * p.H * nseg), kThreads, smem, s>>>(mq, mk, mv, mo, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }
@@ -57,9 +58,10 @@ cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launc
     FullArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, nck, 1, nck, p.B * p.H, 0,
                p.status, p.g, nullptr, nullptr, 0, nullptr};
     auto kernel = p.chunk == 128 ? gla_fwd_full_kernel<true, 128, true> : gla_fwd_full_kernel<true, 64, true>;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const uint32_t smem = p.chunk == 128 ? Layout<128>::kSmemBytes : Layout<64>::kSmemBytes;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<(unsigned)(p.B * p.H), kThreads, kSmemBytes, s>>>(mrow, mcol, mval, mout, a);
+    kernel<<<(unsigned)(p.B * p.H), kThreads, smem, s>>>(mrow, mcol, mval, mout, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }
@@ -81,9 +83,10 @@ cudaError_t launch_fwd_varlen_full_tc(const VarlenParams &p, cudaStream_t s, int
                                         : gla_fwd_full_kernel<false, 64, true, true>)
                       : (p.chunk == 128 ? gla_fwd_full_kernel<false, 128, false, true>
                                         : gla_fwd_full_kernel<false, 64, false, true>);
-    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)) != cudaSuccess)
+    const uint32_t smem = p.chunk == 128 ? Layout<128>::kSmemBytes : Layout<64>::kSmemBytes;
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
-    kernel<<<(unsigned)(p.nseq * p.H), kThreads, kSmemBytes, s>>>(mq, mk, mv, mo, a);
+    kernel<<<(unsigned)(p.nseq * p.H), kThreads, smem, s>>>(mq, mk, mv, mo, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

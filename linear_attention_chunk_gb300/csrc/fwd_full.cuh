@@ -69,30 +69,49 @@ constexpr int kThreads = 512;
 constexpr uint32_t kBarP = 1, kBarE = 2, kBarH = 3;   // named barriers of the three groups
 constexpr uint32_t kHThreads = 192;
 
-constexpr uint32_t kOffQ = 0;                        // Q: 3 blocks
-constexpr uint32_t kOffStage = 3 * kBlk;             // stage s: K (3 blocks), then V (6 blocks)
-constexpr uint32_t kStK = 0, kStV = 3 * kBlk;        // K~^T's fourth (pad) M block reads V block 0
-constexpr uint32_t kStageBytes = 9 * kBlk;           // 72 KB
 constexpr uint32_t kSbBlk = kDk * 64;                // S_prev copy: [96 rows][32 bf16] blocks, 6 KB
-constexpr uint32_t kOffSb = kOffStage + 2 * kStageBytes;
-constexpr uint32_t kOffPw = kOffSb + 6 * kSbBlk;     // lambda^n, n = 0..128 (+pad)
-constexpr uint32_t kOffPair = kOffPw + 132 * 4;      // pp, pr: packed decay pairs
+constexpr uint32_t kSbBytes = 6 * kSbBlk;            // 36 KB
 enum { BAR_FULLQ, BAR_FULLK0, BAR_FULLK1, BAR_FULLV0, BAR_FULLV1, BAR_QFREE, BAR_KFREE0, BAR_KFREE1, BAR_VFREE0,
        BAR_VFREE1, BAR_QKDONE, BAR_KREADY, BAR_PREADY, BAR_SBREADY, BAR_SFULL, BAR_OFULL, BAR_OEMPTY, BAR_DONE,
        kNumBars };
-constexpr uint32_t kOffBar = kOffPair + 2 * 164 * 4;
 static_assert(kPairLen <= 164, "pair table stride");
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag, 3 x 2 decision slots
-// Per-token decay: the H group's two chunk-decay slots, and the P group's gate
-// arrays for the chunk in hand ([128] running log2-decays, [128] last clearing
-// positions, [128] per-token factors exp(g)).
-constexpr uint32_t kOffHDec = kOffMisc + 32;
-constexpr uint32_t kOffGate = kOffHDec + 16;
 constexpr uint32_t kGateArr = 128 * 12;
-constexpr uint32_t kSmemUsed = kOffGate + kGateArr;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;       // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffSb % 1024 == 0, "tile alignment");
+
+// Shared-memory layout for chunk length kC. Token tiles are blocks of
+// [kC rows][32 bf16] (kC * 64 bytes, 64-byte swizzle): Q 3 blocks; two stages
+// of K (3 blocks) then V (6 blocks), so K~^T's fourth (pad) M block reads V's
+// first; the S_prev copy. At kC = 64 the tiles take half the bytes, and the
+// room holds a second S_prev copy and two output staging buffers, so that
+// neither the state hand-off nor the V slot waits for the output (kDual).
+template <int kC>
+struct Layout {
+    static constexpr bool kDual = kC == 64;
+    static constexpr uint32_t kB = (uint32_t)kC * 64;          // one tile block
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffStage = 3 * kB;
+    static constexpr uint32_t kStK = 0, kStV = 3 * kB;
+    static constexpr uint32_t kStageBytes = 9 * kB;
+    static constexpr uint32_t kOffSb = kOffStage + 2 * kStageBytes;
+    static constexpr uint32_t kNSb = kDual ? 2 : 1;
+    static constexpr uint32_t kOutBytes = 6 * kB;              // kDual: output staging, two buffers
+    static constexpr uint32_t kOffOut = kOffSb + kNSb * kSbBytes;
+    static constexpr uint32_t kOffPw = kOffOut + (kDual ? 2 * kOutBytes : 0);   // lambda^n, n = 0..128 (+pad)
+    static constexpr uint32_t kOffPair = kOffPw + 132 * 4;     // pp, pr: packed decay pairs
+    static constexpr uint32_t kOffBar = kOffPair + 2 * 164 * 4;
+    static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort flag, 3 x 2 decision slots
+    // Per-token decay: the H group's two chunk-decay slots, and the P group's
+    // gate arrays for the chunk in hand ([128] running log2-decays, [128] last
+    // clearing positions, [128] per-token factors exp(g)).
+    static constexpr uint32_t kOffHDec = kOffMisc + 32;
+    static constexpr uint32_t kOffGate = kOffHDec + 16;
+    static constexpr uint32_t kSmemUsed = kOffGate + kGateArr;
+    static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffSb % 1024 == 0 && kOffOut % 1024 == 0,
+                  "tile alignment");
+};
+constexpr uint32_t kSmemBytesMax =
+    Layout<128>::kSmemBytes > Layout<64>::kSmemBytes ? Layout<128>::kSmemBytes : Layout<64>::kSmemBytes;
 
 constexpr uint32_t kTmemCols = 512, kColAP = 0, kColQt = 64, kColO = 128, kColS = 320;
 
@@ -173,6 +192,12 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     const uint32_t base = smem_u32(sm);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     constexpr int C = kC;   // chunk length, 64 or 128
+    using L = Layout<kC>;
+    constexpr bool kDual = L::kDual;
+    constexpr uint32_t kB = L::kB, kOffQ = L::kOffQ, kOffStage = L::kOffStage, kStK = L::kStK, kStV = L::kStV;
+    constexpr uint32_t kStageBytes = L::kStageBytes, kOffSb = L::kOffSb, kOffOut = L::kOffOut, kOffPw = L::kOffPw;
+    constexpr uint32_t kOffPair = L::kOffPair, kOffBar = L::kOffBar, kOffMisc = L::kOffMisc, kOffHDec = L::kOffHDec;
+    constexpr uint32_t kOffGate = L::kOffGate;
     // Token rows of the score, P, Q~ and output tiles: M = C. An M = 64 tile
     // holds row i in TMEM lane 32 (i / 16) + i % 16 (lanes 0-15 of each
     // quadrant), as accumulator and as the A operand read from TMEM.
@@ -263,7 +288,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(BAR_FULLK0 + s), tx3);
 #pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStK + j * kBlk, &tm_k, bar(BAR_FULLK0 + s), 32 * j, h, tokb + t0, bt);
+                for (int j = 0; j < 3; ++j) tma_load_4d(st + kStK + j * kB, &tm_k, bar(BAR_FULLK0 + s), 32 * j, h, tokb + t0, bt);
             }
             __syncwarp();
             nk = c + 1;
@@ -271,7 +296,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(BAR_FULLQ), tx3);
 #pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffQ + j * kBlk, &tm_q, bar(BAR_FULLQ), 32 * j, h, tokb + t0, bt);
+                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffQ + j * kB, &tm_q, bar(BAR_FULLQ), 32 * j, h, tokb + t0, bt);
                 // Q has one buffer: bring the next chunk's tile into L2 now, so that its
                 // load, which waits for this one to be consumed, is served from L2.
                 if (c + 1 < nck)
@@ -284,7 +309,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (lane == 0) {
                 mbar_arrive_expect_tx(bar(BAR_FULLV0 + s), tx6);
 #pragma unroll
-                for (int j = 0; j < 6; ++j) tma_load_4d(st + kStV + j * kBlk, &tm_v, bar(BAR_FULLV0 + s), 32 * j, h, tokb + t0, bt);
+                for (int j = 0; j < 6; ++j) tma_load_4d(st + kStV + j * kB, &tm_v, bar(BAR_FULLV0 + s), 32 * j, h, tokb + t0, bt);
                 // V(c+1)'s slot frees only once the output of chunk c-1 has been stored from
                 // it; bring that tile into L2 now, so that its load is served from L2 (the
                 // per-head decay's forward: measured 62.5 -> 60.6 us on the layer shape; the
@@ -326,7 +351,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                         const uint32_t st = stage(c);
 #pragma unroll
                         for (int ks = 0; ks < 6; ++ks) {
-                            const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
+                            const uint32_t off = (uint32_t)(ks >> 1) * kB + (uint32_t)(ks & 1) * 32;
                             mma_bf16_ss(tmem + kColAP, smem_desc(base + kOffQ + off, 16, 512, 4),
                                         smem_desc(st + kStK + off, 16, 512, 4), idA, ks > 0);
                         }
@@ -346,8 +371,8 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                         const uint32_t st = stage(c);
 #pragma unroll
                         for (int ks = 0; ks < ksteps_tok; ++ks)
-                            mma_bf16_ss(tmem + kColS, smem_desc(st + kStK + (uint32_t)ks * 1024, kBlk, 512, 4),
-                                        smem_desc(st + kStV + (uint32_t)ks * 1024, kBlk, 512, 4), idS, 1);
+                            mma_bf16_ss(tmem + kColS, smem_desc(st + kStK + (uint32_t)ks * 1024, kB, 512, 4),
+                                        smem_desc(st + kStV + (uint32_t)ks * 1024, kB, 512, 4), idS, 1);
                         mma_commit(bar(BAR_SFULL));
                         mma_commit(bar(BAR_KFREE0 + (c & 1)));
                         ++stt;
@@ -361,14 +386,15 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                         (c == 0 || mbar_test(bar(BAR_OEMPTY), (uint32_t)(c - 1) & 1u))) {
                         tc_fence_after();
                         const uint32_t stv = stage(c) + kStV;
+                        const uint32_t sb_prev = base + kOffSb + (kDual ? (uint32_t)(c & 1) * kSbBytes : 0u);
 #pragma unroll
                         for (int ks = 0; ks < 6; ++ks)
                             mma_bf16_ts(tmem + kColO, tmem + kColQt + 8u * (uint32_t)ks,
-                                        smem_desc(base + kOffSb + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
+                                        smem_desc(sb_prev + (uint32_t)ks * 1024, kSbBlk, 512, 4), idO, ks > 0);
 #pragma unroll
                         for (int ks = 0; ks < ksteps_tok; ++ks)
                             mma_bf16_ts(tmem + kColO, tmem + kColAP + 8u * (uint32_t)ks,
-                                        smem_desc(stv + (uint32_t)ks * 1024, kBlk, 512, 4), idO, 1);
+                                        smem_desc(stv + (uint32_t)ks * 1024, kB, 512, 4), idO, 1);
                         mma_commit(bar(BAR_OFULL));
                         ++out;
                         progress = true;
@@ -426,7 +452,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             for (int j = 0; j < 3; ++j)
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    qrow[4 * j + cc] = ld_shared_v4(base + kOffQ + j * kBlk + sw64_offset(trow, (uint32_t)cc));
+                    qrow[4 * j + cc] = ld_shared_v4(base + kOffQ + j * kB + sw64_offset(trow, (uint32_t)cc));
             named_sync(kBarP, 128);
             if (gt == 0) mbar_arrive(bar(BAR_QFREE));
             if (!gwait(bar(BAR_QKDONE), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
@@ -441,7 +467,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                     wk = row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
                 else
                     wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
-                scale_rows<3>(sm + (stage(c) - base) + kStK, row, wk);
+                if (row < (uint32_t)C) scale_rows<3, kB>(sm + (stage(c) - base) + kStK, row, wk);
             }
             fence_proxy_async_smem();
             named_sync(kBarP, 128);
@@ -530,7 +556,16 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (!gwait(bar(BAR_OFULL), (uint32_t)c & 1u, ctl, dec + 2, gt, kBarE, 128, kw)) break;
             tc_fence_after();
             // Stage in V(c)'s slot: ST(c) and OUT(c), its readers, have completed.
-            const uint32_t stg = stage(c) + kStV;
+            // kDual: in output buffer c % 2 instead, so V(c)'s slot is free at once,
+            // once the store from that buffer two chunks ago has been read out.
+            const uint32_t stg = kDual ? base + kOffOut + (uint32_t)(c & 1) * L::kOutBytes : stage(c) + kStV;
+            if constexpr (kDual) {
+                if (gt == 0) {
+                    mbar_arrive(bar(BAR_VFREE0 + (c & 1)));
+                    tma_store_wait_read_1();
+                }
+                named_sync(kBarE, 128);
+            }
             const int t0 = tok0(c);
             // a packed sequence's partial last chunk: rows straight to o
             const bool rowwise = kVar && clen(c) < C;
@@ -538,7 +573,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             const bool row_out = has_row && (int)row < clen(c);
             auto put = [&](const uint32_t (&r)[32], int blk) {
                 if (!rowwise) {
-                    if (has_row) write_row_sw64_bits(sm + (stg - base) + blk * kBlk, row, r, a.scale);
+                    if (has_row) write_row_sw64_bits(sm + (stg - base) + blk * kB, row, r, a.scale);
                 } else if (row_out) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8)
@@ -572,11 +607,11 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                 mbar_arrive(bar(BAR_OEMPTY));
                 if (!rowwise) {
 #pragma unroll
-                    for (int blk = 0; blk < 6; ++blk) tma_store_4d(&tm_o, stg + blk * kBlk, 32 * blk, h, tokb + t0, bt);
+                    for (int blk = 0; blk < 6; ++blk) tma_store_4d(&tm_o, stg + blk * kB, 32 * blk, h, tokb + t0, bt);
                     tma_store_commit();
-                    tma_store_wait_read_all();
+                    if (!kDual) tma_store_wait_read_all();
                 }
-                mbar_arrive(bar(BAR_VFREE0 + (c & 1)));
+                if (!kDual) mbar_arrive(bar(BAR_VFREE0 + (c & 1)));
             }
         }
         if (gt == 0) tma_store_wait_all();
@@ -639,7 +674,9 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             }
             if (!gwait(bar(BAR_SFULL), (uint32_t)c & 1u, ctl, dec + 4, gt, kBarH, kHThreads, kw)) break;
             // the copy is single: OUT(c) must have read it before it changes
-            if (!gwait(bar(BAR_OFULL), (uint32_t)c & 1u, ctl, dec + 4, gt, kBarH, kHThreads, kw)) break;
+            // (kDual: two copies, and OUT(c-1), the last reader of the one rewritten
+            // now, completed before ST(c) was issued)
+            if (!kDual && !gwait(bar(BAR_OFULL), (uint32_t)c & 1u, ctl, dec + 4, gt, kBarH, kHThreads, kw)) break;
             // hT goes out as one 73,728-byte bulk store, staged row-major in the other
             // stage's K and V slots (72 KB, contiguous), free once the output of chunk
             // c-1, staged in that V slot, has been read out (K's last reader, ST(c-1),
@@ -651,7 +688,12 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             tc_fence_after();
             const float wn = last ? 1.f : (kGate ? hdec[(c + 1) & 1] : pw[clen(c + 1)]);
             // the staging row of hT (fp32, 768 bytes): the stage not holding chunk c
-            unsigned char *hrow = write_hT ? sm + (stage(c + 1) - base) + row * (kDv * 4) : nullptr;
+            // (kDual: its 36 KB hold rows 0-47, the S_prev copy OUT(c) does not
+            // read rows 48-95)
+            const uint32_t sb_next = kOffSb + (kDual ? (uint32_t)((c + 1) & 1) * kSbBytes : 0u);
+            unsigned char *hrow = !write_hT ? nullptr
+                                  : (!kDual || row < 48) ? sm + (stage(c + 1) - base) + row * (kDv * 4)
+                                                         : sm + sb_next + (row - 48) * (kDv * 4);
             // Three 32-column blocks, the next block's TMEM load in flight while
             // this one is copied and rescaled.
             auto handle = [&](uint32_t (&r)[32], int blk) {
@@ -666,7 +708,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                             st_shared_v4(smem_u32(hrow + (blk * 32 + e) * 4), r[e], r[e + 1], r[e + 2], r[e + 3]);
                     }
                 } else {
-                    write_row_sw64_bits(sm + kOffSb + blk * kSbBlk, row, r, 1.f);
+                    write_row_sw64_bits(sm + sb_next + blk * kSbBlk, row, r, 1.f);
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * wn);
                     tmem_st_32cols(tl + kColS + 32u * blk, r);
@@ -690,7 +732,13 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             named_sync(kBarH, kHThreads);
             if (gt == 0 && !last) mbar_arrive(bar(BAR_SBREADY));
             if (gt == 0 && write_hT) {
-                bulk_store(a.hT + ((size_t)b * a.H + h) * kDk * kDv, stage(c + 1), kDk * kDv * 4);
+                float *hdst = a.hT + ((size_t)b * a.H + h) * kDk * kDv;
+                if constexpr (kDual) {
+                    bulk_store(hdst, stage(c + 1), 48 * kDv * 4);
+                    bulk_store(hdst + 48 * kDv, base + sb_next, 48 * kDv * 4);
+                } else {
+                    bulk_store(hdst, stage(c + 1), kDk * kDv * 4);
+                }
                 tma_store_commit();
                 hT_staged = true;
             }

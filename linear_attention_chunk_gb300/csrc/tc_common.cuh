@@ -15,11 +15,12 @@ constexpr uint32_t kBlk = 128 * 64;                  // [128 rows][32 bf16] bloc
 constexpr uint32_t kGroupThreads = 128;
 
 // Multiply row `row` of NB (3 or 6) 64-byte-swizzled blocks at blk0 (stride
-// kBlk) in place by w, six 16-byte chunks at a time (loads first, then
-// stores, so the loads overlap). The 64-byte swizzle only permutes a row's
-// chunks, so a row is scaled as it lies; chunks are visited in swizzled
-// order so that the 32 rows a warp touches at once fall in distinct banks.
-template <int NB>
+// kStride, kBlk by default) in place by w, six 16-byte chunks at a time (loads
+// first, then stores, so the loads overlap). The 64-byte swizzle only permutes
+// a row's chunks, so a row is scaled as it lies; chunks are visited in
+// swizzled order so that the 32 rows a warp touches at once fall in distinct
+// banks.
+template <int NB, uint32_t kStride = kBlk>
 __device__ __forceinline__ void scale_rows(unsigned char *blk0, uint32_t row, float w) {
     const uint32_t w2 = pack_bf16x2(w, w);
 #pragma unroll
@@ -28,7 +29,7 @@ __device__ __forceinline__ void scale_rows(unsigned char *blk0, uint32_t row, fl
 #pragma unroll
         for (int i = 0; i < 6; ++i) {
             const int k = h6 + i;
-            v[i] = *reinterpret_cast<const uint4 *>(blk0 + (k >> 2) * kBlk + sw64_offset(row, (uint32_t)(k & 3)));
+            v[i] = *reinterpret_cast<const uint4 *>(blk0 + (k >> 2) * kStride + sw64_offset(row, (uint32_t)(k & 3)));
         }
 #pragma unroll
         for (int i = 0; i < 6; ++i) {
@@ -40,7 +41,7 @@ __device__ __forceinline__ void scale_rows(unsigned char *blk0, uint32_t row, fl
 #pragma unroll
         for (int i = 0; i < 6; ++i) {
             const int k = h6 + i;
-            *reinterpret_cast<uint4 *>(blk0 + (k >> 2) * kBlk + sw64_offset(row, (uint32_t)(k & 3))) = v[i];
+            *reinterpret_cast<uint4 *>(blk0 + (k >> 2) * kStride + sw64_offset(row, (uint32_t)(k & 3))) = v[i];
         }
     }
 }
