@@ -171,14 +171,16 @@ def test_gated_decode(gla, dtype):
 
 # ------------------------------------------------------- variable-length prefill
 @pytest.mark.parametrize("C", [128, 64])
-def test_gated_varlen_matches_oracle_per_sequence(gla, C):
+@pytest.mark.parametrize("H", [4, 12])
+def test_gated_varlen_matches_oracle_per_sequence(gla, C, H):
     """Packed prompts of mixed lengths with per-token gates, each from and
-    into its slot of a state pool; an empty prompt leaves its slot as it is."""
+    into its slot of a state pool; an empty prompt leaves its slot as it is.
+    32 (sequence, head) chains run two CTAs each, 96 chains one CTA each."""
     import torch
     lengths = [0, 1, 63, 65, 128, 129, 300, 700]
-    c = gen.make_varlen_case(lengths, 4, seed=600 + C, n_slots=11)
-    rng = np.random.default_rng(601 + C)
-    g = gen.log_gates(rng, (c.q.shape[0], 4), "gla")
+    c = gen.make_varlen_case(lengths, H, seed=600 + C + H, n_slots=11)
+    rng = np.random.default_rng(601 + C + H)
+    g = gen.log_gates(rng, (c.q.shape[0], H), "gla")
     g[5, 2] = -np.inf                     # clears the state of sequence 2's head 2 inside its prompt
     d = dict(q=to_dev(c.q, "bf16"), k=to_dev(c.k, "bf16"), v=to_dev(c.v, "bf16"),
              cu=torch.from_numpy(c.cu_seqlens).cuda(), slots=torch.from_numpy(c.slots).cuda(), pool=f32_dev(c.pool))
