@@ -34,10 +34,12 @@
 // saved states), warp 1 owns TMEM and issues four MMAs: the scores A = Q K^T
 // and X = dO V^T (N = C), and R1 = dO S_prev^T and E1 = V (G_out/s)^T
 // (N = 96), so that r_i = s D(0..i) q_i.R1_i and e_j = s D(j+1..Cc-1)
-// k_j.E1_j. Warps 2-5, one per TMEM lane quadrant, hold one token row per
-// thread: they form M with the decays walked along the per-token factors,
-// its row sums and (by a transposing warp reduction) its column sums, r, e,
-// z and the two scans, and write dg.
+// k_j.E1_j. Warps 2-9 hold one token row per thread, two warps per TMEM lane
+// quadrant (warps 2-5 and 6-9): they form M with the decays walked along the
+// per-token factors, the first of each pair r and the even 32-column blocks
+// of M, the second e and the odd blocks; each block's column sums come from
+// a transposing warp reduction. Warps 2-5 then add up the row's parts, run
+// the two scans and write dg.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -53,9 +55,10 @@ using namespace ptx;
 using namespace tc;
 
 constexpr int kDk = 96, kDv = 192;
-constexpr int kThreads = 192;
-constexpr uint32_t kBarCompute = 1;                  // named barrier of the four compute warps
-constexpr uint32_t kComputeThreads = 128;
+constexpr int kThreads = 320;
+constexpr uint32_t kBarCompute = 1;                  // named barrier of the eight compute warps
+constexpr uint32_t kBarRows = 2;                     // named barrier of the first four (the scans)
+constexpr uint32_t kComputeThreads = 256;
 constexpr uint32_t kSbBlk = kDk * 64;                // saved state copy: [96 rows][32 bf16] blocks
 constexpr uint32_t kStateCopyBytes = 6 * kSbBlk;
 constexpr uint32_t kOffQ = 0, kOffK = 3 * kBlk, kOffV = 6 * kBlk, kOffDo = 12 * kBlk;
@@ -63,7 +66,8 @@ constexpr uint32_t kOffS = 18 * kBlk, kOffG = kOffS + kStateCopyBytes;
 constexpr uint32_t kOffGate = kOffG + kStateCopyBytes;   // Gl [128] f32, Zc [128] i32, Af [128] f32
 constexpr uint32_t kOffCol = kOffGate + 128 * 12;         // [4][128] column sums of M per warp
 constexpr uint32_t kOffRed = kOffCol + 4 * 128 * 4;       // [3][4] per-warp totals of the scans
-constexpr uint32_t kOffBar = kOffRed + 64;
+constexpr uint32_t kOffXch = kOffRed + 64;                 // [128] e_j, [128] partial row sums, [8] z parts
+constexpr uint32_t kOffBar = kOffXch + (2 * 128 + 8) * 4;
 enum { BAR_LOAD, BAR_MMA, kNumBars };
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;     // tmem base, abort flag
 constexpr uint32_t kSmemUsed = kOffMisc + 16;   // + the compute warps' verdict at +8
@@ -209,14 +213,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---------------------------------------- warps 2-5: one token row each
+        // ------------------------- warps 2-9: one token row each, two warps per row
         const uint32_t quad = (uint32_t)(warp & 3);
+        const uint32_t sub = (uint32_t)(warp - 2) >> 2;           // 0: warps 2-5, 1: warps 6-9
         const uint32_t row = quad * 32 + (uint32_t)lane;
-        const uint32_t ct = (uint32_t)threadIdx.x - 64;
+        const uint32_t ct = (uint32_t)threadIdx.x - 64;          // 0..255
         const uint32_t tl = tmem + ((quad * 32) << 16);
         const bool in = (int)row < Cc;
         const int nblk = C / 32;
         const float s = a.scale;
+        float *xe = reinterpret_cast<float *>(sm + kOffXch);     // e_j of each row
+        float *xrow = xe + 128;                                   // the second warp's part of each row sum
+        float *xz = xrow + 128;                                   // per-warp parts of z
         // The chunk's gates: running log2-decays, last clearing positions, factors.
         if (ct < 32) {
             float x[4];
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             gate_scan_store(x, lane, Gl, Zc, Af);
         }
         // One thread waits for the MMAs (which follow the loads); its verdict is
-        // read by all four warps after the barrier, so none skips a barrier that
+        // read by all eight warps after the barrier, so none skips a barrier that
         // the others wait on.
         volatile int *decision = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);
         if (ct == 0) *decision = mbar_wait(bar(BAR_MMA), 0, ctl) && !*abort_flag ? 1 : 0;
@@ -246,29 +254,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     zpart = fmaf(fs.y, fg.y, zpart);
                 }
             }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, d);
+            if (lane == 0) xz[sub * 4 + quad] = zpart;
             const float gi = Gl[row];
             const int zi = Zc[row];
             const int last = Cc - 1;
-            // r_i = s D(0..i) q_i.R1_i, e_j = s D(j+1..Cc-1) k_j.E1_j
-            float rq = 0.f, ek = 0.f;
+            // r_i = s D(0..i) q_i.R1_i (first warp of the pair), e_j = s D(j+1..Cc-1)
+            // k_j.E1_j (second)
+            float dot = 0.f;
+            const uint32_t col0 = sub == 0 ? kColR : kColE;
+            const uint32_t tile = base + (sub == 0 ? kOffQ : kOffK);
 #pragma unroll 1
             for (int blk = 0; blk < 3; ++blk) {
                 uint32_t x[32];
-                tmem_ld_32cols(tl + kColR + 32u * blk, x);
+                tmem_ld_32cols(tl + col0 + 32u * blk, x);
                 tmem_ld_wait();
-                rq += dot_row_sw64(x, base + kOffQ + blk * kBlk, row);
-                tmem_ld_32cols(tl + kColE + 32u * blk, x);
-                tmem_ld_wait();
-                ek += dot_row_sw64(x, base + kOffK + blk * kBlk, row);
+                dot += dot_row_sw64(x, tile + blk * kBlk, row);
             }
-            const float r_i = in && zi < 0 ? s * exp2f(gi) * rq : 0.f;
-            const float e_j = in && Zc[last] <= (int)row ? s * exp2f(Gl[last] - gi) * ek : 0.f;
-            // M row i = row: blocks of 32 columns j < i, weights D(j+1..i) walked
-            // leftwards from each block's last column (the diagonal block from the
-            // row's own column, which is excluded).
+            const float r_i = sub == 0 && in && zi < 0 ? s * exp2f(gi) * dot : 0.f;
+            if (sub == 1) xe[row] = in && Zc[last] <= (int)row ? s * exp2f(Gl[last] - gi) * dot : 0.f;
+            // M row i = row: blocks of 32 columns j < i (this warp's half of them),
+            // weights D(j+1..i) walked leftwards from each block's last column (the
+            // diagonal block from the row's own column, which is excluded).
             float rowsum = 0.f;
 #pragma unroll 1
-            for (int bj = 0; bj < nblk; ++bj) {
+            for (int bj = (int)sub; bj < nblk; bj += 2) {
                 float m[32];
                 if (bj <= (int)quad) {
                     uint32_t xa[32], xx[32];
@@ -300,37 +311,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 colp[quad * 128 + 32 * bj + lane] = warp_transpose_sum(m, lane);
             }
-            // Scans over the chunk's rows: w_u = col_u - row_u + e_u (exclusive
-            // prefix), r_i (inclusive suffix); z over the block.
+            if (sub == 1) xrow[row] = rowsum;
             named_sync(kBarCompute, kComputeThreads);
-            float col = 0.f;
-            for (int qd = 0; qd < 4; ++qd) col += colp[qd * 128 + row];
-            const float w = in ? col - rowsum + e_j : 0.f;
-            float wi = w, rs = r_i, zs = zpart;
+            if (sub == 0) {
+                // Scans over the chunk's rows: w_u = col_u - row_u + e_u (exclusive
+                // prefix), r_i (inclusive suffix); z over the block.
+                float col = 0.f;
+                for (int qd = 0; qd < 4; ++qd) col += colp[qd * 128 + row];
+                const float w = in ? col - (rowsum + xrow[row]) + xe[row] : 0.f;
+                float wi = w, rs = r_i;
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const float yw = __shfl_up_sync(0xffffffffu, wi, d);
-                const float yr = __shfl_down_sync(0xffffffffu, rs, d);
-                if (lane >= d) wi += yw;
-                if (lane + d < 32) rs += yr;
-                zs += __shfl_xor_sync(0xffffffffu, zs, d);
-            }
-            if (lane == 31) red[quad] = wi;          // warp totals of w
-            if (lane == 0) red[4 + quad] = rs;       // warp totals of r
-            if (lane == 0) red[8 + quad] = zs;
-            named_sync(kBarCompute, kComputeThreads);
-            float wpre = 0.f, rsuf = 0.f, z = 0.f;
-            for (int qd = 0; qd < 4; ++qd) {
-                if (qd < (int)quad) wpre += red[qd];
-                if (qd > (int)quad) rsuf += red[4 + qd];
-                z += red[8 + qd];
-            }
-            const float dchunk = Zc[last] < 0 ? exp2f(Gl[last]) : 0.f;
-            float dg = s * dchunk * z + (wpre + wi - w) + (rsuf + rs);
-            if (in) {
-                const size_t gidx = ((size_t)b * a.T + t0 + row) * a.H + h;
-                if (!(a.g[gidx] > kResetLogDecay)) dg = 0.f;   // a clearing gate: exp(g) = 0
-                a.dg[gidx] = dg;
+                for (int d = 1; d < 32; d <<= 1) {
+                    const float yw = __shfl_up_sync(0xffffffffu, wi, d);
+                    const float yr = __shfl_down_sync(0xffffffffu, rs, d);
+                    if (lane >= d) wi += yw;
+                    if (lane + d < 32) rs += yr;
+                }
+                if (lane == 31) red[quad] = wi;          // warp totals of w
+                if (lane == 0) red[4 + quad] = rs;       // warp totals of r
+                named_sync(kBarRows, 128);
+                float wpre = 0.f, rsuf = 0.f, z = 0.f;
+                for (int qd = 0; qd < 4; ++qd) {
+                    if (qd < (int)quad) wpre += red[qd];
+                    if (qd > (int)quad) rsuf += red[4 + qd];
+                }
+                for (int k8 = 0; k8 < 8; ++k8) z += xz[k8];
+                const float dchunk = Zc[last] < 0 ? exp2f(Gl[last]) : 0.f;
+                float dg = s * dchunk * z + (wpre + wi - w) + (rsuf + rs);
+                if (in) {
+                    const size_t gidx = ((size_t)b * a.T + t0 + row) * a.H + h;
+                    if (!(a.g[gidx] > kResetLogDecay)) dg = 0.f;   // a clearing gate: exp(g) = 0
+                    a.dg[gidx] = dg;
+                }
             }
         }
     }
