@@ -15,7 +15,10 @@
 // Work split: one CTA per (b, h, half of dv). Each CTA walks the chunks of
 // its sequence in order and keeps its 96 x 96 slice of the fp32 state in
 // TMEM for the whole sequence. Sibling CTAs (the two dv halves of one head)
-// are adjacent in the grid, so the second read of q and k hits L2.
+// are adjacent in the grid, so the second read of q and k hits L2. With two
+// CTAs per chain, this kernel serves calls with few (sequence, head) chains
+// (two CTAs per chain still within one wave), whose chunk period it
+// shortens; the one-CTA-per-chain kernel (fwd_full.cuh) serves the rest.
 //
 // Warp roles (448 threads):
 //   warp 0      TMA producer: Q, K, V tiles of chunk c into stage c%2
@@ -138,12 +141,8 @@ struct FwdTcArgs {
     const float *g;
 };
 
-// kRev = false: the forward pass. kRev = true: the same chunked recurrence
-// run backwards in time, which is how the backward pass obtains dv and dh0:
-// rows are k tokens, columns q tokens, values dO, the mask keeps col >= row
-// with lambda^(col-row), the row weights swap (lambda^(Cc-1-j) on the
-// readout, lambda^(i+1) on the state update), chunks run last to first, and
-// the state is the state gradient divided by the scale.
+// The forward pass (the backward's reverse-time runs use the one-CTA-per-head
+// kernel of fwd_full.cuh).
 //
 // kGate: the per-token decay of the gated form, S_t = exp(g_t) S_{t-1} +
 // k_t v_t^T. The lambda powers become decays of token runs: lambda^(i-j) ->
@@ -152,7 +151,7 @@ struct FwdTcArgs {
 // at or below kResetLogDecay clears the state: G skips it, and the position
 // of the last such gate, kept beside G, gives any run that holds one the
 // weight 0.
-template <bool kRev, int kC, bool kVar, bool kGate = false>
+template <int kC, bool kVar, bool kGate = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gla_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -195,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_gates = [&](int c, float (&x)[4]) {
         const int lane4 = 4 * (int)(threadIdx.x & 31);
         const float *gh = a.g + ((size_t)bt * a.T + tok0) * a.H + h;
-        const int t0 = (kRev ? nck - 1 - c : cbeg + c) * C, cc = c < nck ? min(C, T - t0) : 0;
+        const int t0 = (cbeg + c) * C, cc = c < nck ? min(C, T - t0) : 0;
 #pragma unroll
         for (int r = 0; r < 4; ++r) x[r] = lane4 + r < cc ? gh[(size_t)(t0 + lane4 + r) * a.H] : 0.f;
     };
@@ -260,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph = ((c >> 1) - 1) & 1;   // phase parity of chunk c-2
             const uint32_t st = base + (uint32_t)s * kStageBytes;
             const uint32_t fb = bar(BAR_FULL0 + s), fv = bar(BAR_FULLV0 + s);
-            const int t0 = (kRev ? nck - 1 - c : cbeg + c) * C;
+            const int t0 = (cbeg + c) * C;
             if (c >= 2 && !lane0_wait(bar(BAR_PREADY0 + s), ph, ctl, lane)) break;
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, tx_qk);
@@ -393,14 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nblk = C / 32;
         const int diag = (int)quad;                               // block holding this warp's diagonal
         uint32_t kw = 0;
-        // P blocks on the masked side of the diagonal (above it forward, below
-        // it in reverse) are zero for every chunk: write them once.
+        // P blocks above the diagonal are zero for every chunk: write them once.
         {
             uint32_t z[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) z[e] = 0u;
             for (int blk = (int)sub; blk < 4; blk += 2) {
-                if (kRev ? (blk >= diag) : (blk <= diag)) continue;
+                if (blk <= diag) continue;
                 tmem_st_16cols(tl + kColP + 16u * blk, z);
             }
             tmem_st_wait();
@@ -416,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
-            const int Cc = min(C, T - (kRev ? nck - 1 - c : cbeg + c) * C);
+            const int Cc = min(C, T - (cbeg + c) * C);
             if constexpr (kGate) {
                 // Every thread of the sub-group is past chunk c-1's reads (the
                 // barrier before its P-ready signal); the named barrier in the
@@ -439,14 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (sub == 0) {
                 // K~ = diag(w) K with w = lambda^(Cc-1-j) (zero past the end of the
-                // sequence), or lambda^(i+1) in reverse; signalled at once.
+                // sequence); signalled at once.
                 float wk;
-                if constexpr (kGate && kRev)   // the decay of the chunk's tokens 0..i
-                    wk = Zc[row] < 0 ? exp2f(Gl[row]) : 0.f;
-                else if constexpr (kGate)      // the decay of tokens j+1..Cc-1
+                if constexpr (kGate)   // the decay of tokens j+1..Cc-1
                     wk = row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
                 else
-                    wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
+                    wk = row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f;
                 scale_rows<3>(sm + (uint32_t)s * kStageBytes + kStageK, row, wk);
                 fence_proxy_async_smem();
                 named_sync(named, kGroupThreads);
@@ -458,15 +454,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             if (sub == 1) {
-                // Q~ = diag(lambda^(i+1)) Q (diag(lambda^(Cc-1-j)) in reverse) into TMEM as the
-                // A operand of Q~ S_prev: lane = token row, column c = dk pair (2c, 2c+1).
+                // Q~ = diag(lambda^(i+1)) Q into TMEM as the A operand of Q~ S_prev:
+                // lane = token row, column c = dk pair (2c, 2c+1).
                 float wq;
-                if constexpr (kGate && kRev)   // the decay of tokens j+1..Cc-1
-                    wq = row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
-                else if constexpr (kGate)      // the decay of the chunk's tokens 0..i
+                if constexpr (kGate)   // the decay of the chunk's tokens 0..i
                     wq = Zc[row] < 0 ? exp2f(Gl[row]) : 0.f;
                 else
-                    wq = kRev ? (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f) : pw[row + 1];
+                    wq = pw[row + 1];
                 const uint32_t wq2 = pack_bf16x2(wq, wq);
                 const unsigned char *qt = sm + (uint32_t)s * kStageBytes + kStageQ;
 #pragma unroll
@@ -488,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Tokens past the end of a ragged chunk have zero q and k, so A is zero there.
             {
                 const int b0 = (int)sub, b1 = (int)sub + 2;
-                const bool has0 = b0 < nblk && (kRev ? b0 >= diag : b0 <= diag);
-                const bool has1 = b1 < nblk && (kRev ? b1 >= diag : b1 <= diag);
+                const bool has0 = b0 < nblk && b0 <= diag;
+                const bool has1 = b1 < nblk && b1 <= diag;
                 if constexpr (kGate) {
                     const float gi = Gl[row];
                     const int zi = Zc[row];
@@ -499,18 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t x[32];
                         tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, x);
                         const bool dg = blk == diag;
-                        if constexpr (kRev) {
-                            // row j, columns i >= j: the walk starts at the block's first column
-                            const int il = 32 * blk;
-                            const float d0 = dg || Zc[il] > (int)row ? 0.f : ex2_approx(Gl[il] - gi);
-                            tmem_ld_wait();
-                            build_p_block_gated_rev(x, dg ? lane : -1, il, d0, Af, tl + kColP + 16u * blk);
-                        } else {
-                            const int jr = 32 * blk + 31;   // the block's last column
-                            const float d0 = dg || zi > jr ? 0.f : ex2_approx(gi - Gl[jr]);
-                            tmem_ld_wait();
-                            build_p_block_gated(x, dg ? lane : 32, 32 * blk, d0, Af, tl + kColP + 16u * blk);
-                        }
+                        const int jr = 32 * blk + 31;   // the block's last column
+                        const float d0 = dg || zi > jr ? 0.f : ex2_approx(gi - Gl[jr]);
+                        tmem_ld_wait();
+                        build_p_block_gated(x, dg ? lane : 32, 32 * blk, d0, Af, tl + kColP + 16u * blk);
                     }
                 } else {
 #pragma unroll 1
@@ -520,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld_32cols(tl + kColR + 128u * s + 32u * blk, x);
                         tmem_ld_wait();
                         pack_scores(x);
-                        build_p_block<kRev>(x, (int)row - 32 * blk, tl + kColP + 16u * blk, pp, pr);
+                        build_p_block<false>(x, (int)row - 32 * blk, tl + kColP + 16u * blk, pp, pr);
                     }
                 }
             }
@@ -547,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (kGate) {
                 if (group_wait(bar(BAR_GDEC0), 0, ctl, mydec, gt, kBarE, kw)) w0 = dslot[0];
             } else {
-                w0 = pw[kRev ? T - (nck - 1) * C : min(C, T - cbeg * C)];
+                w0 = pw[min(C, T - cbeg * C)];
             }
             if (quad < 3) {
                 const float *src =
@@ -577,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
-            const int t0 = (kRev ? nck - 1 - c : cbeg + c) * C;
+            const int t0 = (cbeg + c) * C;
             // State hand-off (rows 0..95 = quadrants 0..2).
             if (!group_wait(bar(BAR_SFULL), c & 1, ctl, mydec, gt, kBarE, kw)) break;
             tc_fence_after();
@@ -592,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (quad < 3) {
                 // rescale by lambda^(length of the next chunk processed)
-                const float wn = last ? 1.f : (kGate ? wgate : (kRev ? pw[C] : pw[min(C, T - t0 - C)]));
+                const float wn = last ? 1.f : (kGate ? wgate : pw[min(C, T - t0 - C)]);
                 unsigned char *sb_next = sm + kOffSb + (uint32_t)(s ^ 1) * kSbBytes;
                 float *dst = (last && last_seg && a.hT)
                                  ? a.hT + (((size_t)b * a.H + h) * kDk + row) * kDv + kDvHalf * half
@@ -720,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kGate>
 cudaError_t launch_chunk_kernel(const CUtensorMap &qm, const CUtensorMap &km, const CUtensorMap &vm,
                                 const CUtensorMap &om, const FwdTcArgs &a, int B, cudaStream_t s, int *launches) {
-    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<false, 128, false, kGate> : gla_fwd_tc_kernel<false, 64, false, kGate>;
+    auto kernel = a.C == 128 ? gla_fwd_tc_kernel<128, false, kGate> : gla_fwd_tc_kernel<64, false, kGate>;
     const uint32_t smem = kGate ? kSmemBytesGated : kSmemBytes;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -786,9 +772,8 @@ cudaError_t launch_fwd_varlen_tc(const VarlenParams &p, cudaStream_t s, int *lau
     FwdTcArgs a{p.log_lambda, p.pool, p.pool, p.scale, 1.f, 1.f, p.total_T, p.H, p.chunk, 0, 1, 0, p.nseq * p.H, 0,
                 p.status, p.cu_seqlens, p.slots, p.n_slots, static_cast<__nv_bfloat16 *>(p.o), p.g};
     // gated: per-token log-decays [total_T, H] packed like q
-    auto kernel = p.g ? (p.chunk == 128 ? gla_fwd_tc_kernel<false, 128, true, true>
-                                        : gla_fwd_tc_kernel<false, 64, true, true>)
-                      : (p.chunk == 128 ? gla_fwd_tc_kernel<false, 128, true> : gla_fwd_tc_kernel<false, 64, true>);
+    auto kernel = p.g ? (p.chunk == 128 ? gla_fwd_tc_kernel<128, true, true> : gla_fwd_tc_kernel<64, true, true>)
+                      : (p.chunk == 128 ? gla_fwd_tc_kernel<128, true> : gla_fwd_tc_kernel<64, true>);
     const uint32_t smem = p.g ? kSmemBytesGated : kSmemBytes;
     if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
