@@ -22,11 +22,15 @@
 //     diag(lambda^(i+1)) Q (columns [64, 112)), the A operands of the output
 //     MMAs; O = [128, 320) the output accumulator; S = [320, 512) the fp32
 //     state, rows 0..95.
-//   Shared memory: Q in one buffer; K and V in two stages; one bf16 copy of
-//     S_prev (the B operand of Q~ S_prev); the output of chunk c staged in
-//     the V slot of its own stage once the state and output MMAs have read V.
+//   Shared memory (the Layout below): Q in one buffer; K and V in two
+//     stages; one bf16 copy of S_prev (the B operand of Q~ S_prev); the
+//     output of chunk c staged in the V slot of its own stage once the state
+//     and output MMAs have read V. At C = 64 the tiles take half the bytes,
+//     and two S_prev copies and two output buffers take the room (kDual).
 //   One P-group warp per TMEM lane quadrant owns its 32 token rows, so P
-//     can overwrite the score columns that warp has already read.
+//     can overwrite the score columns that warp has already read. At C = 64
+//     the score, P, Q~ and output tiles are M = 64 (lanes 0-15 of each
+//     quadrant).
 // Warps (16, 512 threads; a warp reaches the TMEM lanes of quadrant warp % 4):
 //   15          TMA producer
 //   3           TMEM owner and MMA issuer (a non-blocking event loop)
@@ -45,6 +49,10 @@
 //   QK(c)   A = Q K^T               (tiles landed; OUT(c-1) complete: AP free)
 //   ST(c)   S += K~^T V             (K~ scaled; hand-off of c-1 done)
 //   OUT(c)  O = Q~ S_prev + P V     (P, Q~ in TMEM; epilogue of c-1 has read O)
+// The hand-off of chunk c follows ST(c) and (with one S_prev copy) OUT(c).
+// Modes (template flags of full_body): reverse time (the backward's dv), the
+// per-token decay, and the packed variable-length prefill into a state pool;
+// a segmented long sequence runs one CTA per (segment, b, h).
 //
 // The kernel body is a device function so that one launch can run it beside
 // another body on a neighbouring CTA (the backward's dk and dv, bwd_tc.cu).
