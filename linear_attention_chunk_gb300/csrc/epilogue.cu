@@ -11,6 +11,7 @@
 // row, lanes striding over channels, otherwise); the two reductions are
 // shuffles. The fp32 validation
 // path keeps exact sigmoids; the bf16 path uses the fast forms.
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -172,6 +173,41 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(Epilog
     }
 }
 
+// The rest of the epilogue over rows that the forward left normalised in z
+// (y = u / rms(u), bf16, dv = 192): z = y * norm_w * SiLU(g), in place. A
+// stream of 16-byte vectors, eight channels per thread, consecutive threads
+// on consecutive vectors.
+__global__ void __launch_bounds__(256) mixer_finish_bf16_kernel(EpilogueParams p) {
+    const size_t n = (size_t)p.NT * p.H * 24;   // 24 vectors of 8 channels per row
+    for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
+        const size_t r = i / 24;
+        const int cv = (int)(i % 24), h = (int)(r % (size_t)p.H);
+        uint4 *zp = reinterpret_cast<uint4 *>(p.z) + i;
+        const uint4 y16 = __ldcs(zp);
+        const uint4 g16 = __ldcs(reinterpret_cast<const uint4 *>(p.g) + i);
+        float w[8];
+        if (p.norm_w) {
+            const float4 *wr = reinterpret_cast<const float4 *>(p.norm_w + (size_t)h * 192 + 8 * cv);
+            const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
+            w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
+            w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = 1.f;
+        }
+        const uint32_t yw[4] = {y16.x, y16.y, y16.z, y16.w}, gw[4] = {g16.x, g16.y, g16.z, g16.w};
+        uint32_t zw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 yf = unpack_bf16x2(yw[e]), gf = unpack_bf16x2(gw[e]);
+            const float h0 = 0.5f * gf.x, h1 = 0.5f * gf.y;
+            zw[e] = pack_bf16x2(yf.x * w[2 * e] * fmaf(h0, tanh_fast(h0), h0),
+                                yf.y * w[2 * e + 1] * fmaf(h1, tanh_fast(h1), h1));
+        }
+        __stcs(zp, make_uint4(zw[0], zw[1], zw[2], zw[3]));
+    }
+}
+
 template <typename T>
 cudaError_t epilogue_impl(const EpilogueParams &p, cudaStream_t s, int *launches) {
     const size_t rows = (size_t)p.NT * p.H;
@@ -192,6 +228,16 @@ cudaError_t epilogue_impl(const EpilogueParams &p, cudaStream_t s, int *launches
 
 cudaError_t launch_mixer_epilogue(const EpilogueParams &p, bool bf16, cudaStream_t s, int *launches) {
     return bf16 ? epilogue_impl<__nv_bfloat16>(p, s, launches) : epilogue_impl<float>(p, s, launches);
+}
+
+cudaError_t launch_mixer_finish(const EpilogueParams &p, cudaStream_t s, int *launches) {
+    if (p.dv != 192) return cudaErrorInvalidValue;
+    const size_t n = (size_t)p.NT * p.H * 24;
+    if (n == 0) return cudaSuccess;
+    const size_t blocks = std::min<size_t>((n + 255) / 256, (size_t)device_sm_count() * 16);
+    mixer_finish_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    if (launches) ++*launches;
+    return cudaGetLastError();
 }
 
 }  // namespace gla

@@ -112,7 +112,10 @@ struct Layout {
     // clearing positions, [128] per-token factors exp(g)).
     static constexpr uint32_t kOffHDec = kOffMisc + 32;
     static constexpr uint32_t kOffGate = kOffHDec + 16;
-    static constexpr uint32_t kSmemUsed = kOffGate + kGateArr;
+    // The mixer epilogue's normalisation (kEpi): the head's aug row [96] and the
+    // self-augmentation gates of two chunks [2][128].
+    static constexpr uint32_t kOffEpi = kOffGate + kGateArr;
+    static constexpr uint32_t kSmemUsed = kOffEpi + (96 + 256) * 4;
     static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
     static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffSb % 1024 == 0 && kOffOut % 1024 == 0,
@@ -143,6 +146,11 @@ struct FullArgs {
     const int *cu_seqlens, *slots;
     int n_slots;
     __nv_bfloat16 *o;
+    // The mixer epilogue's normalisation (kEpi): the output rows become
+    // y = (o + sigmoid(q . (aug * k)) v) / sqrt(mean(u^2) + eps), aug [H, 96]
+    // fp32 or NULL (zero); the gate and the norm weight follow in a second pass.
+    const float *aug;
+    float eps;
 };
 
 // One elected thread of an n-thread group waits; the verdict is published
@@ -192,7 +200,12 @@ __device__ __forceinline__ float chunk_decay_warp(const float (&x)[4]) {
 // are walked along the factors exp(g); the H group's first warp reduces each
 // chunk's gates to its total decay for the state's rescale, one chunk ahead.
 // `blk` is the CTA's unit: segment blk / BH of chain (b, h) = blk % BH.
-template <bool kRev, int kC, bool kGate = false, bool kVar = false>
+// kEpi (forward, per-head decay, C = 128): each output row leaves normalised,
+// y = u / rms(u) with u = o + sigmoid(q . (aug * k)) v over the head's 192
+// channels. The P group forms the row's gate from its q row (in registers)
+// and its k row (before K is scaled); the E group forms u from O (TMEM) and
+// v (the V slot it stages y into), in two passes over the row.
+template <bool kRev, int kC, bool kGate = false, bool kVar = false, bool kEpi = false>
 __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                           const CUtensorMap &tm_o, const FullArgs &a, int blk) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -206,6 +219,9 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     constexpr uint32_t kStageBytes = L::kStageBytes, kOffSb = L::kOffSb, kOffOut = L::kOffOut, kOffPw = L::kOffPw;
     constexpr uint32_t kOffPair = L::kOffPair, kOffBar = L::kOffBar, kOffMisc = L::kOffMisc, kOffHDec = L::kOffHDec;
     constexpr uint32_t kOffGate = L::kOffGate;
+    static_assert(!kEpi || (!kRev && !kGate && !kVar && kC == 128), "the fused normalisation is a forward at C = 128");
+    float *ep_aug = reinterpret_cast<float *>(sm + L::kOffEpi);   // [96], then the gates [2][128]
+    float *ep_sig = ep_aug + 96;
     // Token rows of the score, P, Q~ and output tiles: M = C. An M = 64 tile
     // holds row i in TMEM lane 32 (i / 16) + i % 16 (lanes 0-15 of each
     // quadrant), as accumulator and as the A operand read from TMEM.
@@ -271,6 +287,8 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         for (int n = threadIdx.x; n < 132; n += kThreads) pw[n] = n <= 128 ? decay_pow(l2, n) : 0.f;
         fill_pair_tables(pp, pr, l2, threadIdx.x, kThreads);
     }
+    if constexpr (kEpi)
+        for (int n = threadIdx.x; n < 96; n += kThreads) ep_aug[n] = a.aug ? a.aug[h * 96 + n] : 0.f;
     if (warp == 3) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -465,6 +483,28 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (gt == 0) mbar_arrive(bar(BAR_QFREE));
             if (!gwait(bar(BAR_QKDONE), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
             tc_fence_after();
+            if constexpr (kEpi) {
+                // the row's self-augmentation gate, from q (registers) and k (before K is scaled)
+                const uint32_t kb = stage(c) + kStK;
+                float dot = 0.f;
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint4 kv = ld_shared_v4(kb + j * kB + sw64_offset(row, (uint32_t)cc));
+                        const uint32_t kw4[4] = {kv.x, kv.y, kv.z, kv.w};
+                        const uint4 qv = qrow[4 * j + cc];
+                        const uint32_t qw4[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int d = 32 * j + 8 * cc + 2 * e;
+                            const float2 qf = unpack_bf16x2(qw4[e]), kf = unpack_bf16x2(kw4[e]);
+                            dot = fmaf(qf.x * ep_aug[d], kf.x, dot);
+                            dot = fmaf(qf.y * ep_aug[d + 1], kf.y, dot);
+                        }
+                    }
+                ep_sig[(c & 1) * 128 + row] = 1.f / (1.f + __expf(-dot));
+            }
             // K~ = diag(lambda^(Cc-1-j)) K in place (zero past the end), or lambda^(i+1)
             // in reverse; signalled at once.
             {
@@ -592,9 +632,49 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                             pack_bf16x2(__uint_as_float(r[e + 6]) * a.scale, __uint_as_float(r[e + 7]) * a.scale));
                 }
             };
-            // Six 32-column blocks, the next block's TMEM load in flight while
-            // this one is converted and staged.
-            {
+            if constexpr (kEpi) {
+                // y = u / rms(u), u = o * scale + sigma * v: one pass over the six
+                // 32-column blocks for the sum of squares, one to write y over this
+                // row's v in the V slot (each thread owns its row).
+                const float sg = ep_sig[(c & 1) * 128 + row];
+                auto u_block = [&](int blk, float (&u)[32]) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(tl + kColO + 32u * blk, r);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint4 vv = ld_shared_v4(stg + blk * kB + sw64_offset(row, (uint32_t)cc));
+                        const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 vf = unpack_bf16x2(vw[e]);
+                            const int m = 8 * cc + 2 * e;
+                            u[m] = fmaf(sg, vf.x, __uint_as_float(r[m]) * a.scale);
+                            u[m + 1] = fmaf(sg, vf.y, __uint_as_float(r[m + 1]) * a.scale);
+                        }
+                    }
+                };
+                float ss = 0.f;
+#pragma unroll 1
+                for (int blk = 0; blk < 6; ++blk) {
+                    float u[32];
+                    u_block(blk, u);
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) ss = fmaf(u[m], u[m], ss);
+                }
+                const float rinv = rsqrtf(ss * (1.f / kDv) + a.eps);
+#pragma unroll 1
+                for (int blk = 0; blk < 6; ++blk) {
+                    float u[32];
+                    u_block(blk, u);
+                    uint32_t yb[32];
+#pragma unroll
+                    for (int m = 0; m < 32; ++m) yb[m] = __float_as_uint(u[m] * rinv);
+                    write_row_sw64_bits(sm + (stg - base) + blk * kB, row, yb, 1.f);
+                }
+            } else {
+                // Six 32-column blocks, the next block's TMEM load in flight while
+                // this one is converted and staged.
                 uint32_t ra[32], rb[32];
                 tmem_ld_32cols(tl + kColO, ra);
 #pragma unroll 1

@@ -737,8 +737,8 @@ size_t fwd_tc_workspace_size(int B, int T, int H, int chunk, bool gated) {
     return seg_workspace_bytes(B, H, plan_segments(B, T, H, chunk), gated);
 }
 
-cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
-    if (p.dk != kDk || p.dv != kDv) return cudaErrorInvalidValue;
+cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches, const EpilogueParams *epi) {
+    if (p.dk != kDk || p.dv != kDv || (epi && p.g)) return cudaErrorInvalidValue;
     // One CTA holds the whole state of a (b, h) chain. Few chains and a long
     // sequence: split each sequence into segments that run in parallel, when
     // the caller gave the workspace for it. Few chains otherwise (two CTAs per
@@ -746,14 +746,25 @@ cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches) {
     const SegPlan plan = plan_segments(p.B, p.T, p.H, p.chunk);
     const bool segmented =
         plan.nseg > 1 && p.workspace && p.workspace_bytes >= seg_workspace_bytes(p.B, p.H, plan, p.g != nullptr);
-    if (!segmented) {
-        if (2L * p.B * p.H <= device_sm_count()) return launch_fwd_half_tc(p, s, launches);
-        return launch_fwd_full_tc(p, nullptr, 1, 0, s, launches);
+    const bool half = !segmented && 2L * p.B * p.H <= device_sm_count();
+    // The mixer epilogue's normalisation rides in the one-CTA-per-chain
+    // kernel's output stage at C = 128, the rest follows as a light pass;
+    // otherwise the whole epilogue follows the forward as its own launch.
+    const bool fused = epi && !half && p.chunk == 128;
+    cudaError_t e;
+    if (half) {
+        e = launch_fwd_half_tc(p, s, launches);
+    } else if (!segmented) {
+        e = launch_fwd_full_tc(p, nullptr, 1, 0, s, launches, fused ? epi : nullptr);
+    } else {
+        float *S_in = nullptr;
+        e = launch_seg_prologue(p, plan, &S_in, s, launches);
+        if (e == cudaSuccess)
+            e = launch_fwd_full_tc(p, S_in, plan.nseg, plan.seg_chunks, s, launches, fused ? epi : nullptr);
     }
-    float *S_in = nullptr;
-    cudaError_t e = launch_seg_prologue(p, plan, &S_in, s, launches);
-    if (e != cudaSuccess) return e;
-    return launch_fwd_full_tc(p, S_in, plan.nseg, plan.seg_chunks, s, launches);
+    if (e == cudaSuccess && epi)
+        e = fused ? launch_mixer_finish(*epi, s, launches) : launch_mixer_epilogue(*epi, true, s, launches);
+    return e;
 }
 
 // Variable-length forward over the packed [1, total_T, H, d] tensors; states

@@ -288,15 +288,14 @@ gla_status gla_chunk_fwd_mixer(const void *q, const void *k, const void *v, cons
         t_launches = launches;
         return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_mixer(T=0)");
     }
-    // The forward writes o into z's buffer; the epilogue then rewrites each
-    // row in place (a warp reads all of a row's inputs before storing it).
+    // The forward writes into z's buffer either the normalised rows, which a
+    // second pass multiplies by the norm weight and the SiLU gate (one CTA per
+    // chain at chunk 128), or o, which the epilogue then rewrites row by row
+    // in place (a warp reads all of a row's inputs before storing it).
     FwdParams p{q, k, v, log_lambda, h0, scale, B, T, H, dk, dv, chunk, z, hT,
                 workspace, workspace ? workspace_bytes : 0, status};
-    e = launch_fwd_tc(p, s, &launches);
-    if (e == cudaSuccess) {
-        EpilogueParams ep{z, q, k, v, g, aug, norm_w, eps, B * T, H, dk, dv, z};
-        e = launch_mixer_epilogue(ep, true, s, &launches);
-    }
+    const EpilogueParams ep{z, q, k, v, g, aug, norm_w, eps, B * T, H, dk, dv, z};
+    e = launch_fwd_tc(p, s, &launches, &ep);
     t_launches = launches;
     return e == cudaSuccess ? GLA_OK : cuda_fail(e, "gla_chunk_fwd_mixer launch");
 }

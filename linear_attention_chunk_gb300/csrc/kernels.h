@@ -81,6 +81,9 @@ struct EpilogueParams {
     void *z;
 };
 cudaError_t launch_mixer_epilogue(const EpilogueParams &p, bool bf16, cudaStream_t s, int *launches);
+// The rest of the epilogue over rows already normalised in place in p.z
+// (bf16, dv = 192): z = y * norm_w * SiLU(g).
+cudaError_t launch_mixer_finish(const EpilogueParams &p, cudaStream_t s, int *launches);
 
 // The causal depthwise Conv1d (width 4) with SiLU (conv.cu). Batched: nseq
 // sequences of T tokens, window n at win_in / win_out + n*4*D (either may be
@@ -120,11 +123,18 @@ cudaError_t launch_copy_state(const float *src, float *dst, size_t n, cudaStream
 // workspace allow, and on the dv-half kernel (two CTAs per chain) when few
 // chains run unsegmented; the variable-length prefill likewise by its
 // number of (sequence, head) chains.
-cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches);
+// epi (or NULL): the mixer epilogue over the output, z in place of o: its
+// normalisation fused into the one-CTA-per-chain kernel's output stage at
+// C = 128 and the rest in launch_mixer_finish, else one launch of
+// launch_mixer_epilogue after the forward.
+cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches, const EpilogueParams *epi = nullptr);
 // The forward with one CTA per (b, h) holding the whole state (fwd_full.cu);
 // S_in (or NULL: p.h0) holds each segment's initial state when nseg > 1.
+// epi (or NULL): the mixer epilogue's normalisation fused into the output
+// stage (per-head decay, chunk 128): rows leave as y = u / rms(u), for
+// launch_mixer_finish to apply the norm weight and the SiLU gate.
 cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int seg_chunks, cudaStream_t s,
-                               int *launches);
+                               int *launches, const EpilogueParams *epi = nullptr);
 // dv and dh0 of the per-token decay's backward on the one-CTA-per-(b, h)
 // kernel in reverse time (p.g required).
 cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launches);

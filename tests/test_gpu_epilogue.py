@@ -120,6 +120,30 @@ def test_forward_with_epilogue(gla, C, T):
         assert torch.equal(hT, hT_plain)
 
 
+@pytest.mark.parametrize("T", [300, 128, 1])
+def test_forward_with_epilogue_fused(gla, T):
+    """With more chains than half the SMs (80 here) and 128-token chunks the
+    forward's output stage normalises each row (u = o + sigmoid(q.(aug k)) v
+    over its rms, o never stored) and a light second pass applies the norm
+    weight and the SiLU gate: ragged tail, exact chunks and a single token,
+    with h0, random decays, and with and without aug and norm_w. Its hT is
+    the plain forward's bit for bit."""
+    import torch
+    c, g, aug, nw = fused_case(1, T, 80, 660 + T, lam_random=True, h0_std=0.1)
+    d = case_to_dev(c)
+    gd = to_dev(g, "bf16")
+    for a, w in ((aug, nw), (None, None)):
+        z, hT = gla.gla_chunk_fwd_mixer(d["q"], d["k"], d["v"], gd, d["ll"], d["h0"], c.scale, 128, f32_dev(a),
+                                        f32_dev(w), 1e-6)
+        assert gla.gla_last_launch_count() == 2
+        gla.gla_check()
+        ref, hT_ref, kappa = fused_reference(c, g, a, w, 1e-6)
+        check_fused(to_host(z), ref, kappa)
+        _, hT_plain = gla.gla_chunk_fwd(d["q"], d["k"], d["v"], d["ll"], d["h0"], c.scale, 128)
+        gla.gla_check()
+        assert torch.equal(hT, hT_plain)
+
+
 def test_forward_epilogue_page_schedule(gla):
     """The page decay schedule (lambda_0 = 0.5 underflows inside a chunk); the
     separate calls (forward, then the standalone epilogue into a new buffer)
