@@ -269,7 +269,8 @@ gla_status gla_decode_step_gated(const void *q, const void *k, const void *v, co
  *   gradient leaving it, from which dg is formed chunk by chunk.
  * GLA_BF16 runs four tensor-core launches (dq, dk, dv side by side, dq and
  * dk on helper streams forked from `stream` and joined back as in
- * gla_chunk_bwd, then dg); GLA_FP32 the validation kernels.
+ * gla_chunk_bwd, then dg after a 4-byte memset of its work counter in the
+ * workspace); GLA_FP32 the validation kernels.
  */
 gla_status gla_chunk_bwd_gated(const void *q, const void *k, const void *v, const float *g,
                                const float *h0, float scale, const void *do_, const float *dhT,
@@ -278,7 +279,8 @@ gla_status gla_chunk_bwd_gated(const void *q, const void *k, const void *v, cons
                                void *workspace, size_t workspace_bytes, void *stream);
 
 /* Bytes of workspace gla_chunk_bwd_gated needs: two states per (b, h, chunk)
- * (bf16: 2 x B x H x ceil(T / chunk) x 36,864 bytes; fp32: twice that). */
+ * (bf16: 2 x B x H x ceil(T / chunk) x 36,864 bytes and a 16-byte work
+ * counter; fp32: 2 x B x H x ceil(T / chunk) x dk x dv x 4 bytes). */
 size_t gla_chunk_bwd_gated_workspace_size(int B, int T, int H, int dk, int dv, int chunk,
                                           gla_dtype dtype);
 

@@ -607,9 +607,15 @@ cudaError_t launch_tr(const void *A, const void *Bt, const void *Ct, void *out, 
 
 }  // namespace
 
-size_t bwd_gated_tc_workspace_size(int B, int T, int H, int chunk) {
+size_t bwd_gated_tc_state_bytes(int B, int T, int H, int chunk) {
     const size_t nck = ((size_t)T + chunk - 1) / chunk;
     return 2 * (size_t)B * H * nck * kStateCopyBytes;
+}
+
+// The two halves of state copies, then the gate-gradient kernel's 16-byte
+// work counter.
+size_t bwd_gated_tc_workspace_size(int B, int T, int H, int chunk) {
+    return bwd_gated_tc_state_bytes(B, T, H, chunk) + 16;
 }
 
 // dq: rows do, columns v, values k, state S from h0, forward in time. Gated:
@@ -629,7 +635,7 @@ cudaError_t launch_bwd_dk_tc(const BwdParams &p, cudaStream_t s, int *launches) 
     if (p.g)
         return launch_tr<true, true>(p.v, p.do_, p.q, p.dk_out, p.dhT, 1.f / p.scale, p,
                                      static_cast<unsigned char *>(p.workspace) +
-                                         bwd_gated_tc_workspace_size(p.B, p.T, p.H, p.chunk) / 2,
+                                         bwd_gated_tc_state_bytes(p.B, p.T, p.H, p.chunk) / 2,
                                      s, launches);
     return launch_tr<true, false>(p.v, p.do_, p.q, p.dk_out, p.dhT, 1.f / p.scale, p, nullptr, s, launches);
 }

@@ -29,18 +29,25 @@
 // difference cancels only inside one chunk, in fp32, from the fp32 score
 // accumulators.
 //
-// One CTA per (b, h, chunk): the chunks are independent, there is no state
-// chain. Warp 0 loads (TMA tiles of q, k, v, do; 1-D bulk copies of the two
-// saved states), warp 1 owns TMEM and issues four MMAs: the scores A = Q K^T
-// and X = dO V^T (N = C), and R1 = dO S_prev^T and E1 = V (G_out/s)^T
-// (N = 96), so that r_i = s D(0..i) q_i.R1_i and e_j = s D(j+1..Cc-1)
-// k_j.E1_j. Warps 2-9 hold one token row per thread, two warps per TMEM lane
-// quadrant (warps 2-5 and 6-9): they form M with the decays walked along the
-// per-token factors, the first of each pair r and the even 32-column blocks
-// of M, the second e and the odd blocks; each block's column sums come from
-// a transposing warp reduction. Warps 2-5 then add up the row's parts, run
-// the two scans and write dg.
+// The chunks are independent, there is no state chain: one persistent CTA
+// per SM takes (b, h, chunk) units from a counter in the workspace until
+// none are left. Warp 0 loads (TMA tiles of q, k, v, do; 1-D bulk copies of
+// the two saved states), warp 1 owns TMEM and issues four MMAs: the scores
+// A = Q K^T and X = dO V^T (N = C), and R1 = dO S_prev^T and E1 = V
+// (G_out/s)^T (N = 96), so that r_i = s D(0..i) q_i.R1_i and e_j =
+// s D(j+1..Cc-1) k_j.E1_j. Warps 2-9 hold one token row per thread, two warps
+// per TMEM lane quadrant (warps 2-5 and 6-9). As soon as a unit's tiles land
+// they take their q (first warp of a pair) or k row (second) into registers
+// and the z sum from the two copies; once its MMAs are complete, shared
+// memory is handed back and the next unit's loads overlap the rest, which
+// reads only TMEM: r and e, and M with the decays walked along the per-token
+// factors, the first of each pair the even 32-column blocks of M, the second
+// the odd ones; each block's column sums come from a transposing warp
+// reduction. Warps 2-5 then add up the row's parts, run the two scans and
+// write dg; the next unit's MMAs wait only for TMEM.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -68,9 +75,12 @@ constexpr uint32_t kOffCol = kOffGate + 128 * 12;         // [4][128] column sum
 constexpr uint32_t kOffRed = kOffCol + 4 * 128 * 4;       // [3][4] per-warp totals of the scans
 constexpr uint32_t kOffXch = kOffRed + 64;                 // [128] e_j, [128] partial row sums, [8] z parts
 constexpr uint32_t kOffBar = kOffXch + (2 * 128 + 8) * 4;
-enum { BAR_LOAD, BAR_MMA, kNumBars };
-constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;     // tmem base, abort flag
-constexpr uint32_t kSmemUsed = kOffMisc + 16;   // + the compute warps' verdict at +8
+// LOAD: a unit's tiles landed (or the end marker); MMA: its products are in
+// TMEM; SMEM: the compute warps are done with its tiles (after MMA); TMEM:
+// they are done with its products.
+enum { BAR_LOAD, BAR_MMA, BAR_SMEM, BAR_TMEM, kNumBars };
+constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;     // tmem base, abort flag, 2 verdicts, 2 unit slots
+constexpr uint32_t kSmemUsed = kOffMisc + 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffS % 1024 == 0 && kOffG % 1024 == 0, "the saved copies keep their 64-byte swizzle phase");
@@ -83,8 +93,9 @@ struct DgArgs {
     const unsigned char *saved_s;      // S_prev copy per (b, h, chunk)
     const unsigned char *saved_g;      // G_out / s copy per (b, h, chunk)
     float *dg;                         // [B, T, H]
+    unsigned int *next_unit;           // work counter, zero at launch
     float scale;
-    int T, H, C, nck;
+    int T, H, C, nck, nunits;
     unsigned int *status;
 };
 
@@ -104,14 +115,23 @@ __device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
     return v[0];
 }
 
-// Dot product of 32 fp32 values (raw bits, from TMEM) with the 32 bf16 of
-// row `row` in a 64-byte-swizzled [128][32] block.
-__device__ __forceinline__ float dot_row_sw64(const uint32_t (&x)[32], uint32_t blk, uint32_t row) {
+// One compute thread waits on an mbarrier; the verdict goes through a
+// two-slot flag so that all eight compute warps take the same branch after
+// their named barrier.
+__device__ __forceinline__ bool compute_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl,
+                                             volatile int *decision, uint32_t ct, uint32_t &k) {
+    if (ct == 0) decision[k & 1] = mbar_wait(bar, parity, ctl) ? 0 : 1;
+    named_sync(kBarCompute, kComputeThreads);
+    return decision[(k++) & 1] == 0;
+}
+
+// Dot product of 32 fp32 values (raw bits, from TMEM) with 32 bf16 held as
+// four 16-byte vectors.
+__device__ __forceinline__ float dot_row_regs(const uint32_t (&x)[32], const uint4 *r) {
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint4 u = ld_shared_v4(blk + sw64_offset(row, (uint32_t)c));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const uint32_t w[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 f = unpack_bf16x2(w[e]);
@@ -130,10 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = smem_u32(sm);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int nc = blockIdx.x % a.nck;
-    const int bh = blockIdx.x / a.nck;
-    const int b = bh / a.H, h = bh % a.H;
-    const int C = a.C, t0 = nc * C, Cc = min(C, a.T - t0);
+    const int C = a.C;
 
     float *Gl = reinterpret_cast<float *>(sm + kOffGate);
     int *Zc = reinterpret_cast<int *>(sm + kOffGate + 512);
@@ -142,6 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *red = reinterpret_cast<float *>(sm + kOffRed);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kOffMisc + 4);
+    volatile int *decision = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);   // [2]
+    volatile int *unit_slot = reinterpret_cast<volatile int *>(sm + kOffMisc + 16); // [2]: unit, or -1 at the end
     const WaitCtl ctl{abort_flag, a.status};
     auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
 
@@ -166,30 +185,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------- loads
         if (lane == 0) {
-            const size_t slot = ((size_t)bh * a.nck + nc) * kStateCopyBytes;
             const uint32_t fb = bar(BAR_LOAD);
-            mbar_arrive_expect_tx(fb, 18u * (uint32_t)C * 64u + 2u * kStateCopyBytes);
+            uint32_t issued = 0;
+            bool failed = false;
+            int u = (int)atomicAdd(a.next_unit, 1u);   // the ticket is taken ahead of the wait
+            for (uint32_t k = 0;; ++k) {
+                // Unit k - 1's tiles are free once its MMAs are complete and the
+                // compute warps have read their rows and the z sum.
+                if (k > 0 && !mbar_wait(bar(BAR_SMEM), (k - 1) & 1u, ctl)) {
+                    failed = true;
+                    break;
+                }
+                if (u >= a.nunits) {
+                    unit_slot[k & 1] = -1;
+                    mbar_arrive(fb);   // completes the phase with no bytes: the end marker
+                    break;
+                }
+                unit_slot[k & 1] = u;
+                const int nc = u % a.nck, bh = u / a.nck;
+                const int b = bh / a.H, h = bh % a.H, t0 = nc * C;
+                const size_t slot = ((size_t)bh * a.nck + nc) * kStateCopyBytes;
+                mbar_arrive_expect_tx(fb, 18u * (uint32_t)C * 64u + 2u * kStateCopyBytes);
 #pragma unroll
-            for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffQ + j * kBlk, &tm_q, fb, 32 * j, h, t0, b);
+                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffQ + j * kBlk, &tm_q, fb, 32 * j, h, t0, b);
 #pragma unroll
-            for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffK + j * kBlk, &tm_k, fb, 32 * j, h, t0, b);
+                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffK + j * kBlk, &tm_k, fb, 32 * j, h, t0, b);
 #pragma unroll
-            for (int j = 0; j < 6; ++j) tma_load_4d(base + kOffV + j * kBlk, &tm_v, fb, 32 * j, h, t0, b);
+                for (int j = 0; j < 6; ++j) tma_load_4d(base + kOffV + j * kBlk, &tm_v, fb, 32 * j, h, t0, b);
 #pragma unroll
-            for (int j = 0; j < 6; ++j) tma_load_4d(base + kOffDo + j * kBlk, &tm_do, fb, 32 * j, h, t0, b);
-            bulk_load(base + kOffS, a.saved_s + slot, kStateCopyBytes, fb);
-            bulk_load(base + kOffG, a.saved_g + slot, kStateCopyBytes, fb);
-            // the copies must have landed before the CTA exits, whatever happens elsewhere
-            mbar_wait_drain(fb, 0, kWaitLimitNs);
+                for (int j = 0; j < 6; ++j) tma_load_4d(base + kOffDo + j * kBlk, &tm_do, fb, 32 * j, h, t0, b);
+                bulk_load(base + kOffS, a.saved_s + slot, kStateCopyBytes, fb);
+                bulk_load(base + kOffG, a.saved_g + slot, kStateCopyBytes, fb);
+                ++issued;
+                u = (int)atomicAdd(a.next_unit, 1u);
+            }
+            // On the error path the last copies may still be in flight: they must
+            // land before the CTA exits. (On the normal path the compute warps
+            // have consumed every unit's tiles before the end marker.)
+            if (failed && issued > 0) mbar_wait_drain(fb, (issued - 1) & 1u, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMAs
         if (lane == 0) {
-            if (mbar_wait(bar(BAR_LOAD), 0, ctl)) {
+            uint32_t committed = 0;
+            const uint32_t idS = idesc_bf16(128, C, false, false);     // scores: both K-major
+            const uint32_t id96 = idesc_bf16(128, kDk, false, false);  // state products: copy K-major
+            for (uint32_t k = 0;; ++k) {
+                if (!mbar_wait(bar(BAR_LOAD), k & 1u, ctl)) break;
+                if (unit_slot[k & 1] < 0) break;
+                // the compute warps are done with unit k - 1's products
+                if (k > 0 && !mbar_wait(bar(BAR_TMEM), (k - 1) & 1u, ctl)) break;
                 tc_fence_after();
-                const uint32_t idS = idesc_bf16(128, C, false, false);     // scores: both K-major
-                const uint32_t id96 = idesc_bf16(128, kDk, false, false);  // state products: copy K-major
 #pragma unroll
                 for (int ks = 0; ks < 6; ++ks) {
                     const uint32_t off = (uint32_t)(ks >> 1) * kBlk + (uint32_t)(ks & 1) * 32;
@@ -207,9 +254,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ss(tmem + kColE, smem_desc(base + kOffV + off, 16, 512, 4),
                                 smem_desc(base + kOffG + soff, 16, 512, 4), id96, ks > 0);
                 }
+                mma_commit(bar(BAR_MMA));
+                ++committed;
             }
-            // Arrives once the MMAs issued (if any) are complete.
-            mma_commit(bar(BAR_MMA));
+            // The MMAs issued must be complete before TMEM is released.
+            if (committed > 0) mbar_wait_drain(bar(BAR_MMA), (committed - 1) & 1u, kWaitLimitNs);
         }
         __syncwarp();
     } else {
@@ -219,29 +268,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t row = quad * 32 + (uint32_t)lane;
         const uint32_t ct = (uint32_t)threadIdx.x - 64;          // 0..255
         const uint32_t tl = tmem + ((quad * 32) << 16);
-        const bool in = (int)row < Cc;
         const int nblk = C / 32;
         const float s = a.scale;
         float *xe = reinterpret_cast<float *>(sm + kOffXch);     // e_j of each row
         float *xrow = xe + 128;                                   // the second warp's part of each row sum
         float *xz = xrow + 128;                                   // per-warp parts of z
-        // The chunk's gates: running log2-decays, last clearing positions, factors.
-        if (ct < 32) {
-            float x[4];
-            const float *gh = a.g + ((size_t)b * a.T + t0) * a.H + h;
+        uint32_t kw = 0;
+        for (uint32_t k = 0;; ++k) {
+            // Every compute thread takes the same branch: one waits, all read the verdict.
+            if (!compute_wait(bar(BAR_LOAD), k & 1u, ctl, decision, ct, kw)) break;
+            const int u = unit_slot[k & 1];
+            if (u < 0) break;
+            const int nc = u % a.nck, bh = u / a.nck;
+            const int b = bh / a.H, h = bh % a.H, t0 = nc * C, Cc = min(C, a.T - t0);
+            const bool in = (int)row < Cc;
+            // The chunk's gates (the first warp): issued now, scanned after the reads below.
+            float gx[4];
+            if (ct < 32) {
+                const float *gh = a.g + ((size_t)b * a.T + t0) * a.H + h;
 #pragma unroll
-            for (int r = 0; r < 4; ++r) x[r] = 4 * lane + r < Cc ? gh[(size_t)(4 * lane + r) * a.H] : 0.f;
-            gate_scan_store(x, lane, Gl, Zc, Af);
-        }
-        // One thread waits for the MMAs (which follow the loads); its verdict is
-        // read by all eight warps after the barrier, so none skips a barrier that
-        // the others wait on.
-        volatile int *decision = reinterpret_cast<volatile int *>(sm + kOffMisc + 8);
-        if (ct == 0) *decision = mbar_wait(bar(BAR_MMA), 0, ctl) && !*abort_flag ? 1 : 0;
-        named_sync(kBarCompute, kComputeThreads);
-        const bool ok = *decision != 0;
-        tc_fence_after();
-        if (ok) {
+                for (int r = 0; r < 4; ++r) gx[r] = 4 * lane + r < Cc ? gh[(size_t)(4 * lane + r) * a.H] : 0.f;
+            }
             // <G_out / s, S_prev> over this thread's share of the two copies (same layout)
             float zpart = 0.f;
             for (uint32_t i = ct; i < kStateCopyBytes / 16; i += kComputeThreads) {
@@ -257,20 +304,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int d = 16; d > 0; d >>= 1) zpart += __shfl_xor_sync(0xffffffffu, zpart, d);
             if (lane == 0) xz[sub * 4 + quad] = zpart;
+            // This thread's q (first warp of a pair) or k row (second), for r or e.
+            uint4 rr[12];
+            {
+                const uint32_t tile = base + (sub == 0 ? kOffQ : kOffK);
+#pragma unroll
+                for (int blk = 0; blk < 3; ++blk)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) rr[4 * blk + c] = ld_shared_v4(tile + blk * kBlk + sw64_offset(row, (uint32_t)c));
+            }
+            if (ct < 32) gate_scan_store(gx, lane, Gl, Zc, Af);
+            // The barrier inside also orders the reads above before the hand-back of
+            // shared memory, and the gate arrays before their readers.
+            if (!compute_wait(bar(BAR_MMA), k & 1u, ctl, decision, ct, kw)) break;
+            if (ct == 0) mbar_arrive(bar(BAR_SMEM));
+            tc_fence_after();
             const float gi = Gl[row];
             const int zi = Zc[row];
             const int last = Cc - 1;
             // r_i = s D(0..i) q_i.R1_i (first warp of the pair), e_j = s D(j+1..Cc-1)
             // k_j.E1_j (second)
             float dot = 0.f;
-            const uint32_t col0 = sub == 0 ? kColR : kColE;
-            const uint32_t tile = base + (sub == 0 ? kOffQ : kOffK);
-#pragma unroll 1
-            for (int blk = 0; blk < 3; ++blk) {
-                uint32_t x[32];
-                tmem_ld_32cols(tl + col0 + 32u * blk, x);
+            {
+                const uint32_t col0 = tl + (sub == 0 ? kColR : kColE);
+                uint32_t x0[32], x1[32];
+                tmem_ld_32cols(col0, x0);
+                tmem_ld_32cols(col0 + 32u, x1);
                 tmem_ld_wait();
-                dot += dot_row_sw64(x, tile + blk * kBlk, row);
+                dot = dot_row_regs(x0, &rr[0]) + dot_row_regs(x1, &rr[4]);
+                tmem_ld_32cols(col0 + 64u, x0);
+                tmem_ld_wait();
+                dot += dot_row_regs(x0, &rr[8]);
             }
             const float r_i = sub == 0 && in && zi < 0 ? s * exp2f(gi) * dot : 0.f;
             if (sub == 1) xe[row] = in && Zc[last] <= (int)row ? s * exp2f(Gl[last] - gi) * dot : 0.f;
@@ -312,7 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 colp[quad * 128 + 32 * bj + lane] = warp_transpose_sum(m, lane);
             }
             if (sub == 1) xrow[row] = rowsum;
+            tc_fence_before();
             named_sync(kBarCompute, kComputeThreads);
+            if (ct == 0) mbar_arrive(bar(BAR_TMEM));   // the next unit's MMAs may overwrite TMEM
             if (sub == 0) {
                 // Scans over the chunk's rows: w_u = col_u - row_u + e_u (exclusive
                 // prefix), r_i (inclusive suffix); z over the block.
@@ -364,12 +430,18 @@ cudaError_t launch_bwd_dg_tc(const BwdParams &p, cudaStream_t s, int *launches) 
     if ((e = make_token_map(&mv, p.v, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     if ((e = make_token_map(&mdo, p.do_, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     const int nck = (p.T + p.chunk - 1) / p.chunk;
-    const unsigned char *ws = static_cast<const unsigned char *>(p.workspace);
-    const size_t half = bwd_gated_tc_workspace_size(p.B, p.T, p.H, p.chunk) / 2;
-    DgArgs a{p.g, ws, ws + half, p.dg, p.scale, p.T, p.H, p.chunk, nck, p.status};
+    const size_t nunits = (size_t)p.B * p.H * nck;
+    if (nunits == 0) return cudaSuccess;
+    if (nunits > 0x7fffffffu - 1024u) return cudaErrorInvalidValue;   // the work counter's range
+    unsigned char *ws = static_cast<unsigned char *>(p.workspace);
+    const size_t half = bwd_gated_tc_state_bytes(p.B, p.T, p.H, p.chunk) / 2;
+    unsigned int *counter = reinterpret_cast<unsigned int *>(ws + 2 * half);
+    if ((e = cudaMemsetAsync(counter, 0, sizeof(unsigned int), s)) != cudaSuccess) return e;
+    DgArgs a{p.g, ws, ws + half, p.dg, counter, p.scale, p.T, p.H, p.chunk, nck, (int)nunits, p.status};
     e = cudaFuncSetAttribute(gla_dg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    gla_dg_kernel<<<(unsigned)((size_t)p.B * p.H * nck), kThreads, kSmemBytes, s>>>(mq, mk, mv, mdo, a);
+    const unsigned grid = (unsigned)std::min<size_t>(nunits, (size_t)device_sm_count());
+    gla_dg_kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, mdo, a);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

@@ -155,7 +155,9 @@ cudaError_t launch_bwd_kv_tc(const BwdParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_gated_tc(const BwdParams &p, cudaStream_t s, int *launches);
 cudaError_t launch_bwd_dg_tc(const BwdParams &p, cudaStream_t s, int *launches);
 // Workspace of the gated backward: two bf16 96 x 192 state copies per
-// (b, h, chunk), in the layout the chunk kernels keep them in shared memory.
+// (b, h, chunk), in the layout the chunk kernels keep them in shared memory
+// (bwd_gated_tc_state_bytes), then a 16-byte work counter of the dg kernel.
+size_t bwd_gated_tc_state_bytes(int B, int T, int H, int chunk);
 size_t bwd_gated_tc_workspace_size(int B, int T, int H, int chunk);
 size_t fwd_tc_workspace_size(int B, int T, int H, int chunk, bool gated = false);
 

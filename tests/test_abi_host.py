@@ -320,7 +320,7 @@ def test_gated_backward_rejects_bad_arguments(L):
     assert bwd(B=0) == binding.GLA_OK
     assert bwd(ws=None) == binding.GLA_ERR_WORKSPACE
     need = binding.gla_chunk_bwd_gated_workspace_size(2, 256, 16, 96, 192, 128)
-    assert need == 2 * 2 * 16 * 2 * 96 * 192 * 2            # two bf16 states per (b, h, chunk)
+    assert need == 2 * 2 * 16 * 2 * 96 * 192 * 2 + 16       # two bf16 states per (b, h, chunk), a counter
     assert bwd(wsb=need - 16) == binding.GLA_ERR_WORKSPACE
     assert "workspace" in L.gla_last_error().decode()
     assert binding.gla_chunk_bwd_gated_workspace_size(1, 300, 2, 8, 16, 64, binding.GLA_FP32) == 2 * 2 * 5 * 8 * 16 * 4
