@@ -263,7 +263,9 @@ gla_status gla_decode_step_gated(const void *q, const void *k, const void *v, co
  * the chunked form of "Challenge 1"; the gate enters each update as its decay).
  *   q, k, v, g, h0, scale, do, dhT, dq, dk_, dv_, dh0 as gla_chunk_bwd, with
  *   g [B,T,H] fp32 (as gla_chunk_fwd_gated) in place of log_lambda;
- *   dg [B,T,H] fp32 (written; 0 for a clearing gate).
+ *   dg [B,T,H] fp32 (written; 0 for a clearing gate). With g_t = ln lambda_h
+ *   for every token, the sum of dg over (b, t) is the gradient of a learned
+ *   per-head log lambda_h.
  *   workspace: at least gla_chunk_bwd_gated_workspace_size() bytes (required
  *   when T > 0). It receives the state entering every chunk and the state
  *   gradient leaving it, from which dg is formed chunk by chunk.
