@@ -32,7 +32,9 @@
 // as C lands, so A and B are read only by the tensor core.
 // One CTA per (b, h), one buffer per tile, each refilled as soon as its
 // readers are done: A after the inter MMA, B after the state MMA, C after the
-// intra MMA (and the copy). The MMA issuer is a non-blocking event loop.
+// intra MMA (and the copy). The B and C refills each close a chain of the
+// chunk period, so all three tiles of the next chunk are prefetched into L2
+// a chunk ahead. The MMA issuer is a non-blocking event loop.
 // Warps: 0 TMA, 1 TMEM + MMA, 2-5 make C~, 6-9 build P, 10-13 state hand-off
 // and output epilogue.
 //
@@ -213,6 +215,16 @@ __device__ __forceinline__ void tr_body(const CUtensorMap &tm_a, const CUtensorM
                 mbar_arrive_expect_tx(bar(BAR_FULLC), tx_c);
 #pragma unroll
                 for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffC + j * kBlk, &tm_c, bar(BAR_FULLC), 32 * j, h, t0, b);
+                // The next chunk's tiles into L2, about a chunk ahead of their loads.
+                if (c + 1 < nck) {
+                    const int t1 = natural(c + 1) * C;
+#pragma unroll
+                    for (int j = 0; j < 6; ++j) tma_prefetch_4d(&tm_a, 32 * j, h, t1, b);
+#pragma unroll
+                    for (int j = 0; j < 6; ++j) tma_prefetch_4d(&tm_b, 32 * j, h, t1, b);
+#pragma unroll
+                    for (int j = 0; j < 3; ++j) tma_prefetch_4d(&tm_c, 32 * j, h, t1, b);
+                }
             }
             __syncwarp();
             nc = c + 1;
