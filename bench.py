@@ -907,8 +907,8 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
     del o, v, g, q, k, z
 
     # The layer forward with the epilogue (gla_chunk_fwd_mixer: the forward's
-    # output stage writes the normalised rows y into z, a second pass applies
-    # the norm weight and the SiLU gate in place).
+    # output stage writes u = o + sigmoid(q . (aug * k)) v into z, a second pass
+    # normalises each row and applies the norm weight and the SiLU gate in place).
     c = gen.layer_fwd(seed=1, B=B, T=T)
     q, k, v = (dev_tensor(x, "bf16", device) for x in (c.q, c.k, c.v))
     ll = torch.from_numpy(c.log_lambda).to(device)
@@ -926,7 +926,7 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
     total, per, win, launches = time_steps(step3, args.steps, args.warmup, dist, stream)
     total = dist.max(total)
     # Algorithmic bytes of the call: q, k, v, g in, z out and hT. The two launches also move
-    # the normalised rows y once more (written by the forward, read back by the second pass):
+    # the rows u once more (written by the forward, read back by the second pass):
     # reported beside it, not counted as work.
     bytes3 = B * T * H * (2 * DK * 2 + 3 * DV * 2) + B * H * STATE_BYTES
     bytes3_moved = bytes3 + B * T * H * (2 * DV * 2)
@@ -935,15 +935,15 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
         "value": B * T * dist.world * args.steps / (total * 1e-3), "unit": "tokens/s",
         "ms_per_step": total / args.steps,
         "config": {"workload": f"layer_fwd_mixer_bf16_B{B}_H16_T{T}_C{CHUNK}", "B": B, "T": T, "H": H,
-                   "epilogue": "normalisation in the forward's output stage, then norm weight and "
-                               "SiLU(g) in place over z (two launches)",
+                   "epilogue": "self-augmentation in the forward's output stage, then RMS norm, "
+                               "norm weight and SiLU(g) in place over z (two launches)",
                    "l2": f"inputs larger than L2 ({bytes3 / 1e6:.0f} MB per step), no flush"},
         "roofline": {"bound": "hbm", "achieved": bytes3 / (avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": bytes3 / (avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                      "traffic": None, "algorithmic_bytes_per_call": bytes3, "avg_call_ms": avg_ms,
                      "bytes_moved_by_both_launches": bytes3_moved, "peak_source": peaks["source"],
-                     "note": "one call = the forward writing y = u / rms(u) into z, then "
-                             "z = y * norm_w * SiLU(g) in place"},
+                     "note": "one call = the forward writing u = o + sigmoid(q.(aug*k)) v into z, "
+                             "then z = u / rms(u) * norm_w * SiLU(g) in place"},
         "gpu_launches": launches,
         "clocks": sampler.summary(*win) if sampler else None,
     }

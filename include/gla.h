@@ -324,10 +324,10 @@ gla_status gla_decode_step(const void *q, const void *k, const void *v,
  *   o: g [B,T,H,dv] bf16, z [B,T,H,dv] bf16, hT and the workspace as for
  *   gla_chunk_fwd. GLA_BF16 only (dk = 96, dv = 192). The forward's launches
  *   and one more, with no scratch memory: at chunk 128 on the one-CTA-per-
- *   (b, h) kernel the forward's output stage applies the self-augmentation
- *   and the RMS normalisation and writes y / norm_w into z, and a second pass
- *   multiplies each row of z in place by norm_w and SiLU(g); otherwise the
- *   forward writes o into z and the epilogue rewrites each row of z in place.
+ *   (b, h) kernel the forward's output stage adds the self-augmentation and
+ *   writes u into z, and a second pass normalises each row of z in place and
+ *   multiplies it by norm_w and SiLU(g); otherwise the forward writes o into
+ *   z and the epilogue rewrites each row of z in place.
  *   z may not alias q, k, v or g.
  */
 gla_status gla_chunk_fwd_mixer(const void *q, const void *k, const void *v, const void *g, const float *log_lambda,

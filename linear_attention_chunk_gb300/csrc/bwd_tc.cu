@@ -670,7 +670,7 @@ cudaError_t launch_bwd_kv_tc(const BwdParams &p, cudaStream_t s, int *launches) 
     const int nck = (p.T + p.chunk - 1) / p.chunk;
     const TrArgs ta{p.log_lambda, p.dhT, p.scale, 1.f / p.scale, p.T, p.H, p.chunk, nck, p.status, nullptr, nullptr};
     const fullhead::FullArgs fa{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, nck, 1, nck,
-                                p.B * p.H, 0, p.status, nullptr, nullptr, nullptr, 0, nullptr, nullptr, 0.f};
+                                p.B * p.H, 0, p.status, nullptr, nullptr, nullptr, 0, nullptr, nullptr};
     auto kernel = p.chunk == 128 ? gla_bwd_kv_kernel<128> : gla_bwd_kv_kernel<64>;
     if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmem)) != cudaSuccess)
         return e;

@@ -11,7 +11,6 @@
 // row, lanes striding over channels, otherwise); the two reductions are
 // shuffles. The fp32 validation
 // path keeps exact sigmoids; the bf16 path uses the fast forms.
-#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -95,6 +94,11 @@ __device__ __forceinline__ float half_sum(float x) {   // over the 16 lanes of a
     return x;
 }
 
+// kFromU: the rows of p.o already hold u (the forward added the
+// self-augmentation); only the normalisation, the norm weight and the gate
+// are applied, and p.o may be p.z (in place: each lane reads the channels it
+// then writes).
+template <bool kFromU>
 __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(EpilogueParams p) {
     const size_t rows = (size_t)p.NT * p.H;
     const size_t row = ((size_t)blockIdx.x * kWarps + threadIdx.x / 32) * 2 + (threadIdx.x / 16) % 2;
@@ -104,16 +108,20 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(Epilog
     const size_t r = live ? row : row - 1;        // (it mirrors its partner and stores nothing)
     const int h = (int)(r % (size_t)p.H);
     const unsigned char *ob = static_cast<const unsigned char *>(p.o) + r * 384;
-    const unsigned char *vb = static_cast<const unsigned char *>(p.v) + r * 384;
     const unsigned char *gb = static_cast<const unsigned char *>(p.g) + r * 384;
     const uint4 o16 = __ldcs(reinterpret_cast<const uint4 *>(ob) + l);
-    const uint4 v16 = __ldcs(reinterpret_cast<const uint4 *>(vb) + l);
     const uint4 g16 = __ldcs(reinterpret_cast<const uint4 *>(gb) + l);
     const uint2 o8 = __ldcs(reinterpret_cast<const uint2 *>(ob + 256) + l);
-    const uint2 v8 = __ldcs(reinterpret_cast<const uint2 *>(vb + 256) + l);
     const uint2 g8 = __ldcs(reinterpret_cast<const uint2 *>(gb + 256) + l);
+    uint4 v16 = make_uint4(0, 0, 0, 0);
+    uint2 v8 = make_uint2(0, 0);
+    if constexpr (!kFromU) {
+        const unsigned char *vb = static_cast<const unsigned char *>(p.v) + r * 384;
+        v16 = __ldcs(reinterpret_cast<const uint4 *>(vb) + l);
+        v8 = __ldcs(reinterpret_cast<const uint2 *>(vb + 256) + l);
+    }
     float dot = 0.f;
-    if (p.aug) {
+    if (!kFromU && p.aug) {
         const unsigned char *qb = static_cast<const unsigned char *>(p.q) + r * 192;
         const unsigned char *kb = static_cast<const unsigned char *>(p.k) + r * 192;
         const uint2 q8 = __ldcs(reinterpret_cast<const uint2 *>(qb) + l);
@@ -132,7 +140,7 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(Epilog
         dot = fmaf(qc.x * a2.x, kc.x, dot);
         dot = fmaf(qc.y * a2.y, kc.y, dot);
     }
-    const float gate = __fdividef(1.f, 1.f + __expf(-half_sum(dot)));
+    const float gate = kFromU ? 0.f : __fdividef(1.f, 1.f + __expf(-half_sum(dot)));
     const uint32_t ow[6] = {o16.x, o16.y, o16.z, o16.w, o8.x, o8.y};
     const uint32_t vw[6] = {v16.x, v16.y, v16.z, v16.w, v8.x, v8.y};
     float u[12];
@@ -173,41 +181,6 @@ __global__ void __launch_bounds__(32 * kWarps) mixer_epilogue_bf16_kernel(Epilog
     }
 }
 
-// The rest of the epilogue over rows that the forward left normalised in z
-// (y = u / rms(u), bf16, dv = 192): z = y * norm_w * SiLU(g), in place. A
-// stream of 16-byte vectors, eight channels per thread, consecutive threads
-// on consecutive vectors.
-__global__ void __launch_bounds__(256) mixer_finish_bf16_kernel(EpilogueParams p) {
-    const size_t n = (size_t)p.NT * p.H * 24;   // 24 vectors of 8 channels per row
-    for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < n; i += (size_t)gridDim.x * 256) {
-        const size_t r = i / 24;
-        const int cv = (int)(i % 24), h = (int)(r % (size_t)p.H);
-        uint4 *zp = reinterpret_cast<uint4 *>(p.z) + i;
-        const uint4 y16 = __ldcs(zp);
-        const uint4 g16 = __ldcs(reinterpret_cast<const uint4 *>(p.g) + i);
-        float w[8];
-        if (p.norm_w) {
-            const float4 *wr = reinterpret_cast<const float4 *>(p.norm_w + (size_t)h * 192 + 8 * cv);
-            const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
-            w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
-            w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = 1.f;
-        }
-        const uint32_t yw[4] = {y16.x, y16.y, y16.z, y16.w}, gw[4] = {g16.x, g16.y, g16.z, g16.w};
-        uint32_t zw[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 yf = unpack_bf16x2(yw[e]), gf = unpack_bf16x2(gw[e]);
-            const float h0 = 0.5f * gf.x, h1 = 0.5f * gf.y;
-            zw[e] = pack_bf16x2(yf.x * w[2 * e] * fmaf(h0, tanh_fast(h0), h0),
-                                yf.y * w[2 * e + 1] * fmaf(h1, tanh_fast(h1), h1));
-        }
-        __stcs(zp, make_uint4(zw[0], zw[1], zw[2], zw[3]));
-    }
-}
-
 template <typename T>
 cudaError_t epilogue_impl(const EpilogueParams &p, cudaStream_t s, int *launches) {
     const size_t rows = (size_t)p.NT * p.H;
@@ -215,7 +188,7 @@ cudaError_t epilogue_impl(const EpilogueParams &p, cudaStream_t s, int *launches
     const size_t blocks = (rows + kWarps - 1) / kWarps;
     if (blocks > 0x7fffffffull) return cudaErrorInvalidValue;
     if (std::is_same<T, __nv_bfloat16>::value && p.dk == 96 && p.dv == 192)
-        mixer_epilogue_bf16_kernel<<<(unsigned)((rows + 2 * kWarps - 1) / (2 * kWarps)), 32 * kWarps, 0, s>>>(p);
+        mixer_epilogue_bf16_kernel<false><<<(unsigned)((rows + 2 * kWarps - 1) / (2 * kWarps)), 32 * kWarps, 0, s>>>(p);
     else if (p.dk == 96 && p.dv == 192)
         mixer_epilogue_kernel<T, 96, 192><<<(unsigned)blocks, 32 * kWarps, 0, s>>>(p);
     else
@@ -231,11 +204,12 @@ cudaError_t launch_mixer_epilogue(const EpilogueParams &p, bool bf16, cudaStream
 }
 
 cudaError_t launch_mixer_finish(const EpilogueParams &p, cudaStream_t s, int *launches) {
-    if (p.dv != 192) return cudaErrorInvalidValue;
-    const size_t n = (size_t)p.NT * p.H * 24;
-    if (n == 0) return cudaSuccess;
-    const size_t blocks = std::min<size_t>((n + 255) / 256, (size_t)device_sm_count() * 16);
-    mixer_finish_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    if (p.dk != 96 || p.dv != 192) return cudaErrorInvalidValue;
+    const size_t rows = (size_t)p.NT * p.H;
+    if (rows == 0) return cudaSuccess;
+    const size_t blocks = (rows + 2 * kWarps - 1) / (2 * kWarps);
+    if (blocks > 0x7fffffffull) return cudaErrorInvalidValue;
+    mixer_epilogue_bf16_kernel<true><<<(unsigned)blocks, 32 * kWarps, 0, s>>>(p);
     if (launches) ++*launches;
     return cudaGetLastError();
 }

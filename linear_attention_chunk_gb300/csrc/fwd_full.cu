@@ -31,7 +31,7 @@ cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int se
     const int nck = (p.T + p.chunk - 1) / p.chunk;
     FullArgs a{p.log_lambda, S_in ? S_in : p.h0, p.hT, p.scale, 1.f, 1.f, p.T, p.H, nck, nseg,
                nseg > 1 ? seg_chunks : nck, p.B * p.H, nseg > 1 ? (size_t)p.B * p.H * kDk * kDv : 0, p.status, p.g,
-               nullptr, nullptr, 0, nullptr, epi ? epi->aug : nullptr, epi ? epi->eps : 0.f};
+               nullptr, nullptr, 0, nullptr, epi ? epi->aug : nullptr};
     auto kernel = epi ? gla_fwd_full_kernel<false, 128, false, false, true>
                 : p.g ? (p.chunk == 128 ? gla_fwd_full_kernel<false, 128, true> : gla_fwd_full_kernel<false, 64, true>)
                       : (p.chunk == 128 ? gla_fwd_full_kernel<false, 128, false>
@@ -57,7 +57,7 @@ cudaError_t launch_bwd_dv_full_tc(const BwdParams &p, cudaStream_t s, int *launc
     if ((e = make_token_map(&mout, p.dv_out, p.B, p.T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     const int nck = (p.T + p.chunk - 1) / p.chunk;
     FullArgs a{p.log_lambda, p.dhT, p.dh0, p.scale, 1.f / p.scale, p.scale, p.T, p.H, nck, 1, nck, p.B * p.H, 0,
-               p.status, p.g, nullptr, nullptr, 0, nullptr, nullptr, 0.f};
+               p.status, p.g, nullptr, nullptr, 0, nullptr, nullptr};
     auto kernel = p.chunk == 128 ? gla_fwd_full_kernel<true, 128, true> : gla_fwd_full_kernel<true, 64, true>;
     const uint32_t smem = p.chunk == 128 ? Layout<128>::kSmemBytes : Layout<64>::kSmemBytes;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -79,8 +79,7 @@ cudaError_t launch_fwd_varlen_full_tc(const VarlenParams &p, cudaStream_t s, int
     if ((e = make_token_map(&mo, p.o, 1, p.total_T, p.H, kDv, p.chunk)) != cudaSuccess) return e;
     // nck and seg_chunks are per sequence (set in the kernel); one segment
     const FullArgs a{p.log_lambda, p.pool, p.pool, p.scale, 1.f, 1.f, p.total_T, p.H, 0, 1, 0, p.nseq * p.H, 0,
-                     p.status, p.g, p.cu_seqlens, p.slots, p.n_slots, static_cast<__nv_bfloat16 *>(p.o), nullptr,
-                     0.f};
+                     p.status, p.g, p.cu_seqlens, p.slots, p.n_slots, static_cast<__nv_bfloat16 *>(p.o), nullptr};
     auto kernel = p.g ? (p.chunk == 128 ? gla_fwd_full_kernel<false, 128, true, true>
                                         : gla_fwd_full_kernel<false, 64, true, true>)
                       : (p.chunk == 128 ? gla_fwd_full_kernel<false, 128, false, true>

@@ -146,11 +146,10 @@ struct FullArgs {
     const int *cu_seqlens, *slots;
     int n_slots;
     __nv_bfloat16 *o;
-    // The mixer epilogue's normalisation (kEpi): the output rows become
-    // y = (o + sigmoid(q . (aug * k)) v) / sqrt(mean(u^2) + eps), aug [H, 96]
-    // fp32 or NULL (zero); the gate and the norm weight follow in a second pass.
+    // The mixer epilogue's self-augmentation (kEpi): the output rows become
+    // u = o + sigmoid(q . (aug * k)) v, aug [H, 96] fp32 or NULL (zero); the
+    // RMS normalisation, the norm weight and the gate follow in a second pass.
     const float *aug;
-    float eps;
 };
 
 // One elected thread of an n-thread group waits; the verdict is published
@@ -200,11 +199,11 @@ __device__ __forceinline__ float chunk_decay_warp(const float (&x)[4]) {
 // are walked along the factors exp(g); the H group's first warp reduces each
 // chunk's gates to its total decay for the state's rescale, one chunk ahead.
 // `blk` is the CTA's unit: segment blk / BH of chain (b, h) = blk % BH.
-// kEpi (forward, per-head decay, C = 128): each output row leaves normalised,
-// y = u / rms(u) with u = o + sigmoid(q . (aug * k)) v over the head's 192
-// channels. The P group forms the row's gate from its q row (in registers)
-// and its k row (before K is scaled); the E group forms u from O (TMEM) and
-// v (the V slot it stages y into), in two passes over the row.
+// kEpi (forward, per-head decay, C = 128): each output row leaves with the
+// self-augmentation added, u = o + sigmoid(q . (aug * k)) v over the head's
+// 192 channels. The P group forms the row's gate from its q row (in
+// registers) and its k row (before K is scaled); the E group forms u from O
+// (TMEM) and v (the V slot it stages u into) in its one pass over the row.
 template <bool kRev, int kC, bool kGate = false, bool kVar = false, bool kEpi = false>
 __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                           const CUtensorMap &tm_o, const FullArgs &a, int blk) {
@@ -633,44 +632,37 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                 }
             };
             if constexpr (kEpi) {
-                // y = u / rms(u), u = o * scale + sigma * v: one pass over the six
-                // 32-column blocks for the sum of squares, one to write y over this
-                // row's v in the V slot (each thread owns its row).
+                // u = o * scale + sigma * v over this row's v in the V slot (each
+                // thread owns its row), the next block's TMEM load in flight while
+                // this one is formed and staged.
                 const float sg = ep_sig[(c & 1) * 128 + row];
-                auto u_block = [&](int blk, float (&u)[32]) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(tl + kColO + 32u * blk, r);
-                    tmem_ld_wait();
+                auto put_u = [&](uint32_t (&r)[32], int blk) {
+                    const uint32_t vrow = stg + blk * kB;
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
-                        const uint4 vv = ld_shared_v4(stg + blk * kB + sw64_offset(row, (uint32_t)cc));
+                        const uint4 vv = ld_shared_v4(vrow + sw64_offset(row, (uint32_t)cc));
                         const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 vf = unpack_bf16x2(vw[e]);
                             const int m = 8 * cc + 2 * e;
-                            u[m] = fmaf(sg, vf.x, __uint_as_float(r[m]) * a.scale);
-                            u[m + 1] = fmaf(sg, vf.y, __uint_as_float(r[m + 1]) * a.scale);
+                            r[m] = __float_as_uint(fmaf(sg, vf.x, __uint_as_float(r[m]) * a.scale));
+                            r[m + 1] = __float_as_uint(fmaf(sg, vf.y, __uint_as_float(r[m + 1]) * a.scale));
                         }
                     }
+                    write_row_sw64_bits(sm + (stg - base) + blk * kB, row, r, 1.f);
                 };
-                float ss = 0.f;
+                uint32_t ra[32], rb[32];
+                tmem_ld_32cols(tl + kColO, ra);
 #pragma unroll 1
-                for (int blk = 0; blk < 6; ++blk) {
-                    float u[32];
-                    u_block(blk, u);
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) ss = fmaf(u[m], u[m], ss);
-                }
-                const float rinv = rsqrtf(ss * (1.f / kDv) + a.eps);
-#pragma unroll 1
-                for (int blk = 0; blk < 6; ++blk) {
-                    float u[32];
-                    u_block(blk, u);
-                    uint32_t yb[32];
-#pragma unroll
-                    for (int m = 0; m < 32; ++m) yb[m] = __float_as_uint(u[m] * rinv);
-                    write_row_sw64_bits(sm + (stg - base) + blk * kB, row, yb, 1.f);
+                for (int bp = 0; bp < 3; ++bp) {
+                    const int blk = 2 * bp;
+                    tmem_ld_wait();
+                    tmem_ld_32cols(tl + kColO + 32u * (blk + 1), rb);
+                    put_u(ra, blk);
+                    tmem_ld_wait();
+                    if (bp < 2) tmem_ld_32cols(tl + kColO + 32u * (blk + 2), ra);
+                    put_u(rb, blk + 1);
                 }
             } else {
                 // Six 32-column blocks, the next block's TMEM load in flight while

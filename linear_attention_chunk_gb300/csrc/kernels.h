@@ -81,8 +81,9 @@ struct EpilogueParams {
     void *z;
 };
 cudaError_t launch_mixer_epilogue(const EpilogueParams &p, bool bf16, cudaStream_t s, int *launches);
-// The rest of the epilogue over rows already normalised in place in p.z
-// (bf16, dv = 192): z = y * norm_w * SiLU(g).
+// The rest of the epilogue over rows of p.o that already hold u = o +
+// sigmoid(q . (aug * k)) v (bf16, dk = 96, dv = 192; p.o may be p.z): the
+// RMS normalisation, the norm weight and SiLU(g), into p.z.
 cudaError_t launch_mixer_finish(const EpilogueParams &p, cudaStream_t s, int *launches);
 
 // The causal depthwise Conv1d (width 4) with SiLU (conv.cu). Batched: nseq
@@ -124,15 +125,16 @@ cudaError_t launch_copy_state(const float *src, float *dst, size_t n, cudaStream
 // chains run unsegmented; the variable-length prefill likewise by its
 // number of (sequence, head) chains.
 // epi (or NULL): the mixer epilogue over the output, z in place of o: its
-// normalisation fused into the one-CTA-per-chain kernel's output stage at
-// C = 128 and the rest in launch_mixer_finish, else one launch of
+// self-augmentation fused into the one-CTA-per-chain kernel's output stage
+// at C = 128 and the rest in launch_mixer_finish, else one launch of
 // launch_mixer_epilogue after the forward.
 cudaError_t launch_fwd_tc(const FwdParams &p, cudaStream_t s, int *launches, const EpilogueParams *epi = nullptr);
 // The forward with one CTA per (b, h) holding the whole state (fwd_full.cu);
 // S_in (or NULL: p.h0) holds each segment's initial state when nseg > 1.
-// epi (or NULL): the mixer epilogue's normalisation fused into the output
-// stage (per-head decay, chunk 128): rows leave as y = u / rms(u), for
-// launch_mixer_finish to apply the norm weight and the SiLU gate.
+// epi (or NULL): the mixer epilogue's self-augmentation fused into the
+// output stage (per-head decay, chunk 128): rows leave as u = o +
+// sigmoid(q . (aug * k)) v, for launch_mixer_finish to normalise them and
+// apply the norm weight and the SiLU gate.
 cudaError_t launch_fwd_full_tc(const FwdParams &p, float *S_in, int nseg, int seg_chunks, cudaStream_t s,
                                int *launches, const EpilogueParams *epi = nullptr);
 // dv and dh0 of the per-token decay's backward on the one-CTA-per-(b, h)
