@@ -940,7 +940,8 @@ def bench_mixer(args, dist, device, stream, peaks, sampler):
                    "l2": f"inputs larger than L2 ({bytes3 / 1e6:.0f} MB per step), no flush"},
         "roofline": {"bound": "hbm", "achieved": bytes3 / (avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": bytes3 / (avg_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                     "traffic": None, "algorithmic_bytes_per_call": bytes3, "avg_call_ms": avg_ms,
+                     "traffic": committed_traffic("mixer_fwd")[0], "algorithmic_bytes_per_call": bytes3,
+                     "avg_call_ms": avg_ms,
                      "bytes_moved_by_both_launches": bytes3_moved, "peak_source": peaks["source"],
                      "note": "one call = the forward writing u = o + sigmoid(q.(aug*k)) v into z, "
                              "then z = u / rms(u) * norm_w * SiLU(g) in place"},
