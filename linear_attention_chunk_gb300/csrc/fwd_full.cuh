@@ -118,6 +118,7 @@ struct Layout {
     static constexpr uint32_t kSmemUsed = kOffEpi + (96 + 256) * 4;
     static constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kOffEpi % 16 == 0, "the aug row is read as float4");
     static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffSb % 1024 == 0 && kOffOut % 1024 == 0,
                   "tile alignment");
 };
@@ -482,28 +483,6 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             if (gt == 0) mbar_arrive(bar(BAR_QFREE));
             if (!gwait(bar(BAR_QKDONE), (uint32_t)c & 1u, ctl, dec, gt, kBarP, 128, kw)) break;
             tc_fence_after();
-            if constexpr (kEpi) {
-                // the row's self-augmentation gate, from q (registers) and k (before K is scaled)
-                const uint32_t kb = stage(c) + kStK;
-                float dot = 0.f;
-#pragma unroll
-                for (int j = 0; j < 3; ++j)
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const uint4 kv = ld_shared_v4(kb + j * kB + sw64_offset(row, (uint32_t)cc));
-                        const uint32_t kw4[4] = {kv.x, kv.y, kv.z, kv.w};
-                        const uint4 qv = qrow[4 * j + cc];
-                        const uint32_t qw4[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int d = 32 * j + 8 * cc + 2 * e;
-                            const float2 qf = unpack_bf16x2(qw4[e]), kf = unpack_bf16x2(kw4[e]);
-                            dot = fmaf(qf.x * ep_aug[d], kf.x, dot);
-                            dot = fmaf(qf.y * ep_aug[d + 1], kf.y, dot);
-                        }
-                    }
-                ep_sig[(c & 1) * 128 + row] = 1.f / (1.f + __expf(-dot));
-            }
             // K~ = diag(lambda^(Cc-1-j)) K in place (zero past the end), or lambda^(i+1)
             // in reverse; signalled at once.
             {
@@ -514,7 +493,40 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
                     wk = row < (uint32_t)Cc && Zc[Cc - 1] <= (int)row ? exp2f(Gl[Cc - 1] - Gl[row]) : 0.f;
                 else
                     wk = kRev ? pw[row + 1] : (row < (uint32_t)Cc ? pw[Cc - 1 - (int)row] : 0.f);
-                if (row < (uint32_t)C) scale_rows<3, kB>(sm + (stage(c) - base) + kStK, row, wk);
+                if constexpr (kEpi) {
+                    // The row's self-augmentation gate from q (registers) and the k row,
+                    // read once: the dot product is taken before the row is scaled.
+                    const uint32_t kb = stage(c) + kStK;
+                    const uint32_t w2 = pack_bf16x2(wk, wk);
+                    float dot = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 3; ++j)
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const uint32_t addr = kb + j * kB + sw64_offset(row, (uint32_t)cc);
+                            uint4 kv = ld_shared_v4(addr);
+                            const uint32_t kw4[4] = {kv.x, kv.y, kv.z, kv.w};
+                            const uint4 qv = qrow[4 * j + cc];
+                            const uint32_t qw4[4] = {qv.x, qv.y, qv.z, qv.w};
+                            const float4 a0 = *reinterpret_cast<const float4 *>(ep_aug + 32 * j + 8 * cc);
+                            const float4 a1 = *reinterpret_cast<const float4 *>(ep_aug + 32 * j + 8 * cc + 4);
+                            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 qf = unpack_bf16x2(qw4[e]), kf = unpack_bf16x2(kw4[e]);
+                                dot = fmaf(qf.x * av[2 * e], kf.x, dot);
+                                dot = fmaf(qf.y * av[2 * e + 1], kf.y, dot);
+                            }
+                            kv.x = mul_bf16x2(kv.x, w2);
+                            kv.y = mul_bf16x2(kv.y, w2);
+                            kv.z = mul_bf16x2(kv.z, w2);
+                            kv.w = mul_bf16x2(kv.w, w2);
+                            st_shared_v4(addr, kv.x, kv.y, kv.z, kv.w);
+                        }
+                    ep_sig[(c & 1) * 128 + row] = 1.f / (1.f + __expf(-dot));
+                } else if (row < (uint32_t)C) {
+                    scale_rows<3, kB>(sm + (stage(c) - base) + kStK, row, wk);
+                }
             }
             fence_proxy_async_smem();
             named_sync(kBarP, 128);
