@@ -486,8 +486,17 @@ __device__ __forceinline__ void tr_body(const CUtensorMap &tm_a, const CUtensorM
                     gate_scan_store(gpre, lane, Gls[(c + 1) & 1], Zcs[(c + 1) & 1], Afs[(c + 1) & 1]);
                     load_gates(c + 2, gpre);
                 }
-                // the saved copy of the state must be read out before the hand-off rewrites it
-                if (gt == 0) tma_store_wait_read_all();
+                // The saved copy of the state must be read out before the hand-off
+                // rewrites it. The bulk groups in flight are the previous copy's and
+                // the previous chunk's output (which reads the staging buffer, not the
+                // copy): wait for all but the most recent, the output, except before
+                // the first chunk, when the initial copy's is the only one.
+                if (gt == 0) {
+                    if (c == 0)
+                        tma_store_wait_read_all();
+                    else
+                        tma_store_wait_read_1();
+                }
             }
             if (!group_wait(bar(BAR_SFULL), c & 1, ctl, dec + 4, gt, kBarE, kw)) break;
             tc_fence_after();
@@ -517,7 +526,14 @@ __device__ __forceinline__ void tr_body(const CUtensorMap &tm_a, const CUtensorM
 
             if (!group_wait(bar(BAR_OFULL), c & 1, ctl, dec + 4, gt, kBarE, kw)) break;
             tc_fence_after();
-            if (gt == 0) tma_store_wait_read_all();
+            // The staging buffer's previous store must be read out; in gated mode the
+            // state copy's store, committed after it, may stay in flight.
+            if (gt == 0) {
+                if (kGate && !last)
+                    tma_store_wait_read_1();
+                else
+                    tma_store_wait_read_all();
+            }
             named_sync(kBarE, kGroupThreads);
             {
                 float wr;
