@@ -272,14 +272,28 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
     auto bar = [&](int i) { return base + kOffBar + 8u * (uint32_t)i; };
     auto stage = [&](int c) { return base + kOffStage + (uint32_t)(c & 1) * kStageBytes; };
 
+    const uint32_t tx3 = 3u * (uint32_t)C * 64u, tx6 = 6u * (uint32_t)C * 64u;
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         for (int i = 0; i < 6; ++i) dec[i] = 0;
         for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), i == BAR_QFREE ? 2u : 1u);
         fence_mbar_init();
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
+        fence_proxy_async_smem();
+        // The first chunk's K, Q and V loads go out now, under the setup below
+        // (decay tables, TMEM allocation); the producer issues the rest.
+        if (nck > 0) {
+            const uint32_t st = stage(0);
+            const int t0 = tok0(0);
+            mbar_arrive_expect_tx(bar(BAR_FULLK0), tx3);
+#pragma unroll
+            for (int j = 0; j < 3; ++j) tma_load_4d(st + kStK + j * kB, &tm_k, bar(BAR_FULLK0), 32 * j, h, tokb + t0, bt);
+            mbar_arrive_expect_tx(bar(BAR_FULLQ), tx3);
+#pragma unroll
+            for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffQ + j * kB, &tm_q, bar(BAR_FULLQ), 32 * j, h, tokb + t0, bt);
+            mbar_arrive_expect_tx(bar(BAR_FULLV0), tx6);
+#pragma unroll
+            for (int j = 0; j < 6; ++j) tma_load_4d(st + kStV + j * kB, &tm_v, bar(BAR_FULLV0), 32 * j, h, tokb + t0, bt);
+        }
         prefetch_tmap(&tm_o);
     }
     if constexpr (!kGate) {   // the gated form has no per-head decay (log_lambda is NULL)
@@ -302,8 +316,8 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         // ------------------------------------------------------- TMA producer
         // K(c) into stage c % 2 once ST(c-2) has completed; Q(c) once QK(c-1)
         // has completed and Q~(c-1) is in TMEM; V(c) into stage c % 2 once the
-        // output of chunk c-2, staged in that slot, has been read out.
-        const uint32_t tx3 = 3u * (uint32_t)C * 64u, tx6 = 6u * (uint32_t)C * 64u;
+        // output of chunk c-2, staged in that slot, has been read out. Chunk 0's
+        // loads went out with the barriers' initialisation.
         int nq = 0, nk = 0, nv = 0;   // chunks whose Q / K / V loads were issued
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
@@ -311,7 +325,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             const int t0 = tok0(c);
             const uint32_t ph2 = (uint32_t)((c >> 1) - 1) & 1u;   // phase parity of chunk c-2
             if (c >= 2 && !lane0_wait(bar(BAR_KFREE0 + s), ph2, ctl, lane)) break;
-            if (lane == 0) {
+            if (lane == 0 && c > 0) {
                 mbar_arrive_expect_tx(bar(BAR_FULLK0 + s), tx3);
 #pragma unroll
                 for (int j = 0; j < 3; ++j) tma_load_4d(st + kStK + j * kB, &tm_k, bar(BAR_FULLK0 + s), 32 * j, h, tokb + t0, bt);
@@ -320,9 +334,12 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             nk = c + 1;
             if (c >= 1 && !lane0_wait(bar(BAR_QFREE), (uint32_t)(c - 1) & 1u, ctl, lane)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar(BAR_FULLQ), tx3);
+                if (c > 0) {
+                    mbar_arrive_expect_tx(bar(BAR_FULLQ), tx3);
 #pragma unroll
-                for (int j = 0; j < 3; ++j) tma_load_4d(base + kOffQ + j * kB, &tm_q, bar(BAR_FULLQ), 32 * j, h, tokb + t0, bt);
+                    for (int j = 0; j < 3; ++j)
+                        tma_load_4d(base + kOffQ + j * kB, &tm_q, bar(BAR_FULLQ), 32 * j, h, tokb + t0, bt);
+                }
                 // Q has one buffer: bring the next chunk's tile into L2 now, so that its
                 // load, which waits for this one to be consumed, is served from L2.
                 if (c + 1 < nck)
@@ -333,9 +350,12 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             nq = c + 1;
             if (c >= 2 && !lane0_wait(bar(BAR_VFREE0 + s), ph2, ctl, lane)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(bar(BAR_FULLV0 + s), tx6);
+                if (c > 0) {
+                    mbar_arrive_expect_tx(bar(BAR_FULLV0 + s), tx6);
 #pragma unroll
-                for (int j = 0; j < 6; ++j) tma_load_4d(st + kStV + j * kB, &tm_v, bar(BAR_FULLV0 + s), 32 * j, h, tokb + t0, bt);
+                    for (int j = 0; j < 6; ++j)
+                        tma_load_4d(st + kStV + j * kB, &tm_v, bar(BAR_FULLV0 + s), 32 * j, h, tokb + t0, bt);
+                }
                 // V(c+1)'s slot frees only once the output of chunk c-1 has been stored from
                 // it; bring that tile into L2 now, so that its load is served from L2 (the
                 // per-head decay's forward: measured 62.5 -> 60.6 us on the layer shape; the
