@@ -279,9 +279,10 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), i == BAR_QFREE ? 2u : 1u);
         fence_mbar_init();
         fence_proxy_async_smem();
-        // The first chunk's K, Q and V loads go out now, under the setup below
-        // (decay tables, TMEM allocation); the producer issues the rest.
-        if (nck > 0) {
+        // The per-head decay's first K, Q and V loads go out now, under the setup
+        // below (decay tables, TMEM allocation); the producer issues the rest (all
+        // of them with the per-token decay, whose forward measured slower this way).
+        if (!kGate && nck > 0) {
             const uint32_t st = stage(0);
             const int t0 = tok0(0);
             mbar_arrive_expect_tx(bar(BAR_FULLK0), tx3);
@@ -316,8 +317,8 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
         // ------------------------------------------------------- TMA producer
         // K(c) into stage c % 2 once ST(c-2) has completed; Q(c) once QK(c-1)
         // has completed and Q~(c-1) is in TMEM; V(c) into stage c % 2 once the
-        // output of chunk c-2, staged in that slot, has been read out. Chunk 0's
-        // loads went out with the barriers' initialisation.
+        // output of chunk c-2, staged in that slot, has been read out. With the
+        // per-head decay chunk 0's loads went out with the barriers' initialisation.
         int nq = 0, nk = 0, nv = 0;   // chunks whose Q / K / V loads were issued
         for (int c = 0; c < nck; ++c) {
             const int s = c & 1;
@@ -325,7 +326,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             const int t0 = tok0(c);
             const uint32_t ph2 = (uint32_t)((c >> 1) - 1) & 1u;   // phase parity of chunk c-2
             if (c >= 2 && !lane0_wait(bar(BAR_KFREE0 + s), ph2, ctl, lane)) break;
-            if (lane == 0 && c > 0) {
+            if (lane == 0 && (kGate || c > 0)) {
                 mbar_arrive_expect_tx(bar(BAR_FULLK0 + s), tx3);
 #pragma unroll
                 for (int j = 0; j < 3; ++j) tma_load_4d(st + kStK + j * kB, &tm_k, bar(BAR_FULLK0 + s), 32 * j, h, tokb + t0, bt);
@@ -334,7 +335,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             nk = c + 1;
             if (c >= 1 && !lane0_wait(bar(BAR_QFREE), (uint32_t)(c - 1) & 1u, ctl, lane)) break;
             if (lane == 0) {
-                if (c > 0) {
+                if (kGate || c > 0) {
                     mbar_arrive_expect_tx(bar(BAR_FULLQ), tx3);
 #pragma unroll
                     for (int j = 0; j < 3; ++j)
@@ -350,7 +351,7 @@ __device__ __forceinline__ void full_body(const CUtensorMap &tm_q, const CUtenso
             nq = c + 1;
             if (c >= 2 && !lane0_wait(bar(BAR_VFREE0 + s), ph2, ctl, lane)) break;
             if (lane == 0) {
-                if (c > 0) {
+                if (kGate || c > 0) {
                     mbar_arrive_expect_tx(bar(BAR_FULLV0 + s), tx6);
 #pragma unroll
                     for (int j = 0; j < 6; ++j)
